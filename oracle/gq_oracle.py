@@ -1,0 +1,274 @@
+"""Plain, slow, float64 oracle of the group-quantized weight-only GEMM.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the product path never imports it.
+
+Sources (the pages this follows):
+  * P1 = "GPU Kernel 工程（09）：量化与融合 kernel" (arganzheng.life,
+    quantization-and-fused-kernels).
+  * P2 = "04 · 分组量化 GEMM 内核" (developer.aliyun.com article 1770277).
+
+What it computes (P2 section 2, the block-wise dot then scale; P1 section 2.1, x ≈ s·(q − z);
+P1 section 8 rule 2, compare against the dequantized weights, not the unquantized ones):
+
+    out[m][n] = Σ_g s[g][n] · Σ_{k ∈ group g} A[m][k] · (q[k][n] − z[g][n])
+
+with activation scale 1 (float activations).  The per-group integer-weighted dot is
+finished before the scale is applied, exactly as the formula states.  All arithmetic is
+float64; products of a bf16/fp32 activation and a small integer are exact in float64 and
+sums of at most a few thousand such terms lose at most a few ulps of float64, far below
+every tolerance used against the GPU.
+"""
+from __future__ import annotations
+
+import math
+import numpy as np
+
+__all__ = [
+    "fp16_bits_to_f64", "bf16_bits_to_f64", "f32_to_f64", "f64_to_bf16_bits",
+    "f64_to_f32", "unpack_int4_k", "unpack_int4_n", "dequantize", "group_gemm",
+    "group_gemm_magnitude", "reference", "tolerance", "check", "quantize_w4_g",
+    "bits_per_weight", "dequantize_brute",
+]
+
+
+# ---------------------------------------------------------------------------------------
+# IEEE-754 binary16 / bfloat16 / binary32 codecs, written from the format definitions.
+# (P1 section 2.1 lists the layouts: FP16 = 1 sign, 5 exponent, 10 mantissa bits;
+#  BF16 = the high 16 bits of an FP32: 1 sign, 8 exponent, 7 mantissa bits.)
+# ---------------------------------------------------------------------------------------
+
+def _decode_ieee(bits: np.ndarray, exp_bits: int, man_bits: int) -> np.ndarray:
+    b = np.asarray(bits).astype(np.int64) & ((1 << (1 + exp_bits + man_bits)) - 1)
+    sign = np.where((b >> (exp_bits + man_bits)) & 1, -1.0, 1.0)
+    e = (b >> man_bits) & ((1 << exp_bits) - 1)
+    f = (b & ((1 << man_bits) - 1)).astype(np.float64)
+    bias = (1 << (exp_bits - 1)) - 1
+    emax = (1 << exp_bits) - 1
+    frac = f / float(1 << man_bits)
+    normal = np.ldexp(1.0 + frac, (e - bias).astype(np.int64))
+    subnormal = np.ldexp(frac, 1 - bias)
+    val = np.where(e == 0, subnormal, normal)
+    val = np.where(e == emax, np.where(f == 0, np.inf, np.nan), val)
+    return sign * val
+
+
+def fp16_bits_to_f64(bits) -> np.ndarray:
+    """binary16 bit patterns -> float64 (exact), including subnormals, inf and NaN."""
+    return _decode_ieee(bits, 5, 10)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bfloat16 bit patterns -> float64 (exact)."""
+    return _decode_ieee(bits, 8, 7)
+
+
+def f32_to_f64(x) -> np.ndarray:
+    """binary32 values -> float64 (exact widening)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """float64 -> bfloat16 bits, round to nearest even (P1 section 2.3: FP32 -> BF16 is
+    RNE), computed directly from float64 (no intermediate fp32 rounding).  Finite inputs
+    beyond the bf16 range round to inf like the hardware conversion."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    sign = (np.signbit(x)).astype(np.uint16) << 15
+    ax = np.abs(x)
+    nan = np.isnan(x)
+    with np.errstate(all="ignore"):
+        m, e = np.frexp(ax)          # ax = m * 2^e, m in [0.5, 1)
+        # a normal bf16 has 8 significant bits: value = integer(2^7..2^8-1) * 2^(E-7)
+        # exponent of the leading bit: E = e - 1; subnormals fix E at -126
+        E = np.maximum(e - 1, -126)
+        scaled = np.ldexp(ax, (7 - E).astype(np.int64))   # integer part holds the significand
+        r = np.rint(scaled)                                # round half to even
+        # renormalize when rounding carried into a new binade
+        carry = r >= 256
+        r = np.where(carry, r / 2, r)
+        E = np.where(carry, E + 1, E)
+        is_sub = r < 128
+        expfield = np.where(is_sub, 0, E + 127).astype(np.int64)
+        manfield = np.where(is_sub, r, r - 128).astype(np.int64)
+        bits = (expfield << 7) | manfield
+        bits = np.where(ax == 0, 0, bits)
+        bits = np.where((expfield >= 255) | np.isinf(ax), 0x7F80, bits)
+    out = (bits.astype(np.uint16) | sign)
+    out = np.where(nan, np.uint16(0x7FC0), out).astype(np.uint16)
+    return out
+
+
+def f64_to_f32(x) -> np.ndarray:
+    """float64 -> float32 with round to nearest even (numpy's conversion)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32)
+
+
+# ---------------------------------------------------------------------------------------
+# Canonical INT4 layouts (P1 section 2.4: eight INT4 values per uint32, element j at
+# bits 4j..4j+3; P1 section 3.1: scales [K/g, N], zero points INT4-packed [K/g, N/8];
+# P1 section 9.4 packs eight consecutive k into one word).
+# ---------------------------------------------------------------------------------------
+
+def unpack_int4_k(words: np.ndarray) -> np.ndarray:
+    """uint32 [K/8][N] -> codes int64 [K][N]; k = 8r + j is read from bits 4j..4j+3."""
+    w = np.asarray(words, dtype=np.uint32)
+    R, N = w.shape
+    q = np.empty((R, 8, N), dtype=np.int64)
+    for j in range(8):
+        q[:, j, :] = (w >> np.uint32(4 * j)) & np.uint32(0xF)
+    return q.reshape(R * 8, N)
+
+
+def unpack_int4_n(words: np.ndarray) -> np.ndarray:
+    """uint32 [R][N/8] -> codes int64 [R][N]; n = 8c + j is read from bits 4j..4j+3."""
+    w = np.asarray(words, dtype=np.uint32)
+    R, C = w.shape
+    z = np.empty((R, C, 8), dtype=np.int64)
+    for j in range(8):
+        z[:, :, j] = (w >> np.uint32(4 * j)) & np.uint32(0xF)
+    return z.reshape(R, C * 8)
+
+
+# ---------------------------------------------------------------------------------------
+# The method.
+# ---------------------------------------------------------------------------------------
+
+def dequantize(q: np.ndarray, z: np.ndarray, s: np.ndarray, G: int) -> np.ndarray:
+    """W_hat[k][n] = s[g][n] * (q[k][n] - z[g][n]), g = k // G   (P1 section 2.1, the
+    affine relation x ≈ s·(q − z); P1 section 9.4 builds W_hat = s·(q − 8) as the
+    reference weights)."""
+    K, N = q.shape
+    qz = q.astype(np.float64).reshape(K // G, G, N) - np.asarray(z, np.float64)[:, None, :]
+    return (qz * np.asarray(s, np.float64)[:, None, :]).reshape(K, N)
+
+
+def group_gemm(A: np.ndarray, q: np.ndarray, z: np.ndarray, s: np.ndarray, G: int) -> np.ndarray:
+    """out[m][n] = Σ_g s[g][n] · Σ_{k∈g} A[m][k]·(q[k][n] − z[g][n])   (P2 section 2: the
+    integer-weighted dot of a whole group finishes before its scale multiplies it).
+
+    A [M][K] float64, q [K][N] integer codes, z [K/G][N] integer zero points,
+    s [K/G][N] float64 scales.  The inner dot is a library matmul over one group.
+    """
+    A = np.asarray(A, np.float64)
+    M, K = A.shape
+    N = q.shape[1]
+    assert K % G == 0 and q.shape[0] == K
+    out = np.zeros((M, N), dtype=np.float64)
+    for g in range(K // G):
+        ks = slice(g * G, (g + 1) * G)
+        d = q[ks, :].astype(np.float64) - np.asarray(z[g], np.float64)[None, :]
+        partial = A[:, ks] @ d
+        out += np.asarray(s[g], np.float64)[None, :] * partial
+    return out
+
+
+def group_gemm_magnitude(A, q, z, s, G) -> np.ndarray:
+    """mag[m][n] = Σ_k |A[m][k] · w[k][n]| with w = s·(q − z): the conditioning term of
+    the tolerance (the size of the terms the sum cancels)."""
+    A = np.abs(np.asarray(A, np.float64))
+    M, K = A.shape
+    N = q.shape[1]
+    out = np.zeros((M, N), dtype=np.float64)
+    for g in range(K // G):
+        ks = slice(g * G, (g + 1) * G)
+        d = np.abs(q[ks, :].astype(np.float64) - np.asarray(z[g], np.float64)[None, :])
+        out += np.abs(np.asarray(s[g], np.float64))[None, :] * (A[:, ks] @ d)
+    return out
+
+
+def reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, w4: bool,
+              act: str, sc: str, rows=None, cols=None):
+    """Decode canonical inputs with this module's own codecs and return (ref, mag), both
+    float64 [len(rows)][len(cols)].
+
+    A_raw:  [M][K] bf16 bits (uint16) if act == "bf16", else float32.
+    codes:  W4: uint32 [K/8][N]; W8: int8 [K][N] (zero point 0).
+    scales: [K/G][N] fp16 / bf16 bits (uint16) or float32, per ``sc``.
+    zeros:  W4 only: uint32 [K/G][N/8] or None (then z = 8, the symmetric point of the
+            INT4 teaching kernel, P1 section 9.4).
+    """
+    A_raw = np.asarray(A_raw)
+    if rows is not None:
+        A_raw = A_raw[np.asarray(rows)]
+    A = bf16_bits_to_f64(A_raw) if act == "bf16" else f32_to_f64(A_raw)
+    ng = K // G
+    cols_ = np.arange(N) if cols is None else np.asarray(cols)
+    if w4:
+        q = unpack_int4_k(np.asarray(codes)[:, cols_])
+        if zeros is None:
+            z = np.full((ng, len(cols_)), 8, dtype=np.int64)
+        else:
+            z = unpack_int4_n(np.asarray(zeros))[:, cols_]
+    else:
+        q = np.asarray(codes)[:, cols_].astype(np.int64)
+        z = np.zeros((ng, len(cols_)), dtype=np.int64)
+    sraw = np.asarray(scales)[:, cols_]
+    if sc == "fp16":
+        s = fp16_bits_to_f64(sraw)
+    elif sc == "bf16":
+        s = bf16_bits_to_f64(sraw)
+    else:
+        s = f32_to_f64(sraw)
+    return group_gemm(A, q, z, s, G), group_gemm_magnitude(A, q, z, s, G)
+
+
+# ---------------------------------------------------------------------------------------
+# Tolerance.  P1 section 8: error of a K-term FP32 accumulation grows like ε·sqrt(K) times
+# the typical product and relative error blows up where the output cancels; so the bound
+# has a relative term (the final rounding of the output) and a conditioning term.
+# ---------------------------------------------------------------------------------------
+
+def tolerance(ref: np.ndarray, mag: np.ndarray, out_dtype: str) -> np.ndarray:
+    """bf16 out: 2^-8·|ref| + 1e-4·mag.  fp32 out: 1e-5·|ref| + 1e-6·mag."""
+    if out_dtype == "bf16":
+        return 2.0 ** -8 * np.abs(ref) + 1e-4 * mag
+    return 1e-5 * np.abs(ref) + 1e-6 * mag
+
+
+def check(out_f64: np.ndarray, ref: np.ndarray, mag: np.ndarray, out_dtype: str):
+    """Return (n_bad, worst err/tol) of a decoded GPU output against the oracle."""
+    tol = tolerance(ref, mag, out_dtype)
+    err = np.abs(np.asarray(out_f64, np.float64) - ref)
+    bad = ~(err <= tol)
+    ratio = float(np.max(err / np.maximum(tol, 1e-300))) if err.size else 0.0
+    return int(bad.sum()), ratio
+
+
+# ---------------------------------------------------------------------------------------
+# The reference quantizer of P1 section 9.4 (symmetric, per-group amax / 7, zero point 8),
+# kept to generate quantized weights from real ones in the checks.
+# ---------------------------------------------------------------------------------------
+
+def quantize_w4_g(W: np.ndarray, G: int = 128):
+    """W [N][K] real -> (q uint8 [N][K] in [0,15], s float64 [N][K/G], W_hat float64 [N][K]).
+
+    s = max(amax(|W_group|) / 7, 1e-8); q = clamp(round(W / s) + 8, 0, 15);
+    W_hat = (q − 8)·s.  round() is round-half-to-even (numpy rint).
+    """
+    N, K = W.shape
+    assert K % G == 0
+    Wg = np.asarray(W, np.float64).reshape(N, K // G, G)
+    s = np.maximum(np.abs(Wg).max(axis=-1, keepdims=True) / 7.0, 1e-8)
+    q = np.clip(np.rint(Wg / s) + 8, 0, 15)
+    W_hat = ((q - 8.0) * s).reshape(N, K)
+    return q.astype(np.uint8).reshape(N, K), s.reshape(N, K // G), W_hat
+
+
+def bits_per_weight(code_bits: int, G: int, scale_bits: int, zero_point_bits: int = 0) -> float:
+    """Storage cost per weight: the code, plus one scale and (optionally) one packed zero
+    point shared by each group of G weights (P1 section 3.1: a g128 fp16 scale adds 0.125
+    bit, an INT4 zero point about 0.03 bit)."""
+    return code_bits + (scale_bits + zero_point_bits) / G
+
+
+def dequantize_brute(q_raw, z_raw, s_vals, G: int, K: int, N: int):
+    """Element-by-element dequantization with Python loops (tiny shapes only): the
+    brute-force side of the oracle's self-check.  q_raw [K][N] ints, z_raw [K/G][N] ints
+    (or a scalar), s_vals [K/G][N] floats."""
+    W = [[0.0] * N for _ in range(K)]
+    for k in range(K):
+        g = k // G
+        for n in range(N):
+            zz = z_raw if np.isscalar(z_raw) else int(z_raw[g][n])
+            W[k][n] = float(s_vals[g][n]) * (int(q_raw[k][n]) - zz)
+    return W

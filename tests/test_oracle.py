@@ -1,0 +1,353 @@
+"""Pins of the float64 oracle against things other than itself (CPU only).
+
+Each test names what fixes the expected value: a value the pages print (tests/golden),
+a closed form, a library routine in a special case, or brute force on tiny inputs.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import gq_synth
+import oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------------------ IEEE codecs
+
+def test_fp16_decoder_matches_library_on_all_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ours = orc.fp16_bits_to_f64(bits)
+    lib = bits.view(np.float16).astype(np.float64)
+    same = (ours == lib) | (np.isnan(ours) & np.isnan(lib))
+    assert same.all()
+
+
+def test_bf16_decoder_matches_library_on_all_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    lib = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    ours = orc.bf16_bits_to_f64(bits)
+    same = (ours == lib) | (np.isnan(ours) & np.isnan(lib))
+    assert same.all()
+
+
+def test_bf16_encoder_matches_library_rne():
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-40, 38, 20000),
+        # exact ties between neighbouring bf16 values: round half to even
+        orc.bf16_bits_to_f64(np.arange(0x3F80, 0x3FA0)) + 2.0 ** -8,
+        orc.bf16_bits_to_f64(np.arange(0x0001, 0x0040)) * 1.5,   # subnormal ties
+        np.array([0.0, -0.0, 3.3895313892515355e38, 3.4e38, -1e-45, 1e-39]),
+    ]).astype(np.float32).astype(np.float64)   # exactly representable in fp32
+    lib = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+    lib = lib.numpy().view(np.uint16)
+    assert np.array_equal(orc.f64_to_bf16_bits(x), lib)
+
+
+def test_bf16_encoder_roundtrip_all_finite_patterns():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = orc.bf16_bits_to_f64(bits)
+    fin = np.isfinite(vals)
+    back = orc.f64_to_bf16_bits(vals[fin])
+    # -0.0 and +0.0 both survive with their sign
+    assert np.array_equal(back, bits[fin])
+
+
+# ------------------------------------------------------------------ magic numbers
+
+def test_magic_constants_printed_on_the_page():
+    for fmt, bits, value in _golden("magic_constants.txt"):
+        b = np.array([int(bits, 16)], dtype=np.uint16)
+        dec = orc.fp16_bits_to_f64(b) if fmt == "fp16" else orc.bf16_bits_to_f64(b)
+        assert dec[0] == float(value), (fmt, bits)
+
+
+def test_magic_identities_exhaustive():
+    """All 16 INT4 codes: the decode forms the CUDA path relies on reach q - 8 exactly."""
+    f16 = lambda b: float(orc.fp16_bits_to_f64(np.array([b], dtype=np.uint16))[0])
+    b16 = lambda b: float(orc.bf16_bits_to_f64(np.array([b], dtype=np.uint16))[0])
+    f32 = lambda b: float(np.array([b], dtype=np.uint32).view(np.float32)[0])
+    for q in range(16):
+        assert f16(0x6400 | q) - f16(0x6408) == q - 8                      # lo nibble, FP16
+        assert f16(0x6400 | (q << 4)) * f16(0x2C00) + f16(0xD480) == q - 8  # hi nibble, FP16
+        assert b16(0x4300 | q) - 136.0 == q - 8                            # lo nibble, BF16
+        assert f32(0x4B000000 | q) - (2.0 ** 23 + 8) == q - 8              # FP32 2^23 form
+        for zp in range(16):                                               # asymmetric point
+            assert b16(0x4300 | q) - b16(0x4300 | zp) == q - zp
+    # the hi-nibble form does not carry over to BF16: bit 7 of the half-word is the
+    # exponent's lowest bit there, so codes >= 8 change the binade (q = 8 lands on 256,
+    # which happens to give 0 = q - 8; every code above it is wrong)
+    wrong = [q for q in range(16) if b16(0x4300 | (q << 4)) / 16.0 - 16.0 != q - 8]
+    assert wrong == list(range(9, 16))
+
+
+def test_int8_magic_identity_all_codes():
+    """Signed INT8 code c -> (c xor 0x80) in the low byte of 2^23 gives 2^23 + c + 128."""
+    for c in range(-128, 128):
+        u = (c & 0xFF) ^ 0x80
+        v = float(np.array([0x4B000000 | u], dtype=np.uint32).view(np.float32)[0])
+        assert v - (2.0 ** 23 + 128) == c
+
+
+# ------------------------------------------------------------------ layouts
+
+def test_int4_word_convention():
+    w = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32)
+    assert orc.unpack_int4_k(w)[:, 0].tolist() == list(range(8))
+    assert orc.unpack_int4_k(w)[:, 1].tolist() == list(range(8, 16))
+    assert orc.unpack_int4_n(w)[0].tolist() == list(range(16))
+
+
+@pytest.mark.parametrize("name", ["tiny_gemv", "asym_m16"])
+def test_unpack_matches_generator_codes(name):
+    cfg = gq_synth.CONFIGS[name]
+    if cfg.K * cfg.N > 1 << 22:
+        cfg = cfg.replace(K=1024, N=512)
+    w = gq_synth.make_weights(cfg, seed=3)
+    assert np.array_equal(orc.unpack_int4_k(w["codes"]), w["q"].astype(np.int64))
+    if w["zeros"] is not None:
+        assert np.array_equal(orc.unpack_int4_n(w["zeros"]), w["z"].astype(np.int64))
+
+
+# ------------------------------------------------------------------ the GEMM itself
+
+def _brute(cfg, inp):
+    """Dequantize element by element, then a triple loop with exact fsum.  Reads the
+    generator's raw integer codes and decodes scales/activations with library routines,
+    so it shares no decoding step with the oracle."""
+    K, N, G = cfg.K, cfg.N, cfg.G
+    if cfg.sc == "fp16":
+        s = inp["scales"].view(np.float16).astype(np.float64)
+    elif cfg.sc == "bf16":
+        s = torch.from_numpy(inp["scales"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    else:
+        s = inp["scales"].astype(np.float64)
+    if cfg.act == "bf16":
+        A = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    else:
+        A = inp["A"].astype(np.float64)
+    z = inp["z"] if inp["z"] is not None else (8 if cfg.w4 else 0)
+    W = orc.dequantize_brute(inp["q"], z, s, G, K, N)
+    M = A.shape[0]
+    out = [[math.fsum(A[m][k] * W[k][n] for k in range(K)) for n in range(N)] for m in range(M)]
+    return np.array(out)
+
+
+SMALL = [
+    gq_synth.Config("w4_sym", M=3, K=256, N=24, G=128),
+    gq_synth.Config("w4_asym", M=2, K=256, N=16, G=32, zp=True, sc="bf16"),
+    gq_synth.Config("w8", M=2, K=96, N=8, G=32, w4=False, act="f32", sc="f32", out="f32",
+                    s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("w4_g128_single_group", M=4, K=128, N=40, G=128, outlier_frac=0.02),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_oracle_matches_brute_force(cfg):
+    inp = gq_synth.make_inputs(cfg, seed=11)
+    ref, mag = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                             N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc)
+    brute = _brute(cfg, inp)
+    assert np.allclose(ref, brute, rtol=1e-12, atol=1e-12 * float(np.max(mag)))
+    assert (mag >= np.abs(ref) * (1 - 1e-12)).all()
+
+
+def test_oracle_subset_rows_cols_match_full():
+    cfg = gq_synth.Config("sub", M=5, K=256, N=64, G=128, zp=True, sc="bf16")
+    inp = gq_synth.make_inputs(cfg, seed=2)
+    kw = dict(K=cfg.K, N=cfg.N, G=cfg.G, w4=True, act="bf16", sc="bf16")
+    full, _ = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], **kw)
+    rows, cols = [4, 0, 2], [63, 1, 8, 9, 40]
+    part, _ = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], rows=rows,
+                            cols=cols, **kw)
+    assert np.array_equal(part, full[np.ix_(rows, cols)])
+
+
+def test_identity_weights_return_activations():
+    """K = N, s = 1, z = 8, q = 9 on the diagonal and 8 elsewhere: W_hat = I, out = A."""
+    K = N = 256
+    q = np.full((K, N), 8, dtype=np.uint8)
+    np.fill_diagonal(q, 9)
+    codes = gq_synth.pack_int4_along_k(q)
+    scales = np.full((K // 128, N), 0x3C00, dtype=np.uint16)       # fp16 1.0
+    A = gq_synth.make_activations(gq_synth.Config("id", M=3, K=K, N=N, G=128), seed=1)
+    ref, _ = orc.reference(A, codes, scales, None, K=K, N=N, G=128, w4=True, act="bf16",
+                           sc="fp16")
+    assert np.array_equal(ref, orc.bf16_bits_to_f64(A))
+
+
+def test_one_hot_weight_selects_one_activation_column():
+    K, N, G = 256, 16, 128
+    q = np.full((K, N), 8, dtype=np.uint8)
+    k0, n0, code = 200, 5, 3
+    q[k0, n0] = code
+    s = np.full((K // G, N), 0.5, dtype=np.float32)
+    codes = gq_synth.pack_int4_along_k(q)
+    scales = gq_synth.f32_to_fp16_bits(s)
+    A = gq_synth.make_activations(gq_synth.Config("oh", M=4, K=K, N=N, G=G), seed=9)
+    ref, _ = orc.reference(A, codes, scales, None, K=K, N=N, G=G, w4=True, act="bf16",
+                           sc="fp16")
+    expect = np.zeros((4, N))
+    expect[:, n0] = 0.5 * (code - 8) * orc.bf16_bits_to_f64(A[:, k0])
+    assert np.array_equal(ref, expect)
+
+
+def test_doubling_scales_doubles_output_exactly():
+    cfg = gq_synth.Config("lin", M=2, K=512, N=32, G=128, zp=True, sc="fp16")
+    inp = gq_synth.make_inputs(cfg, seed=4)
+    kw = dict(K=cfg.K, N=cfg.N, G=cfg.G, w4=True, act="bf16", sc="fp16")
+    r1, _ = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], **kw)
+    s2 = gq_synth.f32_to_fp16_bits(orc.fp16_bits_to_f64(inp["scales"]) * 2)
+    r2, _ = orc.reference(inp["A"], inp["codes"], s2, inp["zeros"], **kw)
+    assert np.array_equal(r2, 2 * r1)
+
+
+def test_integer_case_is_exact():
+    """Integer activations and power-of-two scales: every partial sum is an exact
+    rational; the oracle must equal the exact Fraction sum."""
+    cfg = gq_synth.Config("exact", M=2, K=256, N=8, G=128, zp=True, sc="fp16", a_kind="int",
+                          pow2_scales=True)
+    inp = gq_synth.make_inputs(cfg, seed=6)
+    ref, _ = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                           N=cfg.N, G=cfg.G, w4=True, act="bf16", sc="fp16")
+    A = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    s = inp["scales"].view(np.float16).astype(np.float64)
+    for m in range(cfg.M):
+        for n in range(cfg.N):
+            tot = Fraction(0)
+            for k in range(cfg.K):
+                g = k // cfg.G
+                tot += Fraction(A[m, k]) * Fraction(s[g, n]) * (int(inp["q"][k, n]) - int(inp["z"][g, n]))
+            assert Fraction(ref[m, n]) == tot
+
+
+# ------------------------------------------------------------------ planted mistakes
+
+def _mutant_gemm_no_zero_point(A, q, z, s, G):
+    return orc.group_gemm(A, q, np.zeros_like(z), s, G)
+
+
+def _mutant_gemm_wrong_group_index(A, q, z, s, G):
+    K = q.shape[0]
+    ng = K // G
+    out = np.zeros((A.shape[0], q.shape[1]))
+    for k in range(K):
+        g = k % ng                       # wrong: interleaved instead of contiguous groups
+        out += np.outer(A[:, k], s[g] * (q[k] - z[g]))
+    return out
+
+
+def _mutant_gemm_scale_after_sum(A, q, z, s, G):
+    return (A @ (q.astype(np.float64) - np.repeat(z, G, axis=0))) * s.mean(axis=0)
+
+
+@pytest.mark.parametrize("mutant", [_mutant_gemm_no_zero_point, _mutant_gemm_wrong_group_index,
+                                    _mutant_gemm_scale_after_sum])
+def test_brute_force_pin_catches_planted_mistakes(mutant, monkeypatch):
+    cfg = SMALL[1]   # asymmetric, several groups, non-square
+    inp = gq_synth.make_inputs(cfg, seed=11)
+    brute = _brute(cfg, inp)
+    monkeypatch.setattr(orc.gq_oracle, "group_gemm", mutant)
+    ref, _ = orc.gq_oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"],
+                                     K=cfg.K, N=cfg.N, G=cfg.G, w4=True, act=cfg.act, sc=cfg.sc)
+    assert not np.allclose(ref, brute, rtol=1e-6, atol=1e-9)
+
+
+def test_identity_pin_catches_reversed_nibble_order(monkeypatch):
+    real = orc.gq_oracle.unpack_int4_k
+
+    def reversed_nibbles(words):
+        q = real(words)
+        R = q.shape[0] // 8
+        return q.reshape(R, 8, -1)[:, ::-1, :].reshape(R * 8, -1)
+
+    monkeypatch.setattr(orc.gq_oracle, "unpack_int4_k", reversed_nibbles)
+    K = N = 128
+    q = np.full((K, N), 8, dtype=np.uint8)
+    np.fill_diagonal(q, 9)
+    A = gq_synth.make_activations(gq_synth.Config("id", M=2, K=K, N=N, G=128), seed=1)
+    ref, _ = orc.gq_oracle.reference(A, gq_synth.pack_int4_along_k(q),
+                                     np.full((1, N), 0x3C00, dtype=np.uint16), None, K=K, N=N,
+                                     G=128, w4=True, act="bf16", sc="fp16")
+    assert not np.array_equal(ref, orc.bf16_bits_to_f64(A))
+
+
+# ------------------------------------------------------------------ quantizer and costs
+
+def test_reference_quantizer_error_bound():
+    """P1 section 9.4's quantizer: |W - W_hat| <= s/2 everywhere (W/s stays in [-7, 7], so
+    the clamp never fires), and the largest element of each group is reproduced exactly
+    up to its sign (q - 8 = ±7)."""
+    W = gq_synth.real_weights(16, 512, seed=1)
+    q, s, W_hat = orc.quantize_w4_g(W, G=128)
+    err = np.abs(W.astype(np.float64) - W_hat)
+    s_full = np.repeat(s, 128, axis=1)
+    assert (err <= s_full / 2 * (1 + 1e-12)).all()
+    assert q.min() >= 1 and q.max() <= 15
+    Wg = W.astype(np.float64).reshape(16, 4, 128)
+    idx = np.abs(Wg).argmax(-1)
+    qg = q.reshape(16, 4, 128).astype(int)
+    picked = np.take_along_axis(qg, idx[..., None], -1)[..., 0]
+    assert set(np.unique(picked)) <= {1, 15}
+
+
+def test_format_costs_printed_on_the_page():
+    g = {r[0]: (float(r[1]), float(r[2])) for r in _golden("format_costs.txt")}
+    bpw = orc.bits_per_weight(4, 128, 16, 4)
+    checks = {
+        "scale_bits_g128": orc.bits_per_weight(0, 128, 16),
+        "zero_point_bits_g128": orc.bits_per_weight(0, 128, 0, 4),
+        "w4_g128_bits_per_weight": bpw,
+        "w4_g128_fraction_of_bf16": bpw / 16,
+        "decode_speedup_bound": 16 / bpw,
+        "int8_dot_bound_k4096": 127 * 127 * 4096,
+    }
+    for k, v in checks.items():
+        val, tol = g[k]
+        assert abs(v - val) <= tol, (k, v, val)
+    assert 127 * 127 * 4096 < 2 ** 31
+    assert orc.bits_per_weight(4, 128, 16) == 4.125
+    assert orc.bits_per_weight(8, 32, 32) == 9.0
+
+
+def test_layer_byte_counts_printed_on_the_page():
+    g = {r[0]: (float(r[1]), float(r[2])) for r in _golden("byte_counts.txt")}
+    d, dff, kv = 4096, 14336, 8 * 128
+    shapes = [(d, d + 2 * kv), (d, d), (d, 2 * dff), (dff, d)]      # (K, N) of qkv, o, gate_up, down
+    params = sum(K * N for K, N in shapes)
+    w4 = orc.bits_per_weight(4, 128, 16, 4)
+    vals = {
+        "gemv4096_int4_weight_bytes": 4096 * 4096 * 4 / 8,
+        "gemv4096_int4_scale_bytes": 4096 * 4096 * orc.bits_per_weight(0, 128, 16) / 8,
+        "gemv4096_bf16_weight_bytes": 4096 * 4096 * 2,
+        "layer_bf16_bytes": params * 2,
+        "layer_int4_g128_bytes": params * w4 / 8,
+        "prefill4096_int4_saving_bytes": 4096 * 4096 * (2 - 0.5),
+    }
+    for k, v in vals.items():
+        val, tol = g[k]
+        assert abs(v - val) <= tol, (k, v, val)
+
+
+def test_tolerance_formula():
+    ref = np.array([1.0, -2.0, 0.0])
+    mag = np.array([10.0, 10.0, 10.0])
+    assert np.allclose(orc.tolerance(ref, mag, "bf16"), [2 ** -8 + 1e-3, 2 ** -7 + 1e-3, 1e-3])
+    assert np.allclose(orc.tolerance(ref, mag, "f32"), [1e-5 + 1e-5, 2e-5 + 1e-5, 1e-5])
+    bad, ratio = orc.check(ref + np.array([0.0, 0.0, 2e-3]), ref, mag, "bf16")
+    assert bad == 1 and ratio == pytest.approx(2.0)
