@@ -1,0 +1,390 @@
+#!/usr/bin/env python3
+"""Benchmark of the group-quantized weight-only GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (the metric's M=1 point): the fused gate+up INT4 GEMV of an 8B-class decoder,
+M=1, K=4096, N=28672, G=128, symmetric INT4 codes (zero point 8), fp16 scales, bf16
+activations with 0.1% x50 outliers, bf16 output; synthetic seeded inputs (gq_synth).
+
+One step = one decode token through CALLS_PER_STEP gate+up projections, each call reading
+a different resident weight copy (COPIES copies rotated, 485 MB in total, well above the
+129 MB L2, so every call streams its weights from HBM).  A step is captured once into a
+CUDA graph and replayed; K replays are timed with CUDA events on the launching stream,
+bracketed by a barrier and device synchronization.
+
+Also reported: the roofline of the dominant kernel against the measured HBM copy
+bandwidth, an end-to-end figure through the public C ABI with host buffers (activations
+copied in, output copied out every call), the M=4096 prefill throughput against the
+measured dense BF16 peak, and the float64 CPU oracle timed on a bounded sample.
+
+With --gpus N > 1 (one process per GPU under torchrun) every rank runs an independent
+replica of the same workload (the path does not need to exchange data between GPUs);
+value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gq_synth  # noqa: E402
+
+METRIC = "W4A16 g128 GEMM: HBM GB/s at M=1, TFLOPS at M=4096, % of roofline"
+WORKLOAD = "decode_gateup"
+CALLS_PER_STEP = 100
+COPIES = 8
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def _kernel_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (the summary records the source's sha256); else None."""
+    sp = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "group_quantized_weight_gb300", "csrc", kernel_file)
+    if not (os.path.exists(sp) and os.path.exists(src)):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    txt = open(sp, encoding="utf-8").read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    m_tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not (m_sha and m_tr) or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_oracle_timing(cfg, n_cols: int, budget_s: float):
+    """Time the float64 oracle, as it stands, on the first n_cols columns of the
+    workload (a bounded sample), in a fresh process using every host core for BLAS."""
+    code = f"""
+import sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np, gq_synth, oracle
+cfg = gq_synth.CONFIGS[{cfg.name!r}]
+inp = gq_synth.make_inputs(cfg, seed=0)
+cols = np.arange({n_cols})
+t0 = time.perf_counter(); n = 0
+while True:
+    ref, mag = oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                                N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc, cols=cols)
+    n += 1
+    if time.perf_counter() - t0 > {budget_s}:
+        break
+print(json.dumps({{"calls": n, "seconds": time.perf_counter() - t0}}))
+"""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores))
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if res.returncode != 0:
+        return None, cores, res.stderr[-500:]
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return d, cores, None
+
+
+def _sample_bytes(cfg, n_cols):
+    from group_quantized_weight_gb300.constants import algorithmic_bytes
+    return algorithmic_bytes(cfg.M, cfg.K, n_cols, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+
+
+def run_reference(args):
+    """The reference arm: the float64 CPU oracle on a bounded column sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg = gq_synth.CONFIGS[WORKLOAD]
+    n_cols = 512
+    budget = 0.0   # one call per step
+    import oracle
+    inp = gq_synth.make_inputs(cfg, seed=0)
+    cols = np.arange(n_cols)
+
+    def step():
+        oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K, N=cfg.N,
+                         G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc, cols=cols)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    del budget
+    nbytes = _sample_bytes(cfg, n_cols)
+    value = nbytes * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} M=1 K=4096 N=28672 G=128, first {n_cols} columns "
+                               "per step (float64 CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"one step = the oracle on the first {n_cols} of 28672 columns"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+
+    import group_quantized_weight_gb300 as gq
+    from group_quantized_weight_gb300.constants import algorithmic_bytes, gemm_flops, prec_flags
+
+    cfg = gq_synth.CONFIGS[WORKLOAD]
+    prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    inp = gq_synth.make_inputs(cfg, seed=0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        v = a.view(np.int16) if a.dtype == np.uint16 else (a.view(np.int32) if a.dtype == np.uint32 else a)
+        return torch.from_numpy(v).to(dev)
+
+    codes = to_dev(inp["codes"])
+    packed0 = gq.pack_weights_t(codes, cfg.K, cfg.N, cfg.G, prec)
+    scales0 = to_dev(inp["scales"])
+    W = [packed0] + [packed0.clone() for _ in range(COPIES - 1)]
+    S = [scales0] + [scales0.clone() for _ in range(COPIES - 1)]
+    del codes
+    A = to_dev(inp["A"])
+    out = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(i, a=A, o=out):
+        st = gq.gq_gemm(cfg.M, cfg.K, cfg.N, cfg.G, prec, a.data_ptr(), W[i % COPIES].data_ptr(),
+                        S[i % COPIES].data_ptr(), None, o.data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"gq_gemm failed: {gq.gq_status_string(st)}")
+
+    call(0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(CALLS_PER_STEP):
+            call(i)
+    torch.cuda.synchronize()
+
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_id.startswith("GPU-"):
+            gpu_id = "GPU-" + gpu_id
+    except Exception:
+        gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    launches = args.steps * CALLS_PER_STEP
+    kernel_us = 1e3 * ms / launches
+    value = world * nbytes * launches / (ms * 1e-3) / 1e9
+    peaks, peak_kind = _peaks()
+    achieved = nbytes / (kernel_us * 1e-6) / 1e9
+
+    # end to end through the C ABI with host buffers: pinned A in, pinned out back, per call
+    e2e_calls = 2000
+    A_h = torch.from_numpy(np.ascontiguousarray(inp["A"]).view(np.int16)).pin_memory()
+    out_h = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16).pin_memory()
+    A_d = torch.empty_like(A)
+    for i in range(20):
+        A_d.copy_(A_h, non_blocking=True)
+        call(i, A_d)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_calls):
+        A_d.copy_(A_h, non_blocking=True)
+        call(i, A_d)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": world * nbytes * e2e_calls / e2e_s / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": A_h.numel() * 2 * CALLS_PER_STEP,
+           "d2h_bytes_per_step": out_h.numel() * 2 * CALLS_PER_STEP,
+           "note": "per call: H2D of the activations, gq_gemm, D2H of the output, "
+                   "from pinned host memory, host-launched (no graph)"}
+
+    prefill = None
+    if not args.no_prefill and rank == 0:
+        prefill = _prefill(gq, torch, dev, peaks, peak_kind)
+
+    traffic = _kernel_traffic("gq_decode.cu", "w4_mma_decode_decode_gateup.md")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: M=1 K=4096 N=28672 G=128 W4A16 sym, fp16 scales, "
+                               "bf16 act/out",
+                   "step": f"{CALLS_PER_STEP} gq_gemm calls replayed from one CUDA graph",
+                   "l2": f"inputs larger than L2: {COPIES} rotated weight copies "
+                         f"({COPIES * nbytes / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "w4_mma_decode_kernel", "peak_source": f"hbm_gbs of {peak_kind}",
+                     "kernel_us": kernel_us},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if prefill:
+        line["prefill"] = prefill
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        d, cores, err = _cpu_oracle_timing(cfg, 4096, 10.0)
+        if d:
+            per_call = d["seconds"] / d["calls"]
+            line["cpu_baseline"] = {
+                "value": _sample_bytes(cfg, 4096) / per_call / 1e9, "unit": "GB/s",
+                "cores": cores, "kind": "oracle",
+                "sample": f"float64 oracle on the first 4096 of 28672 columns, "
+                          f"{d['calls']} calls in {d['seconds']:.1f} s"}
+        else:
+            line["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": cores,
+                                    "kind": "oracle", "sample": f"failed: {err}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _prefill(gq, torch, dev, peaks, peak_kind):
+    """M=4096 K=4096 N=14336 prefill: TFLOPS of gq_gemm vs the measured dense BF16 peak."""
+    from group_quantized_weight_gb300.constants import gemm_flops, prec_flags
+    cfg = gq_synth.CONFIGS["prefill"]
+    prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    w = gq_synth.make_weights(cfg, seed=0)
+    a = gq_synth.make_activations(cfg, seed=0)
+    codes = torch.from_numpy(w["codes"].view(np.int32)).to(dev)
+    packed = gq.pack_weights_t(codes, cfg.K, cfg.N, cfg.G, prec)
+    S = torch.from_numpy(w["scales"].view(np.int16)).to(dev)
+    A = torch.from_numpy(a.view(np.int16)).to(dev)
+    out = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
+    res = gq.gq_bench(cfg.M, cfg.K, cfg.N, cfg.G, prec, A.data_ptr(), [packed.data_ptr()],
+                      [S.data_ptr()], None, out.data_ptr(), warmup=3, iters=10,
+                      use_graph=False, stream=torch.cuda.current_stream().cuda_stream)
+    us = res["us_per_call"]
+    tflops = gemm_flops(cfg.M, cfg.K, cfg.N) / (us * 1e-6) / 1e12
+    plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    return {"workload": "prefill: M=4096 K=4096 N=14336 G=128 W4A16 sym", "us": us,
+            "tflops": tflops, "peak_tflops": peaks["bf16_tflops"],
+            "frac": tflops / peaks["bf16_tflops"], "peak_source": f"bf16_tflops of {peak_kind}",
+            "path": plan["path"]}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,153 @@
+"""Python binding of libgq, the GB300 group-quantized weight-only GEMM.
+
+Argument marshalling only: every function forwards to the C ABI of ``include/gq.h`` with
+the same name; all computation happens in the library's CUDA kernels.  The library must
+have been built (``group_quantized_weight_gb300.build.build()``); importing this module
+without it raises ImportError — there is no fallback.
+
+Tensors are passed as raw device pointers; the ``*_t`` helpers accept torch tensors and
+pass ``tensor.data_ptr()`` and torch's current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .constants import (GQ_W4, GQ_ZP, GQ_ACT_F32, GQ_SC_BF16, GQ_SC_F32, GQ_OUT_F32,  # noqa: F401
+                        GQ_OK, STATUS_NAMES, GqError, algorithmic_bytes, gemm_flops, prec_flags)
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgq.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libgq.so is not built ({_LIB_PATH}); run "
+                      "group_quantized_weight_gb300.build.build() first")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+LIB_PATH = _LIB_PATH
+
+_i, _p, _sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+
+
+class gq_plan_t(ctypes.Structure):
+    _fields_ = [("path", _i), ("nsplit", _i), ("m_tile", _i), ("n_tile", _i),
+                ("grid_x", _i), ("grid_y", _i), ("grid_z", _i), ("block_threads", _i),
+                ("smem_bytes", _sz), ("workspace_bytes", _sz)]
+
+
+class gq_bench_args(ctypes.Structure):
+    _fields_ = [("M", _i), ("K", _i), ("N", _i), ("G", _i), ("prec", _i), ("A", _p),
+                ("Wq", ctypes.POINTER(_p)), ("scales", ctypes.POINTER(_p)),
+                ("zeros", ctypes.POINTER(_p)), ("n_copies", _i), ("out", _p),
+                ("warmup", _i), ("iters", _i), ("use_graph", _i), ("stream", _p)]
+
+
+class gq_bench_result(ctypes.Structure):
+    _fields_ = [("us_per_call", ctypes.c_double), ("launches_per_call", _i)]
+
+
+_SIGS = {
+    "gq_packed_bytes": [_i, _i, _i, _i, ctypes.POINTER(_sz)],
+    "gq_pack_weights": [_i, _i, _i, _i, _p, _p, _p],
+    "gq_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
+    "gq_set_workspace": [_p, _sz],
+    "gq_gemm": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
+    "gq_bench": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
+    "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
+    "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
+    "gq_device_error": [_i],
+    "gq_status_string": [_i],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_char_p if _name == "gq_status_string" else _i
+
+EXPORTED = tuple(_SIGS)
+
+
+def _check(st: int, what: str) -> None:
+    if st != GQ_OK:
+        raise GqError(st, f"{what}: {_lib.gq_status_string(st).decode()}")
+
+
+def gq_status_string(status: int) -> str:
+    return _lib.gq_status_string(status).decode()
+
+
+def gq_packed_bytes(K: int, N: int, G: int, prec: int) -> int:
+    out = _sz()
+    _check(_lib.gq_packed_bytes(K, N, G, prec, ctypes.byref(out)), "gq_packed_bytes")
+    return out.value
+
+
+def gq_pack_weights(K, N, G, prec, codes_ptr, packed_ptr, stream=None) -> int:
+    """Raw call; returns the status."""
+    return _lib.gq_pack_weights(K, N, G, prec, codes_ptr, packed_ptr, stream)
+
+
+def gq_workspace_size(M: int, K: int, N: int, G: int, prec: int) -> int:
+    out = _sz()
+    _check(_lib.gq_workspace_size(M, K, N, G, prec, ctypes.byref(out)), "gq_workspace_size")
+    return out.value
+
+
+def gq_set_workspace(ptr, nbytes: int) -> int:
+    return _lib.gq_set_workspace(ptr, nbytes)
+
+
+def gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream=None) -> int:
+    """Raw call; returns the status."""
+    return _lib.gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream)
+
+
+def gq_plan(M: int, K: int, N: int, G: int, prec: int, sm_count: int = 0) -> dict:
+    p = gq_plan_t()
+    _check(_lib.gq_plan(M, K, N, G, prec, sm_count, ctypes.byref(p)), "gq_plan")
+    return {f: getattr(p, f) for f, _ in gq_plan_t._fields_}
+
+
+def gq_zsplit(units: int, nsplit: int, z: int):
+    b, e = _i(), _i()
+    _check(_lib.gq_zsplit(units, nsplit, z, ctypes.byref(b), ctypes.byref(e)), "gq_zsplit")
+    return b.value, e.value
+
+
+def gq_device_error(clear: bool = False) -> int:
+    return _lib.gq_device_error(1 if clear else 0)
+
+
+def gq_bench(M, K, N, G, prec, A_ptr, Wq_ptrs, scales_ptrs, zeros_ptrs, out_ptr, *, warmup=3,
+             iters=100, use_graph=True, stream=None) -> dict:
+    n = len(Wq_ptrs)
+    arr = _p * n
+    args = gq_bench_args(M, K, N, G, prec, A_ptr, arr(*Wq_ptrs), arr(*scales_ptrs),
+                         arr(*zeros_ptrs) if zeros_ptrs else None, n, out_ptr, warmup, iters,
+                         1 if use_graph else 0, stream)
+    res = gq_bench_result()
+    _check(_lib.gq_bench(ctypes.byref(args), ctypes.byref(res)), "gq_bench")
+    return {"us_per_call": res.us_per_call, "launches_per_call": res.launches_per_call}
+
+
+# ------------------------------------------------------------------ torch conveniences
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def pack_weights_t(codes, K: int, N: int, G: int, prec: int, stream=None):
+    """codes: device tensor in the canonical layout -> packed device tensor (uint8)."""
+    import torch
+    packed = torch.empty(gq_packed_bytes(K, N, G, prec), dtype=torch.uint8, device=codes.device)
+    _check(gq_pack_weights(K, N, G, prec, codes.data_ptr(), packed.data_ptr(),
+                           _stream_ptr(stream)), "gq_pack_weights")
+    return packed
+
+
+def gemm_t(A, Wq, scales, zeros, out, M: int, K: int, N: int, G: int, prec: int, stream=None):
+    """out <- gq_gemm(...) on torch's current stream; raises GqError on a bad status."""
+    _check(gq_gemm(M, K, N, G, prec, A.data_ptr(), Wq.data_ptr(), scales.data_ptr(),
+                   zeros.data_ptr() if zeros is not None else None, out.data_ptr(),
+                   _stream_ptr(stream)), "gq_gemm")
+    return out

@@ -1,0 +1,64 @@
+// Internal declarations shared by the translation units of libgq (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gq.h"
+
+namespace gq {
+
+// Packed W4 layout: 16-column tiles x 64-k chunks; a chunk is 32 lanes x 16 bytes.
+constexpr int kTileN = 16;
+constexpr int kChunkK = 64;
+// Packed W8 layout: [K/16][N][16 bytes].
+constexpr int kChunkK8 = 16;
+
+// Small-M tensor-core decode kernel: warps per CTA (each warp owns one 16-column tile).
+constexpr int kDecWarps = 8;
+constexpr int kDecMaxMT = 4;           // up to 4 x 8 = 32 rows of A per CTA
+// INT8 CUDA-core decode kernel: one column per thread.
+constexpr int kQ8Threads = 128;
+constexpr int kQ8MaxRows = 32;
+
+enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2 };
+
+struct Plan {
+  int path;
+  int nsplit;
+  int units;        // number of split units along K
+  int unit_k;       // k per unit (a whole number of groups)
+  int m_tile;       // rows per CTA
+  int mt;           // n8 MMA blocks per CTA (path 0)
+  int n_tile;       // columns per CTA
+  int grid_x, grid_y, grid_z;
+  int block_threads;
+  size_t smem_bytes;
+  size_t part_bytes;     // split-K partials
+  size_t counter_bytes;  // arrival counters
+  size_t workspace_bytes;
+};
+
+// scale / output type codes used as template parameters
+enum ScaleType { kScF16 = 0, kScBF16 = 1, kScF32 = 2 };
+
+int validate(int M, int K, int N, int G, int prec);
+int make_plan(int M, int K, int N, int G, int prec, int sm_count, Plan *p);
+size_t packed_bytes(int K, int N, int prec);
+int device_sm_count(int *sms);
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed,
+                           cudaStream_t s);
+cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed,
+                           cudaStream_t s);
+cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int prec,
+                              const void *A, const void *Wq, const void *scales,
+                              const void *zeros, void *out, float *part,
+                              unsigned *counters, cudaStream_t s);
+cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
+                             const void *A, const void *Wq, const void *scales,
+                             void *out, float *part, unsigned *counters, cudaStream_t s);
+
+}  // namespace gq

@@ -1,0 +1,83 @@
+// Offline repack of canonical weight codes into the device layouts gq_gemm streams.
+//
+// W4 ("GPU Kernel 工程（09）：量化与融合 kernel", section 3.3 item 1, and the interleaved nibble
+// order required by the magic-number decode of section 2.4):
+//   packed[t][c][lane][word j], t = 16-column tile, c = 64-k chunk, j = 16-k step in the
+//   chunk.  Word j of lane L holds the eight codes lane L needs as the A operand of one
+//   m16n8k16 tensor-core MMA whose rows are output columns n and whose columns are k:
+//     pair i (i = 0..3) = rows r = L/4 + 8*(i & 1), k = 16j + 2*(L%4) + 8*(i >> 1) + {0,1}
+//   with the first k of the pair at bits 4i..4i+3 and the second at bits 4i+16..4i+19,
+//   so that (word >> 4i) & 0x000F000F leaves the two codes in the low bits of the two
+//   16-bit halves, ready for the BF16 magic 0x4300.
+// W8: packed[c][n][b] = codes[16c + b][n] (16 consecutive k of one column per 16 bytes).
+#include "gq_internal.h"
+
+namespace gq {
+
+__global__ void pack_w4_kernel(int K, int N, const uint32_t *__restrict__ codes,
+                               uint32_t *__restrict__ packed, size_t total_words) {
+  const int nchunks = K / kChunkK;
+  for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total_words;
+       o += (size_t)gridDim.x * blockDim.x) {
+    const int j = (int)(o & 3);
+    const int lane = (int)((o >> 2) & 31);
+    const size_t tc = o >> 7;                  // tile * nchunks + chunk
+    const int c = (int)(tc % nchunks);
+    const int t = (int)(tc / nchunks);
+    uint32_t word = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = (lane >> 2) + 8 * (i & 1);
+      const int n = t * kTileN + r;
+      const int k = c * kChunkK + 16 * j + 2 * (lane & 3) + 8 * (i >> 1);   // even
+      uint32_t lo = 0, hi = 0;
+      if (n < N) {
+        const uint32_t src = codes[(size_t)(k >> 3) * N + n];  // holds k and k + 1
+        lo = (src >> (4 * (k & 7))) & 0xFu;
+        hi = (src >> (4 * ((k + 1) & 7))) & 0xFu;
+      }
+      word |= lo << (4 * i);
+      word |= hi << (4 * i + 16);
+    }
+    packed[o] = word;
+  }
+}
+
+__global__ void pack_w8_kernel(int K, int N, const int8_t *__restrict__ codes,
+                               uint8_t *__restrict__ packed, size_t total_vecs) {
+  for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total_vecs;
+       o += (size_t)gridDim.x * blockDim.x) {
+    const int n = (int)(o % N);
+    const size_t c = o / N;
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const uint32_t v = (uint8_t)codes[(c * 16 + b) * (size_t)N + n];
+      w[b >> 2] |= v << (8 * (b & 3));
+    }
+    reinterpret_cast<uint4 *>(packed)[o] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+static int grid_for(size_t work, int threads) {
+  size_t b = (work + threads - 1) / threads;
+  if (b > 65535u * 8u) b = 65535u * 8u;
+  return (int)(b ? b : 1);
+}
+
+cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed,
+                           cudaStream_t s) {
+  const size_t tiles = (size_t)(N + kTileN - 1) / kTileN;
+  const size_t total = tiles * (size_t)(K / kChunkK) * 128;
+  pack_w4_kernel<<<grid_for(total, 256), 256, 0, s>>>(K, N, codes, packed, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed,
+                           cudaStream_t s) {
+  const size_t total = (size_t)(K / kChunkK8) * N;
+  pack_w8_kernel<<<grid_for(total, 256), 256, 0, s>>>(K, N, codes, packed, total);
+  return cudaGetLastError();
+}
+
+}  // namespace gq

@@ -1,0 +1,171 @@
+/*
+ * gq.h — group-quantized weight-only GEMM on one NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * The operation (the group-wise GEMM of "04 · 分组量化 GEMM 内核", section 2, with the
+ * activation scale fixed to 1; the affine relation x ≈ s·(q − z) of "GPU Kernel 工程（09）：
+ * 量化与融合 kernel", section 2.1):
+ *
+ *     out[m][n] = Σ_g s[g][n] · Σ_{k ∈ group g} A[m][k] · (q[k][n] − z[g][n])
+ *
+ * for 0 ≤ m < M, 0 ≤ n < N, groups of G consecutive k.  Every group's dot product is
+ * finished before its scale multiplies it; accumulation is FP32.
+ *
+ * Conventions for every call below:
+ *   - Matrices are row-major and dense (no leading-dimension argument).
+ *   - "device" pointers are CUDA device memory owned by the caller; the library never
+ *     frees or retains them beyond the call (the workspace of gq_set_workspace excepted).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  gq_pack_weights and
+ *     gq_gemm only enqueue work on it and return; they never synchronize the device.
+ *   - Every call returns a gq_status.  Arguments are validated before anything is
+ *     launched: an invalid call launches nothing and leaves every buffer untouched.
+ *     Nothing is thrown across the ABI and nothing aborts the process.
+ */
+#ifndef GQ_H_
+#define GQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gq_status {
+  GQ_OK = 0,
+  GQ_ERR_INVALID_ARG = 1,  /* shape, null pointer or flag combination outside the contract */
+  GQ_ERR_UNSUPPORTED = 2,  /* legal in principle, not implemented (e.g. an unsupported G)   */
+  GQ_ERR_ALIGNMENT = 3,    /* a pointer is not 16-byte aligned                              */
+  GQ_ERR_WORKSPACE = 4,    /* the registered workspace is smaller than gq_workspace_size    */
+  GQ_ERR_CUDA = 5,         /* a CUDA runtime call or a launch failed                        */
+  GQ_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up (sticky, see gq_device_error) */
+  GQ_ERR_NO_DEVICE = 7     /* no CUDA device of compute capability 10.3 is current          */
+} gq_status;
+
+/* `prec`: a bit field describing the operand types. */
+#define GQ_W4      0x01  /* INT4 codes in [0,15]; clear = INT8 codes in [-128,127], z = 0     */
+#define GQ_ZP      0x02  /* W4 only: per-group INT4 zero points given; clear = z = 8 (W4)     */
+#define GQ_ACT_F32 0x04  /* activations fp32; clear = bf16                                     */
+#define GQ_SC_BF16 0x08  /* scales bf16                                                        */
+#define GQ_SC_F32  0x10  /* scales fp32; neither SC flag = fp16                                */
+#define GQ_OUT_F32 0x20  /* output fp32; clear = bf16 (round to nearest even)                  */
+
+/*
+ * Supported operand combinations (anything else returns GQ_ERR_UNSUPPORTED):
+ *   W4 : activations bf16; scales fp16, bf16 or fp32; zero points optional; out bf16 or fp32.
+ *   W8 : activations fp32; scales fp32; no zero points; out fp32 or bf16.
+ * Shape contract: M ≥ 0, N ≥ 0 (either 0 is a valid empty call), N % 8 == 0, G in
+ * {32, 64, 128, 256}, K ≥ G, K % G == 0, and K % 64 == 0 for W4 (K % 16 == 0 for W8).
+ */
+
+/* ---------------------------------------------------------------------------------------
+ * Canonical input layouts (what callers hold):
+ *   A       [M][K]      bf16 or fp32.
+ *   codes   W4: uint32 [K/8][N]: word (r, n) holds k = 8r..8r+7 of column n, element j in
+ *               bits 4j..4j+3 (the INT4 packing of "量化与融合 kernel" section 2.4 and its
+ *               INT4 GEMV of section 9.4).
+ *           W8: int8 [K][N] (the int8 code matrix of "分组量化 GEMM 内核" section 3.2).
+ *   scales  [K/G][N]    fp16, bf16 or fp32 ("量化与融合 kernel" section 3.1).
+ *   zeros   uint32 [K/G][N/8]: word (g, c) holds n = 8c..8c+7, element j in bits 4j
+ *           (the [K/g, N/8] INT4 zero points of section 3.1).
+ *   out     [M][N]      bf16 or fp32.
+ * ------------------------------------------------------------------------------------- */
+
+/* Size in bytes of the packed weight buffer for (K, N, G, prec).  Host only; touches no
+ * device.  W4: ceil(N/16)·16 · K/2 bytes (N is padded to whole 16-column tiles);
+ * W8: K·N bytes.  Errors: GQ_ERR_INVALID_ARG for a shape outside the contract or a NULL
+ * `bytes`. */
+int gq_packed_bytes(int K, int N, int G, int prec, size_t *bytes);
+
+/* Repack canonical codes into the device layout that gq_gemm reads (the offline repack of
+ * "量化与融合 kernel" section 3.3, item 1: the interleaved order lets one 16-byte load be
+ * decoded in registers directly into tensor-core operand fragments).
+ *   codes   device, canonical layout above (W4 uint32 [K/8][N]; W8 int8 [K][N]).
+ *   packed  device, gq_packed_bytes(...) bytes, written entirely (padding included).
+ * Deterministic; asynchronous on `stream`.  Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT
+ * (either pointer not 16-byte aligned), CUDA. */
+int gq_pack_weights(int K, int N, int G, int prec, const void *codes, void *packed,
+                    void *stream);
+
+/* Scratch bytes gq_gemm needs for this problem on the current device (split-K partial
+ * sums and per-tile arrival counters; 0 when the problem is not split).  Host only, but
+ * reads the current device's SM count.  Errors: INVALID_ARG, UNSUPPORTED, NO_DEVICE. */
+int gq_workspace_size(int M, int K, int N, int G, int prec, size_t *bytes);
+
+/* Register caller-owned device scratch for the current device (NULL, 0 = drop it and go
+ * back to the library-owned buffer).  The library zeroes it once here (synchronously) and
+ * afterwards keeps its counters at zero between calls.  Calls that overlap in time on
+ * different streams must not share one workspace.  Errors: ALIGNMENT (not 256-byte
+ * aligned), CUDA. */
+int gq_set_workspace(void *dev_ptr, size_t bytes);
+
+/* out = the group-quantized GEMM above.
+ *   A       device [M][K], bf16 (or fp32 with GQ_ACT_F32).
+ *   Wq      device, packed by gq_pack_weights with the same (K, N, G, prec).
+ *   scales  device [K/G][N].
+ *   zeros   device [K/G][N/8] uint32 with GQ_ZP, else must be NULL.
+ *   out     device [M][N], fully overwritten.
+ * Path choice depends only on (M, K, N, G, prec) and the device's SM count, so a given
+ * problem on a given device always produces the same bits.  Scratch comes from the
+ * registered workspace, else from a library-owned per-device buffer allocated (once, and
+ * grown when a larger problem needs it) on first use — that first use synchronizes the
+ * device and must not happen during stream capture.  All pointers 16-byte aligned.
+ * Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, NO_DEVICE. */
+int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
+            const void *scales, const void *zeros, void *out, void *stream);
+
+/* Timing harness.  Runs `warmup` untimed and then `iters` timed gq_gemm calls back to back
+ * on `stream`, call i reading weight copy i % n_copies (so that copies larger than L2 in
+ * total make every call read from HBM), and reports the mean time per call from CUDA
+ * events recorded on `stream`.  With use_graph != 0 the `iters` calls are captured once
+ * into a CUDA graph and the graph is replayed (no host launch overhead); the workspace
+ * must already exist then (call gq_gemm once first).  Synchronizes `stream`. */
+typedef struct gq_bench_args {
+  int M, K, N, G, prec;
+  const void *A;
+  const void *const *Wq;       /* n_copies device pointers (host array) */
+  const void *const *scales;   /* n_copies device pointers (host array) */
+  const void *const *zeros;    /* n_copies device pointers, or NULL without GQ_ZP */
+  int n_copies;
+  void *out;
+  int warmup, iters, use_graph;
+  void *stream;
+} gq_bench_args;
+
+typedef struct gq_bench_result {
+  double us_per_call;          /* mean device time per gq_gemm call */
+  int launches_per_call;       /* kernels one gq_gemm call launches for this problem */
+} gq_bench_result;
+
+int gq_bench(const gq_bench_args *args, gq_bench_result *result);
+
+/* Host-only description of the launch gq_gemm would make (for tests and reports).
+ * sm_count > 0 overrides the device query, so it works without a GPU. */
+typedef struct gq_plan_t {
+  int path;          /* 0 = small-M tensor-core decode (mma.sync), 1 = INT8 CUDA-core decode,
+                        2 = large-M tcgen05 prefill */
+  int nsplit;        /* K-slices of whole groups (1 = no split) */
+  int m_tile;        /* rows of A one CTA covers */
+  int n_tile;        /* output columns one CTA covers */
+  int grid_x, grid_y, grid_z;
+  int block_threads;
+  size_t smem_bytes; /* dynamic shared memory per CTA */
+  size_t workspace_bytes;
+} gq_plan_t;
+
+int gq_plan(int M, int K, int N, int G, int prec, int sm_count, gq_plan_t *plan);
+
+/* Slice z of the split of `units` equal work units into nsplit contiguous slices, as
+ * "分组量化 GEMM 内核" section 3.3 defines it: base = units / nsplit, rem = units % nsplit,
+ * begin = z·base + min(z, rem), end = begin + base + (z < rem).  Host only. */
+int gq_zsplit(int units, int nsplit, int z, int *begin, int *end);
+
+/* Sticky device-side error word of the current device (0 = none; GQ_ERR_TIMEOUT after a
+ * bounded wait gave up).  Reading it synchronizes the device; `clear` resets it. */
+int gq_device_error(int clear);
+
+const char *gq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQ_H_ */

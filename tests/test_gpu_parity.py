@@ -1,0 +1,252 @@
+"""Parity of the CUDA path with the float64 oracle (GPU).
+
+Every test calls the library through its C ABI (ctypes) on seeded synthetic inputs and
+compares element by element with the oracle: per element
+  bf16 out: |gpu - ref| <= 2^-8 |ref| + 1e-4 mag,   fp32 out: |gpu - ref| <= 1e-5 |ref| + 1e-6 mag
+with mag = Σ_k |A[m][k] w[k][n]|.  Integer-valued activations with power-of-two scales make
+every partial sum exact, and there the output must equal the oracle bit for bit.
+"""
+import numpy as np
+import pytest
+
+import gq_synth
+import oracle
+from helpers import alloc_out, load, np_to_dev, out_to_f64, prec_of, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def gq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return load()
+
+
+def _oracle(cfg, inp, rows=None, cols=None):
+    return oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                            N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc, rows=rows,
+                            cols=cols)
+
+
+def _assert_parity(cfg, got, ref, mag):
+    assert np.isfinite(got).all()
+    bad, ratio = oracle.check(got, ref, mag, cfg.out)
+    assert bad == 0, f"{cfg.name}: {bad} elements out of tolerance (worst err/tol {ratio:.3g})"
+    return ratio
+
+
+def _full_case(gq, cfg, seed=0):
+    inp = gq_synth.make_inputs(cfg, seed=seed)
+    out, _ = run_gemm(gq, cfg, inp)
+    ref, mag = _oracle(cfg, inp)
+    return _assert_parity(cfg, out_to_f64(out, cfg.out), ref, mag)
+
+
+# ------------------------------------------------------------------ small, full compare
+
+W4_SHAPES = [
+    gq_synth.Config("w4_tiny", M=1, K=512, N=512, G=128),
+    gq_synth.Config("w4_single_group", M=2, K=128, N=64, G=128),
+    gq_synth.Config("w4_ragged_n", M=3, K=1024, N=264, G=128),
+    gq_synth.Config("w4_g32", M=5, K=512, N=136, G=32, zp=True, sc="bf16"),
+    gq_synth.Config("w4_g64_f32scale", M=4, K=768, N=128, G=64, sc="f32"),
+    gq_synth.Config("w4_g256", M=1, K=2048, N=96, G=256, zp=True),
+    gq_synth.Config("w4_out_f32", M=7, K=1024, N=80, G=128, out="f32"),
+    gq_synth.Config("w4_outliers", M=1, K=4096, N=2048, G=128, outlier_frac=0.001),
+    gq_synth.Config("w4_asym_m16", M=16, K=8192, N=512, G=128, zp=True, sc="bf16"),
+]
+
+
+@pytest.mark.parametrize("cfg", W4_SHAPES, ids=lambda c: c.name)
+def test_w4_small_shapes(gq, cfg):
+    _full_case(gq, cfg)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 9, 15, 16, 17, 31, 32, 33, 64, 65, 127, 128, 129])
+def test_w4_m_sweep(gq, M):
+    cfg = gq_synth.Config(f"w4_m{M}", M=M, K=512, N=264, G=128, zp=(M % 2 == 0))
+    _full_case(gq, cfg, seed=M)
+
+
+Q8_SHAPES = [
+    gq_synth.Config("q8_m1", M=1, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_m3_g64", M=3, K=512, N=136, G=64, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_m33_g128", M=33, K=1024, N=72, G=128, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_bf16_out", M=2, K=256, N=64, G=32, w4=False, act="f32", sc="f32",
+                    out="bf16", s_lo=1e-3, s_hi=1e-2),
+]
+
+
+@pytest.mark.parametrize("cfg", Q8_SHAPES, ids=lambda c: c.name)
+def test_q8_small_shapes(gq, cfg):
+    _full_case(gq, cfg)
+
+
+# ------------------------------------------------------------------ exact arithmetic
+
+@pytest.mark.parametrize("cfg", [
+    gq_synth.Config("exact_w4", M=3, K=4096, N=264, G=128, zp=True, a_kind="int", pow2_scales=True),
+    gq_synth.Config("exact_w4_f32out", M=16, K=1024, N=128, G=32, a_kind="int", pow2_scales=True,
+                    out="f32", sc="f32"),
+    gq_synth.Config("exact_q8", M=2, K=2048, N=256, G=32, w4=False, act="f32", sc="f32", out="f32",
+                    a_kind="int", pow2_scales=True),
+], ids=lambda c: c.name)
+def test_integer_inputs_are_bit_exact(gq, cfg):
+    inp = gq_synth.make_inputs(cfg, seed=1)
+    out, _ = run_gemm(gq, cfg, inp)
+    ref, _ = _oracle(cfg, inp)
+    h = out.cpu().numpy()
+    if cfg.out == "bf16":
+        assert np.array_equal(h.view(np.uint16), oracle.f64_to_bf16_bits(ref))
+    else:
+        assert np.array_equal(h.astype(np.float64), ref)
+
+
+# ------------------------------------------------------------------ the workloads
+
+@pytest.mark.parametrize("name", ["tiny_gemv", "decode_gateup", "q8_m1", "q8_m32"])
+def test_workload_full_compare(gq, name):
+    _full_case(gq, gq_synth.CONFIGS[name])
+
+
+@pytest.mark.parametrize("name", ["asym_m16", "prefill"])
+def test_workload_sampled(gq, name):
+    """Full-size run; the oracle recomputes a sample of rows and columns (ragged edges
+    included) one by one."""
+    cfg = gq_synth.CONFIGS[name]
+    inp = gq_synth.make_inputs(cfg, seed=0)
+    out, _ = run_gemm(gq, cfg, inp)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, cfg.M - 1], rng.choice(cfg.M, min(cfg.M, 24), replace=False)]))
+    cols = np.unique(np.concatenate([[0, 1, 127, 128, cfg.N - 1],
+                                     rng.choice(cfg.N, 1024, replace=False)]))
+    ref, mag = _oracle(cfg, inp, rows=rows, cols=cols)
+    got = out_to_f64(out, cfg.out)[np.ix_(rows, cols)]
+    _assert_parity(cfg, got, ref, mag)
+
+
+@pytest.mark.parametrize("name", ["decode_gateup", "asym_m16", "q8_m1"])
+def test_bitwise_deterministic(gq, name):
+    cfg = gq_synth.CONFIGS[name]
+    inp = gq_synth.make_inputs(cfg, seed=0)
+    prec = prec_of(cfg)
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    A, S = np_to_dev(inp["A"]), np_to_dev(inp["scales"])
+    Z = np_to_dev(inp["zeros"]) if inp["zeros"] is not None else None
+    outs = []
+    for _ in range(3):
+        o = alloc_out(cfg.M, cfg.N, cfg.out)
+        gq.gemm_t(A, packed, S, Z, o, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+        outs.append(o)
+    torch.cuda.synchronize()
+    b = [o.view(torch.int16 if cfg.out == "bf16" else torch.int32) for o in outs]
+    assert torch.equal(b[0], b[1]) and torch.equal(b[0], b[2])
+
+
+# ------------------------------------------------------------------ layout, API edges
+
+def _unpack_w4_device_layout(packed: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Host reading of the documented packed layout (include/gq.h and gq_pack.cu):
+    [tile][chunk][lane][word j], pair i of word j = rows L/4 + 8(i&1), k = 16j + 2(L%4)
+    + 8(i>>1) + {0, 1} at bits 4i and 4i+16."""
+    words = packed.view(np.uint32)
+    tiles = (N + 15) // 16
+    nch = K // 64
+    w = words.reshape(tiles, nch, 32, 4)
+    q = np.zeros((K, tiles * 16), dtype=np.int64)
+    for lane in range(32):
+        for j in range(4):
+            for i in range(4):
+                r = lane // 4 + 8 * (i & 1)
+                kk = 16 * j + 2 * (lane % 4) + 8 * (i >> 1)
+                ww = w[:, :, lane, j]                         # [tiles][chunks]
+                for e, sh in ((0, 4 * i), (1, 4 * i + 16)):
+                    vals = (ww >> sh) & 0xF
+                    for t in range(tiles):
+                        q[np.arange(nch) * 64 + kk + e, t * 16 + r] = vals[t]
+    return q[:, :N]
+
+
+def test_pack_roundtrip_w4(gq):
+    cfg = gq_synth.Config("pack", M=1, K=256, N=40, G=128)
+    inp = gq_synth.make_weights(cfg, seed=5)
+    from group_quantized_weight_gb300.constants import GQ_W4
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, GQ_W4)
+    q = _unpack_w4_device_layout(packed.cpu().numpy(), cfg.K, cfg.N)
+    assert np.array_equal(q, inp["q"].astype(np.int64))
+
+
+def test_pack_roundtrip_w8(gq):
+    cfg = gq_synth.Config("pack8", M=1, K=64, N=24, G=32, w4=False, act="f32", sc="f32", out="f32")
+    inp = gq_synth.make_weights(cfg, seed=5)
+    from group_quantized_weight_gb300.constants import GQ_ACT_F32, GQ_SC_F32
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, GQ_ACT_F32 | GQ_SC_F32)
+    p = packed.cpu().numpy().view(np.int8).reshape(cfg.K // 16, cfg.N, 16)
+    q = p.transpose(0, 2, 1).reshape(cfg.K, cfg.N)
+    assert np.array_equal(q, inp["q"])
+
+
+def test_empty_problem_leaves_output_untouched(gq):
+    from group_quantized_weight_gb300.constants import GQ_W4
+    o = torch.full((4, 16), 3.0, dtype=torch.bfloat16, device="cuda")
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    assert gq.gq_gemm(0, 512, 16, 128, GQ_W4, d.data_ptr(), d.data_ptr(), d.data_ptr(), None,
+                      o.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    assert (o == 3.0).all()
+
+
+def test_misaligned_pointer_is_rejected_on_device(gq):
+    from group_quantized_weight_gb300.constants import GQ_W4
+    d = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    base = d.data_ptr()
+    assert gq.gq_gemm(1, 512, 16, 128, GQ_W4, base + 2, base, base, None, base, None) == 3
+
+
+def test_user_workspace_matches_library_workspace(gq):
+    cfg = gq_synth.CONFIGS["decode_gateup"].replace(N=4096)
+    inp = gq_synth.make_inputs(cfg, seed=2)
+    ref_out, packed = run_gemm(gq, cfg, inp)
+    prec = prec_of(cfg)
+    need = gq.gq_workspace_size(cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    assert need > 0
+    A, S = np_to_dev(inp["A"]), np_to_dev(inp["scales"])
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    try:
+        assert gq.gq_set_workspace(small.data_ptr(), 256) == 0
+        o = alloc_out(cfg.M, cfg.N, cfg.out)
+        st = gq.gq_gemm(cfg.M, cfg.K, cfg.N, cfg.G, prec, A.data_ptr(), packed.data_ptr(),
+                        S.data_ptr(), None, o.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert st == 4                                             # GQ_ERR_WORKSPACE
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        assert gq.gq_set_workspace(ws.data_ptr(), need) == 0
+        for _ in range(2):
+            o = alloc_out(cfg.M, cfg.N, cfg.out)
+            gq.gemm_t(A, packed, S, None, o, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+            torch.cuda.synchronize()
+            assert torch.equal(o.view(torch.int16), ref_out.view(torch.int16))
+    finally:
+        assert gq.gq_set_workspace(None, 0) == 0
+
+
+def test_graph_capture_of_gemm(gq):
+    """gq_gemm enqueues only kernels (after its scratch exists), so it can be captured."""
+    cfg = gq_synth.CONFIGS["tiny_gemv"]
+    inp = gq_synth.make_inputs(cfg, seed=0)
+    ref_out, packed = run_gemm(gq, cfg, inp)
+    prec = prec_of(cfg)
+    A, S = np_to_dev(inp["A"]), np_to_dev(inp["scales"])
+    o = alloc_out(cfg.M, cfg.N, cfg.out)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gq.gemm_t(A, packed, S, None, o, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), ref_out.view(torch.int16))

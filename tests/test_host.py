@@ -1,0 +1,130 @@
+"""Host-side checks of libgq (CPU only): the library loads and exports every symbol of
+include/gq.h, argument validation, the launch plan, the z-split and the work model."""
+import os
+import re
+
+import pytest
+
+import gq_synth
+from helpers import ROOT, load
+
+gq = load()
+from group_quantized_weight_gb300 import constants as C  # noqa: E402
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "gq.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gq_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    import ctypes
+    names = _header_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(gq.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(gq.EXPORTED)
+
+
+def test_status_strings():
+    assert gq.gq_status_string(0) == "ok"
+    for s in range(1, 8):
+        assert gq.gq_status_string(s) not in ("ok", "unknown status")
+
+
+def test_zsplit_is_the_pages_partition():
+    """The z-split of the group-wise GEMM blog (section 3.3): contiguous, disjoint,
+    covering, sizes differing by at most one, larger slices first."""
+    for units in (1, 2, 5, 32, 64, 97):
+        for nsplit in range(1, min(units, 70) + 1):
+            spans = [gq.gq_zsplit(units, nsplit, z) for z in range(nsplit)]
+            assert spans[0][0] == 0 and spans[-1][1] == units
+            for (b0, e0), (b1, e1) in zip(spans, spans[1:]):
+                assert e0 == b1
+            sizes = [e - b for b, e in spans]
+            assert max(sizes) - min(sizes) <= 1 and sizes == sorted(sizes, reverse=True)
+            base, rem = divmod(units, nsplit)
+            assert sizes.count(base + 1) == rem
+    with pytest.raises(C.GqError):
+        gq.gq_zsplit(4, 0, 0)
+
+
+def test_packed_bytes():
+    assert gq.gq_packed_bytes(4096, 28672, 128, C.GQ_W4) == 4096 * 28672 // 2
+    assert gq.gq_packed_bytes(512, 24, 128, C.GQ_W4) == 512 * 32 // 2        # padded to 2 tiles
+    assert gq.gq_packed_bytes(2048, 12288, 32, C.GQ_ACT_F32 | C.GQ_SC_F32) == 2048 * 12288
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 4096, 28672, 100, C.GQ_W4), 2),          # G outside {32, 64, 128, 256}
+    ((1, 4000, 512, 32, C.GQ_W4), 2),             # W4 needs K % 64 == 0
+    ((1, 192, 512, 128, C.GQ_W4), 1),             # K % G != 0
+    ((1, 512, 12, 128, C.GQ_W4), 1),              # N % 8 != 0
+    ((1, 512, 16, 128, C.GQ_W4 | C.GQ_SC_BF16 | C.GQ_SC_F32), 1),
+    ((1, 512, 16, 128, C.GQ_W4 | C.GQ_ACT_F32), 2),
+    ((1, 512, 16, 32, C.GQ_ZP | C.GQ_ACT_F32 | C.GQ_SC_F32), 1),   # INT8 has no zero point
+    ((1, 512, 16, 32, C.GQ_ACT_F32), 2),          # INT8 needs fp32 scales
+    ((-1, 512, 16, 128, C.GQ_W4), 1),
+    ((1, 512, 16, 128, 0x400), 1),                # unknown flag
+])
+def test_invalid_calls_are_rejected_before_any_launch(args, status):
+    """No device exists here: an invalid call must return its status before touching one."""
+    M, K, N, G, prec = args
+    st = gq.gq_gemm(M, K, N, G, prec, 16, 16, 16, None, 16, None)
+    assert st == status
+    with pytest.raises(C.GqError) as e:
+        gq.gq_plan(M, K, N, G, prec, sm_count=152)
+    assert e.value.status == status
+
+
+def test_null_and_misaligned_pointers():
+    assert gq.gq_gemm(1, 512, 16, 128, C.GQ_W4, None, 16, 16, None, 16, None) == 1
+    assert gq.gq_gemm(1, 512, 16, 128, C.GQ_W4, 8, 16, 16, None, 16, None) == 3
+    # zero points passed without GQ_ZP (and the reverse)
+    assert gq.gq_gemm(1, 512, 16, 128, C.GQ_W4, 16, 16, 16, 16, 16, None) == 1
+    assert gq.gq_gemm(1, 512, 16, 128, C.GQ_W4 | C.GQ_ZP, 16, 16, 16, None, 16, None) == 1
+    assert gq.gq_pack_weights(512, 16, 128, C.GQ_W4, 8, 16, None) == 3
+    # empty problems are valid and launch nothing
+    assert gq.gq_gemm(0, 512, 16, 128, C.GQ_W4, 16, 16, 16, None, 16, None) == 0
+    assert gq.gq_gemm(4, 512, 0, 128, C.GQ_W4, 16, 16, 16, None, 16, None) == 0
+
+
+@pytest.mark.parametrize("name", list(gq_synth.CONFIGS))
+def test_plan_is_a_pure_function_of_shape(name):
+    cfg = gq_synth.CONFIGS[name]
+    from helpers import prec_of
+    p1 = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec_of(cfg), sm_count=152)
+    p2 = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec_of(cfg), sm_count=152)
+    assert p1 == p2
+    units = cfg.K // max(cfg.G, 64 if cfg.w4 else cfg.G)
+    assert 1 <= p1["nsplit"] <= units
+    assert p1["grid_y"] == p1["nsplit"]
+    assert p1["grid_x"] * p1["n_tile"] >= cfg.N
+    assert p1["grid_z"] * p1["m_tile"] >= cfg.M
+    assert p1["smem_bytes"] <= 200 * 1024
+    if p1["nsplit"] == 1:
+        assert p1["workspace_bytes"] == 0
+    else:
+        assert p1["workspace_bytes"] >= p1["nsplit"] * cfg.M * cfg.N * 4
+
+
+def test_decode_plan_fills_the_machine():
+    cfg = gq_synth.CONFIGS["decode_gateup"]
+    p = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, C.GQ_W4, sm_count=152)
+    assert p["path"] == 0
+    assert p["grid_x"] * p["grid_y"] * p["grid_z"] >= 152 * 4
+
+
+def test_algorithmic_bytes_match_the_worked_figures():
+    # configurations' byte counts, and the page's M=1 N=K=4096 INT4 GEMV (8 MiB of
+    # weights + 256 KiB of fp16 scales, plus 8 KiB of activations and 8 KiB of output)
+    assert C.algorithmic_bytes(1, 4096, 28672, 128, True, False, "bf16", "fp16", "bf16") == 60620800
+    assert C.algorithmic_bytes(1, 512, 512, 128, True, False, "bf16", "fp16", "bf16") == 137216
+    assert C.algorithmic_bytes(1, 2048, 12288, 32, False, False, "f32", "f32", "f32") == 28368896
+    assert C.algorithmic_bytes(16, 8192, 28672, 128, True, True, "bf16", "bf16", "bf16") == 123207680
+    assert C.algorithmic_bytes(4096, 4096, 14336, 128, True, False, "bf16", "fp16", "bf16") == 181272576
+    assert C.algorithmic_bytes(1, 4096, 4096, 128, True, False, "bf16", "fp16", "bf16") == \
+        (8 << 20) + (256 << 10) + 8192 + 8192
+    assert C.gemm_flops(4096, 4096, 14336) == 481036337152
