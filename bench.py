@@ -201,6 +201,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--calls-per-step", type=int, default=CALLS_PER_STEP,
+                    help="gq_gemm calls per step (a smaller value for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -252,8 +255,9 @@ def main():
     call(0)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
+    calls_per_step = args.calls_per_step
     with torch.cuda.graph(graph):
-        for i in range(CALLS_PER_STEP):
+        for i in range(calls_per_step):
             call(i)
     torch.cuda.synchronize()
 
@@ -288,16 +292,49 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
-    launches = args.steps * CALLS_PER_STEP
+    launches = args.steps * calls_per_step
     kernel_us = 1e3 * ms / launches
     value = world * nbytes * launches / (ms * 1e-3) / 1e9
     peaks, peak_kind = _peaks()
     achieved = nbytes / (kernel_us * 1e-6) / 1e9
 
-    # end to end through the C ABI with host buffers: pinned A in, pinned out back, per call
+    e2e = _e2e(args, torch, np, inp, A, out, call, world, nbytes, calls_per_step)
+
+    prefill = None
+    if not args.no_prefill and rank == 0:
+        prefill = _prefill(gq, torch, dev, peaks, peak_kind)
+
+    traffic = _kernel_traffic("gq_decode.cu", "w4_stripe_decode_decode_gateup.md")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: M=1 K=4096 N=28672 G=128 W4A16 sym, fp16 scales, "
+                               "bf16 act/out",
+                   "step": f"{calls_per_step} gq_gemm calls replayed from one CUDA graph",
+                   "l2": f"inputs larger than L2: {COPIES} rotated weight copies "
+                         f"({COPIES * nbytes / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "w4_stripe_kernel", "peak_source": f"hbm_gbs of {peak_kind}",
+                     "kernel_us": kernel_us},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    return _finish(args, line, prefill, rank, world, cfg, dist)
+
+
+def _e2e(args, torch, np, inp, A, out, call, world, nbytes, calls_per_step):
+    """End to end through the C ABI with host buffers: per call, the activations are copied
+    in from pinned host memory, gq_gemm runs, and the output is copied back."""
+    if args.no_e2e:
+        return None
     e2e_calls = 2000
     A_h = torch.from_numpy(np.ascontiguousarray(inp["A"]).view(np.int16)).pin_memory()
-    out_h = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16).pin_memory()
+    out_h = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
     A_d = torch.empty_like(A)
     for i in range(20):
         A_d.copy_(A_h, non_blocking=True)
@@ -311,36 +348,14 @@ def main():
         out_h.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e = {"value": world * nbytes * e2e_calls / e2e_s / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": A_h.numel() * 2 * CALLS_PER_STEP,
-           "d2h_bytes_per_step": out_h.numel() * 2 * CALLS_PER_STEP,
-           "note": "per call: H2D of the activations, gq_gemm, D2H of the output, "
-                   "from pinned host memory, host-launched (no graph)"}
+    return {"value": world * nbytes * e2e_calls / e2e_s / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": A_h.numel() * 2 * calls_per_step,
+            "d2h_bytes_per_step": out_h.numel() * 2 * calls_per_step,
+            "note": "per call: H2D of the activations, gq_gemm, D2H of the output, "
+                    "from pinned host memory, host-launched (no graph)"}
 
-    prefill = None
-    if not args.no_prefill and rank == 0:
-        prefill = _prefill(gq, torch, dev, peaks, peak_kind)
 
-    traffic = _kernel_traffic("gq_decode.cu", "w4_mma_decode_decode_gateup.md")
-    line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: M=1 K=4096 N=28672 G=128 W4A16 sym, fp16 scales, "
-                               "bf16 act/out",
-                   "step": f"{CALLS_PER_STEP} gq_gemm calls replayed from one CUDA graph",
-                   "l2": f"inputs larger than L2: {COPIES} rotated weight copies "
-                         f"({COPIES * nbytes / 1e6:.0f} MB)",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "w4_mma_decode_kernel", "peak_source": f"hbm_gbs of {peak_kind}",
-                     "kernel_us": kernel_us},
-        "e2e": e2e,
-        "gpu_launches": launches,
-        "clocks": clocks,
-    }
+def _finish(args, line, prefill, rank, world, cfg, dist):
     if prefill:
         line["prefill"] = prefill
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -50,7 +50,8 @@ class Config:
     z_hi: int = 11
     outlier_frac: float = 0.0   # fraction of each activation row multiplied by outlier_mult
     outlier_mult: float = 50.0
-    a_kind: str = "normal"      # "normal" | "int" (integer-valued activations in [-8, 8])
+    a_kind: str = "normal"      # "normal" | "int" (integers in [-8, 8]) | "wide" (see a_spread)
+    a_spread: int = 0           # "wide": N(0,1) times 2^U{-a_spread..a_spread} per element
     pow2_scales: bool = False   # scales drawn from {2^-8 .. 2^-5} (exact-arithmetic cases)
 
     def replace(self, **kw) -> "Config":
@@ -119,6 +120,9 @@ def make_activations(cfg: Config, seed: int = 0, M: int | None = None) -> np.nda
     rng = _rng(seed, _T_A)
     if cfg.a_kind == "int":
         a = rng.integers(-8, 9, size=(M, cfg.K)).astype(np.float32)
+    elif cfg.a_kind == "wide":
+        e = rng.integers(-cfg.a_spread, cfg.a_spread + 1, size=(M, cfg.K))
+        a = np.ldexp(rng.standard_normal((M, cfg.K)), e).astype(np.float32)
     else:
         a = rng.standard_normal((M, cfg.K)).astype(np.float32)
     if cfg.outlier_frac > 0:

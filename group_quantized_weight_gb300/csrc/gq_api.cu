@@ -71,6 +71,29 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const size_t kSmemCap = 96u << 10;   // activation slice budget per CTA (bytes)
   const int Mc = M > 0 ? M : 1;
   const int Nc = N > 0 ? N : 8;
+  const size_t stripe_smem = (prec & GQ_W4) && Mc <= 8 ? stripe_smem_bytes(Mc, K, G, prec) : 0;
+  if ((prec & GQ_W4) && Mc <= 8 && stripe_smem <= (220u << 10)) {   // one CTA per SM
+    // striped persistent decode: one CTA of kStrWarps warps per SM, one stripe per warp
+    p->path = kPathStripe;
+    p->mt = Mc <= 4 ? 1 : 2;   // MMA blocks
+    p->m_tile = 8;
+    p->n_tile = kTileN;
+    p->unit_k = G > kChunkK ? G : kChunkK;
+    p->units = ceil_div(Nc, kTileN) * (K / p->unit_k);
+    int W = sms * kStrWarps;            // one CTA of kStrWarps warps per SM
+    if (W > p->units) W = p->units;
+    p->nsplit = W;
+    p->grid_x = ceil_div(W, kStrWarps);
+    p->grid_y = p->grid_z = 1;
+    p->block_threads = kStrWarps * 32;
+    p->smem_bytes = stripe_smem;
+    p->part_bytes = round_up((size_t)W * 2 * kTileN * 8 * sizeof(float), 256);
+    p->counter_bytes = kCounterRegionBytes;
+    if ((size_t)ceil_div(Nc, kTileN) * sizeof(unsigned) > kCounterRegionBytes)
+      return GQ_ERR_UNSUPPORTED;
+    p->workspace_bytes = p->part_bytes + p->counter_bytes;
+    return GQ_OK;
+  }
   if (prec & GQ_W4) {
     p->path = kPathMmaDecode;
     const int rows = Mc < 8 * kDecMaxMT ? Mc : 8 * kDecMaxMT;
@@ -112,7 +135,9 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   p->grid_y = p->nsplit;
   if (p->nsplit > 1) {
     p->part_bytes = round_up((size_t)p->nsplit * Mc * Nc * sizeof(float), 256);
-    p->counter_bytes = round_up((size_t)p->grid_x * p->grid_z * sizeof(unsigned), 256);
+    p->counter_bytes = kCounterRegionBytes;
+    if ((size_t)p->grid_x * p->grid_z * sizeof(unsigned) > kCounterRegionBytes)
+      return GQ_ERR_UNSUPPORTED;
   }
   p->workspace_bytes = p->part_bytes + p->counter_bytes;
   return GQ_OK;
@@ -297,11 +322,13 @@ static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const 
   void *ws = nullptr;
   st = get_scratch(p.workspace_bytes, &ws);
   if (st != GQ_OK) return st;
-  float *part = (float *)ws;
-  unsigned *counters = ws ? (unsigned *)((char *)ws + p.part_bytes) : nullptr;
+  unsigned *counters = (unsigned *)ws;
+  float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  if (p.path == kPathMmaDecode)
+  if (p.path == kPathStripe)
+    e = launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
+  else if (p.path == kPathMmaDecode)
     e = launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else
     e = launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);

@@ -18,15 +18,21 @@ constexpr int kChunkK8 = 16;
 // Small-M tensor-core decode kernel: warps per CTA (each warp owns one 16-column tile).
 constexpr int kDecWarps = 8;
 constexpr int kDecMaxMT = 4;           // up to 4 x 8 = 32 rows of A per CTA
+// Striped small-M decode kernel (M <= 8): warps per CTA, one CTA per SM.
+constexpr int kStrWarps = 16;
 // INT8 CUDA-core decode kernel: one column per thread.
 constexpr int kQ8Threads = 128;
 constexpr int kQ8MaxRows = 32;
 
-enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2 };
+// Scratch layout: a fixed region of arrival counters at offset 0 (every call leaves them
+// at zero, and no problem's partial sums ever overlap them), then the partial sums.
+constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
+
+enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3 };
 
 struct Plan {
   int path;
-  int nsplit;
+  int nsplit;       // K slices (paths 0, 1) or warp stripes (path 3)
   int units;        // number of split units along K
   int unit_k;       // k per unit (a whole number of groups)
   int m_tile;       // rows per CTA
@@ -57,6 +63,11 @@ cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int pre
                               const void *A, const void *Wq, const void *scales,
                               const void *zeros, void *out, float *part,
                               unsigned *counters, cudaStream_t s);
+size_t stripe_smem_bytes(int M, int K, int G, int prec);
+cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int prec,
+                                const void *A, const void *Wq, const void *scales,
+                                const void *zeros, void *out, float *part,
+                                unsigned *counters, cudaStream_t s);
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,
                              void *out, float *part, unsigned *counters, cudaStream_t s);

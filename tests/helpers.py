@@ -43,10 +43,10 @@ def np_to_dev(a: np.ndarray):
 
 def out_to_f64(out, out_dtype: str) -> np.ndarray:
     import oracle
-    h = out.cpu().numpy()
+    import torch
     if out_dtype == "bf16":
-        return oracle.bf16_bits_to_f64(h.view(np.uint16))
-    return h.astype(np.float64)
+        return oracle.bf16_bits_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
+    return out.cpu().numpy().astype(np.float64)
 
 
 def alloc_out(M: int, N: int, out_dtype: str, fill: float = float("nan")):

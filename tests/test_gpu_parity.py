@@ -90,6 +90,15 @@ def test_q8_small_shapes(gq, cfg):
 
 # ------------------------------------------------------------------ exact arithmetic
 
+@pytest.mark.parametrize("M,spread", [(1, 100), (2, 50), (3, 25), (4, 25), (7, 25)])
+def test_wide_dynamic_range_activations(gq, M, spread):
+    """Activations spread over 2^(2 * spread) within a row: the decode path carries bf16
+    activations into fp16 MMA operands by exponent bands, which must stay exact."""
+    cfg = gq_synth.Config(f"wide_m{M}", M=M, K=2048, N=264, G=128, zp=(M % 2 == 1),
+                          a_kind="wide", a_spread=spread)
+    _full_case(gq, cfg, seed=M)
+
+
 @pytest.mark.parametrize("cfg", [
     gq_synth.Config("exact_w4", M=3, K=4096, N=264, G=128, zp=True, a_kind="int", pow2_scales=True),
     gq_synth.Config("exact_w4_f32out", M=16, K=1024, N=128, G=32, a_kind="int", pow2_scales=True,
@@ -101,11 +110,11 @@ def test_integer_inputs_are_bit_exact(gq, cfg):
     inp = gq_synth.make_inputs(cfg, seed=1)
     out, _ = run_gemm(gq, cfg, inp)
     ref, _ = _oracle(cfg, inp)
-    h = out.cpu().numpy()
     if cfg.out == "bf16":
-        assert np.array_equal(h.view(np.uint16), oracle.f64_to_bf16_bits(ref))
+        h = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(h, oracle.f64_to_bf16_bits(ref))
     else:
-        assert np.array_equal(h.astype(np.float64), ref)
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
 
 
 # ------------------------------------------------------------------ the workloads
