@@ -51,6 +51,7 @@ _SIGS = {
     "gq_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
     "gq_set_workspace": [_p, _sz],
     "gq_gemm": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
+    "gq_gemm_static_scratch": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_bench": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
     "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
@@ -98,6 +99,17 @@ def gq_set_workspace(ptr, nbytes: int) -> int:
 def gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream=None) -> int:
     """Raw call; returns the status."""
     return _lib.gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream)
+
+
+def gq_gemm_static_scratch(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr,
+                           stream=None) -> int:
+    """gq_gemm that never allocates: scratch comes from a fixed array inside the library
+    (GQ_STATIC_SCRATCH_BYTES).  Raw call; returns the status."""
+    return _lib.gq_gemm_static_scratch(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr,
+                                       out_ptr, stream)
+
+
+GQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 def gq_plan(M: int, K: int, N: int, G: int, prec: int, sm_count: int = 0) -> dict:

@@ -113,6 +113,27 @@ int gq_set_workspace(void *dev_ptr, size_t bytes);
 int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
             const void *scales, const void *zeros, void *out, void *stream);
 
+/* gq_gemm without any device allocation.  The pages have no counterpart: this call exists
+ * for callers that cannot allocate device memory — serving runtimes that reserve all
+ * device memory up front and forbid allocation once running, latency-critical loops where
+ * an allocation and the device synchronization it may bring are not acceptable, and
+ * embedders that route every device allocation through their own allocator.
+ *   Arguments, layouts, results and errors are those of gq_gemm, computed by the same
+ * kernels.  The split-K scratch comes from one array of GQ_STATIC_SCRATCH_BYTES compiled
+ * into the library (every GPU that loads the library holds it until the process exits)
+ * instead of the registered or library-owned workspace; a problem whose scratch
+ * (gq_workspace_size) exceeds it returns GQ_ERR_WORKSPACE and launches nothing.
+ *   The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture.  Every call clears the arrival counters it uses (an asynchronous memset
+ * on `stream`).  All calls on a device share the one array, which keeps the last call's
+ * contents, so calls that overlap on the GPU — different streams, or host threads without
+ * ordering between them — race on it and must be serialized by the caller. */
+#define GQ_STATIC_SCRATCH_BYTES (4u << 20)
+int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, const void *A,
+                           const void *Wq, const void *scales, const void *zeros, void *out,
+                           void *stream);
+
 /* Timing harness.  Runs `warmup` untimed and then `iters` timed gq_gemm calls back to back
  * on `stream`, call i reading weight copy i % n_copies (so that copies larger than L2 in
  * total make every call read from HBM), and reports the mean time per call from CUDA
