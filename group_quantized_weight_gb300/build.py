@@ -37,7 +37,7 @@ def _newest_header() -> float:
 
 
 def _compile(nvcc: str, src: str, obj: str, verbose: bool) -> str:
-    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC",
            "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")

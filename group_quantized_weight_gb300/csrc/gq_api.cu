@@ -72,13 +72,13 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const int Mc = M > 0 ? M : 1;
   const int Nc = N > 0 ? N : 8;
   const size_t stripe_smem = (prec & GQ_W4) && Mc <= 8 ? stripe_smem_bytes(Mc, K, G, prec) : 0;
-  if ((prec & GQ_W4) && Mc <= 8 && stripe_smem <= (220u << 10)) {   // one CTA per SM
+  if ((prec & GQ_W4) && Mc <= 8 && stripe_smem <= (200u << 10)) {   // one CTA per SM
     // striped persistent decode: one CTA of kStrWarps warps per SM, one stripe per warp
     p->path = kPathStripe;
     p->mt = Mc <= 4 ? 1 : 2;   // MMA blocks
     p->m_tile = 8;
     p->n_tile = kTileN;
-    p->unit_k = G > kChunkK ? G : kChunkK;
+    p->unit_k = (G > kChunkK ? G : kChunkK) * stripe_unit_groups(K, G);
     p->units = ceil_div(Nc, kTileN) * (K / p->unit_k);
     int W = sms * kStrWarps;            // one CTA of kStrWarps warps per SM
     if (W > p->units) W = p->units;

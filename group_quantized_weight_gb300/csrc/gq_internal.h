@@ -64,6 +64,7 @@ cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int pre
                               const void *zeros, void *out, float *part,
                               unsigned *counters, cudaStream_t s);
 size_t stripe_smem_bytes(int M, int K, int G, int prec);
+int stripe_unit_groups(int K, int G);
 cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int prec,
                                 const void *A, const void *Wq, const void *scales,
                                 const void *zeros, void *out, float *part,

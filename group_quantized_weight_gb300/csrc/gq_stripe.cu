@@ -1,5 +1,6 @@
 // Striped small-M decode kernel (M <= 8) of the group-quantized weight-only GEMM.
 #include <type_traits>
+#include <utility>
 
 #include "gq_device.cuh"
 
@@ -18,10 +19,9 @@ namespace gq {
 // warps w_a < ... < w_b is summed by the warp that completes it, adding the partials in
 // warp order w_a, ..., w_b (fixed order: bitwise reproducible).
 //
-// Streaming: every lane copies its own 16 bytes of each chunk into a shared-memory ring
-// of kStages chunks with cp.async (the group scales and zero-point words of a unit travel
-// in the same commit group as the unit's first chunk), so kStages chunks per warp are in
-// flight without holding registers.
+// Streaming: each lane keeps kStages chunks (16 bytes each) of its stripe in flight in a
+// register ring, loaded kStages chunks ahead of use; the scales and zero-point words of a
+// unit are loaded together with the unit's weights.
 //
 // Decode: the FP16 form of the magic-number trick of section 2.4 of the same page, which
 // needs one shift per eight codes: (w & 0x000F000F) | 0x64006400 is fp16(1024 + q) for the
@@ -46,7 +46,7 @@ namespace gq {
 // in the stream start launching at once, and it reads none of its inputs and writes none
 // of its outputs before griddepcontrol.wait (the end of the previous kernel).
 
-constexpr int kStages = 8;    // chunks in flight per lane
+constexpr int kStages = 8;    // chunks in flight per lane (register ring)
 
 __device__ __forceinline__ int warp_of_unit(int u, int U, int W) {
   const int base = U / W, rem = U % W;
@@ -75,6 +75,24 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
   return r;
 }
 
+// (a & b) | c in one LOP3
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// Decode constants, passed as a kernel parameter: the instructions read them from the
+// parameter bank instead of materializing immediates around every use.
+struct DecodeConsts {
+  uint32_t lo_mask;     // 0x000F000F: codes in bits 0-3 and 16-19
+  uint32_t hi_mask;     // 0x00F000F0: codes in bits 4-7 and 20-23
+  uint32_t magic;       // 0x64006400: fp16 1024 in both halves
+  uint32_t sixteenth;   // 0x2C002C00: fp16 1/16 in both halves
+  uint32_t lo_sym;      // 0x64086408: fp16 (1024 + 8), symmetric zero point
+  uint32_t hi_sym;      // 0xD480D480: fp16 -(64 + 8)
+};
+
 // Fix-up of a tile that a stripe covers only in part.  `val` holds the lane's combined
 // value for rows m = lane_row(...) (set by the caller), columns n0 and n0 + 8.
 __device__ __forceinline__ void stripe_fixup(float v0, float v1, int mrow, bool owner,
@@ -88,17 +106,22 @@ __device__ __forceinline__ void stripe_fixup(float v0, float v1, int mrow, bool 
     pp[mrow * kTileN + r0] = v0;
     pp[mrow * kTileN + r0 + 8] = v1;
   }
-  __threadfence();
+  // __syncwarp orders the lanes' partial stores before lane 0's release; the acq_rel
+  // read-modify-write publishes them and, in the last arriver, makes every other
+  // contributor's partials visible to the loads below
   __syncwarp();
   unsigned last = 0;
   if (lane == 0) {
-    const unsigned prev = atomicAdd(counters + t, (unsigned)held_units);
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;"
+                 : "=r"(prev)
+                 : "l"(counters + t), "r"((unsigned)held_units)
+                 : "memory");
     last = (prev + (unsigned)held_units == (unsigned)Cu) ? 1u : 0u;
     if (last) counters[t] = 0u;     // every contributor has arrived: leave it at zero
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
-  __threadfence();
   const int wa = warp_of_unit(t * Cu, U, W), wb = warp_of_unit(t * Cu + Cu - 1, U, W);
   for (int idx = lane; idx < M * kTileN; idx += 32) {
     const int m = idx / kTileN, nl = idx - m * kTileN;
@@ -114,23 +137,23 @@ __device__ __forceinline__ void stripe_fixup(float v0, float v1, int mrow, bool 
   }
 }
 
-// MT: n8 MMA blocks (1 for M <= 4, 2 for M <= 8)
-template <int G, int SC, bool ZP, int MT>
+// MT: n8 MMA blocks (1 for M <= 4, 2 for M <= 8); UG: a K unit is UG * max(G, 64) values
+// of k (UG = 2 halves the per-unit work when K allows it).
+template <int G, int SC, bool ZP, int MT, int UG>
 __global__ void __launch_bounds__(kStrWarps * 32, 1)
 w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
                  const void *__restrict__ scales, const uint32_t *__restrict__ zeros,
                  void *__restrict__ out, float *__restrict__ part,
-                 unsigned *__restrict__ counters, int M, int K, int N, int W, int out_f32) {
-  constexpr int UK = G > kChunkK ? G : kChunkK;   // k per unit
+                 unsigned *__restrict__ counters, int M, int K, int N, int W, int out_f32,
+                 const DecodeConsts dk) {
+  constexpr int UK = (G > kChunkK ? G : kChunkK) * UG;   // k per unit
   constexpr int UCH = UK / kChunkK;               // chunks per unit
   constexpr int GPU = UK / G;                     // groups per unit
   constexpr int SPG = G / 16;                     // 16-k MMA steps per group
-  constexpr int RU = kStages / UCH;               // units per ring cycle
-  constexpr int SRU = 2 * RU;                     // scale-ring slots (units)
+  constexpr int PF = kStages / UCH;               // units in flight (kStages chunks)
   constexpr int ES = SC == kScF32 ? 4 : 2;        // bytes per scale
-  constexpr int SPIECE = 16 * ES / 4;             // 4-byte pieces per group's 16 scales
-  static_assert(kStages % UCH == 0, "a ring cycle holds whole units");
-  static_assert(GPU * SPIECE <= 32 && 2 * GPU <= 32, "one lane per copied piece");
+  static_assert(kStages % UCH == 0, "the register ring holds whole units");
+  typedef typename std::conditional<SC == kScF32, uint32_t, unsigned short>::type sc_t;
 
   extern __shared__ __align__(16) uint32_t smem[];
   __shared__ int s_emax[8], s_emin[8];
@@ -145,68 +168,60 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
   int u0 = 0, u1 = 0;
   if (gw < W) zsplit_dev(U, W, gw, u0, u1);
   const int nu = u1 - u0;                          // units in this warp's stripe
-  const int nc = nu * UCH;                         // chunks in this warp's stripe
   const int r0 = lane >> 2, q = lane & 3;
   if (threadIdx.x < 8) {
     s_emax[threadIdx.x] = 0;
     s_emin[threadIdx.x] = 255;
   }
-
-  // shared memory: [weight ring][scale ring][zero-point ring][band rows][raw A]
-  uint4 *wring = reinterpret_cast<uint4 *>(smem) + (size_t)warp * kStages * 32;
-  uint32_t *sring = smem + kStrWarps * kStages * 128 + warp * (SRU * GPU * 16);
-  uint32_t *zring = smem + kStrWarps * kStages * 128 + kStrWarps * SRU * GPU * 16 +
-                    warp * (SRU * GPU * 2);
+  // shared memory: [band rows][raw A]
   const int RS = act_row_words(C);
-  uint32_t *bands = smem + kStrWarps * (kStages * 128 + SRU * GPU * 18);
+  uint32_t *bands = smem;
   uint32_t *araw = bands + (1 + 2 * M) * RS;     // zero row + two band rows per row
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- the copy side: chunk c of the stripe goes to ring slot c % kStages
+  // ---- the load side: weights of PF units ahead in registers, with their scales
   const uint4 *wsrc = Wp + (size_t)u0 * UCH * 32 + lane;
-  const uint32_t wdst = (uint32_t)__cvta_generic_to_shared(wring + lane);
-  const uint32_t sdst = (uint32_t)__cvta_generic_to_shared(sring);
-  const uint32_t zdst = (uint32_t)__cvta_generic_to_shared(zring);
-  int ht = u0 / Cu, hu = u0 - ht * Cu;             // tile and unit of the copy head
-  int hunit = 0;                                   // stripe-relative unit of the copy head
-  auto issue_meta = [&]() {                        // scales (+ zero words) of the head unit
-    const int slot = hunit & (SRU - 1);
+  const size_t srow = (size_t)N;                   // elements per scale row
+  int ht = u0 / Cu, hu = u0 - ht * Cu;             // tile and unit of the load head
+  const sc_t *hsa = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0, N - 1);
+  const sc_t *hsb = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0 + 8, N - 1);
+  const uint32_t *hza = zeros + min(2 * ht, NW - 1), *hzb = zeros + min(2 * ht + 1, NW - 1);
+  size_t hg = (size_t)hu * GPU;                    // group index of the head unit
+  uint4 buf[PF][UCH];
+  uint32_t sr[PF][GPU][2], zr[PF][GPU][2];
+  auto load_unit = [&](auto slot, int k) {         // unit k of the stripe into ring slot P
+    constexpr int P = decltype(slot)::value;
+#pragma unroll
+    for (int ch = 0; ch < UCH; ++ch)
+      buf[P][ch] = ld_stream(wsrc + (size_t)(k * UCH + ch) * 32);
 #pragma unroll
     for (int gi = 0; gi < GPU; ++gi) {
-      const int g = hu * GPU + gi;
-      if (lane >= gi * SPIECE && lane < (gi + 1) * SPIECE) {
-        const int pc = lane - gi * SPIECE;
-        const int n = min(ht * kTileN + pc * (4 / ES), N - (4 / ES));
-        const char *src = reinterpret_cast<const char *>(scales) + ((size_t)g * N + n) * ES;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                         sdst + 4u * ((slot * GPU + gi) * 16 + pc)),
-                     "l"(src)
-                     : "memory");
-      }
-      if (ZP && lane >= 2 * gi && lane < 2 * gi + 2) {
-        const int h = lane - 2 * gi;
-        const uint32_t *src = zeros + (size_t)g * NW + min(2 * ht + h, NW - 1);
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                         zdst + 4u * ((slot * GPU + gi) * 2 + h)),
-                     "l"(src)
-                     : "memory");
+      sr[P][gi][0] = (uint32_t)__ldg(hsa + (hg + gi) * srow);
+      sr[P][gi][1] = (uint32_t)__ldg(hsb + (hg + gi) * srow);
+      if (ZP) {
+        zr[P][gi][0] = __ldg(hza + (hg + gi) * NW);
+        zr[P][gi][1] = __ldg(hzb + (hg + gi) * NW);
       }
     }
-    ++hunit;
-    if (++hu == Cu) { hu = 0; ++ht; }
-  };
-  auto issue_chunk = [&](int c, int slot) {        // chunk c of the stripe
-    if (c < nc) {
-      if (c % UCH == 0) issue_meta();
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(wdst + 512u * slot),
-                   "l"(wsrc + (size_t)c * 32)
-                   : "memory");
+    hg += GPU;
+    if (++hu == Cu) {
+      hu = 0;
+      hg = 0;
+      ++ht;
+      hsa = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0, N - 1);
+      hsb = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0 + 8, N - 1);
+      hza = zeros + min(2 * ht, NW - 1);
+      hzb = zeros + min(2 * ht + 1, NW - 1);
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
   };
-#pragma unroll
-  for (int c = 0; c < kStages - 1; ++c) issue_chunk(c, c);
+  auto prefetch = [&](auto slot) {
+    constexpr int P = decltype(slot)::value;
+    if (P < nu) load_unit(slot, P);
+  };
+  [&]<int... P>(std::integer_sequence<int, P...>) {
+    (prefetch(std::integral_constant<int, P>()), ...);
+  }(std::make_integer_sequence<int, PF>());
 
   // ---- stage A: exponent bands as fp16, permuted for the B operands
   {
@@ -278,10 +293,7 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
     }
   }
   __syncthreads();
-  if (nu <= 0) {
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    return;
-  }
+  if (nu <= 0) return;
 
   // B-operand rows of this lane (MMA column r0 of each block = band r0 % 2 of row r0 / 2),
   // or the zero row
@@ -304,153 +316,126 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
   auto zhi_of = [&](uint32_t zw) -> uint32_t {     // fp16(-(64 + z)) in both halves
     return (0xD400u | (((zw >> (4 * r0)) & 0xFu) << 4)) * 0x00010001u;
   };
-  auto sc_at = [&](int slot, int gi, int row) -> float {   // scale of (unit slot, group, row)
-    // each (unit slot, group) owns 64 bytes: 16 scales of ES bytes
-    const char *b = reinterpret_cast<const char *>(sring) + (slot * GPU + gi) * 64 + row * ES;
-    if (SC == kScF32) return *reinterpret_cast<const float *>(b);
-    const unsigned short v = *reinterpret_cast<const unsigned short *>(b);
-    if (SC == kScBF16) return __uint_as_float((uint32_t)v << 16);
-    return __half2float(__ushort_as_half(v));
+  auto scale_f = [&](uint32_t bits) -> float {
+    if (SC == kScF32) return __uint_as_float(bits);
+    if (SC == kScBF16) return __uint_as_float(bits << 16);
+    return __half2float(__ushort_as_half((unsigned short)bits));
   };
 
   int t = u0 / Cu, ul = u0 - t * Cu;               // tile and unit being computed
   const int t_first = t;
   int tile_u0 = ul;
-  float acc[MT][4], dacc[2][MT][4];
+  float acc[MT][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[mt][e] = dacc[0][mt][e] = dacc[1][mt][e] = 0.f;
-  float pa = 0.f, pb = 0.f;                        // scales of the group awaiting its promote
-  bool pend = false;
+  for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
-  auto promote = [&](auto parc) {
-    constexpr int PAR = decltype(parc)::value;
+  // one unit from ring slot P; the slot is refilled with unit k + PF first
+  auto step = [&](auto slot, int k) {
+    constexpr int P = decltype(slot)::value;
+    uint4 cur[UCH];
+    uint32_t sv[GPU][2], zw[GPU][2];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      acc[mt][0] = fmaf(pa, dacc[PAR][mt][0], acc[mt][0]);
-      acc[mt][1] = fmaf(pa, dacc[PAR][mt][1], acc[mt][1]);
-      acc[mt][2] = fmaf(pb, dacc[PAR][mt][2], acc[mt][2]);
-      acc[mt][3] = fmaf(pb, dacc[PAR][mt][3], acc[mt][3]);
+    for (int ch = 0; ch < UCH; ++ch) cur[ch] = buf[P][ch];
+#pragma unroll
+    for (int gi = 0; gi < GPU; ++gi) {
+      sv[gi][0] = sr[P][gi][0];
+      sv[gi][1] = sr[P][gi][1];
+      if (ZP) { zw[gi][0] = zr[P][gi][0]; zw[gi][1] = zr[P][gi][1]; }
+    }
+    if (k + PF < nu) load_unit(slot, k + PF);
+
+    uint32_t zl = ZP ? zlo_of(zw[0][0]) : dk.lo_sym, zh = ZP ? zhi_of(zw[0][1]) : dk.hi_sym;
+    float d[MT][4];
+    const uint32_t *bp[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) bp[mt] = brow[mt] + ul * (UCH * 32);
+#pragma unroll
+    for (int ch = 0; ch < UCH; ++ch) {
+      uint32_t bq[MT][8];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const uint4 lo = *reinterpret_cast<const uint4 *>(bp[mt] + ch * 32);
+        const uint4 hi = *reinterpret_cast<const uint4 *>(bp[mt] + ch * 32 + 16);
+        bq[mt][0] = lo.x; bq[mt][1] = lo.y; bq[mt][2] = lo.z; bq[mt][3] = lo.w;
+        bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
+      }
+      const uint32_t words[4] = {cur[ch].x, cur[ch].y, cur[ch].z, cur[ch].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int stp = ch * 4 + j;                   // compile-time
+        const uint32_t w = words[j], w8 = w >> 8;
+        const uint32_t a0 = hsub2_u(lop3_and_or(w, dk.lo_mask, dk.magic), zl);
+        const uint32_t a1 = hfma2_u(lop3_and_or(w, dk.hi_mask, dk.magic), dk.sixteenth, zh);
+        const uint32_t a2 = hsub2_u(lop3_and_or(w8, dk.lo_mask, dk.magic), zl);
+        const uint32_t a3 = hfma2_u(lop3_and_or(w8, dk.hi_mask, dk.magic), dk.sixteenth, zh);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          if (stp % SPG == 0) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.f;
+          mma_16816_f16(d[mt], a0, a1, a2, a3, bq[mt][2 * j], bq[mt][2 * j + 1]);
+        }
+        if ((stp + 1) % SPG == 0) {                // a whole group: scale it in
+          const int gi = stp / SPG;
+          const float fa = scale_f(sv[gi][0]), fb = scale_f(sv[gi][1]);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            acc[mt][0] = fmaf(fa, d[mt][0], acc[mt][0]);
+            acc[mt][1] = fmaf(fa, d[mt][1], acc[mt][1]);
+            acc[mt][2] = fmaf(fb, d[mt][2], acc[mt][2]);
+            acc[mt][3] = fmaf(fb, d[mt][3], acc[mt][3]);
+          }
+          if (ZP && gi + 1 < GPU) {
+            zl = zlo_of(zw[gi + 1 < GPU ? gi + 1 : 0][0]);
+            zh = zhi_of(zw[gi + 1 < GPU ? gi + 1 : 0][1]);
+          }
+        }
+      }
+    }
+
+    // end of a tile, or of the stripe: combine the bands, then store or fix up
+    ++ul;
+    if (ul == Cu || k + 1 == nu) {
+      const bool whole = (tile_u0 == 0 && ul == Cu);
+      float *pp = part + ((size_t)gw * 2 + (t == t_first ? 0 : 1)) * (kTileN * 8);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        // lane (r0, q) holds columns 2q, 2q + 1 (both bands of row mt * 4 + q) of rows
+        // n0 = r0 and r0 + 8
+        const int mrow = mt * 4 + q;
+        const int emax = mrow < M ? s_emax[mrow] : 127;
+        const float v0 = ldexpf(acc[mt][0], emax - 142) + ldexpf(acc[mt][1], emax - 174);
+        const float v1 = ldexpf(acc[mt][2], emax - 142) + ldexpf(acc[mt][3], emax - 174);
+        if (mrow < M) {
+          if (whole) {
+            const int n0 = t * kTileN + r0;
+            if (n0 < N) store_out_rt(out, (size_t)mrow * N + n0, v0, out_f32 != 0);
+            if (n0 + 8 < N) store_out_rt(out, (size_t)mrow * N + n0 + 8, v1, out_f32 != 0);
+          } else {
+            pp[mrow * kTileN + r0] = v0;
+            pp[mrow * kTileN + r0 + 8] = v1;
+          }
+        }
+        acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      }
+      if (!whole)
+        stripe_fixup(0.f, 0.f, 0, false, part, counters, out, M, N, t, t == t_first ? 0 : 1,
+                     gw, ul - tile_u0, Cu, U, W, out_f32 != 0);
+      if (ul == Cu) { ul = 0; ++t; tile_u0 = 0; }
     }
   };
 
-  for (int ub = 0; ub < nu; ub += RU) {
-#pragma unroll
-    for (int p = 0; p < RU; ++p) {
-      const int uu = ub + p;
-      if (uu >= nu) break;
-      const int sslot = uu & (SRU - 1);
-      uint32_t zl = 0x64086408u, zh = 0xD480D480u;   // symmetric: z = 8
-#pragma unroll
-      for (int ch = 0; ch < UCH; ++ch) {
-        const int slot = p * UCH + ch;               // compile-time ring slot
-        const int c = uu * UCH + ch;
-        issue_chunk(c + kStages - 1, (slot + kStages - 1) % kStages);
-        asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
-        __syncwarp();
-        if (ch == 0 && ZP) {
-          zl = zlo_of(zring[(sslot * GPU) * 2 + 0]);
-          zh = zhi_of(zring[(sslot * GPU) * 2 + 1]);
-        }
-        const uint4 cw = *reinterpret_cast<const uint4 *>(
-            reinterpret_cast<const char *>(wring) + (size_t)slot * 512 + lane * 16);
-        uint32_t bq[MT][8];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t *ap = brow[mt] + (ul * UCH + ch) * 32;
-          const uint4 lo = *reinterpret_cast<const uint4 *>(ap);
-          const uint4 hi = *reinterpret_cast<const uint4 *>(ap + 16);
-          bq[mt][0] = lo.x; bq[mt][1] = lo.y; bq[mt][2] = lo.z; bq[mt][3] = lo.w;
-          bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
-        }
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int stp = ch * 4 + j;                 // compile-time
-          const int gi = stp / SPG;
-          constexpr int dummy = 0;
-          (void)dummy;
-          const uint32_t w = words[j], w8 = w >> 8;
-          const uint32_t a0 = hsub2_u((w & 0x000F000Fu) | 0x64006400u, zl);
-          const uint32_t a1 = hfma2_u((w & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, zh);
-          const uint32_t a2 = hsub2_u((w8 & 0x000F000Fu) | 0x64006400u, zl);
-          const uint32_t a3 = hfma2_u((w8 & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, zh);
-          if ((p * GPU + gi) & 1) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              if (stp % SPG == 0) dacc[1][mt][0] = dacc[1][mt][1] = dacc[1][mt][2] = dacc[1][mt][3] = 0.f;
-              mma_16816_f16(dacc[1][mt], a0, a1, a2, a3, bq[mt][2 * j], bq[mt][2 * j + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              if (stp % SPG == 0) dacc[0][mt][0] = dacc[0][mt][1] = dacc[0][mt][2] = dacc[0][mt][3] = 0.f;
-              mma_16816_f16(dacc[0][mt], a0, a1, a2, a3, bq[mt][2 * j], bq[mt][2 * j + 1]);
-            }
-          }
-          if ((stp + 1) % SPG == 0) {              // group done: scale in the previous one
-            const float na = sc_at(sslot, gi, r0), nb = sc_at(sslot, gi, r0 + 8);
-            if (pend) {
-              if ((p * GPU + gi) & 1) promote(std::integral_constant<int, 0>());
-              else promote(std::integral_constant<int, 1>());
-            }
-            pa = na;
-            pb = nb;
-            pend = true;
-            if (ZP && gi + 1 < GPU) {
-              zl = zlo_of(zring[(sslot * GPU + (gi + 1 < GPU ? gi + 1 : 0)) * 2 + 0]);
-              zh = zhi_of(zring[(sslot * GPU + (gi + 1 < GPU ? gi + 1 : 0)) * 2 + 1]);
-            }
-          }
-        }
-      }
-
-      // end of a tile, or of the stripe: combine the bands, then store or fix up
-      ++ul;
-      const bool stripe_end = (uu + 1 == nu);
-      if (ul == Cu || stripe_end) {
-        if ((p * GPU + GPU - 1) & 1) promote(std::integral_constant<int, 1>());   // last group
-        else promote(std::integral_constant<int, 0>());
-        pend = false;
-        float *pp = part + ((size_t)gw * 2 + (t == t_first ? 0 : 1)) * (kTileN * 8);
-        const bool whole = (tile_u0 == 0 && ul == Cu);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          // lane (r0, q) holds columns 2q, 2q + 1 (both bands of row mt * 4 + q) of rows
-          // n0 = r0 and r0 + 8
-          const int mrow = mt * 4 + q;
-          const int emax = mrow < M ? s_emax[mrow] : 127;
-          const float v0 = ldexpf(acc[mt][0], emax - 142) + ldexpf(acc[mt][1], emax - 174);
-          const float v1 = ldexpf(acc[mt][2], emax - 142) + ldexpf(acc[mt][3], emax - 174);
-          if (mrow < M) {
-            if (whole) {
-              const int n0 = t * kTileN + r0;
-              if (n0 < N) store_out_rt(out, (size_t)mrow * N + n0, v0, out_f32 != 0);
-              if (n0 + 8 < N) store_out_rt(out, (size_t)mrow * N + n0 + 8, v1, out_f32 != 0);
-            } else {
-              pp[mrow * kTileN + r0] = v0;
-              pp[mrow * kTileN + r0 + 8] = v1;
-            }
-          }
-          acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-        }
-        if (!whole)
-          stripe_fixup(0.f, 0.f, 0, false, part, counters, out, M, N, t,
-                       t == t_first ? 0 : 1, gw, ul - tile_u0, Cu, U, W, out_f32 != 0);
-        if (ul == Cu) { ul = 0; ++t; tile_u0 = 0; }
-      }
-    }
+  for (int k0 = 0; k0 < nu; k0 += PF) {
+    [&]<int... P>(std::integer_sequence<int, P...>) {
+      ((k0 + P < nu ? (step(std::integral_constant<int, P>(), k0 + P), 0) : 0), ...);
+    }(std::make_integer_sequence<int, PF>());
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-template <int G, int SC, bool ZP, int MT>
+template <int G, int SC, bool ZP, int MT, int UG>
 static cudaError_t launch_stripe_t(const Plan &p, int prec, int M, int K, int N,
                                    const void *A, const void *Wq, const void *scales,
                                    const void *zeros, void *out, float *part,
                                    unsigned *counters, cudaStream_t s) {
-  auto kern = w4_stripe_kernel<G, SC, ZP, MT>;
+  auto kern = w4_stripe_kernel<G, SC, ZP, MT, UG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
   if (e != cudaSuccess) return e;
@@ -470,16 +455,36 @@ static cudaError_t launch_stripe_t(const Plan &p, int prec, int M, int K, int N,
   return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4 *>(Wq),
                             reinterpret_cast<const uint16_t *>(A), scales,
                             reinterpret_cast<const uint32_t *>(zeros), out, part, counters,
-                            M, K, N, p.nsplit, out_f32);
+                            M, K, N, p.nsplit, out_f32,
+                            DecodeConsts{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x2C002C00u,
+                                         0x64086408u, 0xD480D480u});
 }
 
-template <int G, int SC, bool ZP>
+// units of two groups when K allows it (G = 64, 128), one group otherwise
+int stripe_unit_groups(int K, int G) {
+  const int base = G > kChunkK ? G : kChunkK;
+  return ((G == 64 || G == 128) && K % (2 * base) == 0) ? 2 : 1;
+}
+
+template <int G, int SC, bool ZP, int UG>
 static cudaError_t launch_stripe_m(const Plan &p, int prec, int M, int K, int N,
                                    const void *A, const void *Wq, const void *scales,
                                    const void *zeros, void *out, float *part, unsigned *cnt,
                                    cudaStream_t s) {
-  if (M <= 4) return launch_stripe_t<G, SC, ZP, 1>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  return launch_stripe_t<G, SC, ZP, 2>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+  if (M <= 4) return launch_stripe_t<G, SC, ZP, 1, UG>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+  return launch_stripe_t<G, SC, ZP, 2, UG>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+}
+
+template <int G, int SC, bool ZP>
+static cudaError_t launch_stripe_u(const Plan &p, int prec, int M, int K, int N,
+                                   const void *A, const void *Wq, const void *scales,
+                                   const void *zeros, void *out, float *part, unsigned *cnt,
+                                   cudaStream_t s) {
+  if constexpr (G == 64 || G == 128) {
+    if (stripe_unit_groups(K, G) == 2)
+      return launch_stripe_m<G, SC, ZP, 2>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+  }
+  return launch_stripe_m<G, SC, ZP, 1>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
 }
 
 template <int G, int SC>
@@ -488,8 +493,8 @@ static cudaError_t launch_stripe_z(const Plan &p, int prec, int M, int K, int N,
                                    const void *zeros, void *out, float *part, unsigned *cnt,
                                    cudaStream_t s) {
   if (prec & GQ_ZP)
-    return launch_stripe_m<G, SC, true>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  return launch_stripe_m<G, SC, false>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+    return launch_stripe_u<G, SC, true>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+  return launch_stripe_u<G, SC, false>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
 }
 
 template <int G>
@@ -505,13 +510,10 @@ static cudaError_t launch_stripe_g(const Plan &p, int prec, int M, int K, int N,
 }
 
 size_t stripe_smem_bytes(int M, int K, int G, int prec) {
-  const int UK = G > kChunkK ? G : kChunkK;
-  const int RU = kStages / (UK / kChunkK);
-  const int GPU = UK / G;
-  const size_t ring = (size_t)kStrWarps * (kStages * 128 + 2 * RU * GPU * 18) * 4;
-  const size_t bands = (size_t)(1 + 2 * M) * (K / kChunkK * 32 + 16) * 4;
+  (void)G;
   (void)prec;
-  return ring + bands + (size_t)M * K * 2;
+  const size_t bands = (size_t)(1 + 2 * M) * (K / kChunkK * 32 + 16) * 4;
+  return bands + (size_t)M * K * 2;
 }
 
 cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int prec,
