@@ -304,7 +304,7 @@ def main():
     if not args.no_prefill and rank == 0:
         prefill = _prefill(gq, torch, dev, peaks, peak_kind)
 
-    traffic = _kernel_traffic("gq_decode.cu", "w4_stripe_decode_decode_gateup.md")
+    traffic = _kernel_traffic("gq_stripe.cu", "w4_stripe_decode_decode_gateup.md")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -393,12 +393,28 @@ def _prefill(gq, torch, dev, peaks, peak_kind):
                       [S.data_ptr()], None, out.data_ptr(), warmup=3, iters=10,
                       use_graph=False, stream=torch.cuda.current_stream().cuda_stream)
     us = res["us_per_call"]
-    tflops = gemm_flops(cfg.M, cfg.K, cfg.N) / (us * 1e-6) / 1e12
+    flops = gemm_flops(cfg.M, cfg.K, cfg.N)
+    tflops = flops / (us * 1e-6) / 1e12
     plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    # context: the same product as a dense BF16 GEMM in cuBLAS (weights already BF16)
+    Wd = torch.randn(cfg.N, cfg.K, device=dev).to(torch.bfloat16)
+    Ad = torch.randn(cfg.M, cfg.K, device=dev).to(torch.bfloat16)
+    for _ in range(3):
+        torch.matmul(Ad, Wd.t())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(10):
+        torch.matmul(Ad, Wd.t())
+    e1.record()
+    torch.cuda.synchronize()
+    cublas_us = e0.elapsed_time(e1) * 100.0
+    del Wd, Ad
     return {"workload": "prefill: M=4096 K=4096 N=14336 G=128 W4A16 sym", "us": us,
             "tflops": tflops, "peak_tflops": peaks["bf16_tflops"],
             "frac": tflops / peaks["bf16_tflops"], "peak_source": f"bf16_tflops of {peak_kind}",
-            "path": plan["path"]}
+            "path": plan["path"], "cublas_bf16_dense_us": cublas_us,
+            "cublas_bf16_dense_tflops": flops / (cublas_us * 1e-6) / 1e12}
 
 
 if __name__ == "__main__":

@@ -57,22 +57,30 @@ _SIGS = {
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
     "gq_device_error": [_i],
     "gq_status_string": [_i],
+    "gq_last_error_detail": [],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
-    _f.restype = ctypes.c_char_p if _name == "gq_status_string" else _i
+    _f.restype = ctypes.c_char_p if _name in ("gq_status_string", "gq_last_error_detail") else _i
 
 EXPORTED = tuple(_SIGS)
 
 
 def _check(st: int, what: str) -> None:
     if st != GQ_OK:
-        raise GqError(st, f"{what}: {_lib.gq_status_string(st).decode()}")
+        msg = f"{what}: {_lib.gq_status_string(st).decode()}"
+        if st == 5:
+            msg += f" ({_lib.gq_last_error_detail().decode()})"
+        raise GqError(st, msg)
 
 
 def gq_status_string(status: int) -> str:
     return _lib.gq_status_string(status).decode()
+
+
+def gq_last_error_detail() -> str:
+    return _lib.gq_last_error_detail().decode()
 
 
 def gq_packed_bytes(K: int, N: int, G: int, prec: int) -> int:

@@ -69,7 +69,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 logs.append(f.result())
     if jobs or not os.path.exists(LIB):
         tmp = LIB + ".tmp"
-        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr}")

@@ -4,6 +4,8 @@
 #include <string.h>
 #include <vector>
 
+#include <cstdio>
+
 #include "gq_internal.h"
 
 namespace gq {
@@ -92,6 +94,22 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     if ((size_t)ceil_div(Nc, kTileN) * sizeof(unsigned) > kCounterRegionBytes)
       return GQ_ERR_UNSUPPORTED;
     p->workspace_bytes = p->part_bytes + p->counter_bytes;
+    return GQ_OK;
+  }
+  if (M >= kPrefillMinM && prefill_supported(M, K, N, G, prec)) {
+    // large M: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
+    p->path = kPathPrefill;
+    p->m_tile = 256;
+    p->n_tile = 128;
+    p->unit_k = G;
+    p->units = K / G;
+    const int tiles = ceil_div(N, 128) * ceil_div(M, 256);
+    p->grid_x = tiles < sms ? tiles : sms;
+    p->grid_y = p->grid_z = 1;
+    p->nsplit = 1;
+    p->block_threads = 320;
+    p->smem_bytes = prefill_smem_bytes();
+    p->workspace_bytes = 0;
     return GQ_OK;
   }
   if (prec & GQ_W4) {
@@ -190,11 +208,21 @@ static int get_scratch(size_t need, void **out) {
   return GQ_OK;
 }
 
+static thread_local char g_detail[160];
+void note_cuda_error(const char *where, cudaError_t e) {
+  snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorName(e));
+}
+void note_cuda_error_code(const char *where, int code) {
+  snprintf(g_detail, sizeof(g_detail), "%s: error %d", where, code);
+}
+
 }  // namespace gq
 
 using namespace gq;
 
 extern "C" {
+
+const char *gq_last_error_detail(void) { return gq::g_detail; }
 
 const char *gq_status_string(int status) {
   switch (status) {
@@ -326,13 +354,19 @@ static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const 
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  if (p.path == kPathStripe)
+  if (p.path == kPathPrefill)
+    e = launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
+  else if (p.path == kPathStripe)
     e = launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else if (p.path == kPathMmaDecode)
     e = launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else
     e = launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
-  if (e != cudaSuccess) { cudaGetLastError(); return GQ_ERR_CUDA; }
+  if (e != cudaSuccess) {
+    note_cuda_error("launch", e);
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
   return GQ_OK;
 }
 
@@ -396,8 +430,8 @@ int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
 }
 
 int gq_device_error(int clear) {
-  (void)clear;
-  return GQ_OK;
+  const int v = prefill_read_error(clear);
+  return v;
 }
 
 }  // extern "C"

@@ -69,6 +69,18 @@ cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int 
                                 const void *A, const void *Wq, const void *scales,
                                 const void *zeros, void *out, float *part,
                                 unsigned *counters, cudaStream_t s);
+size_t prefill_smem_bytes();
+bool prefill_supported(int M, int K, int N, int G, int prec);
+cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                           const void *Wq, const void *scales, const void *zeros, void *out,
+                           cudaStream_t s);
+int prefill_read_error(int clear);
+
+// Records why a call is about to return GQ_ERR_CUDA (thread-local; read by gq_last_error_detail).
+void note_cuda_error(const char *where, cudaError_t e);
+void note_cuda_error_code(const char *where, int code);
+// smallest M routed to the tensor-core prefill kernel
+constexpr int kPrefillMinM = 128;
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,
                              void *out, float *part, unsigned *counters, cudaStream_t s);

@@ -1,0 +1,570 @@
+// Large-M ("prefill") kernel of the group-quantized weight-only GEMM: TMA + tcgen05 + TMEM.
+//
+// Where the path is a dense contraction ("GPU Kernel 工程（09）：量化与融合 kernel", section 3.2:
+// at prefill both BF16 and INT4 GEMMs are compute-bound), the dequantized weights feed the
+// 5th-generation tensor cores.  Roles inside one persistent CTA per SM:
+//   warp 0      TMA producer: per 64-k stage, the packed codes of a 128-column tile (one
+//               3-D box of 8 x 512 bytes) and the 256 x 64 bf16 activation tile (128-byte
+//               swizzle) into a 4-stage shared-memory ring.
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
+//               M = 128 (weight columns n) x N = 256 (activation rows m) x K = 16, BF16 x
+//               BF16 -> FP32, into one of two TMEM accumulators (one per group parity).
+//   warps 2-9   workers: dequantize the next group's stages into the UMMA operand layout
+//               (K-major, 128-byte swizzle) and scale the finished group into FP32 running
+//               sums (tcgen05.ld; one scale per thread: a TMEM lane is one column n).
+// The operand tiles hold the exact integers q - z (bf16 represents |q - z| <= 15 exactly);
+// each group's FP32 result is multiplied by its scale after the whole group, as the
+// group-wise GEMM of "04 · 分组量化 GEMM 内核", section 2 requires.  Rounding s * (q - z) to
+// bf16 inside the operand would change the result by far more than the output's rounding.
+//
+// Every mbarrier wait is bounded; a wait that gives up records GQ_ERR_TIMEOUT in a device
+// error word, every role then leaves its loop, and TMEM is released before the CTA exits.
+#include <atomic>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gq_internal.h"
+
+namespace gq {
+
+constexpr int kPfStages = 4;                 // pipeline depth (64-k stages)
+constexpr int kPfTileN = 128;                // weight columns per tile (TMEM lanes)
+constexpr int kPfTileM = 256;                // activation rows per tile (TMEM columns)
+constexpr int kPfThreads = 320;              // 10 warps
+constexpr uint32_t kPfPackedBytes = 8 * 512;                  // packed codes per stage
+constexpr uint32_t kPfActBytes = kPfTileM * 64 * 2;           // activations per stage
+constexpr uint32_t kPfDqBytes = kPfTileN * 64 * 2;            // dequantized weights per stage
+constexpr uint32_t kPfStageBytes = kPfActBytes + kPfDqBytes + kPfPackedBytes;   // 53248
+constexpr long long kPfWaitCycles = 4000000000ll;              // bounded waits (~2 s)
+
+static __device__ int g_prefill_error;        // sticky status (GQ_ERR_TIMEOUT), read by the host
+static __device__ unsigned g_prefill_abort;     // token of the launch that gave up
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+// Wait for the phase of parity `parity` to complete.  Bounded: gives up (false) once another
+// role of the same launch gave up, or after kPfWaitCycles SM clock cycles (about two
+// seconds), recording GQ_ERR_TIMEOUT (sticky) and this launch's token.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned token) {
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255u) == 0u) {
+      if (*(volatile unsigned *)&g_prefill_abort == token) return false;   // this launch gave up
+      if (clock64() - t0 > kPfWaitCycles) {
+        atomicExch(&g_prefill_abort, token);
+        atomicExch(&g_prefill_error, GQ_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// UMMA shared-memory descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
+// apart (stride byte offset), leading byte offset unused for swizzled K-major (1).
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= (uint64_t)1 << 16;                          // leading byte offset (unused)
+  d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset
+  d |= (uint64_t)1 << 46;                          // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t lop3_ao(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+struct PrefillConsts {
+  uint32_t lo_mask;   // 0x000F000F
+  uint32_t magic;     // 0x43004300: bf16 128 in both halves
+  uint32_t sym;       // 0x43084308: bf16 (128 + 8)
+};
+
+// ------------------------------------------------------------------ the kernel
+
+template <int SPG, int SC, bool ZP>
+__global__ void __launch_bounds__(kPfThreads, 1)
+w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_a,
+                  const void *__restrict__ scales, const uint32_t *__restrict__ zeros,
+                  __nv_bfloat16 *__restrict__ out_bf16, float *__restrict__ out_f32,
+                  int M, int K, int N, int out_f32_flag, const PrefillConsts pc,
+                  unsigned token) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kPfStages], bar_empty[kPfStages],
+      bar_dq[kPfStages], bar_acc_full[2], bar_acc_empty[2];
+  __shared__ uint32_t s_tmem;
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // stage layout: [activations 32 KB][dequantized weights 16 KB][packed codes 4 KB]
+  auto act_at = [&](int s) { return smem + (size_t)s * kPfStageBytes; };
+  auto dq_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes; };
+  auto pk_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes + kPfDqBytes; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = K / (SPG * 64);                   // groups (K / G)
+  const int tiles_n = (N + kPfTileN - 1) / kPfTileN;
+  const int tiles_m = (M + kPfTileM - 1) / kPfTileM;
+  const int tiles = tiles_n * tiles_m;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+      mbar_init(smem_u32(&bar_dq[s]), 256);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_acc_full[b]), 1);
+      mbar_init(smem_u32(&bar_acc_empty[b]), 256);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {   // TMEM: two accumulators of 256 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                     smem_u32(&s_tmem))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_w) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
+      uint32_t i = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        const int tn = tile % tiles_n, tm = tile / tiles_n;
+        for (int kc = 0; kc < K / 64 && ok; ++kc, ++i) {
+          const int s = i % kPfStages;
+          ok = mbar_wait(smem_u32(&bar_empty[s]), ((i / kPfStages) & 1) ^ 1, token);
+          if (!ok) break;
+          const uint32_t fb = smem_u32(&bar_full[s]);
+          mbar_expect_tx(fb, kPfActBytes + kPfPackedBytes);
+          tma_load_3d(smem_u32(pk_at(s)), &map_w, fb, 0, kc, tn * 8);
+          tma_load_2d(smem_u32(act_at(s)), &map_a, fb, kc * 64, tm * kPfTileM);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kPfTileN, kPfTileM);
+      uint32_t i = 0, gg = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        for (int g = 0; g < ng && ok; ++g, ++gg) {
+          const int b = gg & 1;
+          ok = mbar_wait(smem_u32(&bar_acc_empty[b]), ((gg >> 1) & 1) ^ 1, token);
+          if (!ok) break;
+          tc_fence_after();
+          for (int st = 0; st < SPG; ++st, ++i) {
+            const int s = i % kPfStages;
+            const uint32_t ph = (i / kPfStages) & 1;
+            ok = mbar_wait(smem_u32(&bar_full[s]), ph, token) && mbar_wait(smem_u32(&bar_dq[s]), ph, token);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t da = umma_desc_sw128(smem_u32(dq_at(s)));
+            const uint64_t db = umma_desc_sw128(smem_u32(act_at(s)));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)   // 16 k per MMA: advance 32 bytes = 2 descriptor units
+              umma_bf16(tmem + (uint32_t)b * kPfTileM, da + 2 * k, db + 2 * k, idesc,
+                        (st | k) != 0 ? 1u : 0u);
+            umma_commit(smem_u32(&bar_empty[s]));        // stage consumed
+          }
+          if (!ok) break;
+          umma_commit(smem_u32(&bar_acc_full[b]));       // group finished
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- workers
+    const int wk = warp - 2;                       // 0..7
+    const int lq = warp & 3;                       // TMEM lane quarter this warp may access
+    const int half = wk >> 2;                      // activation-row half of the tile
+    const int row = lq * 32 + lane;                // TMEM lane = weight column within the tile
+    const int NW = N >> 3;
+    // dequantization: worker wk owns the 16-column sub-tile wk of every stage, lane `lane`
+    // its 16-byte fragment: rows r0 = lane / 4 and r0 + 8, k = 16j + 2(lane % 4) + 8h + {0,1}
+    const int r0 = lane >> 2, qq = lane & 3;
+    float sum[128];
+    uint32_t i_dq = 0;                             // next stage to dequantize
+    uint32_t gg = 0;                               // next group to promote
+    bool ok = true;
+
+    auto dequant_stage = [&](int tn, int kc) -> bool {
+      const int s = i_dq % kPfStages;
+      const uint32_t ph = (i_dq / kPfStages) & 1;
+      // the dequantized slot was read by the MMA of stage i_dq - kPfStages; the codes of
+      // stage i_dq have arrived
+      if (!mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, token)) return false;
+      if (!mbar_wait(smem_u32(&bar_full[s]), ph, token)) return false;
+      uint32_t zlo = pc.sym, zhi = pc.sym;
+      if (ZP) {
+        const int g = kc / SPG;
+        const int n = tn * kPfTileN + wk * 16 + r0;
+        const uint32_t wa = __ldg(zeros + (size_t)g * NW + min(n >> 3, NW - 1));
+        const uint32_t wb = __ldg(zeros + (size_t)g * NW + min((n + 8) >> 3, NW - 1));
+        zlo = (0x4300u | ((wa >> (4 * (n & 7))) & 0xFu)) * 0x00010001u;
+        zhi = (0x4300u | ((wb >> (4 * ((n + 8) & 7))) & 0xFu)) * 0x00010001u;
+      }
+      const uint4 f = *reinterpret_cast<const uint4 *>(pk_at(s) + wk * 512 + lane * 16);
+      const uint32_t words[4] = {f.x, f.y, f.z, f.w};
+      uint8_t *dq = dq_at(s);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {               // pair p: bits 4p and 4p + 16
+          const uint32_t v = bsub2(lop3_ao(words[j] >> (4 * p), pc.lo_mask, pc.magic),
+                                   (p & 1) ? zhi : zlo);
+          const int n = wk * 16 + r0 + 8 * (p & 1);
+          const int k = 16 * j + 2 * qq + 8 * (p >> 1);
+          const uint32_t off = n * 128 + ((((k >> 3) ^ (n & 7)) << 4)) + (k & 7) * 2;
+          *reinterpret_cast<uint32_t *>(dq + off) = v;
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic -> tensor core
+      mbar_arrive(smem_u32(&bar_dq[s]));
+      ++i_dq;
+      return true;
+    };
+
+    // stage sequence of the worker: the tiles of this CTA, 64-k stages in order
+    int dq_tile = blockIdx.x, dq_kc = 0;           // next stage to dequantize
+    auto dequant_next_group = [&]() -> bool {       // SPG stages = one group
+      for (int st = 0; st < SPG; ++st) {
+        if (dq_tile >= tiles) return true;
+        if (!dequant_stage(dq_tile % tiles_n, dq_kc)) return false;
+        if (++dq_kc == K / 64) { dq_kc = 0; dq_tile += gridDim.x; }
+      }
+      return true;
+    };
+    ok = dequant_next_group();                      // group 0 ahead of the loop
+
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      const int tn = tile % tiles_n, tm = tile / tiles_n;
+      const int ncol = min(tn * kPfTileN + row, N - 1);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) sum[c] = 0.f;
+      for (int g = 0; g < ng && ok; ++g, ++gg) {
+        ok = dequant_next_group();                  // keep the tensor core fed
+        if (!ok) break;
+        float sc;
+        if (SC == kScF32)
+          sc = __ldg(reinterpret_cast<const float *>(scales) + (size_t)g * N + ncol);
+        else if (SC == kScBF16)
+          sc = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(scales) +
+                                               (size_t)g * N + ncol)
+                               << 16);
+        else
+          sc = __half2float(__ushort_as_half(
+              __ldg(reinterpret_cast<const unsigned short *>(scales) + (size_t)g * N + ncol)));
+        const int b = gg & 1;
+        ok = mbar_wait(smem_u32(&bar_acc_full[b]), (gg >> 1) & 1, token);
+        ok = __all_sync(0xffffffffu, ok);         // tcgen05.ld below is warp-collective
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)b * kPfTileM +
+                               (uint32_t)half * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          float v[16];
+          tmem_ld16(taddr + c4 * 16, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) sum[c4 * 16 + c] = fmaf(sc, v[c], sum[c4 * 16 + c]);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_acc_empty[b]));
+      }
+      if (!ok) break;
+      // the tile's output: column n = tn * 128 + row, rows m = tm * 256 + half * 128 + c
+      const int n = tn * kPfTileN + row;
+      if (n < N) {
+        const int mb = tm * kPfTileM + half * 128;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {     // fully unrolled: sum[] stays in registers
+          const int m = mb + c;
+          if (m < M) {
+            if (out_f32_flag)
+              out_f32[(size_t)m * N + n] = sum[c];
+            else
+              out_bf16[(size_t)m * N + n] = __float2bfloat16_rn(sum[c]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+// cuTensorMapEncodeTiled is a driver-API call; it is fetched through the runtime so that the
+// library does not link libcuda directly (it then loads on machines without a driver).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (f) return f;
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  f = reinterpret_cast<EncodeTiledFn>(p);
+  fn.store(f);
+  return f;
+}
+
+static int encode_maps(int M, int K, int N, const void *A, const void *Wq, CUtensorMap *mw,
+                       CUtensorMap *ma) {
+  // packed codes as uint32 [tiles][K/64 chunks][128 words]
+  const cuuint64_t wdims[3] = {128, (cuuint64_t)(K / 64), (cuuint64_t)((N + 15) / 16)};
+  const cuuint64_t wstr[2] = {512, (cuuint64_t)(K / 64) * 512};
+  const cuuint32_t wbox[3] = {128, 1, 8};
+  const cuuint32_t ones[3] = {1, 1, 1};
+  const EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    note_cuda_error_code("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1);
+    return GQ_ERR_CUDA;
+  }
+  CUresult r = enc(mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(Wq),
+                                      wdims, wstr, wbox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    note_cuda_error_code("cuTensorMapEncodeTiled(packed codes)", (int)r);
+    return GQ_ERR_CUDA;
+  }
+  // activations bf16 [M][K], 256 rows x 64 k per box, 128-byte swizzle
+  const cuuint64_t adims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t astr[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t abox[2] = {64, (cuuint32_t)kPfTileM};
+  r = enc(ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(A), adims,
+                             astr, abox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    note_cuda_error_code("cuTensorMapEncodeTiled(activations)", (int)r);
+    return GQ_ERR_CUDA;
+  }
+  return GQ_OK;
+}
+
+// per-launch token: a launch that gives up marks only itself
+static unsigned next_token() {
+  static std::atomic<unsigned> t{0};
+  return t.fetch_add(1u) + 1u;
+}
+
+size_t prefill_smem_bytes() { return (size_t)kPfStages * kPfStageBytes + 1024; }
+
+bool prefill_supported(int M, int K, int N, int G, int prec) {
+  if (!(prec & GQ_W4) || (prec & GQ_ACT_F32)) return false;
+  if (!(G == 64 || G == 128 || G == 256)) return false;
+  return M >= 1 && N >= 8 && K % G == 0 && K % 64 == 0;
+}
+
+template <int SPG, int SC, bool ZP>
+static cudaError_t launch_pf(const Plan &p, int M, int K, int N, int prec, const CUtensorMap &mw,
+                             const CUtensorMap &ma, const void *scales, const void *zeros,
+                             void *out, cudaStream_t s) {
+  auto kern = w4_prefill_kernel<SPG, SC, ZP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)p.smem_bytes);
+  if (e != cudaSuccess) {
+    note_cuda_error("cudaFuncSetAttribute(prefill)", e);
+    return e;
+  }
+  const bool f32 = (prec & GQ_OUT_F32) != 0;
+  kern<<<p.grid_x, kPfThreads, p.smem_bytes, s>>>(
+      mw, ma, scales, reinterpret_cast<const uint32_t *>(zeros),
+      f32 ? nullptr : reinterpret_cast<__nv_bfloat16 *>(out), f32 ? reinterpret_cast<float *>(out) : nullptr,
+      M, K, N, f32 ? 1 : 0, PrefillConsts{0x000F000Fu, 0x43004300u, 0x43084308u},
+      next_token());
+  return cudaGetLastError();
+}
+
+template <int SPG, int SC>
+static cudaError_t launch_pf_z(const Plan &p, int M, int K, int N, int prec, const CUtensorMap &mw,
+                               const CUtensorMap &ma, const void *scales, const void *zeros,
+                               void *out, cudaStream_t s) {
+  if (prec & GQ_ZP) return launch_pf<SPG, SC, true>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+  return launch_pf<SPG, SC, false>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+}
+
+template <int SPG>
+static cudaError_t launch_pf_s(const Plan &p, int M, int K, int N, int prec, const CUtensorMap &mw,
+                               const CUtensorMap &ma, const void *scales, const void *zeros,
+                               void *out, cudaStream_t s) {
+  if (prec & GQ_SC_F32) return launch_pf_z<SPG, kScF32>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+  if (prec & GQ_SC_BF16) return launch_pf_z<SPG, kScBF16>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+  return launch_pf_z<SPG, kScF16>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+}
+
+cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                           const void *Wq, const void *scales, const void *zeros, void *out,
+                           cudaStream_t s) {
+  CUtensorMap mw, ma;
+  if (encode_maps(M, K, N, A, Wq, &mw, &ma) != GQ_OK) return cudaErrorInvalidValue;
+  switch (G) {
+    case 64: return launch_pf_s<1>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+    case 128: return launch_pf_s<2>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+    case 256: return launch_pf_s<4>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int prefill_read_error(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  if (clear && v) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_prefill_error, &z, sizeof(int));
+  }
+  return v;
+}
+
+}  // namespace gq

@@ -186,6 +186,11 @@ int gq_device_error(int clear);
 
 const char *gq_status_string(int status);
 
+/* Text describing the last GQ_ERR_CUDA returned on the calling host thread: which CUDA call
+ * failed and its error name (for example "launch: cudaErrorInvalidValue").  Empty if none.
+ * The string is owned by the library and valid until the thread's next failing call. */
+const char *gq_last_error_detail(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -117,6 +117,36 @@ def test_integer_inputs_are_bit_exact(gq, cfg):
         assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
 
 
+# ------------------------------------------------------------------ large M (tcgen05 path)
+
+PREFILL_SHAPES = [
+    gq_synth.Config("pf_base", M=256, K=512, N=256, G=128),
+    gq_synth.Config("pf_ragged", M=300, K=1024, N=392, G=128, zp=True, sc="bf16"),
+    gq_synth.Config("pf_g64_f32", M=128, K=256, N=136, G=64, sc="f32", out="f32"),
+    gq_synth.Config("pf_g256", M=520, K=2048, N=264, G=256, zp=True),
+    gq_synth.Config("pf_tall", M=1100, K=512, N=128, G=128, outlier_frac=0.01),
+]
+
+
+@pytest.mark.parametrize("cfg", PREFILL_SHAPES, ids=lambda c: c.name)
+def test_prefill_shapes(gq, cfg):
+    from group_quantized_weight_gb300.constants import prec_flags
+    plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out))
+    assert plan["path"] == 2
+    _full_case(gq, cfg)
+    assert gq.gq_device_error() == 0
+
+
+def test_prefill_integer_inputs_are_bit_exact(gq):
+    cfg = gq_synth.Config("pf_exact", M=384, K=1024, N=256, G=128, zp=True, a_kind="int",
+                          pow2_scales=True)
+    inp = gq_synth.make_inputs(cfg, seed=2)
+    out, _ = run_gemm(gq, cfg, inp)
+    ref, _ = _oracle(cfg, inp)
+    h = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(h, oracle.f64_to_bf16_bits(ref))
+
+
 # ------------------------------------------------------------------ the workloads
 
 @pytest.mark.parametrize("name", ["tiny_gemv", "decode_gateup", "q8_m1", "q8_m32"])
