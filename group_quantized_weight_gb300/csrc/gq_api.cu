@@ -107,7 +107,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->grid_x = tiles < sms ? tiles : sms;
     p->grid_y = p->grid_z = 1;
     p->nsplit = 1;
-    p->block_threads = 320;
+    p->block_threads = kPrefillThreads;
     p->smem_bytes = prefill_smem_bytes();
     p->workspace_bytes = 0;
     return GQ_OK;

@@ -81,6 +81,7 @@ void note_cuda_error(const char *where, cudaError_t e);
 void note_cuda_error_code(const char *where, int code);
 // smallest M routed to the tensor-core prefill kernel
 constexpr int kPrefillMinM = 128;
+constexpr int kPrefillThreads = 512;   // block size of the prefill kernel
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,
                              void *out, float *part, unsigned *counters, cudaStream_t s);

@@ -32,7 +32,9 @@ namespace gq {
 constexpr int kPfStages = 4;                 // pipeline depth (64-k stages)
 constexpr int kPfTileN = 128;                // weight columns per tile (TMEM lanes)
 constexpr int kPfTileM = 256;                // activation rows per tile (TMEM columns)
-constexpr int kPfThreads = 320;              // 10 warps
+constexpr int kPfThreads = 512;              // 16 warps = 4 warpgroups
+constexpr int kPfDqWarps = 4;                // warpgroup 1
+constexpr int kPfSumWarps = 8;               // warpgroups 2 and 3
 constexpr uint32_t kPfPackedBytes = 8 * 512;                  // packed codes per stage
 constexpr uint32_t kPfActBytes = kPfTileM * 64 * 2;           // activations per stage
 constexpr uint32_t kPfDqBytes = kPfTileN * 64 * 2;            // dequantized weights per stage
@@ -115,6 +117,18 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset
   d |= (uint64_t)1 << 46;                          // descriptor version (sm_100 family)
   d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// UMMA shared-memory descriptor: K-major operand without swizzle, made of 8-row x 16-byte
+// core matrices; `lbo` = bytes between core matrices adjacent in K, `sbo` = bytes between
+// 8-row groups.
+__device__ __forceinline__ uint64_t umma_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;                          // descriptor version; swizzle field 0 = none
   return d;
 }
 
@@ -220,6 +234,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   auto pk_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes + kPfDqBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wg = warp >> 2;                        // warpgroup: role and register budget
   const int ng = K / (SPG * 64);                   // groups (K / G)
   const int tiles_n = (N + kPfTileN - 1) / kPfTileN;
   const int tiles_m = (M + kPfTileM - 1) / kPfTileM;
@@ -229,11 +244,11 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
       mbar_init(smem_u32(&bar_empty[s]), 1);
-      mbar_init(smem_u32(&bar_dq[s]), 256);
+      mbar_init(smem_u32(&bar_dq[s]), kPfDqWarps);        // one arrival per dequant warp
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_acc_full[b]), 1);
-      mbar_init(smem_u32(&bar_acc_empty[b]), 256);
+      mbar_init(smem_u32(&bar_acc_empty[b]), kPfSumWarps);  // one per promotion warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -248,7 +263,12 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == 0) {
+  // Register budgets per warpgroup (launched with kPfThreads x 128 = 65,536): roles 56,
+  // dequantization 88, promotion 176 each for two warpgroups; 7,168 + 11,264 + 2 x 22,528 =
+  // 63,488 registers in total, within the launch's 65,536.
+  if (wg == 0) {
+   asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_w) : "memory");
@@ -269,7 +289,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kPfTileN, kPfTileM);
@@ -287,11 +307,13 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             ok = mbar_wait(smem_u32(&bar_full[s]), ph, token) && mbar_wait(smem_u32(&bar_dq[s]), ph, token);
             if (!ok) break;
             tc_fence_after();
-            const uint64_t da = umma_desc_sw128(smem_u32(dq_at(s)));
+            // weights: core matrices, 16 k = two of them = 256 bytes = 16 descriptor units;
+            // activations: 128-byte swizzle, 16 k = 32 bytes = 2 descriptor units
+            const uint64_t da = umma_desc_plain(smem_u32(dq_at(s)), 128, 1024);
             const uint64_t db = umma_desc_sw128(smem_u32(act_at(s)));
 #pragma unroll
-            for (int k = 0; k < 4; ++k)   // 16 k per MMA: advance 32 bytes = 2 descriptor units
-              umma_bf16(tmem + (uint32_t)b * kPfTileM, da + 2 * k, db + 2 * k, idesc,
+            for (int k = 0; k < 4; ++k)
+              umma_bf16(tmem + (uint32_t)b * kPfTileM, da + 16 * k, db + 2 * k, idesc,
                         (st | k) != 0 ? 1u : 0u);
             umma_commit(smem_u32(&bar_empty[s]));        // stage consumed
           }
@@ -301,88 +323,95 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
       }
     }
     __syncwarp();
-  } else {
-    // ---------------------------------------------------------------- workers
-    const int wk = warp - 2;                       // 0..7
-    const int lq = warp & 3;                       // TMEM lane quarter this warp may access
-    const int half = wk >> 2;                      // activation-row half of the tile
-    const int row = lq * 32 + lane;                // TMEM lane = weight column within the tile
+   }
+  } else if (wg == 1) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    // ---------------------------------------------------------------- dequantization
+    // Warp d of the warpgroup owns 16-column sub-tiles 2d and 2d + 1 of every stage; lane
+    // `lane` holds the 16-byte fragment of each: rows r0 = lane / 4 and r0 + 8 of the
+    // sub-tile, k = 16j + 2(lane % 4) + 8h + {0,1}.  The dequantized operand is K-major core
+    // matrices (8 rows x 16 bytes), core matrix (8-row group rg, 8-k group kg) at
+    // rg * 1024 + kg * 128; pair p of word j of a fragment is core matrix
+    // (2 sub + (p & 1), 2j + (p >> 1)), byte 16 r0 + 4 (lane % 4) = 4 lane inside it.
+    const int d = warp & 3;
+    const int r0 = lane >> 2;
     const int NW = N >> 3;
-    // dequantization: worker wk owns the 16-column sub-tile wk of every stage, lane `lane`
-    // its 16-byte fragment: rows r0 = lane / 4 and r0 + 8, k = 16j + 2(lane % 4) + 8h + {0,1}
-    const int r0 = lane >> 2, qq = lane & 3;
-    float sum[128];
-    uint32_t i_dq = 0;                             // next stage to dequantize
-    uint32_t gg = 0;                               // next group to promote
+    uint32_t i = 0;
     bool ok = true;
-
-    auto dequant_stage = [&](int tn, int kc) -> bool {
-      const int s = i_dq % kPfStages;
-      const uint32_t ph = (i_dq / kPfStages) & 1;
-      // the dequantized slot was read by the MMA of stage i_dq - kPfStages; the codes of
-      // stage i_dq have arrived
-      if (!mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, token)) return false;
-      if (!mbar_wait(smem_u32(&bar_full[s]), ph, token)) return false;
-      uint32_t zlo = pc.sym, zhi = pc.sym;
-      if (ZP) {
-        const int g = kc / SPG;
-        const int n = tn * kPfTileN + wk * 16 + r0;
-        const uint32_t wa = __ldg(zeros + (size_t)g * NW + min(n >> 3, NW - 1));
-        const uint32_t wb = __ldg(zeros + (size_t)g * NW + min((n + 8) >> 3, NW - 1));
-        zlo = (0x4300u | ((wa >> (4 * (n & 7))) & 0xFu)) * 0x00010001u;
-        zhi = (0x4300u | ((wb >> (4 * ((n + 8) & 7))) & 0xFu)) * 0x00010001u;
-      }
-      const uint4 f = *reinterpret_cast<const uint4 *>(pk_at(s) + wk * 512 + lane * 16);
-      const uint32_t words[4] = {f.x, f.y, f.z, f.w};
-      uint8_t *dq = dq_at(s);
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      const int tn = tile % tiles_n;
+      for (int g = 0; g < ng && ok; ++g) {
+        uint32_t zl[2] = {pc.sym, pc.sym}, zh[2] = {pc.sym, pc.sym};
+        if (ZP) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+          for (int u = 0; u < 2; ++u) {
+            const int n = tn * kPfTileN + (2 * d + u) * 16 + r0;
+            const uint32_t wa = __ldg(zeros + (size_t)g * NW + min(n >> 3, NW - 1));
+            const uint32_t wb = __ldg(zeros + (size_t)g * NW + min((n + 8) >> 3, NW - 1));
+            zl[u] = (0x4300u | ((wa >> (4 * (n & 7))) & 0xFu)) * 0x00010001u;
+            zh[u] = (0x4300u | ((wb >> (4 * ((n + 8) & 7))) & 0xFu)) * 0x00010001u;
+          }
+        }
+        for (int st = 0; st < SPG; ++st, ++i) {
+          const int s = i % kPfStages;
+          const uint32_t ph = (i / kPfStages) & 1;
+          // the slot was read by the MMA of stage i - kPfStages; the codes of stage i arrived
+          ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, token) &&
+               mbar_wait(smem_u32(&bar_full[s]), ph, token);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {               // pair p: bits 4p and 4p + 16
-          const uint32_t v = bsub2(lop3_ao(words[j] >> (4 * p), pc.lo_mask, pc.magic),
-                                   (p & 1) ? zhi : zlo);
-          const int n = wk * 16 + r0 + 8 * (p & 1);
-          const int k = 16 * j + 2 * qq + 8 * (p >> 1);
-          const uint32_t off = n * 128 + ((((k >> 3) ^ (n & 7)) << 4)) + (k & 7) * 2;
-          *reinterpret_cast<uint32_t *>(dq + off) = v;
+          for (int u = 0; u < 2; ++u) {
+            const uint4 f =
+                *reinterpret_cast<const uint4 *>(pk_at(s) + (2 * d + u) * 512 + lane * 16);
+            const uint32_t words[4] = {f.x, f.y, f.z, f.w};
+            uint8_t *dq = dq_at(s) + (2 * d + u) * 2048 + lane * 4;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {        // pair p: bits 4p and 4p + 16
+                const uint32_t v = bsub2(lop3_ao(words[j] >> (4 * p), pc.lo_mask, pc.magic),
+                                         (p & 1) ? zh[u] : zl[u]);
+                *reinterpret_cast<uint32_t *>(dq + (p & 1) * 1024 + (2 * j + (p >> 1)) * 128) = v;
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic -> tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_dq[s]));
         }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic -> tensor core
-      mbar_arrive(smem_u32(&bar_dq[s]));
-      ++i_dq;
-      return true;
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
+    // ---------------------------------------------------------------- promotion, epilogue
+    const int wq = warp - 8;                       // 0..7
+    const int lq = warp & 3;                       // TMEM lane quarter this warp may access
+    const int half = wq >> 2;                      // activation-row half of the tile
+    const int row = lq * 32 + lane;                // TMEM lane = weight column within the tile
+    const bool odd = (lane & 1) != 0;
+    auto load_scale = [&](int ncol, int g) -> float {
+      if (SC == kScF32)
+        return __ldg(reinterpret_cast<const float *>(scales) + (size_t)g * N + ncol);
+      if (SC == kScBF16)
+        return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(scales) +
+                                               (size_t)g * N + ncol)
+                               << 16);
+      return __half2float(__ushort_as_half(
+          __ldg(reinterpret_cast<const unsigned short *>(scales) + (size_t)g * N + ncol)));
     };
-
-    // stage sequence of the worker: the tiles of this CTA, 64-k stages in order
-    int dq_tile = blockIdx.x, dq_kc = 0;           // next stage to dequantize
-    auto dequant_next_group = [&]() -> bool {       // SPG stages = one group
-      for (int st = 0; st < SPG; ++st) {
-        if (dq_tile >= tiles) return true;
-        if (!dequant_stage(dq_tile % tiles_n, dq_kc)) return false;
-        if (++dq_kc == K / 64) { dq_kc = 0; dq_tile += gridDim.x; }
-      }
-      return true;
-    };
-    ok = dequant_next_group();                      // group 0 ahead of the loop
-
+    float sum[128];
+    uint32_t gg = 0;
+    bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       const int tn = tile % tiles_n, tm = tile / tiles_n;
       const int ncol = min(tn * kPfTileN + row, N - 1);
 #pragma unroll
       for (int c = 0; c < 128; ++c) sum[c] = 0.f;
-      for (int g = 0; g < ng && ok; ++g, ++gg) {
-        ok = dequant_next_group();                  // keep the tensor core fed
-        if (!ok) break;
-        float sc;
-        if (SC == kScF32)
-          sc = __ldg(reinterpret_cast<const float *>(scales) + (size_t)g * N + ncol);
-        else if (SC == kScBF16)
-          sc = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(scales) +
-                                               (size_t)g * N + ncol)
-                               << 16);
-        else
-          sc = __half2float(__ushort_as_half(
-              __ldg(reinterpret_cast<const unsigned short *>(scales) + (size_t)g * N + ncol)));
+      float sc_next = load_scale(ncol, 0);
+      for (int g = 0; g < ng; ++g, ++gg) {
+        const float sc = sc_next;
+        if (g + 1 < ng) sc_next = load_scale(ncol, g + 1);   // one group ahead
         const int b = gg & 1;
         ok = mbar_wait(smem_u32(&bar_acc_full[b]), (gg >> 1) & 1, token);
         ok = __all_sync(0xffffffffu, ok);         // tcgen05.ld below is warp-collective
@@ -391,29 +420,38 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         const uint32_t taddr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)b * kPfTileM +
                                (uint32_t)half * 128;
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          float v[16];
-          tmem_ld16(taddr + c4 * 16, v);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float v[32];
+          tmem_ld32(taddr + c4 * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) sum[c4 * 16 + c] = fmaf(sc, v[c], sum[c4 * 16 + c]);
+          for (int c = 0; c < 32; ++c) sum[c4 * 32 + c] = fmaf(sc, v[c], sum[c4 * 32 + c]);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_acc_empty[b]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[b]));
       }
       if (!ok) break;
-      // the tile's output: column n = tn * 128 + row, rows m = tm * 256 + half * 128 + c
+      // the tile's output: column n = tn * 128 + row, rows m = tm * 256 + half * 128 + c.
+      // Lanes pair up (lane, lane ^ 1) to write two adjacent columns per store: for rows
+      // (m, m + 1) the even lane writes row m, columns (n, n + 1), the odd lane row m + 1,
+      // columns (n - 1, n).  N is even, so both columns of a pair are in or out of range.
       const int n = tn * kPfTileN + row;
-      if (n < N) {
-        const int mb = tm * kPfTileM + half * 128;
+      const int mb = tm * kPfTileM + half * 128;
+      const int ncol0 = n - (odd ? 1 : 0);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {     // fully unrolled: sum[] stays in registers
-          const int m = mb + c;
-          if (m < M) {
-            if (out_f32_flag)
-              out_f32[(size_t)m * N + n] = sum[c];
-            else
-              out_bf16[(size_t)m * N + n] = __float2bfloat16_rn(sum[c]);
+      for (int c = 0; c < 128; c += 2) {
+        const float mine_keep = odd ? sum[c + 1] : sum[c];
+        const float mine_send = odd ? sum[c] : sum[c + 1];
+        const float other = __shfl_xor_sync(0xffffffffu, mine_send, 1);
+        const float lo = odd ? other : mine_keep, hi = odd ? mine_keep : other;
+        const int m = mb + c + (odd ? 1 : 0);
+        if (m < M && ncol0 < N) {
+          if (out_f32_flag) {
+            *reinterpret_cast<float2 *>(out_f32 + (size_t)m * N + ncol0) = make_float2(lo, hi);
+          } else {
+            *reinterpret_cast<__nv_bfloat162 *>(out_bf16 + (size_t)m * N + ncol0) =
+                __floats2bfloat162_rn(lo, hi);
           }
         }
       }
