@@ -73,27 +73,41 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const size_t kSmemCap = 96u << 10;   // activation slice budget per CTA (bytes)
   const int Mc = M > 0 ? M : 1;
   const int Nc = N > 0 ? N : 8;
-  const size_t stripe_smem = (prec & GQ_W4) && Mc <= 8 ? stripe_smem_bytes(Mc, K, G, prec) : 0;
-  if ((prec & GQ_W4) && Mc <= 8 && stripe_smem <= (200u << 10)) {   // one CTA per SM
-    // striped persistent decode: one CTA of kStrWarps warps per SM, one stripe per warp
+  // striped persistent decode (M <= 8): one CTA of kStrWarps warps per SM over a
+  // contiguous range of (tile, 256-k slot) pairs; whole tiles per CTA when that keeps the
+  // SMs within 10% of even, else equal slot ranges with a cross-CTA reduction
+  const size_t kStripeSmemCap = 227u * 1024u - 1024u;   // minus the static shared memory
+  const int slots = stripe_supported(Mc, K, G, prec) ? stripe_slots_for(Mc, K, G, prec, kStripeSmemCap) : 0;
+  if (slots >= 2) {
     p->path = kPathStripe;
     p->mt = Mc <= 4 ? 1 : 2;   // MMA blocks
     p->m_tile = 8;
     p->n_tile = kTileN;
-    p->unit_k = (G > kChunkK ? G : kChunkK) * stripe_unit_groups(K, G);
-    p->units = ceil_div(Nc, kTileN) * (K / p->unit_k);
-    int W = sms * kStrWarps;            // one CTA of kStrWarps warps per SM
-    if (W > p->units) W = p->units;
-    p->nsplit = W;
-    p->grid_x = ceil_div(W, kStrWarps);
-    p->grid_y = p->grid_z = 1;
+    p->unit_k = stripe_slot_k();
+    const int T = ceil_div(Nc, kTileN), spt = K / p->unit_k;
+    p->units = T * spt;
+    p->slots = slots;
     p->block_threads = kStrWarps * 32;
-    p->smem_bytes = stripe_smem;
-    p->part_bytes = round_up((size_t)W * 2 * kTileN * 8 * sizeof(float), 256);
-    p->counter_bytes = kCounterRegionBytes;
-    if ((size_t)ceil_div(Nc, kTileN) * sizeof(unsigned) > kCounterRegionBytes)
-      return GQ_ERR_UNSUPPORTED;
-    p->workspace_bytes = p->part_bytes + p->counter_bytes;
+    p->smem_bytes = stripe_smem_bytes(Mc, K, G, prec, slots);
+    p->grid_y = p->grid_z = 1;
+    const int per = ceil_div(T, sms);
+    if (T >= sms && (double)T >= 0.9 * (double)sms * per) {
+      p->grid_x = sms;
+      p->split_count = T;
+      p->split_mult = spt;
+      p->workspace_bytes = 0;
+    } else {
+      int grid = ceil_div(p->units, kStrWarps);
+      if (grid > sms) grid = sms;
+      p->grid_x = grid;
+      p->split_count = p->units;
+      p->split_mult = 1;
+      p->part_bytes = round_up((size_t)grid * 8 * kTileN * sizeof(float), 256);
+      p->counter_bytes = kCounterRegionBytes;
+      if ((size_t)T * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
+      p->workspace_bytes = p->part_bytes + p->counter_bytes;
+    }
+    p->nsplit = p->grid_x;
     return GQ_OK;
   }
   if (M >= kPrefillMinM && prefill_supported(M, K, N, G, prec)) {
@@ -431,7 +445,8 @@ int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
 
 int gq_device_error(int clear) {
   const int v = prefill_read_error(clear);
-  return v;
+  const int w = stripe_read_error(clear);
+  return v != 0 ? v : w;
 }
 
 }  // extern "C"

@@ -44,6 +44,8 @@ struct Plan {
   size_t part_bytes;     // split-K partials
   size_t counter_bytes;  // arrival counters
   size_t workspace_bytes;
+  int split_count, split_mult;   // path 3: CTA c owns slots zsplit(split_count, grid, c) * split_mult
+  int slots;                     // path 3: ring slots per warp
 };
 
 // scale / output type codes used as template parameters
@@ -63,8 +65,10 @@ cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int pre
                               const void *A, const void *Wq, const void *scales,
                               const void *zeros, void *out, float *part,
                               unsigned *counters, cudaStream_t s);
-size_t stripe_smem_bytes(int M, int K, int G, int prec);
-int stripe_unit_groups(int K, int G);
+bool stripe_supported(int M, int K, int G, int prec);
+size_t stripe_smem_bytes(int M, int K, int G, int prec, int slots);
+int stripe_slots_for(int M, int K, int G, int prec, size_t smem_cap);
+int stripe_slot_k();
 cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int prec,
                                 const void *A, const void *Wq, const void *scales,
                                 const void *zeros, void *out, float *part,
@@ -75,6 +79,7 @@ cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, 
                            const void *Wq, const void *scales, const void *zeros, void *out,
                            cudaStream_t s);
 int prefill_read_error(int clear);
+int stripe_read_error(int clear);
 
 // Records why a call is about to return GQ_ERR_CUDA (thread-local; read by gq_last_error_detail).
 void note_cuda_error(const char *where, cudaError_t e);

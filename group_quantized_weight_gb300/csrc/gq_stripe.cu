@@ -1,58 +1,56 @@
 // Striped small-M decode kernel (M <= 8) of the group-quantized weight-only GEMM.
+//
+// Work partition.  The packed weights are a sequence of 16-column tiles, each tile's K
+// contiguous, so the flattened sequence of (tile, slot) pairs — a slot is 256 consecutive k
+// of one tile, 2 KB of codes — is one contiguous byte stream.  CTA c (one per SM) owns a
+// contiguous range of slots and its 16 warps split that range into contiguous sub-ranges
+// (the striped partitioning of "GPU Kernel 工程（09）：量化与融合 kernel", section 3.3 item 4:
+// every SM gets the same amount of work for any shape).  When there are enough tiles the
+// CTA ranges are whole tiles, so no tile is shared between SMs; otherwise they are equal
+// slot ranges and a tile may be shared by neighbouring CTAs.  Every partial sum is a sum of
+// whole scaled groups, combined in a fixed order (warps in order inside a CTA, then CTAs in
+// order), so the result is bitwise reproducible.
+//
+// Streaming.  Each warp owns a ring of S shared-memory slots.  Lane 0 fills a slot with TMA
+// bulk copies (cp.async.bulk, completion counted in bytes on the slot's mbarrier): the
+// slot's 2 KB of packed codes and, per group, the scales of the tile's 16 columns.  A slot
+// is refilled with the slot S ahead as soon as the warp has decoded it.
+//
+// Decode: the FP16 form of the magic-number trick of section 2.4 of the same page, one
+// shift per eight codes: (w & 0x000F000F) | 0x64006400 is fp16(1024 + q) for the codes in
+// bits 0-3 and 16-19, one fp16x2 subtraction of fp16(1024 + z) leaves q - z;
+// (w & 0x00F000F0) | 0x64006400 is fp16(1024 + 16q) for bits 4-7 and 20-23, and one fp16x2
+// FMA with 1/16 and -(64 + z) leaves q - z; w >> 8 exposes the other four codes.  Every
+// value is an exact small integer.
+//
+// The MMA is FP16 x FP16 -> FP32 (mma.sync m16n8k16) with the 16 MMA rows on the tile's 16
+// output columns, so the bf16 activations are carried into fp16 exactly by exponent bands:
+// for activation row m with largest exponent field Emax, band b (b = 0, 1) holds the
+// elements whose exponent field lies in (Emax - 32(b+1), Emax - 32b], scaled by
+// 2^(142 - Emax + 32b) so that they land in [2^-16, 2^16) where fp16 represents every bf16
+// significand exactly.  Row m's two bands are MMA columns 2m and 2m + 1; the column sums
+// are scaled back by the inverse powers of two and added band 0 first.  Every activation
+// larger than 2^-64 times its row's largest one is represented exactly; smaller ones are
+// treated as zero.  Each group starts a fresh FP32 accumulator (zero input) and is
+// multiplied by its scale after its last MMA step.
+//
+// The kernel is launched with programmatic stream serialization: it lets the next kernel
+// in the stream start launching at once, and it reads none of its inputs and writes none
+// of its outputs before griddepcontrol.wait (the end of the previous kernel).
 #include <type_traits>
-#include <utility>
 
 #include "gq_device.cuh"
 
 namespace gq {
 
-// ------------------------------------------------------------------ W4, striped variant
+constexpr int kSlotChunks = 4;                          // 64-k chunks per slot
+constexpr int kSlotK = kSlotChunks * kChunkK;           // 256 k
+constexpr int kMaxSlots = 4;                            // ring slots per warp
+constexpr long long kStripeWaitCycles = 4000000000ll;   // bounded waits: about two seconds
 
-// Persistent decode kernel for M <= 8.  The flattened space of (16-column tile, K unit)
-// pairs is cut into W contiguous, equal stripes, one per warp (the striped partitioning of
-// "GPU Kernel 工程（09）：量化与融合 kernel", section 3.3 item 4: every SM gets the same amount
-// of work for any shape, at the price of a few cross-warp reductions).  The packed layout
-// stores each tile's chunks contiguously and the tiles one after another, so a stripe is
-// one contiguous range of memory that the warp streams front to back.  A K unit is
-// max(G, 64) values of k, a whole number of groups, so every partial sum is a sum of whole
-// scaled groups.  A tile covered by one warp is stored directly; a tile split between
-// warps w_a < ... < w_b is summed by the warp that completes it, adding the partials in
-// warp order w_a, ..., w_b (fixed order: bitwise reproducible).
-//
-// Streaming: each lane keeps kStages chunks (16 bytes each) of its stripe in flight in a
-// register ring, loaded kStages chunks ahead of use; the scales and zero-point words of a
-// unit are loaded together with the unit's weights.
-//
-// Decode: the FP16 form of the magic-number trick of section 2.4 of the same page, which
-// needs one shift per eight codes: (w & 0x000F000F) | 0x64006400 is fp16(1024 + q) for the
-// codes in bits 0-3 and 16-19, one fp16x2 subtraction of fp16(1024 + z) leaves q - z;
-// (w & 0x00F000F0) | 0x64006400 is fp16(1024 + 16q) for bits 4-7 and 20-23, and one fp16x2
-// FMA with 1/16 and -(64 + z) leaves q - z; w >> 8 exposes the other four codes.  Every
-// value is an exact small integer.
-//
-// The MMA is FP16 x FP16 -> FP32 with the 16 MMA rows on output columns n, so the bf16
-// activations are carried into fp16 exactly by exponent bands: for activation row m with
-// largest exponent field Emax, band b (b = 0, 1) holds the elements whose exponent field
-// lies in (Emax - 32(b+1), Emax - 32b], scaled by 2^(142 - Emax + 32b) so that they land in
-// [2^-16, 2^16) where fp16 represents every bf16 significand exactly.  Row m's two bands
-// are MMA columns 2m and 2m + 1; the column sums are scaled back by the inverse powers of
-// two and added band 0 first.  Every activation larger than 2^-64 times its row's largest
-// one is represented exactly; smaller ones are treated as zero.
-//
-// Each group's accumulator is scaled into the tile sums one group later (accumulators
-// alternate by group parity), so the FP32 scaling never waits on the MMA chain.
-//
-// The kernel is launched with programmatic stream serialization: it lets the next kernel
-// in the stream start launching at once, and it reads none of its inputs and writes none
-// of its outputs before griddepcontrol.wait (the end of the previous kernel).
-
-constexpr int kStages = 8;    // chunks in flight per lane (register ring)
-
-__device__ __forceinline__ int warp_of_unit(int u, int U, int W) {
-  const int base = U / W, rem = U % W;
-  const int big = rem * (base + 1);
-  return u < big ? u / (base + 1) : rem + (u - big) / base;
-}
+// Sticky device-side status of this kernel (GQ_ERR_TIMEOUT after a bounded wait gave up),
+// read by the host through stripe_read_error.
+static __device__ int g_stripe_error;
 
 __device__ __forceinline__ void mma_16816_f16(float d[4], uint32_t a0, uint32_t a1,
                                               uint32_t a2, uint32_t a3, uint32_t b0,
@@ -61,6 +59,16 @@ __device__ __forceinline__ void mma_16816_f16(float d[4], uint32_t a0, uint32_t 
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// the same MMA with a zero accumulator input (the first step of a group)
+__device__ __forceinline__ void mma_16816_f16_zc(float d[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
@@ -82,6 +90,33 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return r;
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Wait until the mbarrier phase of parity `parity` completes.  Bounded: after about two
+// seconds it records GQ_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool slot_wait(uint32_t bar, uint32_t parity) {
+  long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (it == 0) {
+      t0 = clock64();
+    } else if ((it & 63u) == 0u && clock64() - t0 > kStripeWaitCycles) {
+      atomicExch(&g_stripe_error, GQ_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Decode constants, passed as a kernel parameter: the instructions read them from the
 // parameter bank instead of materializing immediates around every use.
 struct DecodeConsts {
@@ -93,143 +128,121 @@ struct DecodeConsts {
   uint32_t hi_sym;      // 0xD480D480: fp16 -(64 + 8)
 };
 
-// Fix-up of a tile that a stripe covers only in part.  `val` holds the lane's combined
-// value for rows m = lane_row(...) (set by the caller), columns n0 and n0 + 8.
-__device__ __forceinline__ void stripe_fixup(float v0, float v1, int mrow, bool owner,
-                                             float *part, unsigned *counters, void *out,
-                                             int M, int N, int t, int slot, int gw,
-                                             int held_units, int Cu, int U, int W,
-                                             bool out_f32) {
-  const int lane = threadIdx.x & 31, r0 = lane >> 2;
-  float *pp = part + ((size_t)gw * 2 + slot) * (kTileN * 8);
-  if (owner && mrow < M) {
-    pp[mrow * kTileN + r0] = v0;
-    pp[mrow * kTileN + r0 + 8] = v1;
-  }
-  // __syncwarp orders the lanes' partial stores before lane 0's release; the acq_rel
-  // read-modify-write publishes them and, in the last arriver, makes every other
-  // contributor's partials visible to the loads below
-  __syncwarp();
-  unsigned last = 0;
-  if (lane == 0) {
-    unsigned prev;
-    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;"
-                 : "=r"(prev)
-                 : "l"(counters + t), "r"((unsigned)held_units)
-                 : "memory");
-    last = (prev + (unsigned)held_units == (unsigned)Cu) ? 1u : 0u;
-    if (last) counters[t] = 0u;     // every contributor has arrived: leave it at zero
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  const int wa = warp_of_unit(t * Cu, U, W), wb = warp_of_unit(t * Cu + Cu - 1, U, W);
-  for (int idx = lane; idx < M * kTileN; idx += 32) {
-    const int m = idx / kTileN, nl = idx - m * kTileN;
-    float s = 0.f;
-    for (int w2 = wa; w2 <= wb; ++w2) {
-      int b2, e2;
-      zsplit_dev(U, W, w2, b2, e2);
-      const int sl = (b2 / Cu == t) ? 0 : 1;
-      s += __ldcg(part + ((size_t)w2 * 2 + sl) * (kTileN * 8) + m * kTileN + nl);
-    }
-    const int n = t * kTileN + nl;
-    if (n < N) store_out_rt(out, (size_t)m * N + n, s, out_f32);
-  }
+struct StripeParams {
+  const uint8_t *Wp;          // packed codes
+  const uint16_t *A;          // activations, bf16 [M][K]
+  const void *scales;         // [K/G][N]
+  const uint32_t *zeros;      // [K/G][N/8] or NULL
+  void *out;                  // [M][N]
+  float *part;                // [gridDim.x][8][16] per-CTA partial sums (shared tiles only)
+  unsigned *counters;         // per-tile arrival counters (shared tiles only)
+  int M, K, N;
+  int split_count, split_mult;   // CTA c owns slots zsplit(split_count, grid, c) * split_mult
+  int S;                         // ring slots per warp
+  int out_f32;
+  DecodeConsts dk;
+};
+
+// Shared-memory layout (dynamic): [bands][rings][pieces][raw A]
+//   bands  (1 + 2M) rows of act_row_words(K / 64) words: a zero row, then two exponent
+//          bands per activation row, permuted so that a lane gets the B operands of four
+//          consecutive 16-k MMA steps with two 16-byte loads
+//   rings  kStrWarps x S slots of slot_bytes: 2 KB of codes, then the group scales
+//   pieces kStrWarps x 2 x M x 16 floats: a warp's partial sums of its first and last tile
+//   raw A  M x K bf16 (prologue only)
+__host__ __device__ constexpr int stripe_groups_per_slot(int G) { return kSlotK / G; }
+__host__ __device__ constexpr int stripe_slot_bytes(int G, int es) {
+  return kSlotChunks * 512 + stripe_groups_per_slot(G) * 16 * es;
 }
 
-// MT: n8 MMA blocks (1 for M <= 4, 2 for M <= 8); UG: a K unit is UG * max(G, 64) values
-// of k (UG = 2 halves the per-unit work when K allows it).
-template <int G, int SC, bool ZP, int MT, int UG>
-__global__ void __launch_bounds__(kStrWarps * 32, 1)
-w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
-                 const void *__restrict__ scales, const uint32_t *__restrict__ zeros,
-                 void *__restrict__ out, float *__restrict__ part,
-                 unsigned *__restrict__ counters, int M, int K, int N, int W, int out_f32,
-                 const DecodeConsts dk) {
-  constexpr int UK = (G > kChunkK ? G : kChunkK) * UG;   // k per unit
-  constexpr int UCH = UK / kChunkK;               // chunks per unit
-  constexpr int GPU = UK / G;                     // groups per unit
-  constexpr int SPG = G / 16;                     // 16-k MMA steps per group
-  constexpr int PF = kStages / UCH;               // units in flight (kStages chunks)
-  constexpr int ES = SC == kScF32 ? 4 : 2;        // bytes per scale
-  static_assert(kStages % UCH == 0, "the register ring holds whole units");
+template <int G, int SC, bool ZP, int MT>
+__global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const StripeParams p) {
+  constexpr int ES = SC == kScF32 ? 4 : 2;          // bytes per scale
+  constexpr int GPS = stripe_groups_per_slot(G);    // groups per slot
+  constexpr int SPG = G / 16;                       // 16-k MMA steps per group
+  constexpr int SLOTB = stripe_slot_bytes(G, ES);
   typedef typename std::conditional<SC == kScF32, uint32_t, unsigned short>::type sc_t;
 
-  extern __shared__ __align__(16) uint32_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kStrWarps][kMaxSlots];
   __shared__ int s_emax[8], s_emin[8];
   asm volatile("griddepcontrol.launch_dependents;");
+
+  const int M = p.M, K = p.K, N = p.N, S = p.S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kStrWarps + warp;
-  const int C = K / kChunkK;
-  const int Cu = K / UK;
-  const int T = (N + kTileN - 1) / kTileN;
-  const int U = T * Cu;
-  const int NW = N >> 3;
-  int u0 = 0, u1 = 0;
-  if (gw < W) zsplit_dev(U, W, gw, u0, u1);
-  const int nu = u1 - u0;                          // units in this warp's stripe
   const int r0 = lane >> 2, q = lane & 3;
+  const int C = K / kChunkK;                        // chunks per tile
+  const int SPT = K / kSlotK;                       // slots per tile
+  int cb, ce;                                       // this CTA's slots
+  zsplit_dev(p.split_count, gridDim.x, blockIdx.x, cb, ce);
+  cb *= p.split_mult;
+  ce *= p.split_mult;
+  int wb, we;                                       // this warp's slots
+  zsplit_dev(ce - cb, kStrWarps, warp, wb, we);
+  wb += cb;
+  we += cb;
+  const int n = we - wb;
+
+  const int RS = act_row_words(C);
+  uint32_t *bands = reinterpret_cast<uint32_t *>(smem);
+  uint8_t *rings = smem + (((size_t)(1 + 2 * M) * RS * 4 + 127) & ~(size_t)127);
+  uint8_t *ring = rings + (size_t)warp * S * SLOTB;
+  float *pieces = reinterpret_cast<float *>(rings + (size_t)kStrWarps * S * SLOTB);
+  uint32_t *araw = reinterpret_cast<uint32_t *>(pieces + kStrWarps * 2 * M * kTileN);
+
   if (threadIdx.x < 8) {
     s_emax[threadIdx.x] = 0;
     s_emin[threadIdx.x] = 255;
   }
-  // shared memory: [band rows][raw A]
-  const int RS = act_row_words(C);
-  uint32_t *bands = smem;
-  uint32_t *araw = bands + (1 + 2 * M) * RS;     // zero row + two band rows per row
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[warp][s])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- the load side: weights of PF units ahead in registers, with their scales
-  const uint4 *wsrc = Wp + (size_t)u0 * UCH * 32 + lane;
-  const size_t srow = (size_t)N;                   // elements per scale row
-  int ht = u0 / Cu, hu = u0 - ht * Cu;             // tile and unit of the load head
-  const sc_t *hsa = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0, N - 1);
-  const sc_t *hsb = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0 + 8, N - 1);
-  const uint32_t *hza = zeros + min(2 * ht, NW - 1), *hzb = zeros + min(2 * ht + 1, NW - 1);
-  size_t hg = (size_t)hu * GPU;                    // group index of the head unit
-  uint4 buf[PF][UCH];
-  uint32_t sr[PF][GPU][2], zr[PF][GPU][2];
-  auto load_unit = [&](auto slot, int k) {         // unit k of the stripe into ring slot P
-    constexpr int P = decltype(slot)::value;
+  // ---- the load side (lane 0): the next slot of this warp's range into the next ring slot
+  const sc_t *const Sg = reinterpret_cast<const sc_t *>(p.scales);
+  int hv = wb, ht = wb / SPT, hj = wb - (wb / SPT) * SPT, hs = 0;   // head: slot, tile, in-tile, ring
+  auto issue_next = [&]() {
+    const uint32_t bar = smem_addr(&bars[warp][hs]);
+    const uint32_t dst = smem_addr(ring + (size_t)hs * SLOTB);
+    const int cols = min(kTileN, N - ht * kTileN);  // 16, or 8 in a ragged last tile
+    const uint32_t sbytes = (uint32_t)(cols * ES);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"((uint32_t)(kSlotChunks * 512) + GPS * sbytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(p.Wp + (size_t)hv * (kSlotChunks * 512)), "r"((uint32_t)(kSlotChunks * 512)), "r"(bar)
+        : "memory");
+    const sc_t *src = Sg + (size_t)hj * GPS * N + (size_t)ht * kTileN;
 #pragma unroll
-    for (int ch = 0; ch < UCH; ++ch)
-      buf[P][ch] = ld_stream(wsrc + (size_t)(k * UCH + ch) * 32);
-#pragma unroll
-    for (int gi = 0; gi < GPU; ++gi) {
-      sr[P][gi][0] = (uint32_t)__ldg(hsa + (hg + gi) * srow);
-      sr[P][gi][1] = (uint32_t)__ldg(hsb + (hg + gi) * srow);
-      if (ZP) {
-        zr[P][gi][0] = __ldg(hza + (hg + gi) * NW);
-        zr[P][gi][1] = __ldg(hzb + (hg + gi) * NW);
-      }
-    }
-    hg += GPU;
-    if (++hu == Cu) {
-      hu = 0;
-      hg = 0;
+    for (int gi = 0; gi < GPS; ++gi)
+      asm volatile(
+          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              dst + kSlotChunks * 512 + gi * 16 * ES),
+          "l"(src + (size_t)gi * N), "r"(sbytes), "r"(bar)
+          : "memory");
+    ++hv;
+    if (++hj == SPT) {
+      hj = 0;
       ++ht;
-      hsa = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0, N - 1);
-      hsb = reinterpret_cast<const sc_t *>(scales) + min(ht * kTileN + r0 + 8, N - 1);
-      hza = zeros + min(2 * ht, NW - 1);
-      hzb = zeros + min(2 * ht + 1, NW - 1);
     }
+    if (++hs == S) hs = 0;
   };
-  auto prefetch = [&](auto slot) {
-    constexpr int P = decltype(slot)::value;
-    if (P < nu) load_unit(slot, P);
-  };
-  [&]<int... P>(std::integer_sequence<int, P...>) {
-    (prefetch(std::integral_constant<int, P>()), ...);
-  }(std::make_integer_sequence<int, PF>());
+  if (lane == 0)
+    for (int i = 0; i < S && i < n; ++i) issue_next();
 
   // ---- stage A: exponent bands as fp16, permuted for the B operands
   {
     const int n16 = (M * K) >> 3;                  // 16-byte pieces of A
-    const uint32_t dst0 = (uint32_t)__cvta_generic_to_shared(araw);
+    const uint32_t dst0 = smem_addr(araw);
     for (int i = threadIdx.x; i < n16; i += blockDim.x)
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i),
-                   "l"(reinterpret_cast<const uint4 *>(A) + i)
+                   "l"(reinterpret_cast<const uint4 *>(p.A) + i)
                    : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
@@ -237,28 +250,20 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();                                 // raw A visible; s_emax / s_emin set
   const int wpr = K >> 1;                          // bf16 pairs per row
+  // exponent range of each row: the magnitude bits (bits & 0x7FFF) order like the values
   for (int m = 0; m < M; ++m) {
-    int emx = 0, emn = 255;
+    unsigned mx = 0u, mn = 0xFFFFu;
     for (int w = threadIdx.x; w < wpr; w += blockDim.x) {
-      const uint32_t raw = araw[m * wpr + w];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t bits = (raw >> (16 * h)) & 0xFFFFu;
-        if (bits & 0x7FFFu) {
-          const int e = (bits >> 7) & 0xFF;
-          emx = max(emx, e);
-          emn = min(emn, e);
-        }
-      }
+      const uint32_t mag = araw[m * wpr + w] & 0x7FFF7FFFu;
+      const uint32_t lo = mag & 0xFFFFu, hi = mag >> 16;
+      mx = max(mx, max(lo, hi));
+      mn = min(mn, min(lo ? lo : 0xFFFFu, hi ? hi : 0xFFFFu));   // smallest non-zero
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      emx = max(emx, __shfl_xor_sync(0xffffffffu, emx, o));
-      emn = min(emn, __shfl_xor_sync(0xffffffffu, emn, o));
-    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    mn = __reduce_min_sync(0xffffffffu, mn);
     if (lane == 0) {
-      atomicMax(&s_emax[m], emx);
-      atomicMin(&s_emin[m], emn);
+      atomicMax(&s_emax[m], (int)(mx >> 7));
+      atomicMin(&s_emin[m], (int)(mn >> 7));
     }
   }
   __syncthreads();
@@ -268,7 +273,25 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
     const int emax = s_emax[m], emin = s_emin[m];
     const int nbu = emin > emax ? 0 : min(2, ((emax - emin) >> 5) + 1);
     if (b >= nbu) continue;
-    const int sb = 142 - emax + 32 * b;            // scale exponent of band b
+    const int sb_ = 142 - emax + 32 * b;           // scale exponent of band b
+    uint32_t *brw = bands + (1 + v) * RS;
+    if (nbu == 1 && emax < 255) {
+      // every non-zero element of the row lies in band 0: scale them all by 2^sb (two exact
+      // power-of-two products, each factor a normal float) and round to fp16, which is
+      // exact for bf16 significands in [2^-16, 2^16)
+      const int s1 = sb_ / 2, s2 = sb_ - s1;
+      const float c1 = __int_as_float((127 + s1) << 23), c2 = __int_as_float((127 + s2) << 23);
+      for (int w = threadIdx.x; w < wpr; w += blockDim.x) {
+        const uint32_t raw = araw[m * wpr + w];
+        const __half2 h = __floats2half2_rn(__uint_as_float(raw << 16) * c1 * c2,
+                                            __uint_as_float(raw & 0xFFFF0000u) * c1 * c2);
+        const int kk = 2 * w;
+        const int c = kk >> 6, r = kk & 63, j = r >> 4, hh = (r >> 3) & 1, qq = (r & 7) >> 1;
+        brw[c * 32 + (j >> 1) * 16 + qq * 4 + (j & 1) * 2 + hh] =
+            *reinterpret_cast<const uint32_t *>(&h);
+      }
+      continue;
+    }
     for (int w = threadIdx.x; w < wpr; w += blockDim.x) {
       const uint32_t raw = araw[m * wpr + w];
       uint32_t pair = 0u;
@@ -279,21 +302,20 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
         if ((bits & 0x7FFFu) && ((emax - ex) >> 5) == b) {
           float f;
           if (ex == 255)
-            f = __uint_as_float(bits << 16);                       // inf / nan stay so
+            f = __uint_as_float(bits << 16);                        // inf / nan stay so
           else if (ex == 0)
-            f = ldexpf(__uint_as_float(bits << 16), sb);           // bf16 subnormal
+            f = ldexpf(__uint_as_float(bits << 16), sb_);           // bf16 subnormal
           else
-            f = __uint_as_float((bits << 16) + ((uint32_t)sb << 23));  // exponent + sb
+            f = __uint_as_float((bits << 16) + ((uint32_t)sb_ << 23));  // exponent + sb
           pair |= (uint32_t)__half_as_ushort(__float2half_rn(f)) << (16 * h);
         }
       }
       const int kk = 2 * w;
       const int c = kk >> 6, r = kk & 63, j = r >> 4, hh = (r >> 3) & 1, qq = (r & 7) >> 1;
-      bands[(1 + v) * RS + c * 32 + (j >> 1) * 16 + qq * 4 + (j & 1) * 2 + hh] = pair;
+      brw[c * 32 + (j >> 1) * 16 + qq * 4 + (j & 1) * 2 + hh] = pair;
     }
   }
   __syncthreads();
-  if (nu <= 0) return;
 
   // B-operand rows of this lane (MMA column r0 of each block = band r0 % 2 of row r0 / 2),
   // or the zero row
@@ -321,61 +343,104 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
     if (SC == kScBF16) return __uint_as_float(bits << 16);
     return __half2float(__ushort_as_half((unsigned short)bits));
   };
+  const int NW = N >> 3;
+  // zero-point words of the slot (tile tz, slot jz of the tile): groups jz * GPS + gi,
+  // column words 2 tz and 2 tz + 1
+  auto load_zeros = [&](int tz, int jz, uint32_t (&z)[GPS][2]) {
+#pragma unroll
+    for (int gi = 0; gi < GPS; ++gi) {
+      const uint32_t *zr = p.zeros + (size_t)(jz * GPS + gi) * NW;
+      z[gi][0] = __ldg(zr + min(2 * tz, NW - 1));
+      z[gi][1] = __ldg(zr + min(2 * tz + 1, NW - 1));
+    }
+  };
+  const int t_first = wb / SPT;
+  int t = t_first, j = wb - t_first * SPT;
+  int j0 = j;                                      // first slot of this warp's share of t
+  uint32_t zcur[GPS][2], znext[GPS][2];
+  if (ZP && n > 0) load_zeros(t, j, znext);
 
-  int t = u0 / Cu, ul = u0 - t * Cu;               // tile and unit being computed
-  const int t_first = t;
-  int tile_u0 = ul;
   float acc[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 
-  // one unit from ring slot P; the slot is refilled with unit k + PF first
-  auto step = [&](auto slot, int k) {
-    constexpr int P = decltype(slot)::value;
-    uint4 cur[UCH];
-    uint32_t sv[GPU][2], zw[GPU][2];
+  // End of the warp's share of tile t (slots j0 .. j1 - 1): combine the bands, then store
+  // a whole tile or keep the share's partial sums for the CTA's reduction.
+  auto flush = [&](int j1) {
 #pragma unroll
-    for (int ch = 0; ch < UCH; ++ch) cur[ch] = buf[P][ch];
-#pragma unroll
-    for (int gi = 0; gi < GPU; ++gi) {
-      sv[gi][0] = sr[P][gi][0];
-      sv[gi][1] = sr[P][gi][1];
-      if (ZP) { zw[gi][0] = zr[P][gi][0]; zw[gi][1] = zr[P][gi][1]; }
+    for (int mt = 0; mt < MT; ++mt) {
+      // lane (r0, q) holds columns 2q, 2q + 1 (both bands of row mt * 4 + q) of the tile's
+      // columns r0 and r0 + 8
+      const int mrow = mt * 4 + q;
+      const int emax = mrow < M ? s_emax[mrow] : 127;
+      const float v0 = ldexpf(acc[mt][0], emax - 142) + ldexpf(acc[mt][1], emax - 174);
+      const float v1 = ldexpf(acc[mt][2], emax - 142) + ldexpf(acc[mt][3], emax - 174);
+      acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+      if (mrow >= M) continue;
+      if (j0 == 0 && j1 == SPT) {
+        const int n0 = t * kTileN + r0;
+        if (n0 < N) store_out_rt(p.out, (size_t)mrow * N + n0, v0, p.out_f32 != 0);
+        if (n0 + 8 < N) store_out_rt(p.out, (size_t)mrow * N + n0 + 8, v1, p.out_f32 != 0);
+      } else {
+        float *pc = pieces + ((warp * 2 + (t == t_first ? 0 : 1)) * M + mrow) * kTileN;
+        pc[r0] = v0;
+        pc[r0 + 8] = v1;
+      }
     }
-    if (k + PF < nu) load_unit(slot, k + PF);
+  };
 
-    uint32_t zl = ZP ? zlo_of(zw[0][0]) : dk.lo_sym, zh = ZP ? zhi_of(zw[0][1]) : dk.hi_sym;
-    float d[MT][4];
-    const uint32_t *bp[MT];
+  int s = 0;
+  uint32_t ph = 0;
+  for (int i = 0; i < n; ++i) {
+    slot_wait(smem_addr(&bars[warp][s]), ph);
+    if (ZP) {
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) bp[mt] = brow[mt] + ul * (UCH * 32);
+      for (int gi = 0; gi < GPS; ++gi) {
+        zcur[gi][0] = znext[gi][0];
+        zcur[gi][1] = znext[gi][1];
+      }
+      if (i + 1 < n) {
+        if (j + 1 < SPT) load_zeros(t, j + 1, znext);
+        else load_zeros(t + 1, 0, znext);
+      }
+    }
+    const uint8_t *slot = ring + (size_t)s * SLOTB;
+    const uint8_t *ssc = slot + kSlotChunks * 512;          // the slot's scales
 #pragma unroll
-    for (int ch = 0; ch < UCH; ++ch) {
+    for (int ch = 0; ch < kSlotChunks; ++ch) {
+      const uint4 wv = *reinterpret_cast<const uint4 *>(slot + ch * 512 + lane * 16);
       uint32_t bq[MT][8];
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const uint4 lo = *reinterpret_cast<const uint4 *>(bp[mt] + ch * 32);
-        const uint4 hi = *reinterpret_cast<const uint4 *>(bp[mt] + ch * 32 + 16);
+        const uint32_t *bp = brow[mt] + (j * kSlotChunks + ch) * 32;
+        const uint4 lo = *reinterpret_cast<const uint4 *>(bp);
+        const uint4 hi = *reinterpret_cast<const uint4 *>(bp + 16);
         bq[mt][0] = lo.x; bq[mt][1] = lo.y; bq[mt][2] = lo.z; bq[mt][3] = lo.w;
         bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
       }
-      const uint32_t words[4] = {cur[ch].x, cur[ch].y, cur[ch].z, cur[ch].w};
+      const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+      float d[MT][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int stp = ch * 4 + j;                   // compile-time
-        const uint32_t w = words[j], w8 = w >> 8;
-        const uint32_t a0 = hsub2_u(lop3_and_or(w, dk.lo_mask, dk.magic), zl);
-        const uint32_t a1 = hfma2_u(lop3_and_or(w, dk.hi_mask, dk.magic), dk.sixteenth, zh);
-        const uint32_t a2 = hsub2_u(lop3_and_or(w8, dk.lo_mask, dk.magic), zl);
-        const uint32_t a3 = hfma2_u(lop3_and_or(w8, dk.hi_mask, dk.magic), dk.sixteenth, zh);
+      for (int jj = 0; jj < 4; ++jj) {
+        const int stp = ch * 4 + jj;                 // compile-time 16-k step of the slot
+        const int gi = stp / SPG;
+        const uint32_t zl = ZP ? zlo_of(zcur[gi][0]) : p.dk.lo_sym;
+        const uint32_t zh = ZP ? zhi_of(zcur[gi][1]) : p.dk.hi_sym;
+        const uint32_t w = words[jj], w8 = w >> 8;
+        const uint32_t a0 = hsub2_u(lop3_and_or(w, p.dk.lo_mask, p.dk.magic), zl);
+        const uint32_t a1 = hfma2_u(lop3_and_or(w, p.dk.hi_mask, p.dk.magic), p.dk.sixteenth, zh);
+        const uint32_t a2 = hsub2_u(lop3_and_or(w8, p.dk.lo_mask, p.dk.magic), zl);
+        const uint32_t a3 = hfma2_u(lop3_and_or(w8, p.dk.hi_mask, p.dk.magic), p.dk.sixteenth, zh);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          if (stp % SPG == 0) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.f;
-          mma_16816_f16(d[mt], a0, a1, a2, a3, bq[mt][2 * j], bq[mt][2 * j + 1]);
+          if (stp % SPG == 0)
+            mma_16816_f16_zc(d[mt], a0, a1, a2, a3, bq[mt][2 * jj], bq[mt][2 * jj + 1]);
+          else
+            mma_16816_f16(d[mt], a0, a1, a2, a3, bq[mt][2 * jj], bq[mt][2 * jj + 1]);
         }
-        if ((stp + 1) % SPG == 0) {                // a whole group: scale it in
-          const int gi = stp / SPG;
-          const float fa = scale_f(sv[gi][0]), fb = scale_f(sv[gi][1]);
+        if ((stp + 1) % SPG == 0) {                 // a whole group: scale it in
+          const sc_t *sg = reinterpret_cast<const sc_t *>(ssc + gi * 16 * ES);
+          const float fa = scale_f((uint32_t)sg[r0]), fb = scale_f((uint32_t)sg[r0 + 8]);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             acc[mt][0] = fmaf(fa, d[mt][0], acc[mt][0]);
@@ -383,148 +448,205 @@ w4_stripe_kernel(const uint4 *__restrict__ Wp, const uint16_t *__restrict__ A,
             acc[mt][2] = fmaf(fb, d[mt][2], acc[mt][2]);
             acc[mt][3] = fmaf(fb, d[mt][3], acc[mt][3]);
           }
-          if (ZP && gi + 1 < GPU) {
-            zl = zlo_of(zw[gi + 1 < GPU ? gi + 1 : 0][0]);
-            zh = zhi_of(zw[gi + 1 < GPU ? gi + 1 : 0][1]);
-          }
         }
       }
     }
-
-    // end of a tile, or of the stripe: combine the bands, then store or fix up
-    ++ul;
-    if (ul == Cu || k + 1 == nu) {
-      const bool whole = (tile_u0 == 0 && ul == Cu);
-      float *pp = part + ((size_t)gw * 2 + (t == t_first ? 0 : 1)) * (kTileN * 8);
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        // lane (r0, q) holds columns 2q, 2q + 1 (both bands of row mt * 4 + q) of rows
-        // n0 = r0 and r0 + 8
-        const int mrow = mt * 4 + q;
-        const int emax = mrow < M ? s_emax[mrow] : 127;
-        const float v0 = ldexpf(acc[mt][0], emax - 142) + ldexpf(acc[mt][1], emax - 174);
-        const float v1 = ldexpf(acc[mt][2], emax - 142) + ldexpf(acc[mt][3], emax - 174);
-        if (mrow < M) {
-          if (whole) {
-            const int n0 = t * kTileN + r0;
-            if (n0 < N) store_out_rt(out, (size_t)mrow * N + n0, v0, out_f32 != 0);
-            if (n0 + 8 < N) store_out_rt(out, (size_t)mrow * N + n0 + 8, v1, out_f32 != 0);
-          } else {
-            pp[mrow * kTileN + r0] = v0;
-            pp[mrow * kTileN + r0 + 8] = v1;
-          }
-        }
-        acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-      }
-      if (!whole)
-        stripe_fixup(0.f, 0.f, 0, false, part, counters, out, M, N, t, t == t_first ? 0 : 1,
-                     gw, ul - tile_u0, Cu, U, W, out_f32 != 0);
-      if (ul == Cu) { ul = 0; ++t; tile_u0 = 0; }
+    // every lane has consumed the slot (its shared-memory reads fed the instructions above);
+    // order those generic-proxy reads before the bulk copy's writes, then refill
+    __syncwarp();
+    if (lane == 0 && i + S < n) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue_next();
     }
-  };
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+    if (++j == SPT) {
+      flush(SPT);
+      ++t;
+      j = 0;
+      j0 = 0;
+    }
+  }
+  if (n > 0 && j != 0) flush(j);
 
-  for (int k0 = 0; k0 < nu; k0 += PF) {
-    [&]<int... P>(std::integer_sequence<int, P...>) {
-      ((k0 + P < nu ? (step(std::integral_constant<int, P>(), k0 + P), 0) : 0), ...);
-    }(std::make_integer_sequence<int, PF>());
+  // ---- reduction of the tiles shared between warps (shared memory) and CTAs (global)
+  __syncthreads();
+  // A tile is reduced by the lowest warp of the CTA that holds part of it: this warp for its
+  // first tile unless a lower warp ends inside that tile, and for its last tile when that
+  // differs from its first.  A share that covers a whole tile was stored already.
+  for (int pass = 0; pass < 2 && n > 0; ++pass) {
+    const int tt = pass == 0 ? t_first : (we - 1) / SPT;
+    if (pass == 1 && tt == t_first) break;
+    const int tb = tt * SPT, te = tb + SPT;         // the tile's slots
+    if (max(tb, wb) == tb && min(te, we) == te) continue;          // stored directly
+    if (pass == 0 && wb > cb && wb % SPT != 0) continue;          // a lower warp reduces it
+    const bool cta_whole = tb >= cb && te <= ce;
+    const bool cta_first = tb >= cb;               // the CTA holds the tile's first slot
+    for (int base = 0; base < M * kTileN; base += 32) {
+      const int idx = base + lane;
+      const int m = idx / kTileN, nl = idx - m * kTileN;
+      float sum = 0.f;
+      if (idx < M * kTileN) {
+        // the CTA's share: warps warp, warp + 1, ... while they hold slots of the tile
+        for (int w2 = warp; w2 < kStrWarps; ++w2) {
+          int b2, e2;
+          zsplit_dev(ce - cb, kStrWarps, w2, b2, e2);
+          b2 += cb;
+          e2 += cb;
+          if (e2 <= b2 || b2 >= te) break;
+          sum += pieces[((w2 * 2 + (b2 / SPT == tt ? 0 : 1)) * M + m) * kTileN + nl];
+        }
+      }
+      if (cta_whole) {
+        const int nn = tt * kTileN + nl;
+        if (idx < M * kTileN && nn < N) store_out_rt(p.out, (size_t)m * N + nn, sum, p.out_f32 != 0);
+      } else if (!cta_first) {
+        // a contributor: publish this CTA's share (counted in below)
+        if (idx < M * kTileN) p.part[(size_t)blockIdx.x * (8 * kTileN) + m * kTileN + nl] = sum;
+      } else {
+        // the reducer: wait for the CTAs after this one, then add their shares in order
+        if (base == 0 && lane == 0) {
+          const unsigned target = (unsigned)(te - ce);
+          const long long c0 = clock64();
+          for (;;) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.counters + tt) : "memory");
+            if (v == target) break;
+            if (clock64() - c0 > kStripeWaitCycles) {
+              atomicExch(&g_stripe_error, GQ_ERR_TIMEOUT);
+              break;
+            }
+            __nanosleep(64);
+          }
+          p.counters[tt] = 0u;                     // every contributor has arrived
+        }
+        __syncwarp();
+        if (idx < M * kTileN) {
+          for (int c2 = blockIdx.x + 1; c2 < (int)gridDim.x; ++c2) {
+            int b2, e2;
+            zsplit_dev(p.split_count, gridDim.x, c2, b2, e2);
+            if (b2 * p.split_mult >= te) break;
+            sum += __ldcg(p.part + (size_t)c2 * (8 * kTileN) + m * kTileN + nl);
+          }
+          const int nn = tt * kTileN + nl;
+          if (nn < N) store_out_rt(p.out, (size_t)m * N + nn, sum, p.out_f32 != 0);
+        }
+      }
+    }
+    if (!cta_whole && !cta_first) {
+      // __syncwarp orders the lanes' stores before lane 0's release, which publishes them
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p.counters + tt),
+                     "r"((unsigned)(min(te, ce) - max(tb, cb)))
+                     : "memory");
+    }
   }
 }
 
-template <int G, int SC, bool ZP, int MT, int UG>
-static cudaError_t launch_stripe_t(const Plan &p, int prec, int M, int K, int N,
-                                   const void *A, const void *Wq, const void *scales,
-                                   const void *zeros, void *out, float *part,
-                                   unsigned *counters, cudaStream_t s) {
-  auto kern = w4_stripe_kernel<G, SC, ZP, MT, UG>;
+template <int G, int SC, bool ZP, int MT>
+static cudaError_t launch_stripe_t(const Plan &pl, const StripeParams &sp, cudaStream_t s) {
+  auto kern = w4_stripe_kernel<G, SC, ZP, MT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)p.smem_bytes);
+                                       (int)pl.smem_bytes);
   if (e != cudaSuccess) return e;
-  const int out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   // programmatic stream serialization: the next kernel may begin launching while this one
   // runs; this kernel touches its inputs and outputs only after griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid_x);
-  cfg.blockDim = dim3(p.block_threads);
-  cfg.dynamicSmemBytes = p.smem_bytes;
+  cfg.gridDim = dim3(pl.grid_x);
+  cfg.blockDim = dim3(pl.block_threads);
+  cfg.dynamicSmemBytes = pl.smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint4 *>(Wq),
-                            reinterpret_cast<const uint16_t *>(A), scales,
-                            reinterpret_cast<const uint32_t *>(zeros), out, part, counters,
-                            M, K, N, p.nsplit, out_f32,
-                            DecodeConsts{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x2C002C00u,
-                                         0x64086408u, 0xD480D480u});
-}
-
-// units of two groups when K allows it (G = 64, 128), one group otherwise
-int stripe_unit_groups(int K, int G) {
-  const int base = G > kChunkK ? G : kChunkK;
-  return ((G == 64 || G == 128) && K % (2 * base) == 0) ? 2 : 1;
-}
-
-template <int G, int SC, bool ZP, int UG>
-static cudaError_t launch_stripe_m(const Plan &p, int prec, int M, int K, int N,
-                                   const void *A, const void *Wq, const void *scales,
-                                   const void *zeros, void *out, float *part, unsigned *cnt,
-                                   cudaStream_t s) {
-  if (M <= 4) return launch_stripe_t<G, SC, ZP, 1, UG>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  return launch_stripe_t<G, SC, ZP, 2, UG>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+  return cudaLaunchKernelEx(&cfg, kern, sp);
 }
 
 template <int G, int SC, bool ZP>
-static cudaError_t launch_stripe_u(const Plan &p, int prec, int M, int K, int N,
-                                   const void *A, const void *Wq, const void *scales,
-                                   const void *zeros, void *out, float *part, unsigned *cnt,
-                                   cudaStream_t s) {
-  if constexpr (G == 64 || G == 128) {
-    if (stripe_unit_groups(K, G) == 2)
-      return launch_stripe_m<G, SC, ZP, 2>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  }
-  return launch_stripe_m<G, SC, ZP, 1>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+static cudaError_t launch_stripe_m(const Plan &pl, const StripeParams &sp, cudaStream_t s) {
+  if (sp.M <= 4) return launch_stripe_t<G, SC, ZP, 1>(pl, sp, s);
+  return launch_stripe_t<G, SC, ZP, 2>(pl, sp, s);
 }
 
 template <int G, int SC>
-static cudaError_t launch_stripe_z(const Plan &p, int prec, int M, int K, int N,
-                                   const void *A, const void *Wq, const void *scales,
-                                   const void *zeros, void *out, float *part, unsigned *cnt,
-                                   cudaStream_t s) {
-  if (prec & GQ_ZP)
-    return launch_stripe_u<G, SC, true>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  return launch_stripe_u<G, SC, false>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+static cudaError_t launch_stripe_z(const Plan &pl, int prec, const StripeParams &sp, cudaStream_t s) {
+  if (prec & GQ_ZP) return launch_stripe_m<G, SC, true>(pl, sp, s);
+  return launch_stripe_m<G, SC, false>(pl, sp, s);
 }
 
 template <int G>
-static cudaError_t launch_stripe_g(const Plan &p, int prec, int M, int K, int N,
-                                   const void *A, const void *Wq, const void *scales,
-                                   const void *zeros, void *out, float *part, unsigned *cnt,
-                                   cudaStream_t s) {
-  if (prec & GQ_SC_F32)
-    return launch_stripe_z<G, kScF32>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  if (prec & GQ_SC_BF16)
-    return launch_stripe_z<G, kScBF16>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
-  return launch_stripe_z<G, kScF16>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, cnt, s);
+static cudaError_t launch_stripe_g(const Plan &pl, int prec, const StripeParams &sp, cudaStream_t s) {
+  if (prec & GQ_SC_F32) return launch_stripe_z<G, kScF32>(pl, prec, sp, s);
+  if (prec & GQ_SC_BF16) return launch_stripe_z<G, kScBF16>(pl, prec, sp, s);
+  return launch_stripe_z<G, kScF16>(pl, prec, sp, s);
 }
 
-size_t stripe_smem_bytes(int M, int K, int G, int prec) {
-  (void)G;
-  (void)prec;
-  const size_t bands = (size_t)(1 + 2 * M) * (K / kChunkK * 32 + 16) * 4;
-  return bands + (size_t)M * K * 2;
+int stripe_read_error(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_stripe_error, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  if (clear && v) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_stripe_error, &z, sizeof(int));
+  }
+  return v;
 }
 
-cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int prec,
+bool stripe_supported(int M, int K, int G, int prec) {
+  return (prec & GQ_W4) && !(prec & GQ_ACT_F32) && M >= 1 && M <= 8 && K % kSlotK == 0 &&
+         G <= kSlotK;
+}
+
+size_t stripe_smem_bytes(int M, int K, int G, int prec, int slots) {
+  const int es = (prec & GQ_SC_F32) ? 4 : 2;
+  const size_t bands =
+      (((size_t)(1 + 2 * M) * act_row_words(K / kChunkK) * 4) + 127) & ~(size_t)127;
+  const size_t rings = (size_t)kStrWarps * slots * stripe_slot_bytes(G, es);
+  const size_t pieces = (size_t)kStrWarps * 2 * M * kTileN * 4;
+  return bands + rings + pieces + (size_t)M * K * 2;
+}
+
+int stripe_slots_for(int M, int K, int G, int prec, size_t smem_cap) {
+  for (int s = kMaxSlots; s >= 2; --s)
+    if (stripe_smem_bytes(M, K, G, prec, s) <= smem_cap) return s;
+  return 0;
+}
+
+int stripe_slot_k() { return kSlotK; }
+
+cudaError_t launch_stripe_decode(const Plan &pl, int M, int K, int N, int G, int prec,
                                  const void *A, const void *Wq, const void *scales,
                                  const void *zeros, void *out, float *part,
                                  unsigned *counters, cudaStream_t s) {
+  StripeParams sp;
+  sp.Wp = reinterpret_cast<const uint8_t *>(Wq);
+  sp.A = reinterpret_cast<const uint16_t *>(A);
+  sp.scales = scales;
+  sp.zeros = reinterpret_cast<const uint32_t *>(zeros);
+  sp.out = out;
+  sp.part = part;
+  sp.counters = counters;
+  sp.M = M;
+  sp.K = K;
+  sp.N = N;
+  sp.split_count = pl.split_count;
+  sp.split_mult = pl.split_mult;
+  sp.S = pl.slots;
+  sp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
+  sp.dk = DecodeConsts{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x2C002C00u, 0x64086408u,
+                       0xD480D480u};
   switch (G) {
-    case 32: return launch_stripe_g<32>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, counters, s);
-    case 64: return launch_stripe_g<64>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, counters, s);
-    case 128: return launch_stripe_g<128>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, counters, s);
-    case 256: return launch_stripe_g<256>(p, prec, M, K, N, A, Wq, scales, zeros, out, part, counters, s);
+    case 32: return launch_stripe_g<32>(pl, prec, sp, s);
+    case 64: return launch_stripe_g<64>(pl, prec, sp, s);
+    case 128: return launch_stripe_g<128>(pl, prec, sp, s);
+    case 256: return launch_stripe_g<256>(pl, prec, sp, s);
     default: return cudaErrorInvalidValue;
   }
 }

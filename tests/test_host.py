@@ -107,15 +107,21 @@ def test_plan_is_a_pure_function_of_shape(name):
         assert p1["workspace_bytes"] == 0
         assert p1["smem_bytes"] <= 227 * 1024
         return
-    assert p1["smem_bytes"] <= 200 * 1024
     if p1["path"] == 3:
-        # striped decode: one stripe per warp, never more stripes than (tile, unit) pairs
+        # striped decode: one CTA per SM at most, each over a contiguous range of (tile,
+        # 256-k slot) pairs; whole tiles per CTA need no scratch, equal slot ranges need
+        # per-CTA partial sums and per-tile counters
         tiles = (cfg.N + 15) // 16
-        assert cfg.M <= 8
-        assert 1 <= p1["nsplit"] <= tiles * units
-        assert p1["grid_x"] * p1["block_threads"] // 32 >= p1["nsplit"]
-        assert p1["workspace_bytes"] >= p1["nsplit"] * 2 * 16 * 8 * 4
+        assert cfg.M <= 8 and cfg.K % 256 == 0
+        assert 1 <= p1["grid_x"] <= min(152, tiles * cfg.K // 256)
+        assert p1["nsplit"] == p1["grid_x"]
+        assert p1["smem_bytes"] <= 227 * 1024
+        if p1["workspace_bytes"]:
+            assert p1["workspace_bytes"] >= p1["grid_x"] * 8 * 16 * 4 + 4 * tiles
+        else:
+            assert tiles >= 152
         return
+    assert p1["smem_bytes"] <= 200 * 1024
     assert 1 <= p1["nsplit"] <= units
     assert p1["grid_y"] == p1["nsplit"]
     assert p1["grid_x"] * p1["n_tile"] >= cfg.N
@@ -130,7 +136,16 @@ def test_decode_plan_fills_the_machine():
     cfg = gq_synth.CONFIGS["decode_gateup"]
     p = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, C.GQ_W4, sm_count=152)
     assert p["path"] == 3
-    assert p["grid_x"] >= 152
+    assert p["grid_x"] == 152
+    # 1792 tiles over 152 SMs: whole tiles per CTA (11 or 12), no scratch
+    assert p["workspace_bytes"] == 0
+
+
+def test_small_decode_plan_splits_slots_between_ctas():
+    p = gq.gq_plan(1, 4096, 1024, 128, C.GQ_W4, sm_count=152)
+    assert p["path"] == 3
+    assert p["grid_x"] == 64          # 64 tiles x 16 slots, 16 warps per CTA
+    assert p["workspace_bytes"] > 0
 
 
 def test_algorithmic_bytes_match_the_worked_figures():

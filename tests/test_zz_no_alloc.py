@@ -26,7 +26,7 @@ def gq():
 
 
 @pytest.mark.parametrize("cfg", [
-    gq_synth.CONFIGS["decode_gateup"],                       # striped decode, split tiles
+    gq_synth.Config("nsa_stripe_m1", M=1, K=4096, N=2048, G=128),   # striped decode, CTAs share tiles
     gq_synth.Config("nsa_asym_m3", M=3, K=2048, N=1032, G=128, zp=True, sc="bf16"),
     gq_synth.Config("nsa_q8_m1", M=1, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),        # INT8 decode, K split
