@@ -202,6 +202,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table of the five configurations")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the M sweep against a dense BF16 GEMM")
     ap.add_argument("--calls-per-step", type=int, default=CALLS_PER_STEP,
                     help="gq_gemm calls per step (a smaller value for profiler runs)")
     args = ap.parse_args()
@@ -303,6 +307,12 @@ def main():
     prefill = None
     if not args.no_prefill and rank == 0:
         prefill = _prefill(gq, torch, dev, peaks, peak_kind)
+    configs = None
+    if not args.no_configs and rank == 0:
+        configs = _all_configs(gq, torch, dev, peaks, peak_kind)
+    sweep = None
+    if not args.no_sweep and rank == 0:
+        sweep = _m_sweep(gq, torch, dev, peaks)
 
     traffic = _kernel_traffic("gq_stripe.cu", "w4_stripe_decode_decode_gateup.md")
     line = {
@@ -324,6 +334,10 @@ def main():
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if configs:
+        line["configs"] = configs
+    if sweep:
+        line["m_sweep"] = sweep
     return _finish(args, line, prefill, rank, world, cfg, dist)
 
 
@@ -375,6 +389,116 @@ def _finish(args, line, prefill, rank, world, cfg, dist):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+L2_BYTES = 126 * 2 ** 20   # GB300 L2 (about 126 MiB usable)
+
+
+def _dev_inputs(torch, dev, inp):
+    def to_dev(a):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        v = a.view(np.int16) if a.dtype == np.uint16 else (a.view(np.int32) if a.dtype == np.uint32 else a)
+        return torch.from_numpy(v).to(dev)
+    return {k: to_dev(inp[k]) for k in ("codes", "scales", "zeros", "A")}
+
+
+def _all_configs(gq, torch, dev, peaks, peak_kind):
+    """Every workload of the benchmark set: mean time per gq_gemm call (CUDA graph of back to
+    back calls, rotating weight copies so that the weights come from HBM whenever they fit
+    at most a third of L2 per copy), HBM GB/s of the algorithmic bytes, TFLOPS, and the
+    fraction of the roofline that bounds it (HBM below M = 128, dense BF16 above)."""
+    from group_quantized_weight_gb300.constants import algorithmic_bytes, gemm_flops, prec_flags
+    out = []
+    for name in ("tiny_gemv", "decode_gateup", "q8_m1", "q8_m32", "asym_m16", "prefill"):
+        cfg = gq_synth.CONFIGS[name]
+        prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+        d = _dev_inputs(torch, dev, gq_synth.make_inputs(cfg, seed=0))
+        packed = gq.pack_weights_t(d["codes"], cfg.K, cfg.N, cfg.G, prec)
+        nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+        wbytes = packed.numel() + d["scales"].numel() * d["scales"].element_size()
+        copies = 1 if cfg.M >= 128 else int(max(1, min(8, -(-3 * L2_BYTES // max(wbytes, 1)))))
+        W = [packed] + [packed.clone() for _ in range(copies - 1)]
+        S = [d["scales"]] + [d["scales"].clone() for _ in range(copies - 1)]
+        Z = None
+        if d["zeros"] is not None:
+            Z = [d["zeros"]] + [d["zeros"].clone() for _ in range(copies - 1)]
+        odt = torch.float32 if cfg.out == "f32" else torch.bfloat16
+        o = torch.empty((cfg.M, cfg.N), dtype=odt, device=dev)
+        big = cfg.M >= 128
+        res = gq.gq_bench(cfg.M, cfg.K, cfg.N, cfg.G, prec, d["A"].data_ptr(),
+                          [w.data_ptr() for w in W], [x.data_ptr() for x in S],
+                          [z.data_ptr() for z in Z] if Z else None, o.data_ptr(),
+                          warmup=3, iters=10 if big else 200, use_graph=not big,
+                          stream=torch.cuda.current_stream().cuda_stream)
+        us = res["us_per_call"]
+        gbs = nbytes / (us * 1e-6) / 1e9
+        tf = gemm_flops(cfg.M, cfg.K, cfg.N) / (us * 1e-6) / 1e12
+        plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
+        row = {"workload": name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "G": cfg.G,
+               "path": plan["path"], "us": us, "GB/s": gbs, "TFLOPS": tf,
+               "l2": "from HBM" if copies * wbytes > 2 * L2_BYTES else "L2-resident weights"}
+        if big:
+            row.update(bound="tensor", frac=tf / peaks["bf16_tflops"],
+                       peak=f"bf16_tflops of {peak_kind}")
+        else:
+            row.update(bound="hbm", frac=gbs / peaks["hbm_gbs"], peak=f"hbm_gbs of {peak_kind}")
+        out.append(row)
+        del W, S, Z, d, packed, o
+        torch.cuda.empty_cache()
+    return out
+
+
+def _m_sweep(gq, torch, dev, peaks):
+    """K=4096 N=14336 G=128 W4A16 (fp16 scales, bf16 out) against the same product as a dense
+    BF16 GEMM (torch.matmul on cuBLAS, weights already BF16) for M = 1 ... 4096: time per
+    call of each, their ratio, and the smallest M at which the INT4 path is the slower."""
+    from group_quantized_weight_gb300.constants import prec_flags
+    base = gq_synth.Config("sweep", M=1, K=4096, N=14336, G=128)
+    prec = prec_flags(True, False, "bf16", "fp16", "bf16")
+    w = gq_synth.make_weights(base, seed=0)
+    codes = torch.from_numpy(w["codes"].view(np.int32)).to(dev)
+    packed = gq.pack_weights_t(codes, base.K, base.N, base.G, prec)
+    S = torch.from_numpy(w["scales"].view(np.int16)).to(dev)
+    del codes
+    copies = 4
+    W = [packed] + [packed.clone() for _ in range(copies - 1)]
+    Ss = [S] + [S.clone() for _ in range(copies - 1)]
+    Wd = [torch.randn(base.N, base.K, device=dev).to(torch.bfloat16) for _ in range(copies)]
+    rows = []
+    crossover = None
+    stream = torch.cuda.current_stream()
+    for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096):
+        a = gq_synth.make_activations(base, seed=0, M=M)
+        A = torch.from_numpy(a.view(np.int16)).to(dev)
+        o = torch.empty((M, base.N), dtype=torch.bfloat16, device=dev)
+        iters = 200 if M <= 64 else (50 if M <= 512 else 10)
+        res = gq.gq_bench(M, base.K, base.N, base.G, prec, A.data_ptr(), [x.data_ptr() for x in W],
+                          [x.data_ptr() for x in Ss], None, o.data_ptr(), warmup=3, iters=iters,
+                          use_graph=M < 128, stream=stream.cuda_stream)
+        Ad = A.view(torch.bfloat16)
+        for i in range(3):
+            torch.matmul(Ad, Wd[i % copies].t())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(iters):
+            torch.matmul(Ad, Wd[i % copies].t())
+        e1.record()
+        torch.cuda.synchronize()
+        dense_us = e0.elapsed_time(e1) * 1e3 / iters
+        us = res["us_per_call"]
+        if crossover is None and us > dense_us:
+            crossover = M
+        rows.append({"M": M, "int4_us": us, "bf16_dense_us": dense_us, "speedup": dense_us / us,
+                     "path": gq.gq_plan(M, base.K, base.N, base.G, prec)["path"]})
+    del W, Ss, Wd
+    torch.cuda.empty_cache()
+    return {"shape": "K=4096 N=14336 G=128 W4A16 sym fp16 scales vs torch.matmul bf16",
+            "weights": f"{copies} rotated copies of each (INT4 {copies * 29.4:.0f} MB, "
+                       f"BF16 {copies * 117.4:.0f} MB)",
+            "crossover_M": crossover, "rows": rows}
 
 
 def _prefill(gq, torch, dev, peaks, peak_kind):

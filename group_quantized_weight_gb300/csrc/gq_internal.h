@@ -19,7 +19,7 @@ constexpr int kChunkK8 = 16;
 constexpr int kDecWarps = 8;
 constexpr int kDecMaxMT = 4;           // up to 4 x 8 = 32 rows of A per CTA
 // Striped small-M decode kernel (M <= 8): warps per CTA, one CTA per SM.
-constexpr int kStrWarps = 16;
+constexpr int kStrWarps = 24;
 // INT8 CUDA-core decode kernel: one column per thread.
 constexpr int kQ8Threads = 128;
 constexpr int kQ8MaxRows = 32;

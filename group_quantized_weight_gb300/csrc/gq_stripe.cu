@@ -45,7 +45,7 @@ namespace gq {
 
 constexpr int kSlotChunks = 4;                          // 64-k chunks per slot
 constexpr int kSlotK = kSlotChunks * kChunkK;           // 256 k
-constexpr int kMaxSlots = 4;                            // ring slots per warp
+constexpr int kMaxSlots = 3;                            // ring slots per warp
 constexpr long long kStripeWaitCycles = 4000000000ll;   // bounded waits: about two seconds
 
 // Sticky device-side status of this kernel (GQ_ERR_TIMEOUT after a bounded wait gave up),
@@ -83,11 +83,21 @@ __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) 
   return r;
 }
 
-// (a & b) | c in one LOP3
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+// (a & MASK) | c in one LOP3: the mask is an immediate of the instruction and c a register
+// (with both constants taken from memory operands the compiler emits two instructions)
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t c) {
   uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(c));
   return r;
+}
+
+// x * 2^e for e in [-174, 127], rounded once.  2^e is a normal float for e >= -126; below
+// that, x is first scaled by 2^-64 (exact unless |x| < 2^-62, in which case the result is
+// below 2^-188 and rounds to zero either way) and then by 2^(e + 64).
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  if (e >= -126) return x * __int_as_float((127 + e) << 23);
+  return x * __int_as_float((127 - 64) << 23) * __int_as_float((127 + 64 + e) << 23);
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -117,16 +127,11 @@ __device__ __forceinline__ bool slot_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Decode constants, passed as a kernel parameter: the instructions read them from the
-// parameter bank instead of materializing immediates around every use.
-struct DecodeConsts {
-  uint32_t lo_mask;     // 0x000F000F: codes in bits 0-3 and 16-19
-  uint32_t hi_mask;     // 0x00F000F0: codes in bits 4-7 and 20-23
-  uint32_t magic;       // 0x64006400: fp16 1024 in both halves
-  uint32_t sixteenth;   // 0x2C002C00: fp16 1/16 in both halves
-  uint32_t lo_sym;      // 0x64086408: fp16 (1024 + 8), symmetric zero point
-  uint32_t hi_sym;      // 0xD480D480: fp16 -(64 + 8)
-};
+// decode constants (fp16x2 bit patterns)
+constexpr uint32_t kMagic = 0x64006400u;       // 1024 in both halves
+constexpr uint32_t kSixteenth = 0x2C002C00u;   // 1/16
+constexpr uint32_t kLoSym = 0x64086408u;       // 1024 + 8: the symmetric zero point
+constexpr uint32_t kHiSym = 0xD480D480u;       // -(64 + 8)
 
 struct StripeParams {
   const uint8_t *Wp;          // packed codes
@@ -140,16 +145,14 @@ struct StripeParams {
   int split_count, split_mult;   // CTA c owns slots zsplit(split_count, grid, c) * split_mult
   int S;                         // ring slots per warp
   int out_f32;
-  DecodeConsts dk;
 };
 
-// Shared-memory layout (dynamic): [bands][rings][pieces][raw A]
+// Shared-memory layout (dynamic): [bands][rings][pieces]
 //   bands  (1 + 2M) rows of act_row_words(K / 64) words: a zero row, then two exponent
 //          bands per activation row, permuted so that a lane gets the B operands of four
 //          consecutive 16-k MMA steps with two 16-byte loads
 //   rings  kStrWarps x S slots of slot_bytes: 2 KB of codes, then the group scales
 //   pieces kStrWarps x 2 x M x 16 floats: a warp's partial sums of its first and last tile
-//   raw A  M x K bf16 (prologue only)
 __host__ __device__ constexpr int stripe_groups_per_slot(int G) { return kSlotK / G; }
 __host__ __device__ constexpr int stripe_slot_bytes(int G, int es) {
   return kSlotChunks * 512 + stripe_groups_per_slot(G) * 16 * es;
@@ -161,6 +164,9 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   constexpr int GPS = stripe_groups_per_slot(G);    // groups per slot
   constexpr int SPG = G / 16;                       // 16-k MMA steps per group
   constexpr int SLOTB = stripe_slot_bytes(G, ES);
+  constexpr int LPG = ES;                           // 16-byte parts per group's 16 scales
+  constexpr int NL = GPS * LPG;                     // lanes copying scales (at most 32)
+  static_assert(NL <= 32, "one 16-byte scale part per lane");
   typedef typename std::conditional<SC == kScF32, uint32_t, unsigned short>::type sc_t;
 
   extern __shared__ __align__(128) uint8_t smem[];
@@ -188,7 +194,6 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   uint8_t *rings = smem + (((size_t)(1 + 2 * M) * RS * 4 + 127) & ~(size_t)127);
   uint8_t *ring = rings + (size_t)warp * S * SLOTB;
   float *pieces = reinterpret_cast<float *>(rings + (size_t)kStrWarps * S * SLOTB);
-  uint32_t *araw = reinterpret_cast<uint32_t *>(pieces + kStrWarps * 2 * M * kTileN);
 
   if (threadIdx.x < 8) {
     s_emax[threadIdx.x] = 0;
@@ -196,68 +201,86 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   }
   if (lane == 0) {
     for (int s = 0; s < S; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bars[warp][s])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&bars[warp][s])),
+                   "n"(1 + NL)
+                   : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- the load side (lane 0): the next slot of this warp's range into the next ring slot
-  const sc_t *const Sg = reinterpret_cast<const sc_t *>(p.scales);
-  int hv = wb, ht = wb / SPT, hj = wb - (wb / SPT) * SPT, hs = 0;   // head: slot, tile, in-tile, ring
+  // ---- the load side: the next slot of this warp's range into the next ring slot.  One lane
+  // issues the bulk copy of the slot's 2 KB of codes (operands broadcast from lane 0, so the
+  // compiler sees them warp-uniform); lanes 0 .. NL-1 each copy 16 bytes of the slot's group
+  // scales with cp.async and report completion on the slot's mbarrier
+  // (cp.async.mbarrier.arrive.noinc), which therefore expects 1 + NL arrivals per phase.
+  // Source pointers advance by a fixed stride per slot and are recomputed at tile changes.
+  const size_t srow = (size_t)N * ES;               // bytes per scale row
+  const uint8_t *hw = p.Wp + (size_t)wb * (kSlotChunks * 512);
+  int ht = wb / SPT, hj = wb - ht * SPT, hs = 0;
+  const int lg = lane / LPG, lp = lane - lg * LPG;  // this lane's scale group and 16-byte part
+  const uint8_t *lsc = nullptr;                     // this lane's scale source in the head slot
+  bool lcopy = false;                               // the part lies inside the tile's columns
+  auto head_tile = [&]() {
+    lsc = reinterpret_cast<const uint8_t *>(p.scales) + (size_t)(hj * GPS + lg) * srow +
+          (size_t)ht * kTileN * ES + lp * 16;
+    lcopy = lane < NL && lp * 16 < min(kTileN, N - ht * kTileN) * ES;
+  };
+  head_tile();
   auto issue_next = [&]() {
     const uint32_t bar = smem_addr(&bars[warp][hs]);
-    const uint32_t dst = smem_addr(ring + (size_t)hs * SLOTB);
-    const int cols = min(kTileN, N - ht * kTileN);  // 16, or 8 in a ragged last tile
-    const uint32_t sbytes = (uint32_t)(cols * ES);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                 "r"((uint32_t)(kSlotChunks * 512) + GPS * sbytes)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(p.Wp + (size_t)hv * (kSlotChunks * 512)), "r"((uint32_t)(kSlotChunks * 512)), "r"(bar)
-        : "memory");
-    const sc_t *src = Sg + (size_t)hj * GPS * N + (size_t)ht * kTileN;
-#pragma unroll
-    for (int gi = 0; gi < GPS; ++gi)
+    const uint32_t dst = smem_addr(ring + hs * SLOTB);
+    const uint32_t ubar = __shfl_sync(0xffffffffu, bar, 0);
+    const uint32_t udst = __shfl_sync(0xffffffffu, dst, 0);
+    const unsigned long long usrc = __shfl_sync(0xffffffffu, (unsigned long long)hw, 0);
+    if (lane == 0) {
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(ubar),
+                   "n"(kSlotChunks * 512)
+                   : "memory");
       asm volatile(
-          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-              dst + kSlotChunks * 512 + gi * 16 * ES),
-          "l"(src + (size_t)gi * N), "r"(sbytes), "r"(bar)
+          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(udst),
+          "l"(usrc), "n"(kSlotChunks * 512), "r"(ubar)
           : "memory");
-    ++hv;
+    }
+    if (lane < NL) {
+      if (lcopy)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + kSlotChunks * 512 + lg * 16 * ES + lp * 16),
+                     "l"(lsc)
+                     : "memory");
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+    }
+    hw += kSlotChunks * 512;
     if (++hj == SPT) {
       hj = 0;
       ++ht;
+      head_tile();
+    } else {
+      lsc += GPS * srow;
     }
-    if (++hs == S) hs = 0;
+    hs = hs + 1 == S ? 0 : hs + 1;
   };
-  if (lane == 0)
-    for (int i = 0; i < S && i < n; ++i) issue_next();
+  for (int i = 0; i < S && i < n; ++i) issue_next();
 
-  // ---- stage A: exponent bands as fp16, permuted for the B operands
-  {
-    const int n16 = (M * K) >> 3;                  // 16-byte pieces of A
-    const uint32_t dst0 = smem_addr(araw);
-    for (int i = threadIdx.x; i < n16; i += blockDim.x)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + 16u * i),
-                   "l"(reinterpret_cast<const uint4 *>(p.A) + i)
-                   : "memory");
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
+  // ---- stage A: exponent bands as fp16, permuted for the B operands.  Each thread reads
+  // 16-byte pieces of A (8 consecutive k of one row) from global memory: once for the row's
+  // exponent range, once more to convert and store them.
   for (int idx = threadIdx.x; idx < RS; idx += blockDim.x) bands[idx] = 0u;   // zero row 0
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();                                 // raw A visible; s_emax / s_emin set
-  const int wpr = K >> 1;                          // bf16 pairs per row
+  const int ppr = K >> 3;                          // pieces per row
+  const uint4 *A4 = reinterpret_cast<const uint4 *>(p.A);
   // exponent range of each row: the magnitude bits (bits & 0x7FFF) order like the values
   for (int m = 0; m < M; ++m) {
     unsigned mx = 0u, mn = 0xFFFFu;
-    for (int w = threadIdx.x; w < wpr; w += blockDim.x) {
-      const uint32_t mag = araw[m * wpr + w] & 0x7FFF7FFFu;
-      const uint32_t lo = mag & 0xFFFFu, hi = mag >> 16;
-      mx = max(mx, max(lo, hi));
-      mn = min(mn, min(lo ? lo : 0xFFFFu, hi ? hi : 0xFFFFu));   // smallest non-zero
+    for (int pc = threadIdx.x; pc < ppr; pc += blockDim.x) {
+      const uint4 v = A4[(size_t)m * ppr + pc];
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t mag = wv[e] & 0x7FFF7FFFu;
+        const uint32_t lo = mag & 0xFFFFu, hi = mag >> 16;
+        mx = max(mx, max(lo, hi));
+        mn = min(mn, min(lo ? lo : 0xFFFFu, hi ? hi : 0xFFFFu));   // smallest non-zero
+      }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
     mn = __reduce_min_sync(0xffffffffu, mn);
@@ -267,7 +290,8 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
     }
   }
   __syncthreads();
-  // band row 1 + 2m + b holds band b of activation row m (only if the row needs it)
+  // band row 1 + 2m + b holds band b of activation row m (only if the row needs it).  The
+  // four words of piece pc (k = 8 pc .. 8 pc + 7) go to base(pc) + 0, 4, 8, 12 of the row.
   for (int v = 0; v < 2 * M; ++v) {
     const int m = v >> 1, b = v & 1;
     const int emax = s_emax[m], emin = s_emin[m];
@@ -275,44 +299,43 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
     if (b >= nbu) continue;
     const int sb_ = 142 - emax + 32 * b;           // scale exponent of band b
     uint32_t *brw = bands + (1 + v) * RS;
-    if (nbu == 1 && emax < 255) {
-      // every non-zero element of the row lies in band 0: scale them all by 2^sb (two exact
-      // power-of-two products, each factor a normal float) and round to fp16, which is
-      // exact for bf16 significands in [2^-16, 2^16)
-      const int s1 = sb_ / 2, s2 = sb_ - s1;
-      const float c1 = __int_as_float((127 + s1) << 23), c2 = __int_as_float((127 + s2) << 23);
-      for (int w = threadIdx.x; w < wpr; w += blockDim.x) {
-        const uint32_t raw = araw[m * wpr + w];
-        const __half2 h = __floats2half2_rn(__uint_as_float(raw << 16) * c1 * c2,
-                                            __uint_as_float(raw & 0xFFFF0000u) * c1 * c2);
-        const int kk = 2 * w;
-        const int c = kk >> 6, r = kk & 63, j = r >> 4, hh = (r >> 3) & 1, qq = (r & 7) >> 1;
-        brw[c * 32 + (j >> 1) * 16 + qq * 4 + (j & 1) * 2 + hh] =
-            *reinterpret_cast<const uint32_t *>(&h);
-      }
-      continue;
-    }
-    for (int w = threadIdx.x; w < wpr; w += blockDim.x) {
-      const uint32_t raw = araw[m * wpr + w];
-      uint32_t pair = 0u;
+    const bool fast = nbu == 1 && emax < 255;
+    // every non-zero element of a single-band row lies in band 0: scale them all by 2^sb
+    // (two exact power-of-two products, each factor a normal float) and round to fp16, which
+    // is exact for bf16 significands in [2^-16, 2^16)
+    const int s1 = sb_ / 2, s2 = sb_ - s1;
+    const float c1 = __int_as_float((127 + s1) << 23), c2 = __int_as_float((127 + s2) << 23);
+    for (int pc = threadIdx.x; pc < ppr; pc += blockDim.x) {
+      const uint4 vv = A4[(size_t)m * ppr + pc];
+      const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
+      uint32_t *dst = brw + (pc >> 3) * 32 + ((pc & 7) >> 2) * 16 + ((pc >> 1) & 1) * 2 + (pc & 1);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t bits = (raw >> (16 * h)) & 0xFFFFu;
-        const int ex = (bits >> 7) & 0xFF;
-        if ((bits & 0x7FFFu) && ((emax - ex) >> 5) == b) {
-          float f;
-          if (ex == 255)
-            f = __uint_as_float(bits << 16);                        // inf / nan stay so
-          else if (ex == 0)
-            f = ldexpf(__uint_as_float(bits << 16), sb_);           // bf16 subnormal
-          else
-            f = __uint_as_float((bits << 16) + ((uint32_t)sb_ << 23));  // exponent + sb
-          pair |= (uint32_t)__half_as_ushort(__float2half_rn(f)) << (16 * h);
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t raw = wv[e];
+        uint32_t pair = 0u;
+        if (fast) {
+          const __half2 h = __floats2half2_rn(__uint_as_float(raw << 16) * c1 * c2,
+                                              __uint_as_float(raw & 0xFFFF0000u) * c1 * c2);
+          pair = *reinterpret_cast<const uint32_t *>(&h);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t bits = (raw >> (16 * h)) & 0xFFFFu;
+            const int ex = (bits >> 7) & 0xFF;
+            if ((bits & 0x7FFFu) && ((emax - ex) >> 5) == b) {
+              float f;
+              if (ex == 255)
+                f = __uint_as_float(bits << 16);                        // inf / nan stay so
+              else if (ex == 0)
+                f = ldexpf(__uint_as_float(bits << 16), sb_);           // bf16 subnormal
+              else
+                f = __uint_as_float((bits << 16) + ((uint32_t)sb_ << 23));  // exponent + sb
+              pair |= (uint32_t)__half_as_ushort(__float2half_rn(f)) << (16 * h);
+            }
+          }
         }
+        dst[4 * e] = pair;
       }
-      const int kk = 2 * w;
-      const int c = kk >> 6, r = kk & 63, j = r >> 4, hh = (r >> 3) & 1, qq = (r & 7) >> 1;
-      brw[c * 32 + (j >> 1) * 16 + qq * 4 + (j & 1) * 2 + hh] = pair;
     }
   }
   __syncthreads();
@@ -373,8 +396,8 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
       // columns r0 and r0 + 8
       const int mrow = mt * 4 + q;
       const int emax = mrow < M ? s_emax[mrow] : 127;
-      const float v0 = ldexpf(acc[mt][0], emax - 142) + ldexpf(acc[mt][1], emax - 174);
-      const float v1 = ldexpf(acc[mt][2], emax - 142) + ldexpf(acc[mt][3], emax - 174);
+      const float v0 = scale_pow2(acc[mt][0], emax - 142) + scale_pow2(acc[mt][1], emax - 174);
+      const float v1 = scale_pow2(acc[mt][2], emax - 142) + scale_pow2(acc[mt][3], emax - 174);
       acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
       if (mrow >= M) continue;
       if (j0 == 0 && j1 == SPT) {
@@ -424,13 +447,13 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
       for (int jj = 0; jj < 4; ++jj) {
         const int stp = ch * 4 + jj;                 // compile-time 16-k step of the slot
         const int gi = stp / SPG;
-        const uint32_t zl = ZP ? zlo_of(zcur[gi][0]) : p.dk.lo_sym;
-        const uint32_t zh = ZP ? zhi_of(zcur[gi][1]) : p.dk.hi_sym;
+        const uint32_t zl = ZP ? zlo_of(zcur[gi][0]) : kLoSym;
+        const uint32_t zh = ZP ? zhi_of(zcur[gi][1]) : kHiSym;
         const uint32_t w = words[jj], w8 = w >> 8;
-        const uint32_t a0 = hsub2_u(lop3_and_or(w, p.dk.lo_mask, p.dk.magic), zl);
-        const uint32_t a1 = hfma2_u(lop3_and_or(w, p.dk.hi_mask, p.dk.magic), p.dk.sixteenth, zh);
-        const uint32_t a2 = hsub2_u(lop3_and_or(w8, p.dk.lo_mask, p.dk.magic), zl);
-        const uint32_t a3 = hfma2_u(lop3_and_or(w8, p.dk.hi_mask, p.dk.magic), p.dk.sixteenth, zh);
+        const uint32_t a0 = hsub2_u(lop3_and_or<0x000F000Fu>(w, kMagic), zl);
+        const uint32_t a1 = hfma2_u(lop3_and_or<0x00F000F0u>(w, kMagic), kSixteenth, zh);
+        const uint32_t a2 = hsub2_u(lop3_and_or<0x000F000Fu>(w8, kMagic), zl);
+        const uint32_t a3 = hfma2_u(lop3_and_or<0x00F000F0u>(w8, kMagic), kSixteenth, zh);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           if (stp % SPG == 0)
@@ -454,8 +477,8 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
     // every lane has consumed the slot (its shared-memory reads fed the instructions above);
     // order those generic-proxy reads before the bulk copy's writes, then refill
     __syncwarp();
-    if (lane == 0 && i + S < n) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (i + S < n) {
+      if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue_next();
     }
     if (++s == S) {
@@ -610,7 +633,7 @@ size_t stripe_smem_bytes(int M, int K, int G, int prec, int slots) {
       (((size_t)(1 + 2 * M) * act_row_words(K / kChunkK) * 4) + 127) & ~(size_t)127;
   const size_t rings = (size_t)kStrWarps * slots * stripe_slot_bytes(G, es);
   const size_t pieces = (size_t)kStrWarps * 2 * M * kTileN * 4;
-  return bands + rings + pieces + (size_t)M * K * 2;
+  return bands + rings + pieces;
 }
 
 int stripe_slots_for(int M, int K, int G, int prec, size_t smem_cap) {
@@ -640,8 +663,6 @@ cudaError_t launch_stripe_decode(const Plan &pl, int M, int K, int N, int G, int
   sp.split_mult = pl.split_mult;
   sp.S = pl.slots;
   sp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
-  sp.dk = DecodeConsts{0x000F000Fu, 0x00F000F0u, 0x64006400u, 0x2C002C00u, 0x64086408u,
-                       0xD480D480u};
   switch (G) {
     case 32: return launch_stripe_g<32>(pl, prec, sp, s);
     case 64: return launch_stripe_g<64>(pl, prec, sp, s);
