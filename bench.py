@@ -411,6 +411,7 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
     fraction of the roofline that bounds it (HBM below M = 128, dense BF16 above)."""
     from group_quantized_weight_gb300.constants import algorithmic_bytes, gemm_flops, prec_flags
     out = []
+    side = torch.cuda.Stream()           # graph capture needs a stream other than the legacy one
     for name in ("tiny_gemv", "decode_gateup", "q8_m1", "q8_m32", "asym_m16", "prefill"):
         cfg = gq_synth.CONFIGS[name]
         prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
@@ -431,14 +432,16 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
                           [w.data_ptr() for w in W], [x.data_ptr() for x in S],
                           [z.data_ptr() for z in Z] if Z else None, o.data_ptr(),
                           warmup=3, iters=10 if big else 200, use_graph=not big,
-                          stream=torch.cuda.current_stream().cuda_stream)
+                          stream=side.cuda_stream)
         us = res["us_per_call"]
         gbs = nbytes / (us * 1e-6) / 1e9
         tf = gemm_flops(cfg.M, cfg.K, cfg.N) / (us * 1e-6) / 1e12
         plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
         row = {"workload": name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "G": cfg.G,
                "path": plan["path"], "us": us, "GB/s": gbs, "TFLOPS": tf,
-               "l2": "from HBM" if copies * wbytes > 2 * L2_BYTES else "L2-resident weights"}
+               "weight_copies": copies,
+               "l2": ("from HBM (rotated copies exceed L2)" if copies * wbytes > L2_BYTES
+                      else "weights fit in L2")}
         if big:
             row.update(bound="tensor", frac=tf / peaks["bf16_tflops"],
                        peak=f"bf16_tflops of {peak_kind}")
@@ -468,7 +471,8 @@ def _m_sweep(gq, torch, dev, peaks):
     Wd = [torch.randn(base.N, base.K, device=dev).to(torch.bfloat16) for _ in range(copies)]
     rows = []
     crossover = None
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()         # graph capture needs a stream other than the legacy one
+    torch.cuda.synchronize()
     for M in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096):
         a = gq_synth.make_activations(base, seed=0, M=M)
         A = torch.from_numpy(a.view(np.int16)).to(dev)

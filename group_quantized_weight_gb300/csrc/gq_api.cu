@@ -73,11 +73,11 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const size_t kSmemCap = 96u << 10;   // activation slice budget per CTA (bytes)
   const int Mc = M > 0 ? M : 1;
   const int Nc = N > 0 ? N : 8;
+  const size_t kCtaSmemCap = 227u * 1024u - 1024u;   // minus the static shared memory
   // striped persistent decode (M <= 8): one CTA of kStrWarps warps per SM over a
   // contiguous range of (tile, 256-k slot) pairs; whole tiles per CTA when that keeps the
   // SMs within 10% of even, else equal slot ranges with a cross-CTA reduction
-  const size_t kStripeSmemCap = 227u * 1024u - 1024u;   // minus the static shared memory
-  const int slots = stripe_supported(Mc, K, G, prec) ? stripe_slots_for(Mc, K, G, prec, kStripeSmemCap) : 0;
+  const int slots = stripe_supported(Mc, K, G, prec) ? stripe_slots_for(Mc, K, G, prec, kCtaSmemCap) : 0;
   if (slots >= 2) {
     p->path = kPathStripe;
     p->mt = Mc <= 4 ? 1 : 2;   // MMA blocks
@@ -412,27 +412,39 @@ int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   int rc = GQ_OK;
+  auto cuda_ok = [&](cudaError_t e, const char *where) {
+    if (e == cudaSuccess) return true;
+    note_cuda_error(where, e);
+    rc = GQ_ERR_CUDA;
+    return false;
+  };
   if (a->use_graph) {
-    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) rc = GQ_ERR_CUDA;
-    for (int i = 0; i < a->iters && rc == GQ_OK; ++i) rc = call(i);
-    cudaGraph_t g2 = nullptr;
-    if (cudaStreamEndCapture(s, &g2) != cudaSuccess) rc = GQ_ERR_CUDA;
-    graph = g2;
-    if (rc == GQ_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = GQ_ERR_CUDA;
-    if (rc == GQ_OK && cudaGraphLaunch(exec, s) != cudaSuccess) rc = GQ_ERR_CUDA;   // warm
+    // capture needs a stream other than the legacy default stream
+    if (cuda_ok(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal), "cudaStreamBeginCapture")) {
+      for (int i = 0; i < a->iters && rc == GQ_OK; ++i) rc = call(i);
+      cudaGraph_t g2 = nullptr;
+      const cudaError_t ee = cudaStreamEndCapture(s, &g2);
+      if (rc == GQ_OK) cuda_ok(ee, "cudaStreamEndCapture");
+      graph = g2;
+    }
+    if (rc == GQ_OK) cuda_ok(cudaGraphInstantiate(&exec, graph, 0), "cudaGraphInstantiate");
+    if (rc == GQ_OK) cuda_ok(cudaGraphLaunch(exec, s), "cudaGraphLaunch");   // warm
   }
   if (rc == GQ_OK) {
     cudaEventRecord(e0, s);
     if (a->use_graph) {
-      if (cudaGraphLaunch(exec, s) != cudaSuccess) rc = GQ_ERR_CUDA;
+      cuda_ok(cudaGraphLaunch(exec, s), "cudaGraphLaunch");
     } else {
       for (int i = 0; i < a->iters && rc == GQ_OK; ++i) rc = call(i);
     }
     cudaEventRecord(e1, s);
   }
-  if (cudaStreamSynchronize(s) != cudaSuccess) rc = GQ_ERR_CUDA;
+  {
+    const cudaError_t es = cudaStreamSynchronize(s);
+    if (rc == GQ_OK) cuda_ok(es, "cudaStreamSynchronize");
+  }
   float ms = 0.f;
-  if (rc == GQ_OK && cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) rc = GQ_ERR_CUDA;
+  if (rc == GQ_OK) cuda_ok(cudaEventElapsedTime(&ms, e0, e1), "cudaEventElapsedTime");
   if (exec) cudaGraphExecDestroy(exec);
   if (graph) cudaGraphDestroy(graph);
   cudaEventDestroy(e0);

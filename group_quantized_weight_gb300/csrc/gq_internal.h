@@ -81,6 +81,7 @@ cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, 
 int prefill_read_error(int clear);
 int stripe_read_error(int clear);
 
+
 // Records why a call is about to return GQ_ERR_CUDA (thread-local; read by gq_last_error_detail).
 void note_cuda_error(const char *where, cudaError_t e);
 void note_cuda_error_code(const char *where, int code);

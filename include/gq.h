@@ -139,7 +139,8 @@ int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, const void *A,
  * total make every call read from HBM), and reports the mean time per call from CUDA
  * events recorded on `stream`.  With use_graph != 0 the `iters` calls are captured once
  * into a CUDA graph and the graph is replayed (no host launch overhead); the workspace
- * must already exist then (call gq_gemm once first).  Synchronizes `stream`. */
+ * must already exist then (call gq_gemm once first), and `stream` must not be the legacy
+ * default stream (NULL), which cannot be captured.  Synchronizes `stream`. */
 typedef struct gq_bench_args {
   int M, K, N, G, prec;
   const void *A;
@@ -162,8 +163,9 @@ int gq_bench(const gq_bench_args *args, gq_bench_result *result);
 /* Host-only description of the launch gq_gemm would make (for tests and reports).
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {
-  int path;          /* 0 = small-M tensor-core decode (mma.sync), 1 = INT8 CUDA-core decode,
-                        2 = large-M tcgen05 prefill */
+  int path;          /* 0 = small-M tensor-core decode (mma.sync, K split across CTAs),
+                        1 = INT8 CUDA-core decode, 2 = large-M tcgen05 prefill,
+                        3 = striped decode (M <= 8, warps stream contiguous slot ranges) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
   int n_tile;        /* output columns one CTA covers */
