@@ -110,6 +110,38 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->nsplit = p->grid_x;
     return GQ_OK;
   }
+  // small batch (M <= 64): persistent CTAs over (K slice, tile range) pairs, activation
+  // slices in shared memory, slices added by the last CTA of each tile range
+  if (Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)) {
+    const int ksl = batch_slice_k(Mc, K);
+    const int slots = batch_slots_for(Mc, ksl, G, prec, kCtaSmemCap);
+    if (slots >= 2) {
+      const int ks = K / ksl, rb = ceil_div(Mc, 32);
+      int cps = sms / (ks * rb);
+      if (cps < 1) cps = 1;
+      p->path = kPathBatch;
+      p->mt = 4;
+      p->m_tile = 32;
+      p->n_tile = kTileN;
+      p->unit_k = ksl;
+      p->units = ks;
+      p->nsplit = ks;
+      p->split_count = cps;
+      p->slots = slots;
+      p->grid_x = ks * cps;
+      p->grid_y = 1;
+      p->grid_z = rb;
+      p->block_threads = 16 * 32;
+      p->smem_bytes = batch_smem_bytes(Mc, ksl, G, prec, slots);
+      if (ks > 1) {
+        p->part_bytes = round_up((size_t)ks * Mc * Nc * sizeof(float), 256);
+        p->counter_bytes = kCounterRegionBytes;
+        if ((size_t)rb * cps * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
+      }
+      p->workspace_bytes = p->part_bytes + p->counter_bytes;
+      return GQ_OK;
+    }
+  }
   if (M >= kPrefillMinM && prefill_supported(M, K, N, G, prec)) {
     // large M: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
     p->path = kPathPrefill;
@@ -372,6 +404,8 @@ static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const 
     e = launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
   else if (p.path == kPathStripe)
     e = launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
+  else if (p.path == kPathBatch)
+    e = launch_batch(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else if (p.path == kPathMmaDecode)
     e = launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else
@@ -458,7 +492,8 @@ int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
 int gq_device_error(int clear) {
   const int v = prefill_read_error(clear);
   const int w = stripe_read_error(clear);
-  return v != 0 ? v : w;
+  const int x = batch_read_error(clear);
+  return v != 0 ? v : (w != 0 ? w : x);
 }
 
 }  // extern "C"

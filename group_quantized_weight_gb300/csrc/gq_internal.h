@@ -28,7 +28,8 @@ constexpr int kQ8MaxRows = 32;
 // at zero, and no problem's partial sums ever overlap them), then the partial sums.
 constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
 
-enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3 };
+enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3,
+            kPathBatch = 4 };
 
 struct Plan {
   int path;
@@ -80,13 +81,23 @@ cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, 
                            cudaStream_t s);
 int prefill_read_error(int clear);
 int stripe_read_error(int clear);
+bool batch_supported(int M, int K, int G, int prec);
+int batch_slice_k(int M, int K);
+size_t batch_smem_bytes(int M, int K_slice, int G, int prec, int slots);
+int batch_slots_for(int M, int K_slice, int G, int prec, size_t smem_cap);
+cudaError_t launch_batch(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                         const void *Wq, const void *scales, const void *zeros, void *out,
+                         float *part, unsigned *counters, cudaStream_t s);
+int batch_read_error(int clear);
 
 
 // Records why a call is about to return GQ_ERR_CUDA (thread-local; read by gq_last_error_detail).
 void note_cuda_error(const char *where, cudaError_t e);
 void note_cuda_error_code(const char *where, int code);
+// largest M of the small-batch kernel; larger M goes to the tensor-core prefill kernel
+constexpr int kBatchMaxM = 64;
 // smallest M routed to the tensor-core prefill kernel
-constexpr int kPrefillMinM = 128;
+constexpr int kPrefillMinM = 65;
 constexpr int kPrefillThreads = 512;   // block size of the prefill kernel
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,

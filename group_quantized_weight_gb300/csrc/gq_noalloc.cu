@@ -85,6 +85,8 @@ extern "C" int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, cons
     e = launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
   else if (p.path == kPathStripe)
     e = launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
+  else if (p.path == kPathBatch)
+    e = launch_batch(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else if (p.path == kPathMmaDecode)
     e = launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
   else

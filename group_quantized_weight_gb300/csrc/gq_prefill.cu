@@ -2,16 +2,17 @@
 //
 // Where the path is a dense contraction ("GPU Kernel 工程（09）：量化与融合 kernel", section 3.2:
 // at prefill both BF16 and INT4 GEMMs are compute-bound), the dequantized weights feed the
-// 5th-generation tensor cores.  Roles inside one persistent CTA per SM:
-//   warp 0      TMA producer: per 64-k stage, the packed codes of a 128-column tile (one
-//               3-D box of 8 x 512 bytes) and the 256 x 64 bf16 activation tile (128-byte
-//               swizzle) into a 4-stage shared-memory ring.
-//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
-//               M = 128 (weight columns n) x N = 256 (activation rows m) x K = 16, BF16 x
-//               BF16 -> FP32, into one of two TMEM accumulators (one per group parity).
-//   warps 2-9   workers: dequantize the next group's stages into the UMMA operand layout
-//               (K-major, 128-byte swizzle) and scale the finished group into FP32 running
-//               sums (tcgen05.ld; one scale per thread: a TMEM lane is one column n).
+// 5th-generation tensor cores.  Roles inside one persistent CTA per SM (16 warps):
+//   warp 0        TMA producer: per 64-k stage, the packed codes of a 128-column tile (one
+//                 3-D box of 8 x 512 bytes) and the 256 x 64 bf16 activation tile (128-byte
+//                 swizzle) into a 5-stage shared-memory ring.
+//   warp 1        TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
+//                 M = 128 (weight columns n) x N = 256 (activation rows m) x K = 16, BF16 x
+//                 BF16 -> FP32, into one of two TMEM accumulators (one per group parity).
+//   warpgroup 1   dequantization of each stage's codes into one of two K-major operand
+//                 buffers (exact bf16 integers q - z).
+//   warpgroups 2-3  promotion: tcgen05.ld of a finished group, times its scale (one per
+//                 thread: a TMEM lane is one column n), into FP32 running sums; epilogue.
 // The operand tiles hold the exact integers q - z (bf16 represents |q - z| <= 15 exactly);
 // each group's FP32 result is multiplied by its scale after the whole group, as the
 // group-wise GEMM of "04 · 分组量化 GEMM 内核", section 2 requires.  Rounding s * (q - z) to
@@ -29,7 +30,8 @@
 
 namespace gq {
 
-constexpr int kPfStages = 4;                 // pipeline depth (64-k stages)
+constexpr int kPfStages = 5;                 // TMA ring depth (64-k stages)
+constexpr int kPfDqBufs = 2;                 // dequantized-operand buffers
 constexpr int kPfTileN = 128;                // weight columns per tile (TMEM lanes)
 constexpr int kPfTileM = 256;                // activation rows per tile (TMEM columns)
 constexpr int kPfThreads = 512;              // 16 warps = 4 warpgroups
@@ -38,7 +40,7 @@ constexpr int kPfSumWarps = 8;               // warpgroups 2 and 3
 constexpr uint32_t kPfPackedBytes = 8 * 512;                  // packed codes per stage
 constexpr uint32_t kPfActBytes = kPfTileM * 64 * 2;           // activations per stage
 constexpr uint32_t kPfDqBytes = kPfTileN * 64 * 2;            // dequantized weights per stage
-constexpr uint32_t kPfStageBytes = kPfActBytes + kPfDqBytes + kPfPackedBytes;   // 53248
+constexpr uint32_t kPfStageBytes = kPfActBytes + kPfPackedBytes;   // 36864: one TMA stage
 constexpr long long kPfWaitCycles = 4000000000ll;              // bounded waits (~2 s)
 
 static __device__ int g_prefill_error;        // sticky status (GQ_ERR_TIMEOUT), read by the host
@@ -196,10 +198,21 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t lop3_ao(uint32_t a, uint32_t b, uint32_t c) {
+// (a & 0x000F000F) | c in one LOP3: the mask is an immediate of the instruction and c a
+// register (with both constants taken from memory operands the compiler emits two)
+__device__ __forceinline__ uint32_t lo_nibbles(uint32_t a, uint32_t c) {
   uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  asm("lop3.b32 %0, %1, 0x000F000F, %2, 0xEA;" : "=r"(r) : "r"(a), "r"(c));
   return r;
+}
+
+// two FP32 FMAs in one instruction: (x0, x1) * (y, y) + (z0, z1)
+__device__ __forceinline__ void ffma2_bcast(float &z0, float &z1, float x0, float x1, float y) {
+  asm("{\n\t.reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\tmov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 c, a, b, c;\n\tmov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(z0), "+f"(z1)
+      : "f"(x0), "f"(x1), "f"(y));
 }
 
 __device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
@@ -209,7 +222,6 @@ __device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
 }
 
 struct PrefillConsts {
-  uint32_t lo_mask;   // 0x000F000F
   uint32_t magic;     // 0x43004300: bf16 128 in both halves
   uint32_t sym;       // 0x43084308: bf16 (128 + 8)
 };
@@ -225,13 +237,15 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                   unsigned token) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kPfStages], bar_empty[kPfStages],
-      bar_dq[kPfStages], bar_acc_full[2], bar_acc_empty[2];
+      bar_dq[kPfDqBufs], bar_dq_empty[kPfDqBufs], bar_acc_full[2], bar_acc_empty[2];
   __shared__ uint32_t s_tmem;
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // stage layout: [activations 32 KB][dequantized weights 16 KB][packed codes 4 KB]
+  // TMA stage s: [activations 32 KB][packed codes 4 KB]; then kPfDqBufs dequantized
+  // operand buffers of 16 KB
   auto act_at = [&](int s) { return smem + (size_t)s * kPfStageBytes; };
-  auto dq_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes; };
-  auto pk_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes + kPfDqBytes; };
+  auto pk_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes; };
+  auto dq_at = [&](int d) { return smem + (size_t)kPfStages * kPfStageBytes + (size_t)d * kPfDqBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wg = warp >> 2;                        // warpgroup: role and register budget
@@ -243,8 +257,13 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);
-      mbar_init(smem_u32(&bar_dq[s]), kPfDqWarps);        // one arrival per dequant warp
+      // a stage is free once the MMA read its activations (commit) and every dequant warp
+      // read its codes
+      mbar_init(smem_u32(&bar_empty[s]), 1 + kPfDqWarps);
+    }
+    for (int d = 0; d < kPfDqBufs; ++d) {
+      mbar_init(smem_u32(&bar_dq[d]), kPfDqWarps);        // one arrival per dequant warp
+      mbar_init(smem_u32(&bar_dq_empty[d]), 1);           // the MMA's commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_acc_full[b]), 1);
@@ -302,20 +321,22 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           if (!ok) break;
           tc_fence_after();
           for (int st = 0; st < SPG; ++st, ++i) {
-            const int s = i % kPfStages;
-            const uint32_t ph = (i / kPfStages) & 1;
-            ok = mbar_wait(smem_u32(&bar_full[s]), ph, token) && mbar_wait(smem_u32(&bar_dq[s]), ph, token);
+            const int s = i % kPfStages, dbuf = i % kPfDqBufs;
+            const uint32_t ph = (i / kPfStages) & 1, dph = (i / kPfDqBufs) & 1;
+            ok = mbar_wait(smem_u32(&bar_full[s]), ph, token) &&
+                 mbar_wait(smem_u32(&bar_dq[dbuf]), dph, token);
             if (!ok) break;
             tc_fence_after();
             // weights: core matrices, 16 k = two of them = 256 bytes = 16 descriptor units;
             // activations: 128-byte swizzle, 16 k = 32 bytes = 2 descriptor units
-            const uint64_t da = umma_desc_plain(smem_u32(dq_at(s)), 128, 1024);
+            const uint64_t da = umma_desc_plain(smem_u32(dq_at(dbuf)), 128, 1024);
             const uint64_t db = umma_desc_sw128(smem_u32(act_at(s)));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               umma_bf16(tmem + (uint32_t)b * kPfTileM, da + 16 * k, db + 2 * k, idesc,
                         (st | k) != 0 ? 1u : 0u);
-            umma_commit(smem_u32(&bar_empty[s]));        // stage consumed
+            umma_commit(smem_u32(&bar_empty[s]));        // activations consumed
+            umma_commit(smem_u32(&bar_dq_empty[dbuf]));  // dequantized operand consumed
           }
           if (!ok) break;
           umma_commit(smem_u32(&bar_acc_full[b]));       // group finished
@@ -353,10 +374,10 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           }
         }
         for (int st = 0; st < SPG; ++st, ++i) {
-          const int s = i % kPfStages;
-          const uint32_t ph = (i / kPfStages) & 1;
-          // the slot was read by the MMA of stage i - kPfStages; the codes of stage i arrived
-          ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, token) &&
+          const int s = i % kPfStages, dbuf = i % kPfDqBufs;
+          const uint32_t ph = (i / kPfStages) & 1, dph = (i / kPfDqBufs) & 1;
+          // the buffer was read by the MMA of stage i - kPfDqBufs; the codes of stage i arrived
+          ok = mbar_wait(smem_u32(&bar_dq_empty[dbuf]), dph ^ 1, token) &&
                mbar_wait(smem_u32(&bar_full[s]), ph, token);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
@@ -365,12 +386,12 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             const uint4 f =
                 *reinterpret_cast<const uint4 *>(pk_at(s) + (2 * d + u) * 512 + lane * 16);
             const uint32_t words[4] = {f.x, f.y, f.z, f.w};
-            uint8_t *dq = dq_at(s) + (2 * d + u) * 2048 + lane * 4;
+            uint8_t *dq = dq_at(dbuf) + (2 * d + u) * 2048 + lane * 4;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
               for (int p = 0; p < 4; ++p) {        // pair p: bits 4p and 4p + 16
-                const uint32_t v = bsub2(lop3_ao(words[j] >> (4 * p), pc.lo_mask, pc.magic),
+                const uint32_t v = bsub2(lo_nibbles(words[j] >> (4 * p), pc.magic),
                                          (p & 1) ? zh[u] : zl[u]);
                 *reinterpret_cast<uint32_t *>(dq + (p & 1) * 1024 + (2 * j + (p >> 1)) * 128) = v;
               }
@@ -378,7 +399,10 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic -> tensor core
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bar_dq[s]));
+          if (lane == 0) {
+            mbar_arrive(smem_u32(&bar_dq[dbuf]));
+            mbar_arrive(smem_u32(&bar_empty[s]));          // this warp is done with the codes
+          }
         }
       }
     }
@@ -425,7 +449,8 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           tmem_ld32(taddr + c4 * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) sum[c4 * 32 + c] = fmaf(sc, v[c], sum[c4 * 32 + c]);
+          for (int c = 0; c < 32; c += 2)
+            ffma2_bcast(sum[c4 * 32 + c], sum[c4 * 32 + c + 1], v[c], v[c + 1], sc);
         }
         tc_fence_before();
         __syncwarp();
@@ -534,7 +559,9 @@ static unsigned next_token() {
   return t.fetch_add(1u) + 1u;
 }
 
-size_t prefill_smem_bytes() { return (size_t)kPfStages * kPfStageBytes + 1024; }
+size_t prefill_smem_bytes() {
+  return (size_t)kPfStages * kPfStageBytes + (size_t)kPfDqBufs * kPfDqBytes + 1024;
+}
 
 bool prefill_supported(int M, int K, int N, int G, int prec) {
   if (!(prec & GQ_W4) || (prec & GQ_ACT_F32)) return false;
@@ -557,7 +584,7 @@ static cudaError_t launch_pf(const Plan &p, int M, int K, int N, int prec, const
   kern<<<p.grid_x, kPfThreads, p.smem_bytes, s>>>(
       mw, ma, scales, reinterpret_cast<const uint32_t *>(zeros),
       f32 ? nullptr : reinterpret_cast<__nv_bfloat16 *>(out), f32 ? reinterpret_cast<float *>(out) : nullptr,
-      M, K, N, f32 ? 1 : 0, PrefillConsts{0x000F000Fu, 0x43004300u, 0x43084308u},
+      M, K, N, f32 ? 1 : 0, PrefillConsts{0x43004300u, 0x43084308u},
       next_token());
   return cudaGetLastError();
 }

@@ -121,6 +121,18 @@ def test_plan_is_a_pure_function_of_shape(name):
         else:
             assert tiles >= 152
         return
+    if p1["path"] == 4:
+        # small-batch kernel: (K slice, tile range) CTAs x 32-row blocks, at most one wave
+        assert 1 <= cfg.M <= 64 and cfg.K % 256 == 0
+        ks = p1["nsplit"]
+        assert cfg.K % ks == 0 and (cfg.K // ks) % 256 == 0
+        assert min(cfg.M, 32) * (cfg.K // ks) * 2 <= 64 * 1024
+        assert p1["grid_z"] == -(-cfg.M // 32)
+        assert p1["grid_x"] * p1["grid_z"] <= 152
+        assert p1["smem_bytes"] <= 227 * 1024
+        if ks > 1:
+            assert p1["workspace_bytes"] >= ks * cfg.M * cfg.N * 4
+        return
     assert p1["smem_bytes"] <= 200 * 1024
     assert 1 <= p1["nsplit"] <= units
     assert p1["grid_y"] == p1["nsplit"]
