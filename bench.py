@@ -314,7 +314,7 @@ def main():
     if not args.no_sweep and rank == 0:
         sweep = _m_sweep(gq, torch, dev, peaks)
 
-    traffic = _kernel_traffic("gq_stripe.cu", "w4_stripe_decode_decode_gateup.md")
+    traffic = _kernel_traffic("gq_stripe.cu", "w4_stripe_decode_gateup.md")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

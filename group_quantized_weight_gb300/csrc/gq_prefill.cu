@@ -5,12 +5,13 @@
 // 5th-generation tensor cores.  Roles inside one persistent CTA per SM (16 warps):
 //   warp 0        TMA producer: per 64-k stage, the packed codes of a 128-column tile (one
 //                 3-D box of 8 x 512 bytes) and the 256 x 64 bf16 activation tile (128-byte
-//                 swizzle) into a 5-stage shared-memory ring.
+//                 swizzle) into a 4-stage shared-memory ring.
 //   warp 1        TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
 //                 M = 128 (weight columns n) x N = 256 (activation rows m) x K = 16, BF16 x
 //                 BF16 -> FP32, into one of two TMEM accumulators (one per group parity).
-//   warpgroup 1   dequantization of each stage's codes into one of two K-major operand
-//                 buffers (exact bf16 integers q - z).
+//   warpgroup 1   dequantization of each stage's codes into one of four K-major operand
+//                 buffers (exact bf16 integers q - z), so it can run up to three stages
+//                 ahead of the MMA.
 //   warpgroups 2-3  promotion: tcgen05.ld of a finished group, times its scale (one per
 //                 thread: a TMEM lane is one column n), into FP32 running sums; epilogue.
 // The operand tiles hold the exact integers q - z (bf16 represents |q - z| <= 15 exactly);
@@ -30,8 +31,8 @@
 
 namespace gq {
 
-constexpr int kPfStages = 5;                 // TMA ring depth (64-k stages)
-constexpr int kPfDqBufs = 2;                 // dequantized-operand buffers
+constexpr int kPfStages = 4;                 // TMA ring depth (64-k stages)
+constexpr int kPfDqBufs = 4;                 // dequantized-operand buffers
 constexpr int kPfTileN = 128;                // weight columns per tile (TMEM lanes)
 constexpr int kPfTileM = 256;                // activation rows per tile (TMEM columns)
 constexpr int kPfThreads = 512;              // 16 warps = 4 warpgroups
