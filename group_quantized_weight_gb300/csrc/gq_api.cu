@@ -110,6 +110,30 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->nsplit = p->grid_x;
     return GQ_OK;
   }
+  // INT8 codes, M <= 32: CUDA-core FP32 kernel, 64 columns x one K slice per CTA
+  if (Mc <= kQ8BlockMaxM && q8_block_supported(Mc, K, G, prec)) {
+    const int ks = q8_block_slices(Mc, K, Nc, G, sms, kPartCap);
+    if (ks >= 1) {
+      p->path = kPathQ8Block;
+      p->m_tile = Mc;
+      p->n_tile = q8_block_cols();
+      p->unit_k = G;
+      p->units = K / G;
+      p->nsplit = ks;
+      p->grid_x = ceil_div(Nc, p->n_tile) * ks;
+      p->grid_y = p->grid_z = 1;
+      p->block_threads = q8_block_threads();
+      p->smem_bytes = q8_block_smem_bytes(Mc, K, G, ks);
+      if (ks > 1) {
+        p->part_bytes = round_up((size_t)ks * Mc * Nc * sizeof(float), 256);
+        p->counter_bytes = kCounterRegionBytes;
+        if ((size_t)ceil_div(Nc, p->n_tile) * sizeof(unsigned) > kCounterRegionBytes)
+          return GQ_ERR_UNSUPPORTED;
+      }
+      p->workspace_bytes = p->part_bytes + p->counter_bytes;
+      return GQ_OK;
+    }
+  }
   // small batch (M <= 64): persistent CTAs over (K slice, tile range) pairs, activation
   // slices in shared memory, slices added by the last CTA of each tile range
   if (Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)) {
@@ -252,6 +276,29 @@ static int get_scratch(size_t need, void **out) {
   }
   *out = d.ptr;
   return GQ_OK;
+}
+
+cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                        const void *Wq, const void *scales, const void *zeros, void *out,
+                        float *part, unsigned *counters, cudaStream_t s) {
+  switch (p.path) {
+    case kPathPrefill:
+      return launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
+    case kPathStripe:
+      return launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part,
+                                  counters, s);
+    case kPathBatch:
+      return launch_batch(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
+    case kPathMmaDecode:
+      return launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters,
+                               s);
+    case kPathQ8Block:
+      return launch_q8_block(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
+    case kPathQ8Decode:
+      return launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 static thread_local char g_detail[160];
@@ -399,17 +446,8 @@ static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const 
   unsigned *counters = (unsigned *)ws;
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e;
-  if (p.path == kPathPrefill)
-    e = launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
-  else if (p.path == kPathStripe)
-    e = launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
-  else if (p.path == kPathBatch)
-    e = launch_batch(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
-  else if (p.path == kPathMmaDecode)
-    e = launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
-  else
-    e = launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
+  const cudaError_t e = launch_plan(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part,
+                                    counters, s);
   if (e != cudaSuccess) {
     note_cuda_error("launch", e);
     cudaGetLastError();

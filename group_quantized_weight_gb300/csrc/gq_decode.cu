@@ -240,7 +240,8 @@ q8_decode_kernel(const uint4 *__restrict__ Wp, const float *__restrict__ A,
   for (int m = 0; m < MR; ++m) acc[m] = 0.f;
 
   if (n < N) {
-    const uint4 *wp = Wp + (size_t)(kb / kChunkK8) * N + n;
+    const uint4 *wp = Wp + w8_chunk_index(K, N, n, kb / kChunkK8);
+    const int rs = w8_chunk_index(K, N, n, 1) - w8_chunk_index(K, N, n, 0);   // row stride
     const int nch = KS / kChunkK8;
     const int cpg = G / kChunkK8;
     const int g_end = ke / G;
@@ -256,7 +257,7 @@ q8_decode_kernel(const uint4 *__restrict__ Wp, const float *__restrict__ A,
     uint4 buf[kPF];
 #pragma unroll
     for (int i = 0; i < kPF; ++i)
-      buf[i] = (i < nch) ? ld_stream(wp + (size_t)i * N) : make_uint4(0, 0, 0, 0);
+      buf[i] = (i < nch) ? ld_stream(wp + (size_t)i * rs) : make_uint4(0, 0, 0, 0);
 
     for (int c0 = 0; c0 < nch; c0 += kPF) {
 #pragma unroll
@@ -264,7 +265,7 @@ q8_decode_kernel(const uint4 *__restrict__ Wp, const float *__restrict__ A,
         const int c = c0 + i;
         if (c >= nch) break;
         const uint4 cur = buf[i];
-        if (c + kPF < nch) buf[i] = ld_stream(wp + (size_t)(c + kPF) * N);
+        if (c + kPF < nch) buf[i] = ld_stream(wp + (size_t)(c + kPF) * rs);
         const uint32_t words[4] = {cur.x ^ 0x80808080u, cur.y ^ 0x80808080u,
                                    cur.z ^ 0x80808080u, cur.w ^ 0x80808080u};
         float f[16];

@@ -12,8 +12,17 @@ namespace gq {
 // Packed W4 layout: 16-column tiles x 64-k chunks; a chunk is 32 lanes x 16 bytes.
 constexpr int kTileN = 16;
 constexpr int kChunkK = 64;
-// Packed W8 layout: [K/16][N][16 bytes].
+// Packed W8 layout: 64-column blocks stored one after another, each holding its K/16 chunk
+// rows contiguously; a chunk row of block b is w_b = min(64, N - 64b) columns x 16 bytes
+// (16 consecutive k of one column).  K·N bytes in all.
 constexpr int kChunkK8 = 16;
+constexpr int kColBlock8 = 64;
+// 16-byte index of chunk row c (k = 16c .. 16c+15) of column n
+__host__ __device__ inline size_t w8_chunk_index(int K, int N, int n, int c) {
+  const int b = n / kColBlock8, j = n - b * kColBlock8;
+  const int wb = N - b * kColBlock8 < kColBlock8 ? N - b * kColBlock8 : kColBlock8;
+  return (size_t)b * (kColBlock8 / kChunkK8) * K + (size_t)c * wb + j;
+}
 
 // Small-M tensor-core decode kernel: warps per CTA (each warp owns one 16-column tile).
 constexpr int kDecWarps = 8;
@@ -29,7 +38,7 @@ constexpr int kQ8MaxRows = 32;
 constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
 
 enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3,
-            kPathBatch = 4 };
+            kPathBatch = 4, kPathQ8Block = 5 };
 
 struct Plan {
   int path;
@@ -102,5 +111,20 @@ constexpr int kPrefillThreads = 512;   // block size of the prefill kernel
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,
                              void *out, float *part, unsigned *counters, cudaStream_t s);
+// INT8 CUDA-core kernel for M <= kQ8BlockMaxM (64 columns x one K slice per CTA)
+constexpr int kQ8BlockMaxM = 32;
+bool q8_block_supported(int M, int K, int G, int prec);
+size_t q8_block_smem_bytes(int M, int K, int G, int KS);
+int q8_block_slices(int M, int K, int N, int G, int sms, size_t part_cap);
+int q8_block_cols();
+int q8_block_threads();
+cudaError_t launch_q8_block(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                            const void *Wq, const void *scales, void *out, float *part,
+                            unsigned *counters, cudaStream_t s);
+// Launches the kernel of plan p (any path); part and counters may be NULL when the plan
+// needs no workspace.
+cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                        const void *Wq, const void *scales, const void *zeros, void *out,
+                        float *part, unsigned *counters, cudaStream_t s);
 
 }  // namespace gq

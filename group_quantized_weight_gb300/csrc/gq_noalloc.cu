@@ -80,17 +80,8 @@ extern "C" int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, cons
     cudaGetLastError();
     return GQ_ERR_CUDA;
   }
-  cudaError_t e;
-  if (p.path == kPathPrefill)
-    e = launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
-  else if (p.path == kPathStripe)
-    e = launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
-  else if (p.path == kPathBatch)
-    e = launch_batch(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
-  else if (p.path == kPathMmaDecode)
-    e = launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
-  else
-    e = launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
+  const cudaError_t e = launch_plan(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part,
+                                    counters, s);
   if (e != cudaSuccess) {
     note_cuda_error("launch", e);
     cudaGetLastError();

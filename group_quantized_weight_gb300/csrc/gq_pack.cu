@@ -9,7 +9,9 @@
 //   with the first k of the pair at bits 4i..4i+3 and the second at bits 4i+16..4i+19,
 //   so that (word >> 4i) & 0x000F000F leaves the two codes in the low bits of the two
 //   16-bit halves, ready for the BF16 magic 0x4300.
-// W8: packed[c][n][b] = codes[16c + b][n] (16 consecutive k of one column per 16 bytes).
+// W8: 64-column blocks, each with its K/16 chunk rows contiguous: the 16 bytes at chunk row c
+// of column n hold codes[16c + b][n], b = 0..15, so that a warp streaming one block's k range
+// reads one contiguous run of memory.
 #include "gq_internal.h"
 
 namespace gq {
@@ -45,15 +47,19 @@ __global__ void pack_w4_kernel(int K, int N, const uint32_t *__restrict__ codes,
 
 __global__ void pack_w8_kernel(int K, int N, const int8_t *__restrict__ codes,
                                uint8_t *__restrict__ packed, size_t total_vecs) {
+  const size_t per_block = (size_t)(kColBlock8 / kChunkK8) * K;   // 16-byte vectors
   for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total_vecs;
        o += (size_t)gridDim.x * blockDim.x) {
-    const int n = (int)(o % N);
-    const size_t c = o / N;
+    const int b = (int)(o / per_block);
+    const size_t rem = o - (size_t)b * per_block;
+    const int wb = N - b * kColBlock8 < kColBlock8 ? N - b * kColBlock8 : kColBlock8;
+    const size_t c = rem / wb;
+    const int n = b * kColBlock8 + (int)(rem - c * wb);
     uint32_t w[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int b = 0; b < 16; ++b) {
-      const uint32_t v = (uint8_t)codes[(c * 16 + b) * (size_t)N + n];
-      w[b >> 2] |= v << (8 * (b & 3));
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t v = (uint8_t)codes[(c * 16 + e) * (size_t)N + n];
+      w[e >> 2] |= v << (8 * (e & 3));
     }
     reinterpret_cast<uint4 *>(packed)[o] = make_uint4(w[0], w[1], w[2], w[3]);
   }

@@ -164,8 +164,12 @@ int gq_bench(const gq_bench_args *args, gq_bench_result *result);
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {
   int path;          /* 0 = small-M tensor-core decode (mma.sync, K split across CTAs),
-                        1 = INT8 CUDA-core decode, 2 = large-M tcgen05 prefill,
-                        3 = striped decode (M <= 8, warps stream contiguous slot ranges) */
+                        1 = INT8 CUDA-core decode (M > 32), 2 = large-M tcgen05 prefill,
+                        3 = striped decode (M <= 8, warps stream contiguous slot ranges),
+                        4 = small-batch tensor-core kernel (M <= 64, persistent CTAs over
+                            (K slice, tile range) pairs),
+                        5 = INT8 CUDA-core kernel for M <= 32 (64 columns x one K slice
+                            per CTA, paired FP32 FMAs) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
   int n_tile;        /* output columns one CTA covers */

@@ -80,6 +80,13 @@ Q8_SHAPES = [
                     out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("q8_bf16_out", M=2, K=256, N=64, G=32, w4=False, act="f32", sc="f32",
                     out="bf16", s_lo=1e-3, s_hi=1e-2),
+    # rows padded to the warps' row blocks, several K slices, a ragged last column block
+    gq_synth.Config("q8_m12_split", M=12, K=1024, N=200, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_m24_g256", M=24, K=2048, N=136, G=256, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_m32_g64_bf16", M=32, K=512, N=328, G=64, w4=False, act="f32",
+                    sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),
 ]
 
 
@@ -221,13 +228,29 @@ def test_pack_roundtrip_w4(gq):
     assert np.array_equal(q, inp["q"].astype(np.int64))
 
 
+def _unpack_w8_device_layout(packed: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Inverse of the W8 device layout: 64-column blocks one after another, each holding its
+    K/16 rows of 16-byte chunks (16 consecutive k of one column) contiguously; the last
+    block is N mod 64 columns wide when N is not a multiple of 64."""
+    flat = packed.view(np.int8).reshape(-1)
+    q = np.empty((K, N), dtype=np.int8)
+    off = 0
+    for n0 in range(0, N, 64):
+        wb = min(64, N - n0)
+        blk = flat[off:off + (K // 16) * wb * 16].reshape(K // 16, wb, 16)
+        q[:, n0:n0 + wb] = blk.transpose(0, 2, 1).reshape(K, wb)
+        off += (K // 16) * wb * 16
+    assert off == K * N
+    return q
+
+
 def test_pack_roundtrip_w8(gq):
-    cfg = gq_synth.Config("pack8", M=1, K=64, N=24, G=32, w4=False, act="f32", sc="f32", out="f32")
+    cfg = gq_synth.Config("pack8", M=1, K=64, N=152, G=32, w4=False, act="f32", sc="f32",
+                          out="f32")   # two full column blocks and one of 24 columns
     inp = gq_synth.make_weights(cfg, seed=5)
     from group_quantized_weight_gb300.constants import GQ_ACT_F32, GQ_SC_F32
     packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, GQ_ACT_F32 | GQ_SC_F32)
-    p = packed.cpu().numpy().view(np.int8).reshape(cfg.K // 16, cfg.N, 16)
-    q = p.transpose(0, 2, 1).reshape(cfg.K, cfg.N)
+    q = _unpack_w8_device_layout(packed.cpu().numpy(), cfg.K, cfg.N)
     assert np.array_equal(q, inp["q"])
 
 

@@ -91,6 +91,15 @@ def test_null_and_misaligned_pointers():
     assert gq.gq_gemm(4, 512, 0, 128, C.GQ_W4, 16, 16, 16, None, 16, None) == 0
 
 
+
+def _q8_row_blocks(M):
+    """Row blocks of 8 rows a CTA of the INT8 CUDA-core kernel splits M rows into."""
+    rb = 1
+    while rb * 8 < M:
+        rb *= 2
+    return rb
+
+
 @pytest.mark.parametrize("name", list(gq_synth.CONFIGS))
 def test_plan_is_a_pure_function_of_shape(name):
     cfg = gq_synth.CONFIGS[name]
@@ -132,6 +141,25 @@ def test_plan_is_a_pure_function_of_shape(name):
         assert p1["smem_bytes"] <= 227 * 1024
         if ks > 1:
             assert p1["workspace_bytes"] >= ks * cfg.M * cfg.N * 4
+        return
+    if p1["path"] == 5:
+        # INT8 CUDA-core kernel: 64 columns x one K slice of whole groups per CTA, two CTAs
+        # per SM (at most 113 KiB of shared memory each), every warp of a split CTA with a
+        # group; up to 8 rows the fewest slices that fit
+        assert not cfg.w4 and 1 <= cfg.M <= 32
+        ks = p1["nsplit"]
+        groups = cfg.K // cfg.G
+        assert 1 <= ks <= groups
+        assert ks == 1 or groups // ks >= 8 // _q8_row_blocks(cfg.M)
+        assert p1["n_tile"] == 64 and p1["grid_x"] == -(-cfg.N // 64) * ks
+        assert p1["block_threads"] == 256 and p1["grid_y"] == p1["grid_z"] == 1
+        assert p1["smem_bytes"] <= 113 * 1024
+        if cfg.M <= 8 and cfg.M * cfg.K * 4 + 8 * 8 * 1024 <= 113 * 1024:
+            assert ks == 1
+        if ks > 1:
+            assert p1["workspace_bytes"] >= ks * cfg.M * cfg.N * 4
+        else:
+            assert p1["workspace_bytes"] == 0
         return
     assert p1["smem_bytes"] <= 200 * 1024
     assert 1 <= p1["nsplit"] <= units

@@ -28,8 +28,8 @@ def gq():
 @pytest.mark.parametrize("cfg", [
     gq_synth.Config("nsa_stripe_m1", M=1, K=4096, N=2048, G=128),   # striped decode, CTAs share tiles
     gq_synth.Config("nsa_asym_m3", M=3, K=2048, N=1032, G=128, zp=True, sc="bf16"),
-    gq_synth.Config("nsa_q8_m1", M=1, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
-                    out="f32", s_lo=1e-3, s_hi=1e-2),        # INT8 decode, K split
+    gq_synth.Config("nsa_q8_m16", M=16, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),        # INT8 CUDA-core kernel, K split
 ], ids=lambda c: c.name)
 def test_static_scratch_matches_gq_gemm_twice(gq, cfg):
     inp = gq_synth.make_inputs(cfg, seed=4)
