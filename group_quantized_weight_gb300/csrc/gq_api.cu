@@ -110,6 +110,32 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->nsplit = p->grid_x;
     return GQ_OK;
   }
+  // INT8 codes, 9 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 8
+  // rows the CUDA-core kernel below is faster: it is load-latency-bound there)
+  if (Mc > 8 && Mc <= 32 && q8_mma_supported(Mc, K, G, prec)) {
+    const int ks = q8_mma_slices(Mc, K, Nc, G, sms, kPartCap);
+    if (ks >= 1) {
+      p->path = kPathQ8Mma;
+      p->m_tile = (Mc + 7) / 8 * 8;
+      p->mt = (Mc + 7) / 8;
+      p->n_tile = 64;
+      p->unit_k = G;
+      p->units = K / G;
+      p->nsplit = ks;
+      p->grid_x = ceil_div(Nc, 64) * ks;
+      p->grid_y = p->grid_z = 1;
+      p->block_threads = 256;
+      p->smem_bytes = q8_mma_smem_bytes(Mc, K, G, ks);
+      if (ks > 1) {
+        p->part_bytes = round_up((size_t)ks * Mc * Nc * sizeof(float), 256);
+        p->counter_bytes = kCounterRegionBytes;
+        if ((size_t)ceil_div(Nc, 64) * sizeof(unsigned) > kCounterRegionBytes)
+          return GQ_ERR_UNSUPPORTED;
+      }
+      p->workspace_bytes = p->part_bytes + p->counter_bytes;
+      return GQ_OK;
+    }
+  }
   // INT8 codes, M <= 32: CUDA-core FP32 kernel, 64 columns x one K slice per CTA
   if (Mc <= kQ8BlockMaxM && q8_block_supported(Mc, K, G, prec)) {
     const int ks = q8_block_slices(Mc, K, Nc, G, sms, kPartCap);
@@ -292,6 +318,8 @@ cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, con
     case kPathMmaDecode:
       return launch_mma_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters,
                                s);
+    case kPathQ8Mma:
+      return launch_q8_mma(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     case kPathQ8Block:
       return launch_q8_block(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     case kPathQ8Decode:

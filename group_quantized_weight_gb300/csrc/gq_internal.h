@@ -38,7 +38,7 @@ constexpr int kQ8MaxRows = 32;
 constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
 
 enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3,
-            kPathBatch = 4, kPathQ8Block = 5 };
+            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6 };
 
 struct Plan {
   int path;
@@ -121,6 +121,13 @@ int q8_block_threads();
 cudaError_t launch_q8_block(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                             const void *Wq, const void *scales, void *out, float *part,
                             unsigned *counters, cudaStream_t s);
+// INT8 on BF16 tensor cores (codes exact, fp32 activations as three exact BF16 parts)
+bool q8_mma_supported(int M, int K, int G, int prec);
+size_t q8_mma_smem_bytes(int M, int K, int G, int KS);
+int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap);
+cudaError_t launch_q8_mma(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                          const void *Wq, const void *scales, void *out, float *part,
+                          unsigned *counters, cudaStream_t s);
 // Launches the kernel of plan p (any path); part and counters may be NULL when the plan
 // needs no workspace.
 cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, const void *A,

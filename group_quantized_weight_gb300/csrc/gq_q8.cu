@@ -277,6 +277,309 @@ __global__ void __launch_bounds__(kQbThreads, 2) q8_block_kernel(const QbParams 
   }
 }
 
+// ------------------------------------------------------------------ tensor cores
+//
+// The same GEMM on BF16 tensor cores, exactly: every INT8 code is an integer of at most 8
+// bits, exact in BF16, and every fp32 activation is the exact sum of three BF16 parts
+// (a0 = bf16(a), a1 = bf16(a - a0), a2 = a - a0 - a1, each rounding to nearest), so each
+// product code x part is exact in FP32 and the MMA only adds.  Per group the MMAs start
+// from zero and the group's FP32 sum is multiplied by its scale after the whole group, as
+// the group-wise GEMM of "04 · 分组量化 GEMM 内核", section 2 orders it.
+//
+// CTA = 8 warps over one 64-column block and one K slice: warp (mi, kp) owns the 16 columns
+// mi·16 .. +15 (the rows of its m16n8k16 MMAs) and half the slice's groups (kp).  The MMA's
+// 16 k slots are mapped onto the 16 k of a code chunk so that lane (g, t) needs bytes 4t ..
+// 4t+3 of the chunks of columns g and g + 8 (A operand) and activations 4t .. 4t+3 of row g
+// (B operand, one 8-byte load per part): slot 2t + e <-> k = 4t + e, slot 2t + 8 + e <->
+// k = 4t + 2 + e.  A code byte c (two's complement) becomes a BF16 pair element as
+// bf16(128 + (c & 0x7F)) - bf16(128 + (c & 0x80)), both halves built by one LOP3 each.
+
+constexpr int kQmThreads = 256;
+constexpr int kQmPD = 8;                       // ring slots per warp (2 code steps each)
+constexpr int kQmMaxM = 32;
+
+struct QmParams {
+  const uint4 *Wp;            // packed codes, 64-column blocks of K/16 chunk rows
+  const float *A;             // [M][K]
+  const float *S;             // [K/G][N]
+  void *out;                  // [M][N]
+  float *part;                // [KS][M][N] FP32 slice partial sums (KS > 1)
+  unsigned *counters;         // per column block (KS > 1)
+  int M, K, N, G;
+  int KS, NB;
+  int out_f32;
+};
+
+__host__ __device__ inline int q8m_rows8(int M) { return (M + 7) / 8 * 8; }
+// bf16 elements per activation-plane row: the widest slice plus 16 (32 bytes: the eight
+// rows a fragment load touches start in different bank quarters)
+__host__ __device__ inline int q8m_row_stride(int K, int G, int KS) {
+  return ((K / G) + KS - 1) / KS * G + 16;
+}
+__host__ __device__ inline size_t q8m_area_bytes(int M, int K, int G, int KS) {
+  const size_t planes = (size_t)3 * q8m_rows8(M) * q8m_row_stride(K, G, KS) * 2;
+  const size_t red = (size_t)2 * q8m_rows8(M) * 64 * 4;
+  const size_t a = planes > red ? planes : red;
+  return (a + 15) / 16 * 16;
+}
+
+namespace qm {
+
+__device__ __forceinline__ void mma_bf16(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+               "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
+}
+
+// codes in bytes 0 and 2 of x (two's complement) -> the BF16 pair (code0, code1)
+__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t x) {
+  const uint32_t hi = and_or<0x007F007Fu>(x, 0x43004300u);   // 128 + (c & 0x7F)
+  const uint32_t lo = and_or<0x00800080u>(x, 0x43004300u);   // 128 or 256
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(hi), "r"(lo));
+  return d;
+}
+
+}  // namespace qm
+
+template <int NB8>
+__global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p) {
+  using namespace qm;
+  using namespace qb;
+  extern __shared__ __align__(16) unsigned char smq[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int ks = blockIdx.x / p.NB, nb = blockIdx.x - ks * p.NB;
+  const int M = p.M, K = p.K, N = p.N, G = p.G;
+  const int n0 = nb * 64, wb = min(64, N - n0);
+  const int mi = warp & 3, kp = warp >> 2;
+  constexpr int MR8 = NB8 * 8;
+  const int groups = K / G, Wp = q8m_row_stride(K, G, p.KS);
+  int gs0, gs1;                                    // the CTA's groups
+  zsplit_dev(groups, p.KS, ks, gs0, gs1);
+  int gp0, gp1;                                    // this warp's groups
+  zsplit_dev(gs1 - gs0, 2, kp, gp0, gp1);
+  gp0 += gs0;
+  gp1 += gs0;
+  const int k0 = gs0 * G, ksl = (gs1 - gs0) * G;
+  const int cpg = G / kChunkK8;                    // 16-k steps per group (2 .. 16)
+  const int nslot = (gp1 - gp0) * cpg / 2;         // ring slots of this warp (2 steps each)
+
+  // codes: lane copies column mi·16 + (lane & 15) of step (2·slot + lane / 16)
+  const size_t area = q8m_area_bytes(M, K, G, p.KS);
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(smq) + (uint32_t)area +
+                          (uint32_t)(warp * kQmPD * 512);
+  const unsigned char *ring = smq + area + warp * kQmPD * 512;
+  const int ccol = min(mi * 16 + (lane & 15), wb - 1);
+  const uint4 *csrc = p.Wp + (size_t)nb * (64 / kChunkK8) * K +
+                      (size_t)(gp0 * cpg + (lane >> 4)) * wb + ccol;
+  const uint32_t cdst = ring_s + (lane >> 4) * 256 + (lane & 15) * 16;
+#pragma unroll
+  for (int j = 0; j < kQmPD; ++j) {
+    if (j < nslot) cp16(cdst + j * 512, csrc + (size_t)2 * j * wb);
+    cp_commit();
+  }
+
+  // activations of the slice as three BF16 planes [3][MR8][Wp]
+  __nv_bfloat16 *pl = reinterpret_cast<__nv_bfloat16 *>(smq);
+  const int q4 = ksl >> 2;
+  for (int idx = threadIdx.x; idx < MR8 * q4; idx += blockDim.x) {
+    const int m = idx / q4, k = (idx - m * q4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m < M) v = __ldg(reinterpret_cast<const float4 *>(p.A + (size_t)m * K + k0 + k));
+    const float a[4] = {v.x, v.y, v.z, v.w};
+    uint32_t w[3][2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float r0 = a[2 * h], r1 = a[2 * h + 1];
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
+        w[part][h] = *reinterpret_cast<const uint32_t *>(&b);
+        r0 -= __bfloat162float(b.x);
+        r1 -= __bfloat162float(b.y);
+      }
+    }
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+      *reinterpret_cast<uint2 *>(pl + ((size_t)part * MR8 + m) * Wp + k) =
+          make_uint2(w[part][0], w[part][1]);
+  }
+  __syncthreads();
+
+  // scales of the lane's two columns (MMA rows g and g + 8)
+  const int cg = min(mi * 16 + g, wb - 1), cg8 = min(mi * 16 + g + 8, wb - 1);
+  const float *s_g = p.S + n0 + cg, *s_g8 = p.S + n0 + cg8;
+  float acc[NB8][4], d[NB8][4];
+#pragma unroll
+  for (int b = 0; b < NB8; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
+  int grp = gp0;
+  float sc0 = 0.f, sc8 = 0.f;
+  if (gp0 < gp1) {
+    sc0 = __ldg(s_g + (size_t)grp * N);
+    sc8 = __ldg(s_g8 + (size_t)grp * N);
+  }
+  const unsigned char *bbase = reinterpret_cast<const unsigned char *>(pl) +
+                               ((size_t)g * Wp + (gp0 * G - k0) + 4 * t) * 2;
+  int st = 0;                                      // step within the group
+  for (int base = 0; base < nslot; base += kQmPD) {
+#pragma unroll
+    for (int j = 0; j < kQmPD; ++j) {
+      const int sl = base + j;
+      if (sl < nslot) {
+        cp_wait<kQmPD - 1>();                      // this lane's copy of slot sl landed
+        __syncwarp();                              // and so did every other lane's
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const unsigned char *cs = ring + j * 512 + h * 256;
+          const uint32_t wg = *reinterpret_cast<const uint32_t *>(cs + g * 16 + 4 * t);
+          const uint32_t wg8 = *reinterpret_cast<const uint32_t *>(cs + (g + 8) * 16 + 4 * t);
+          const uint32_t a0 = codes_bf16x2(__byte_perm(wg, 0, 0x4140));
+          const uint32_t a2 = codes_bf16x2(__byte_perm(wg, 0, 0x4342));
+          const uint32_t a1 = codes_bf16x2(__byte_perm(wg8, 0, 0x4140));
+          const uint32_t a3 = codes_bf16x2(__byte_perm(wg8, 0, 0x4342));
+          if (st == 0) {
+#pragma unroll
+            for (int b = 0; b < NB8; ++b) d[b][0] = d[b][1] = d[b][2] = d[b][3] = 0.f;
+          }
+          const int kk = (2 * sl + h) * 16;        // k of this step from the warp's first
+#pragma unroll
+          for (int b = 0; b < NB8; ++b) {
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+              const uint2 bv = *reinterpret_cast<const uint2 *>(
+                  bbase + (((size_t)part * MR8 + b * 8) * Wp + kk) * 2);
+              mma_bf16(d[b], a0, a1, a2, a3, bv.x, bv.y);
+            }
+          }
+          if (++st == cpg) {                       // the group is complete: scale it in
+            st = 0;
+#pragma unroll
+            for (int b = 0; b < NB8; ++b) {
+              acc[b][0] = fmaf(sc0, d[b][0], acc[b][0]);
+              acc[b][1] = fmaf(sc0, d[b][1], acc[b][1]);
+              acc[b][2] = fmaf(sc8, d[b][2], acc[b][2]);
+              acc[b][3] = fmaf(sc8, d[b][3], acc[b][3]);
+            }
+            if (++grp < gp1) {
+              sc0 = __ldg(s_g + (size_t)grp * N);
+              sc8 = __ldg(s_g8 + (size_t)grp * N);
+            }
+          }
+        }
+        __syncwarp();                              // every lane has read slot j
+        if (sl + kQmPD < nslot) cp16(cdst + j * 512, csrc + (size_t)2 * (sl + kQmPD) * wb);
+        cp_commit();
+      }
+    }
+  }
+  cp_wait<0>();
+
+  // the two K parts, added in part order: red[kp][row][64 columns]
+  __syncthreads();                                 // every warp is done with the planes
+  float *red = reinterpret_cast<float *>(smq);
+#pragma unroll
+  for (int b = 0; b < NB8; ++b)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = b * 8 + 2 * t + (e & 1), col = mi * 16 + g + 8 * (e >> 1);
+      red[((size_t)kp * MR8 + row) * 64 + col] = acc[b][e];
+    }
+  __syncthreads();
+  const bool split = p.KS > 1;
+  for (int idx = threadIdx.x; idx < M * 64; idx += blockDim.x) {
+    const int m = idx >> 6, c = idx & 63, n = n0 + c;
+    const float sum = red[(size_t)m * 64 + c] + red[((size_t)MR8 + m) * 64 + c];
+    if (c < wb) {
+      if (split)
+        p.part[((size_t)ks * M + m) * N + n] = sum;
+      else
+        store_out_rt(p.out, (size_t)m * N + n, sum, p.out_f32 != 0);
+    }
+  }
+  if (!split) return;
+  if (!last_arriver(p.counters + nb, p.KS)) return;
+  for (int idx = threadIdx.x; idx < M * 64; idx += blockDim.x) {
+    const int m = idx >> 6, c = idx & 63, n = n0 + c;
+    if (c >= wb) continue;
+    float sum = 0.f;
+    for (int s2 = 0; s2 < p.KS; ++s2) sum += __ldcg(p.part + ((size_t)s2 * M + m) * N + n);
+    store_out_rt(p.out, (size_t)m * N + n, sum, p.out_f32 != 0);
+  }
+}
+
+bool q8_mma_supported(int M, int K, int G, int prec) {
+  return !(prec & GQ_W4) && (prec & GQ_ACT_F32) && (prec & GQ_SC_F32) && M >= 1 &&
+         M <= kQmMaxM && G % kChunkK8 == 0 && K % G == 0;
+}
+
+size_t q8_mma_smem_bytes(int M, int K, int G, int KS) {
+  return q8m_area_bytes(M, K, G, KS) + (size_t)8 * kQmPD * 512;
+}
+
+// K slices: as for the CUDA-core kernel, counted against this kernel's shared memory and
+// its two K parts per CTA.
+int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
+  const int groups = K / G;
+  const int nb = (N + 63) / 64;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int ks = 1; ks <= groups; ++ks) {
+    if (ks > 1 && groups / ks < 2) break;          // both K parts keep a group
+    if (ks > 1 && (size_t)ks * M * N * 4 > part_cap) break;
+    if (q8_mma_smem_bytes(M, K, G, ks) > kQbSmemCap) continue;
+    if (M <= 8) return ks;
+    const long waves = ((long)nb * ks + 2L * sms - 1) / (2L * sms);
+    const double cost = (double)waves / ks * (1.0 + 0.05 * ks);
+    if (best == 0 || cost < best_cost * (1.0 - 1e-9)) {
+      best = ks;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_q8_mma(const Plan &pl, int M, int K, int N, int G, int prec, const void *A,
+                          const void *Wq, const void *scales, void *out, float *part,
+                          unsigned *counters, cudaStream_t s) {
+  QmParams qp;
+  qp.Wp = reinterpret_cast<const uint4 *>(Wq);
+  qp.A = reinterpret_cast<const float *>(A);
+  qp.S = reinterpret_cast<const float *>(scales);
+  qp.out = out;
+  qp.part = part;
+  qp.counters = counters;
+  qp.M = M;
+  qp.K = K;
+  qp.N = N;
+  qp.G = G;
+  qp.KS = pl.nsplit;
+  qp.NB = (N + 63) / 64;
+  qp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pl.smem_bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<pl.grid_x, kQmThreads, pl.smem_bytes, s>>>(qp);
+    return cudaGetLastError();
+  };
+  switch ((M + 7) / 8) {
+    case 1: return go(q8_mma_kernel<1>);
+    case 2: return go(q8_mma_kernel<2>);
+    case 3: return go(q8_mma_kernel<3>);
+    case 4: return go(q8_mma_kernel<4>);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 bool q8_block_supported(int M, int K, int G, int prec) {
   return !(prec & GQ_W4) && (prec & GQ_ACT_F32) && (prec & GQ_SC_F32) && M >= 1 &&
          M <= kQ8BlockMaxM && G % kChunkK8 == 0 && K % G == 0;
