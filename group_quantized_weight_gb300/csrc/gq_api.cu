@@ -110,9 +110,9 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->nsplit = p->grid_x;
     return GQ_OK;
   }
-  // INT8 codes, 9 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 8
+  // INT8 codes, 5 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 4
   // rows the CUDA-core kernel below is faster: it is load-latency-bound there)
-  if (Mc > 8 && Mc <= 32 && q8_mma_supported(Mc, K, G, prec)) {
+  if (Mc > 4 && Mc <= 32 && q8_mma_supported(Mc, K, G, prec)) {
     const int ks = q8_mma_slices(Mc, K, Nc, G, sms, kPartCap);
     if (ks >= 1) {
       p->path = kPathQ8Mma;

@@ -322,6 +322,10 @@ __host__ __device__ inline size_t q8m_area_bytes(int M, int K, int G, int KS) {
   const size_t a = planes > red ? planes : red;
   return (a + 15) / 16 * 16;
 }
+// the slice's scales for the CTA's 64 columns: [widest slice's groups][64] fp32
+__host__ __device__ inline size_t q8m_scale_bytes(int K, int G, int KS) {
+  return (size_t)(((K / G) + KS - 1) / KS) * 64 * 4;
+}
 
 namespace qm {
 
@@ -375,9 +379,18 @@ __global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p)
 
   // codes: lane copies column mi·16 + (lane & 15) of step (2·slot + lane / 16)
   const size_t area = q8m_area_bytes(M, K, G, p.KS);
-  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(smq) + (uint32_t)area +
-                          (uint32_t)(warp * kQmPD * 512);
-  const unsigned char *ring = smq + area + warp * kQmPD * 512;
+  const size_t sbytes = q8m_scale_bytes(K, G, p.KS);
+  const uint32_t smq_s = (uint32_t)__cvta_generic_to_shared(smq);
+  // the slice's scales for the block's columns (one commit group, the oldest); pieces past
+  // a narrow block's last column repeat its last four columns
+  const float *ssm = reinterpret_cast<const float *>(smq + area);
+  for (int idx = threadIdx.x; idx < (gs1 - gs0) * 16; idx += blockDim.x) {
+    const int gr = idx >> 4, q = idx & 15, col = min(q * 4, wb - 4);
+    cp16(smq_s + (uint32_t)(area + gr * 256 + q * 16), p.S + (size_t)(gs0 + gr) * N + n0 + col);
+  }
+  cp_commit();
+  const uint32_t ring_s = smq_s + (uint32_t)(area + sbytes) + (uint32_t)(warp * kQmPD * 512);
+  const unsigned char *ring = smq + area + sbytes + warp * kQmPD * 512;
   const int ccol = min(mi * 16 + (lane & 15), wb - 1);
   const uint4 *csrc = p.Wp + (size_t)nb * (64 / kChunkK8) * K +
                       (size_t)(gp0 * cpg + (lane >> 4)) * wb + ccol;
@@ -390,42 +403,55 @@ __global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p)
 
   // activations of the slice as three BF16 planes [3][MR8][Wp]
   __nv_bfloat16 *pl = reinterpret_cast<__nv_bfloat16 *>(smq);
-  const int q4 = ksl >> 2;
-  for (int idx = threadIdx.x; idx < MR8 * q4; idx += blockDim.x) {
-    const int m = idx / q4, k = (idx - m * q4) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m < M) v = __ldg(reinterpret_cast<const float4 *>(p.A + (size_t)m * K + k0 + k));
-    const float a[4] = {v.x, v.y, v.z, v.w};
-    uint32_t w[3][2];
+  const int q4 = ksl >> 2, nq = MR8 * q4;
+  for (int base = threadIdx.x; base < nq; base += 4 * kQmThreads) {
+    float4 vv[4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float r0 = a[2 * h], r1 = a[2 * h + 1];
-#pragma unroll
-      for (int part = 0; part < 3; ++part) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
-        w[part][h] = *reinterpret_cast<const uint32_t *>(&b);
-        r0 -= __bfloat162float(b.x);
-        r1 -= __bfloat162float(b.y);
-      }
+    for (int u = 0; u < 4; ++u) {                  // four independent loads in flight
+      const int idx = base + u * kQmThreads, m = idx / q4;
+      vv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (idx < nq && m < M)
+        vv[u] = __ldg(reinterpret_cast<const float4 *>(p.A + (size_t)m * K + k0 +
+                                                      (idx - m * q4) * 4));
     }
 #pragma unroll
-    for (int part = 0; part < 3; ++part)
-      *reinterpret_cast<uint2 *>(pl + ((size_t)part * MR8 + m) * Wp + k) =
-          make_uint2(w[part][0], w[part][1]);
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * kQmThreads;
+      if (idx >= nq) break;
+      const int m = idx / q4, k = (idx - m * q4) * 4;
+      const float a[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+      uint32_t w[3][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float r0 = a[2 * h], r1 = a[2 * h + 1];
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const __nv_bfloat162 bb = __floats2bfloat162_rn(r0, r1);
+          w[part][h] = *reinterpret_cast<const uint32_t *>(&bb);
+          r0 -= __bfloat162float(bb.x);
+          r1 -= __bfloat162float(bb.y);
+        }
+      }
+#pragma unroll
+      for (int part = 0; part < 3; ++part)
+        *reinterpret_cast<uint2 *>(pl + ((size_t)part * MR8 + m) * Wp + k) =
+            make_uint2(w[part][0], w[part][1]);
+    }
   }
+  cp_wait<kQmPD>();                                // the scales (older than the ring) landed
   __syncthreads();
 
   // scales of the lane's two columns (MMA rows g and g + 8)
   const int cg = min(mi * 16 + g, wb - 1), cg8 = min(mi * 16 + g + 8, wb - 1);
-  const float *s_g = p.S + n0 + cg, *s_g8 = p.S + n0 + cg8;
+  const float *s_g = ssm - (size_t)gs0 * 64 + cg, *s_g8 = ssm - (size_t)gs0 * 64 + cg8;
   float acc[NB8][4], d[NB8][4];
 #pragma unroll
   for (int b = 0; b < NB8; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0.f;
   int grp = gp0;
   float sc0 = 0.f, sc8 = 0.f;
   if (gp0 < gp1) {
-    sc0 = __ldg(s_g + (size_t)grp * N);
-    sc8 = __ldg(s_g8 + (size_t)grp * N);
+    sc0 = s_g[(size_t)grp * 64];
+    sc8 = s_g8[(size_t)grp * 64];
   }
   const unsigned char *bbase = reinterpret_cast<const unsigned char *>(pl) +
                                ((size_t)g * Wp + (gp0 * G - k0) + 4 * t) * 2;
@@ -470,8 +496,8 @@ __global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p)
               acc[b][3] = fmaf(sc8, d[b][3], acc[b][3]);
             }
             if (++grp < gp1) {
-              sc0 = __ldg(s_g + (size_t)grp * N);
-              sc8 = __ldg(s_g8 + (size_t)grp * N);
+              sc0 = s_g[(size_t)grp * 64];
+              sc8 = s_g8[(size_t)grp * 64];
             }
           }
         }
@@ -522,7 +548,7 @@ bool q8_mma_supported(int M, int K, int G, int prec) {
 }
 
 size_t q8_mma_smem_bytes(int M, int K, int G, int KS) {
-  return q8m_area_bytes(M, K, G, KS) + (size_t)8 * kQmPD * 512;
+  return q8m_area_bytes(M, K, G, KS) + q8m_scale_bytes(K, G, KS) + (size_t)8 * kQmPD * 512;
 }
 
 // K slices: as for the CUDA-core kernel, counted against this kernel's shared memory and

@@ -168,9 +168,9 @@ typedef struct gq_plan_t {
                         3 = striped decode (M <= 8, warps stream contiguous slot ranges),
                         4 = small-batch tensor-core kernel (M <= 64, persistent CTAs over
                             (K slice, tile range) pairs),
-                        5 = INT8 CUDA-core kernel for M <= 8 (64 columns x one K slice
+                        5 = INT8 CUDA-core kernel for M <= 4 (64 columns x one K slice
                             per CTA, paired FP32 FMAs),
-                        6 = INT8 on BF16 tensor cores for 9 <= M <= 32 (codes exact in
+                        6 = INT8 on BF16 tensor cores for 5 <= M <= 32 (codes exact in
                             BF16, fp32 activations as three exact BF16 parts) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */

@@ -87,6 +87,15 @@ Q8_SHAPES = [
                     out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("q8_m32_g64_bf16", M=32, K=512, N=328, G=64, w4=False, act="f32",
                     sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),
+    # several column blocks per CTA (the last narrow), K slices of one group for one K part
+    gq_synth.Config("q8_m7_g128", M=7, K=1024, N=1000, G=128, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_m20_blocks", M=20, K=2048, N=4040, G=32, w4=False, act="f32",
+                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8_m24_2blocks", M=24, K=512, N=12248, G=32, w4=False, act="f32",
+                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),     # 2 blocks per CTA
+    gq_synth.Config("q8_m16_5blocks", M=16, K=1024, N=20008, G=64, w4=False, act="f32",
+                    sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),    # 5 blocks per CTA
 ]
 
 
