@@ -227,10 +227,10 @@ def main():
         raise SystemExit("bench.py needs a CUDA device")
 
     import group_quantized_weight_gb300 as gq
-    from group_quantized_weight_gb300.constants import algorithmic_bytes, gemm_flops, prec_flags
+    from group_quantized_weight_gb300.constants import GQ_STATIC_W, algorithmic_bytes, gemm_flops, prec_flags
 
     cfg = gq_synth.CONFIGS[WORKLOAD]
-    prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out) | GQ_STATIC_W
     inp = gq_synth.make_inputs(cfg, seed=0)
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -323,6 +323,8 @@ def main():
         "config": {"workload": f"{WORKLOAD}: M=1 K=4096 N=28672 G=128 W4A16 sym, fp16 scales, "
                                "bf16 act/out",
                    "step": f"{calls_per_step} gq_gemm calls replayed from one CUDA graph",
+                   "weights": "static (GQ_STATIC_W): a call may start streaming its weights "
+                              "before the previous call ends; activations wait for it",
                    "l2": f"inputs larger than L2: {COPIES} rotated weight copies "
                          f"({COPIES * nbytes / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
@@ -409,12 +411,12 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
     back calls, rotating weight copies so that the weights come from HBM whenever they fit
     at most a third of L2 per copy), HBM GB/s of the algorithmic bytes, TFLOPS, and the
     fraction of the roofline that bounds it (HBM below M = 128, dense BF16 above)."""
-    from group_quantized_weight_gb300.constants import algorithmic_bytes, gemm_flops, prec_flags
+    from group_quantized_weight_gb300.constants import GQ_STATIC_W, algorithmic_bytes, gemm_flops, prec_flags
     out = []
     side = torch.cuda.Stream()           # graph capture needs a stream other than the legacy one
     for name in ("tiny_gemv", "decode_gateup", "q8_m1", "q8_m32", "asym_m16", "prefill"):
         cfg = gq_synth.CONFIGS[name]
-        prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+        prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out) | GQ_STATIC_W
         d = _dev_inputs(torch, dev, gq_synth.make_inputs(cfg, seed=0))
         packed = gq.pack_weights_t(d["codes"], cfg.K, cfg.N, cfg.G, prec)
         nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
@@ -457,9 +459,9 @@ def _m_sweep(gq, torch, dev, peaks):
     """K=4096 N=14336 G=128 W4A16 (fp16 scales, bf16 out) against the same product as a dense
     BF16 GEMM (torch.matmul on cuBLAS, weights already BF16) for M = 1 ... 4096: time per
     call of each, their ratio, and the smallest M at which the INT4 path is the slower."""
-    from group_quantized_weight_gb300.constants import prec_flags
+    from group_quantized_weight_gb300.constants import GQ_STATIC_W, prec_flags
     base = gq_synth.Config("sweep", M=1, K=4096, N=14336, G=128)
-    prec = prec_flags(True, False, "bf16", "fp16", "bf16")
+    prec = prec_flags(True, False, "bf16", "fp16", "bf16") | GQ_STATIC_W
     w = gq_synth.make_weights(base, seed=0)
     codes = torch.from_numpy(w["codes"].view(np.int32)).to(dev)
     packed = gq.pack_weights_t(codes, base.K, base.N, base.G, prec)
@@ -507,9 +509,9 @@ def _m_sweep(gq, torch, dev, peaks):
 
 def _prefill(gq, torch, dev, peaks, peak_kind):
     """M=4096 K=4096 N=14336 prefill: TFLOPS of gq_gemm vs the measured dense BF16 peak."""
-    from group_quantized_weight_gb300.constants import gemm_flops, prec_flags
+    from group_quantized_weight_gb300.constants import GQ_STATIC_W, gemm_flops, prec_flags
     cfg = gq_synth.CONFIGS["prefill"]
-    prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out) | GQ_STATIC_W
     w = gq_synth.make_weights(cfg, seed=0)
     a = gq_synth.make_activations(cfg, seed=0)
     codes = torch.from_numpy(w["codes"].view(np.int32)).to(dev)

@@ -8,6 +8,7 @@ GQ_ACT_F32 = 0x04
 GQ_SC_BF16 = 0x08
 GQ_SC_F32 = 0x10
 GQ_OUT_F32 = 0x20
+GQ_STATIC_W = 0x40
 
 GQ_OK = 0
 STATUS_NAMES = {0: "GQ_OK", 1: "GQ_ERR_INVALID_ARG", 2: "GQ_ERR_UNSUPPORTED",

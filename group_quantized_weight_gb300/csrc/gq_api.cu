@@ -16,7 +16,7 @@ static inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 int validate(int M, int K, int N, int G, int prec) {
   if (M < 0 || N < 0 || K <= 0) return GQ_ERR_INVALID_ARG;
-  if (prec & ~(GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_SC_BF16 | GQ_SC_F32 | GQ_OUT_F32))
+  if (prec & ~(GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_SC_BF16 | GQ_SC_F32 | GQ_OUT_F32 | GQ_STATIC_W))
     return GQ_ERR_INVALID_ARG;
   if ((prec & GQ_SC_BF16) && (prec & GQ_SC_F32)) return GQ_ERR_INVALID_ARG;
   if (!(G == 32 || G == 64 || G == 128 || G == 256)) return GQ_ERR_UNSUPPORTED;
@@ -160,7 +160,24 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       return GQ_OK;
     }
   }
-  // small batch (M <= 64): persistent CTAs over (K slice, tile range) pairs, activation
+  if (M >= kPrefillMinM && prefill_supported(M, K, N, G, prec)) {
+    // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
+    p->path = kPathPrefill;
+    p->m_tile = 256;
+    p->n_tile = 128;
+    p->unit_k = G;
+    p->units = K / G;
+    const int tiles = ceil_div(N, 128) * ceil_div(M, 256);
+    p->grid_x = tiles < sms ? tiles : sms;
+    p->grid_y = p->grid_z = 1;
+    p->nsplit = 1;
+    p->block_threads = kPrefillThreads;
+    p->smem_bytes = prefill_smem_bytes();
+    p->workspace_bytes = 0;
+    return GQ_OK;
+  }
+  // small batch (M <= 32, or up to 64 with G = 32): persistent CTAs over (K slice, tile
+  // range) pairs, activation
   // slices in shared memory, slices added by the last CTA of each tile range
   if (Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)) {
     const int ksl = batch_slice_k(Mc, K);
@@ -191,22 +208,6 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       p->workspace_bytes = p->part_bytes + p->counter_bytes;
       return GQ_OK;
     }
-  }
-  if (M >= kPrefillMinM && prefill_supported(M, K, N, G, prec)) {
-    // large M: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
-    p->path = kPathPrefill;
-    p->m_tile = 256;
-    p->n_tile = 128;
-    p->unit_k = G;
-    p->units = K / G;
-    const int tiles = ceil_div(N, 128) * ceil_div(M, 256);
-    p->grid_x = tiles < sms ? tiles : sms;
-    p->grid_y = p->grid_z = 1;
-    p->nsplit = 1;
-    p->block_threads = kPrefillThreads;
-    p->smem_bytes = prefill_smem_bytes();
-    p->workspace_bytes = 0;
-    return GQ_OK;
   }
   if (prec & GQ_W4) {
     p->path = kPathMmaDecode;

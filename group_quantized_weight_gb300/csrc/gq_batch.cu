@@ -122,6 +122,7 @@ struct BtParams {
   int cps;                    // CTAs (tile ranges) per K slice
   int S;                      // ring slots per warp
   int out_f32;
+  int static_w;               // weights may be read before the preceding kernel ends
 };
 
 __host__ __device__ constexpr int batch_groups_per_slot(int G) { return kBtSlotK / G; }
@@ -176,7 +177,9 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
   }
   __syncwarp();
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // inputs written by the preceding kernel are read only after it has ended; static weights
+  // (GQ_STATIC_W) start streaming before that
+  if (!p.static_w) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- the load side: the next slot of this warp's tiles into the next ring slot
   const size_t srow = (size_t)N * ES;               // bytes per scale row
@@ -217,6 +220,7 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
     hs = hs + 1 == S ? 0 : hs + 1;
   };
   for (int l = 0; l < S && l < nloads; ++l) issue_next();
+  if (p.static_w) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- the activation slice: rows m0 .. m0 + Mb - 1, k = ks KSL .. (ks + 1) KSL - 1, as
   // 16-byte pieces (8 k); the four words of piece pc go to base(pc) + 0, 4, 8, 12 of the row
@@ -487,6 +491,7 @@ cudaError_t launch_batch(const Plan &pl, int M, int K, int N, int G, int prec, c
   bp.cps = pl.split_count;
   bp.S = pl.slots;
   bp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
+  bp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   switch (G) {
     case 32: return launch_bt_g<32>(pl, prec, bp, s);
     case 64: return launch_bt_g<64>(pl, prec, bp, s);

@@ -103,10 +103,12 @@ int batch_read_error(int clear);
 // Records why a call is about to return GQ_ERR_CUDA (thread-local; read by gq_last_error_detail).
 void note_cuda_error(const char *where, cudaError_t e);
 void note_cuda_error_code(const char *where, int code);
-// largest M of the small-batch kernel; larger M goes to the tensor-core prefill kernel
+// largest M of the small-batch kernel (it takes 33..64 rows only where the prefill kernel
+// does not apply: G = 32)
 constexpr int kBatchMaxM = 64;
-// smallest M routed to the tensor-core prefill kernel
-constexpr int kPrefillMinM = 65;
+// smallest M routed to the tensor-core prefill kernel: from 33 rows the small-batch kernel
+// needs a second 32-row block and the prefill kernel's 256-row tile is faster
+constexpr int kPrefillMinM = 33;
 constexpr int kPrefillThreads = 512;   // block size of the prefill kernel
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,

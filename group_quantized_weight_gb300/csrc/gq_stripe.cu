@@ -145,6 +145,7 @@ struct StripeParams {
   int split_count, split_mult;   // CTA c owns slots zsplit(split_count, grid, c) * split_mult
   int S;                         // ring slots per warp
   int out_f32;
+  int static_w;                  // weights may be read before the preceding kernel ends
 };
 
 // Shared-memory layout (dynamic): [bands][rings][pieces]
@@ -208,7 +209,9 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   }
   __syncwarp();
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // inputs written by the preceding kernel are read only after it has ended; static weights
+  // (GQ_STATIC_W) start streaming before that
+  if (!p.static_w) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- the load side: the next slot of this warp's range into the next ring slot.  One lane
   // issues the bulk copy of the slot's 2 KB of codes (operands broadcast from lane 0, so the
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
     hs = hs + 1 == S ? 0 : hs + 1;
   };
   for (int i = 0; i < S && i < n; ++i) issue_next();
+  if (p.static_w) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- stage A: exponent bands as fp16, permuted for the B operands.  Each thread reads
   // 16-byte pieces of A (8 consecutive k of one row) from global memory: once for the row's
@@ -663,6 +667,7 @@ cudaError_t launch_stripe_decode(const Plan &pl, int M, int K, int N, int G, int
   sp.split_mult = pl.split_mult;
   sp.S = pl.slots;
   sp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
+  sp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   switch (G) {
     case 32: return launch_stripe_g<32>(pl, prec, sp, s);
     case 64: return launch_stripe_g<64>(pl, prec, sp, s);

@@ -48,6 +48,10 @@ typedef enum gq_status {
 #define GQ_SC_BF16 0x08  /* scales bf16                                                        */
 #define GQ_SC_F32  0x10  /* scales fp32; neither SC flag = fp16                                */
 #define GQ_OUT_F32 0x20  /* output fp32; clear = bf16 (round to nearest even)                  */
+#define GQ_STATIC_W 0x40 /* Wq, scales and zeros are not written by work still running on the
+                            stream (weights loaded once, as in serving): the decode kernels
+                            may start streaming them before the preceding kernel has ended;
+                            activations and outputs still wait for it                         */
 
 /*
  * Supported operand combinations (anything else returns GQ_ERR_UNSUPPORTED):
@@ -164,10 +168,10 @@ int gq_bench(const gq_bench_args *args, gq_bench_result *result);
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {
   int path;          /* 0 = small-M tensor-core decode (mma.sync, K split across CTAs),
-                        1 = INT8 CUDA-core decode (M > 32), 2 = large-M tcgen05 prefill,
+                        1 = INT8 CUDA-core decode (M > 32), 2 = tcgen05 prefill (W4, M >= 33),
                         3 = striped decode (M <= 8, warps stream contiguous slot ranges),
-                        4 = small-batch tensor-core kernel (M <= 64, persistent CTAs over
-                            (K slice, tile range) pairs),
+                        4 = small-batch tensor-core kernel (M <= 32, up to 64 with G = 32;
+                            persistent CTAs over (K slice, tile range) pairs),
                         5 = INT8 CUDA-core kernel for M <= 4 (64 columns x one K slice
                             per CTA, paired FP32 FMAs),
                         6 = INT8 on BF16 tensor cores for 5 <= M <= 32 (codes exact in

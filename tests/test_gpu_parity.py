@@ -141,6 +141,9 @@ PREFILL_SHAPES = [
     gq_synth.Config("pf_g64_f32", M=128, K=256, N=136, G=64, sc="f32", out="f32"),
     gq_synth.Config("pf_g256", M=520, K=2048, N=264, G=256, zp=True),
     gq_synth.Config("pf_tall", M=1100, K=512, N=128, G=128, outlier_frac=0.01),
+    # the smallest row counts the prefill kernel takes: one 256-row tile, mostly past M
+    gq_synth.Config("pf_m33", M=33, K=512, N=136, G=128),
+    gq_synth.Config("pf_m64_zp", M=64, K=1024, N=256, G=64, zp=True, sc="bf16", out="f32"),
 ]
 
 
@@ -321,3 +324,36 @@ def test_graph_capture_of_gemm(gq):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), ref_out.view(torch.int16))
+
+
+# ------------------------------------------------------------------ static-weight launches
+
+@pytest.mark.parametrize("cfg", [
+    gq_synth.Config("static_stripe_m1", M=1, K=4096, N=4096, G=128),
+    gq_synth.Config("static_batch_m16", M=16, K=8192, N=512, G=128, zp=True, sc="bf16"),
+    gq_synth.Config("static_q8_m12", M=12, K=1024, N=200, G=32, w4=False, act="f32",
+                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
+], ids=lambda c: c.name)
+def test_static_weight_flag_gives_the_same_bits(gq, cfg):
+    """GQ_STATIC_W lets a kernel stream its weights before the preceding kernel on the stream
+    has ended; the activations still wait for it.  Back-to-back calls, the second one's
+    activations written by a kernel just before it, give the bits of the plain calls."""
+    from group_quantized_weight_gb300.constants import GQ_STATIC_W
+    inp = gq_synth.make_inputs(cfg, seed=6)
+    prec = prec_of(cfg)
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    A = np_to_dev(inp["A"])
+    S = np_to_dev(inp["scales"])
+    Z = np_to_dev(inp["zeros"]) if inp["zeros"] is not None else None
+    ref = alloc_out(cfg.M, cfg.N, cfg.out)
+    gq.gemm_t(A, packed, S, Z, ref, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    got = [alloc_out(cfg.M, cfg.N, cfg.out) for _ in range(3)]
+    A2 = torch.zeros_like(A)
+    for o in got:
+        A2.zero_()
+        A2.copy_(A)                      # written on the stream right before the call
+        gq.gemm_t(A2, packed, S, Z, o, cfg.M, cfg.K, cfg.N, cfg.G, prec | GQ_STATIC_W)
+    torch.cuda.synchronize()
+    view = torch.int16 if cfg.out == "bf16" else torch.int32
+    for o in got:
+        assert torch.equal(o.view(view), ref.view(view))

@@ -111,7 +111,7 @@ def test_plan_is_a_pure_function_of_shape(name):
     if p1["path"] == 2:
         # tcgen05 prefill: persistent, at most one CTA per SM, no scratch; one CTA holds the
         # shared-memory ring (at most 227 KiB per CTA on sm_103a)
-        assert cfg.M >= 128 and cfg.w4
+        assert cfg.M >= 33 and cfg.w4
         assert 1 <= p1["grid_x"] <= 152
         assert p1["workspace_bytes"] == 0
         assert p1["smem_bytes"] <= 227 * 1024
