@@ -16,12 +16,17 @@ static inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 int validate(int M, int K, int N, int G, int prec) {
   if (M < 0 || N < 0 || K <= 0) return GQ_ERR_INVALID_ARG;
-  if (prec & ~(GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_SC_BF16 | GQ_SC_F32 | GQ_OUT_F32 | GQ_STATIC_W))
+  if (prec & ~(GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_SC_BF16 | GQ_SC_F32 | GQ_OUT_F32 | GQ_STATIC_W |
+               GQ_GATE_UP))
     return GQ_ERR_INVALID_ARG;
   if ((prec & GQ_SC_BF16) && (prec & GQ_SC_F32)) return GQ_ERR_INVALID_ARG;
   if (!(G == 32 || G == 64 || G == 128 || G == 256)) return GQ_ERR_UNSUPPORTED;
   if (K < G || K % G != 0) return GQ_ERR_INVALID_ARG;
   if (N % 8 != 0) return GQ_ERR_INVALID_ARG;
+  if (prec & GQ_GATE_UP) {
+    if (!(prec & GQ_W4)) return GQ_ERR_UNSUPPORTED;
+    if (N % 16 != 0) return GQ_ERR_INVALID_ARG;
+  }
   if (prec & GQ_W4) {
     if (K % kChunkK != 0) return GQ_ERR_UNSUPPORTED;
     if (prec & GQ_ACT_F32) return GQ_ERR_UNSUPPORTED;
@@ -78,6 +83,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   // contiguous range of (tile, 256-k slot) pairs; whole tiles per CTA when that keeps the
   // SMs within 10% of even, else equal slot ranges with a cross-CTA reduction
   const int slots = stripe_supported(Mc, K, G, prec) ? stripe_slots_for(Mc, K, G, prec, kCtaSmemCap) : 0;
+  if ((prec & GQ_GATE_UP) && slots < 2) return GQ_ERR_UNSUPPORTED;   // striped kernel only
   if (slots >= 2) {
     p->path = kPathStripe;
     p->mt = Mc <= 4 ? 1 : 2;   // MMA blocks
@@ -447,7 +453,8 @@ int gq_pack_weights(int K, int N, int G, int prec, const void *codes, void *pack
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
   if (prec & GQ_W4)
-    e = launch_pack_w4(K, N, (const uint32_t *)codes, (uint32_t *)packed, s);
+    e = launch_pack_w4(K, N, (const uint32_t *)codes, (uint32_t *)packed,
+                       (prec & GQ_GATE_UP) != 0, s);
   else
     e = launch_pack_w8(K, N, (const int8_t *)codes, (uint8_t *)packed, s);
   return e == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;

@@ -67,7 +67,7 @@ size_t packed_bytes(int K, int N, int prec);
 int device_sm_count(int *sms);
 
 // launchers (return cudaError_t of the launch)
-cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed,
+cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed, bool gate_up,
                            cudaStream_t s);
 cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed,
                            cudaStream_t s);

@@ -9,6 +9,9 @@
 //   with the first k of the pair at bits 4i..4i+3 and the second at bits 4i+16..4i+19,
 //   so that (word >> 4i) & 0x000F000F leaves the two codes in the low bits of the two
 //   16-bit halves, ready for the BF16 magic 0x4300.
+// W4 fused gate+up (GQ_GATE_UP): tile t holds gate columns 8t .. 8t+7 as rows 0-7 and up
+// columns N/2 + 8t .. as rows 8-15, so one lane's MMA results hold a gate column and its up
+// column side by side.
 // W8: 64-column blocks, each with its K/16 chunk rows contiguous: the 16 bytes at chunk row c
 // of column n hold codes[16c + b][n], b = 0..15, so that a warp streaming one block's k range
 // reads one contiguous run of memory.
@@ -17,7 +20,7 @@
 namespace gq {
 
 __global__ void pack_w4_kernel(int K, int N, const uint32_t *__restrict__ codes,
-                               uint32_t *__restrict__ packed, size_t total_words) {
+                               uint32_t *__restrict__ packed, size_t total_words, int gate_up) {
   const int nchunks = K / kChunkK;
   for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total_words;
        o += (size_t)gridDim.x * blockDim.x) {
@@ -30,7 +33,9 @@ __global__ void pack_w4_kernel(int K, int N, const uint32_t *__restrict__ codes,
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = (lane >> 2) + 8 * (i & 1);
-      const int n = t * kTileN + r;
+      // fused gate+up: tile t holds gate columns 8t .. 8t+7 (rows 0-7) and the matching up
+      // columns F + 8t .. (rows 8-15), F = N / 2
+      const int n = gate_up ? (r < 8 ? 8 * t + r : N / 2 + 8 * t + r - 8) : t * kTileN + r;
       const int k = c * kChunkK + 16 * j + 2 * (lane & 3) + 8 * (i >> 1);   // even
       uint32_t lo = 0, hi = 0;
       if (n < N) {
@@ -71,11 +76,12 @@ static int grid_for(size_t work, int threads) {
   return (int)(b ? b : 1);
 }
 
-cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed,
+cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed, bool gate_up,
                            cudaStream_t s) {
   const size_t tiles = (size_t)(N + kTileN - 1) / kTileN;
   const size_t total = tiles * (size_t)(K / kChunkK) * 128;
-  pack_w4_kernel<<<grid_for(total, 256), 256, 0, s>>>(K, N, codes, packed, total);
+  pack_w4_kernel<<<grid_for(total, 256), 256, 0, s>>>(K, N, codes, packed, total,
+                                                      gate_up ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -127,6 +127,9 @@ __device__ __forceinline__ bool slot_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// silu(g) * u = g / (1 + e^-g) * u in FP32 (CUDA's expf and IEEE division)
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
 // decode constants (fp16x2 bit patterns)
 constexpr uint32_t kMagic = 0x64006400u;       // 1024 in both halves
 constexpr uint32_t kSixteenth = 0x2C002C00u;   // 1/16
@@ -146,6 +149,7 @@ struct StripeParams {
   int S;                         // ring slots per warp
   int out_f32;
   int static_w;                  // weights may be read before the preceding kernel ends
+  int gate_up;                   // fused gate+up: out[m][j] = silu(col j) * (col N/2 + j)
 };
 
 // Shared-memory layout (dynamic): [bands][rings][pieces]
@@ -226,8 +230,12 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   const uint8_t *lsc = nullptr;                     // this lane's scale source in the head slot
   bool lcopy = false;                               // the part lies inside the tile's columns
   auto head_tile = [&]() {
-    lsc = reinterpret_cast<const uint8_t *>(p.scales) + (size_t)(hj * GPS + lg) * srow +
-          (size_t)ht * kTileN * ES + lp * 16;
+    // byte offset of this lane's 16-byte part of the tile's scale row: columns 16 ht .. +15,
+    // or with gate+up the gate columns 8 ht .. +7 then the up columns N/2 + 8 ht .. +7
+    size_t col_bytes = (size_t)ht * kTileN * ES + lp * 16;
+    if (p.gate_up && lp * 16 >= 8 * ES) col_bytes = (size_t)(N / 2 + 8 * ht) * ES + (lp * 16 - 8 * ES);
+    else if (p.gate_up) col_bytes = (size_t)8 * ht * ES + lp * 16;
+    lsc = reinterpret_cast<const uint8_t *>(p.scales) + (size_t)(hj * GPS + lg) * srow + col_bytes;
     lcopy = lane < NL && lp * 16 < min(kTileN, N - ht * kTileN) * ES;
   };
   head_tile();
@@ -377,8 +385,10 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
 #pragma unroll
     for (int gi = 0; gi < GPS; ++gi) {
       const uint32_t *zr = p.zeros + (size_t)(jz * GPS + gi) * NW;
-      z[gi][0] = __ldg(zr + min(2 * tz, NW - 1));
-      z[gi][1] = __ldg(zr + min(2 * tz + 1, NW - 1));
+      // the words of the tile's columns r0 and r0 + 8 (gate+up: gate word tz, up word
+      // N/16 + tz)
+      z[gi][0] = __ldg(zr + min(p.gate_up ? tz : 2 * tz, NW - 1));
+      z[gi][1] = __ldg(zr + min(p.gate_up ? NW / 2 + tz : 2 * tz + 1, NW - 1));
     }
   };
   const int t_first = wb / SPT;
@@ -405,9 +415,14 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
       acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
       if (mrow >= M) continue;
       if (j0 == 0 && j1 == SPT) {
-        const int n0 = t * kTileN + r0;
-        if (n0 < N) store_out_rt(p.out, (size_t)mrow * N + n0, v0, p.out_f32 != 0);
-        if (n0 + 8 < N) store_out_rt(p.out, (size_t)mrow * N + n0 + 8, v1, p.out_f32 != 0);
+        if (p.gate_up) {                           // v0 is gate column 8t + r0, v1 its up column
+          store_out_rt(p.out, (size_t)mrow * (N / 2) + t * 8 + r0, silu_mul(v0, v1),
+                       p.out_f32 != 0);
+        } else {
+          const int n0 = t * kTileN + r0;
+          if (n0 < N) store_out_rt(p.out, (size_t)mrow * N + n0, v0, p.out_f32 != 0);
+          if (n0 + 8 < N) store_out_rt(p.out, (size_t)mrow * N + n0 + 8, v1, p.out_f32 != 0);
+        }
       } else {
         float *pc = pieces + ((warp * 2 + (t == t_first ? 0 : 1)) * M + mrow) * kTileN;
         pc[r0] = v0;
@@ -498,6 +513,21 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   }
   if (n > 0 && j != 0) flush(j);
 
+  // Final value `sum` of tile tt, row m, tile column nl, held by lane idx % 32 of a 32-value
+  // pass (idx = m * 16 + nl; every lane of the warp calls this).  With gate+up the lane of
+  // gate column nl < 8 takes its up value from lane + 8 and stores silu(gate) * up.
+  auto store_tile_value = [&](int tt, int idx, int m, int nl, float sum) {
+    const bool valid = idx < M * kTileN;
+    if (p.gate_up) {
+      const float up = __shfl_down_sync(0xffffffffu, sum, 8);
+      if (valid && nl < 8)
+        store_out_rt(p.out, (size_t)m * (N / 2) + tt * 8 + nl, silu_mul(sum, up), p.out_f32 != 0);
+    } else {
+      const int nn = tt * kTileN + nl;
+      if (valid && nn < N) store_out_rt(p.out, (size_t)m * N + nn, sum, p.out_f32 != 0);
+    }
+  };
+
   // ---- reduction of the tiles shared between warps (shared memory) and CTAs (global)
   __syncthreads();
   // A tile is reduced by the lowest warp of the CTA that holds part of it: this warp for its
@@ -527,8 +557,7 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
         }
       }
       if (cta_whole) {
-        const int nn = tt * kTileN + nl;
-        if (idx < M * kTileN && nn < N) store_out_rt(p.out, (size_t)m * N + nn, sum, p.out_f32 != 0);
+        store_tile_value(tt, idx, m, nl, sum);
       } else if (!cta_first) {
         // a contributor: publish this CTA's share (counted in below)
         if (idx < M * kTileN) p.part[(size_t)blockIdx.x * (8 * kTileN) + m * kTileN + nl] = sum;
@@ -557,9 +586,8 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
             if (b2 * p.split_mult >= te) break;
             sum += __ldcg(p.part + (size_t)c2 * (8 * kTileN) + m * kTileN + nl);
           }
-          const int nn = tt * kTileN + nl;
-          if (nn < N) store_out_rt(p.out, (size_t)m * N + nn, sum, p.out_f32 != 0);
         }
+        store_tile_value(tt, idx, m, nl, sum);
       }
     }
     if (!cta_whole && !cta_first) {
@@ -668,6 +696,7 @@ cudaError_t launch_stripe_decode(const Plan &pl, int M, int K, int N, int G, int
   sp.S = pl.slots;
   sp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   sp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
+  sp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
   switch (G) {
     case 32: return launch_stripe_g<32>(pl, prec, sp, s);
     case 64: return launch_stripe_g<64>(pl, prec, sp, s);

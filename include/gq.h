@@ -48,6 +48,12 @@ typedef enum gq_status {
 #define GQ_SC_BF16 0x08  /* scales bf16                                                        */
 #define GQ_SC_F32  0x10  /* scales fp32; neither SC flag = fp16                                */
 #define GQ_OUT_F32 0x20  /* output fp32; clear = bf16 (round to nearest even)                  */
+#define GQ_GATE_UP  0x80 /* W4 fused gate+up projection: the N = 2F columns are F gate columns
+                            then F up columns, and out is [M][F] = silu(gate) * up (silu(x) =
+                            x / (1 + e^-x), in FP32 on the FP32 GEMM results, then rounded).
+                            gq_pack_weights must get the flag too (it interleaves gate and up
+                            columns tile by tile).  Needs N % 16 == 0 and, in gq_gemm, M <= 8 and
+                            K % 256 == 0 (else GQ_ERR_UNSUPPORTED)                            */
 #define GQ_STATIC_W 0x40 /* Wq, scales and zeros are not written by work still running on the
                             stream (weights loaded once, as in serving): the decode kernels
                             may start streaming them before the preceding kernel has ended;

@@ -27,7 +27,7 @@ __all__ = [
     "fp16_bits_to_f64", "bf16_bits_to_f64", "f32_to_f64", "f64_to_bf16_bits",
     "f64_to_f32", "unpack_int4_k", "unpack_int4_n", "dequantize", "group_gemm",
     "group_gemm_magnitude", "reference", "tolerance", "check", "quantize_w4_g",
-    "bits_per_weight", "dequantize_brute",
+    "bits_per_weight", "dequantize_brute", "silu", "silu_mul_reference",
 ]
 
 
@@ -210,6 +210,34 @@ def reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, w4: bool,
     else:
         s = f32_to_f64(sraw)
     return group_gemm(A, q, z, s, G), group_gemm_magnitude(A, q, z, s, G)
+
+
+# ---------------------------------------------------------------------------------------
+# Fused gate+up epilogue (P1 section 五.2, SiLU-and-mul): the gate_up GEMM's N = 2F columns
+# are F gate columns then F up columns, and the epilogue returns silu(gate) · up, [M][F].
+# ---------------------------------------------------------------------------------------
+
+def silu(x) -> np.ndarray:
+    """silu(x) = x · σ(x) = x / (1 + e^(−x)), in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def silu_mul_reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, act: str,
+                       sc: str, rows=None, cols=None):
+    """out[m][j] = silu(gate[m][j]) · up[m][j] with gate = column j < F = N/2 and up = column
+    F + j of the group GEMM (W4 codes).  Returns (ref, mag) over output columns ``cols``
+    (default all F).  mag carries the GEMM's own error bound through the product to first
+    order: max|silu'| · mag_gate · |up| + |silu(gate)| · mag_up, where |silu'(x)| =
+    |σ(x)·(1 + x·(1 − σ(x)))| < 1.1 for every x, so ``tolerance``/``check`` apply unchanged."""
+    F = N // 2
+    jc = np.arange(F) if cols is None else np.asarray(cols)
+    g, mg = reference(A_raw, codes, scales, zeros, K=K, N=N, G=G, w4=True, act=act, sc=sc,
+                      rows=rows, cols=jc)
+    u, mu = reference(A_raw, codes, scales, zeros, K=K, N=N, G=G, w4=True, act=act, sc=sc,
+                      rows=rows, cols=F + jc)
+    sg = silu(g)
+    return sg * u, 1.1 * mg * np.abs(u) + np.abs(sg) * mu
 
 
 # ---------------------------------------------------------------------------------------

@@ -357,3 +357,67 @@ def test_static_weight_flag_gives_the_same_bits(gq, cfg):
     view = torch.int16 if cfg.out == "bf16" else torch.int32
     for o in got:
         assert torch.equal(o.view(view), ref.view(view))
+
+
+# ------------------------------------------------------------------ fused gate+up epilogue
+
+GATE_UP_SHAPES = [
+    gq_synth.Config("gu_m1", M=1, K=1024, N=512, G=128),
+    gq_synth.Config("gu_m3_zp", M=3, K=2048, N=1024, G=128, zp=True, sc="bf16"),
+    gq_synth.Config("gu_m8_f32", M=8, K=512, N=272, G=64, sc="f32", out="f32"),
+    # 128 tiles on 152 SMs: CTAs split tiles, so the cross-CTA reduction stores the epilogue
+    gq_synth.Config("gu_m1_split", M=1, K=4096, N=2048, G=128, outlier_frac=0.001),
+    gq_synth.Config("gu_m5_g32", M=5, K=1024, N=320, G=32, zp=True),
+]
+
+
+def _gate_up_case(gq, cfg, seed, cols=None):
+    from group_quantized_weight_gb300.constants import GQ_GATE_UP
+    inp = gq_synth.make_inputs(cfg, seed=seed)
+    prec = prec_of(cfg) | GQ_GATE_UP
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    A, S = np_to_dev(inp["A"]), np_to_dev(inp["scales"])
+    Z = np_to_dev(inp["zeros"]) if inp["zeros"] is not None else None
+    out = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+    gq.gemm_t(A, packed, S, Z, out, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    got = out_to_f64(out, cfg.out)
+    ref, mag = oracle.silu_mul_reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"],
+                                         K=cfg.K, N=cfg.N, G=cfg.G, act=cfg.act, sc=cfg.sc,
+                                         cols=cols)
+    if cols is not None:
+        got = got[:, cols]
+    return _assert_parity(cfg, got, ref, mag), (A, packed, S, Z, prec)
+
+
+@pytest.mark.parametrize("cfg", GATE_UP_SHAPES, ids=lambda c: c.name)
+def test_gate_up_silu_mul(gq, cfg):
+    _gate_up_case(gq, cfg, seed=7)
+
+
+def test_gate_up_full_size_sampled_and_repeatable(gq):
+    """The fused gate+up GEMV at the decode size (N = 2·14336), 512 sampled output columns
+    against the oracle; a second call gives the same bits."""
+    cfg = gq_synth.CONFIGS["decode_gateup"]
+    cols = np.random.default_rng(11).choice(cfg.N // 2, 512, replace=False)
+    _, (A, packed, S, Z, prec) = _gate_up_case(gq, cfg, seed=0, cols=cols)
+    o1 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+    o2 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+    gq.gemm_t(A, packed, S, Z, o1, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    gq.gemm_t(A, packed, S, Z, o2, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_pack_gate_up_interleaves_gate_and_up_columns(gq):
+    """Tile t of the gate+up packing holds gate columns 8t .. 8t+7 and up columns
+    N/2 + 8t .. N/2 + 8t + 7, each in the plain packed tile format."""
+    from group_quantized_weight_gb300.constants import GQ_GATE_UP, GQ_W4
+    cfg = gq_synth.Config("pgu", M=1, K=128, N=64, G=128)
+    inp = gq_synth.make_weights(cfg, seed=8)
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, GQ_W4 | GQ_GATE_UP)
+    qp = _unpack_w4_device_layout(packed.cpu().numpy(), cfg.K, cfg.N)   # packed column order
+    F = cfg.N // 2
+    order = np.concatenate([np.r_[8 * t:8 * t + 8, F + 8 * t:F + 8 * t + 8]
+                            for t in range(cfg.N // 16)])
+    assert np.array_equal(qp, inp["q"].astype(np.int64)[:, order])

@@ -215,3 +215,20 @@ def test_algorithmic_bytes_match_the_worked_figures():
     assert C.algorithmic_bytes(1, 4096, 4096, 128, True, False, "bf16", "fp16", "bf16") == \
         (8 << 20) + (256 << 10) + 8192 + 8192
     assert C.gemm_flops(4096, 4096, 14336) == 481036337152
+
+
+def test_gate_up_flag_is_validated_and_planned_on_the_striped_kernel():
+    gu = C.GQ_W4 | C.GQ_GATE_UP
+    # N must hold whole 16-column tiles of 8 gate and 8 up columns; INT8 has no fused epilogue
+    assert gq.gq_gemm(1, 512, 24, 128, gu, 16, 16, 16, None, 16, None) == 1
+    assert gq.gq_gemm(1, 512, 32, 32, C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_GATE_UP,
+                      16, 16, 16, None, 16, None) == 2
+    # only the striped decode kernel (M <= 8, K % 256 == 0) carries the epilogue
+    assert gq.gq_plan(1, 4096, 28672, 128, gu, sm_count=152)["path"] == 3
+    assert gq.gq_plan(8, 1024, 512, 64, gu | C.GQ_ZP, sm_count=152)["path"] == 3
+    for M, K in ((9, 4096), (1, 320)):
+        with pytest.raises(C.GqError) as e:
+            gq.gq_plan(M, K, 1024, 64, gu, sm_count=152)
+        assert e.value.status == 2
+    # the packed size does not change
+    assert gq.gq_packed_bytes(4096, 28672, 128, gu) == gq.gq_packed_bytes(4096, 28672, 128, C.GQ_W4)

@@ -351,3 +351,45 @@ def test_tolerance_formula():
     assert np.allclose(orc.tolerance(ref, mag, "f32"), [1e-5 + 1e-5, 2e-5 + 1e-5, 1e-5])
     bad, ratio = orc.check(ref + np.array([0.0, 0.0, 2e-3]), ref, mag, "bf16")
     assert bad == 1 and ratio == pytest.approx(2.0)
+
+
+# ------------------------------------------------------------------ fused gate+up epilogue
+
+def test_silu_closed_forms_and_odd_part():
+    """silu(x) = x·σ(x): silu(0) = 0; σ(ln 3) = 3/4 and σ(−ln 3) = 1/4, so silu(±ln 3) =
+    ±ln 3 · {3/4, 1/4}; σ(x) + σ(−x) = 1 gives silu(x) − silu(−x) = x for every x; and
+    silu(x) → x, silu(−x) → 0 for large x."""
+    ln3 = math.log(3.0)
+    assert orc.silu(0.0) == 0.0
+    assert abs(orc.silu(ln3) - 0.75 * ln3) <= 1e-15
+    assert abs(orc.silu(-ln3) + 0.25 * ln3) <= 1e-15
+    x = np.random.default_rng(3).normal(0, 4, 1000)
+    assert np.allclose(orc.silu(x) - orc.silu(-x), x, rtol=1e-14, atol=1e-14)
+    assert orc.silu(40.0) == 40.0 and abs(orc.silu(-40.0)) < 1e-15
+
+
+def test_silu_mul_takes_gate_from_the_first_half_and_up_from_the_second():
+    """One-hot weights: gate column j0 = 40·(selected activation 1.0) so silu(gate) = 40 to
+    double precision, up column F + j0 = 0.5·(code − 8)·A[:, k2]; out[:, j0] = 40·up and
+    every other output is silu(0)·0 = 0.  Swapping the halves would give silu(up)·40."""
+    K, N, G = 256, 32, 128
+    F = N // 2
+    q = np.full((K, N), 8, dtype=np.uint8)
+    j0, k1, k2 = 5, 17, 200
+    q[k1, j0] = 9                                  # gate: s·1 at k1
+    q[k2, F + j0] = 3                              # up: s·(3 − 8) at k2
+    s = np.ones((K // G, N), dtype=np.float32)
+    s[:, F + j0] = 0.5
+    s[:, j0] = 40.0
+    codes = gq_synth.pack_int4_along_k(q)
+    scales = gq_synth.f32_to_fp16_bits(s)
+    A = gq_synth.make_activations(gq_synth.Config("gu", M=3, K=K, N=N, G=G), seed=2)
+    A[:, k1] = 0x3F80                              # bf16 1.0
+    ref, mag = orc.silu_mul_reference(A, codes, scales, None, K=K, N=N, G=G, act="bf16",
+                                      sc="fp16")
+    up = 0.5 * (3 - 8) * orc.bf16_bits_to_f64(A[:, k2])
+    expect = np.zeros((3, F))
+    expect[:, j0] = 40.0 * up
+    assert ref.shape == (3, F)
+    assert np.array_equal(ref, expect)
+    assert (mag >= 0).all() and (mag[:, j0] > 0).all()
