@@ -411,24 +411,36 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
     back calls, rotating weight copies so that the weights come from HBM whenever they fit
     at most a third of L2 per copy), HBM GB/s of the algorithmic bytes, TFLOPS, and the
     fraction of the roofline that bounds it (HBM below M = 128, dense BF16 above)."""
-    from group_quantized_weight_gb300.constants import (GQ_GATE_UP, GQ_STATIC_W, algorithmic_bytes,
+    from group_quantized_weight_gb300.constants import (GQ_ACT_F32, GQ_ACT_I8, GQ_GATE_UP,
+                                                        GQ_STATIC_W, algorithmic_bytes,
                                                         gemm_flops, prec_flags)
     out = []
     side = torch.cuda.Stream()           # graph capture needs a stream other than the legacy one
     for name in ("tiny_gemv", "decode_gateup", "decode_gateup_silu", "q8_m1", "q8_m32",
-                 "asym_m16", "prefill"):
+                 "q8a8_m1", "q8a8_m32", "asym_m16", "prefill"):
         # decode_gateup_silu: the gate+up GEMV with the fused SiLU-and-mul epilogue
-        # (GQ_GATE_UP): the same weights, an output of N/2 columns
+        # (GQ_GATE_UP): the same weights, an output of N/2 columns.  q8a8_*: the Q8_0 shapes
+        # with int8 activation codes and per-group scales (GQ_ACT_I8), quantized on the device
+        # by gq_quantize_act before the timed calls
         fused = name == "decode_gateup_silu"
-        cfg = gq_synth.CONFIGS["decode_gateup" if fused else name]
+        a8 = name.startswith("q8a8")
+        cfg = gq_synth.CONFIGS["decode_gateup" if fused else name.replace("q8a8", "q8")]
         prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out) | GQ_STATIC_W
         if fused:
             prec |= GQ_GATE_UP
+        if a8:
+            prec = (prec & ~GQ_ACT_F32) | GQ_ACT_I8
         d = _dev_inputs(torch, dev, gq_synth.make_inputs(cfg, seed=0))
         packed = gq.pack_weights_t(d["codes"], cfg.K, cfg.N, cfg.G, prec)
         nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
         if fused:
             nbytes -= cfg.M * (cfg.N // 2) * 2        # half the bf16 output columns
+        a_ptr, as_ptr = d["A"].data_ptr(), None
+        if a8:                                        # int8 codes + fp32 scales per group
+            Aq, As = gq.quantize_act_t(d["A"], cfg.K, cfg.G, GQ_ACT_F32, stream=side)
+            side.synchronize()
+            a_ptr, as_ptr = Aq.data_ptr(), As.data_ptr()
+            nbytes += cfg.M * cfg.K * (1 - 4) + cfg.M * (cfg.K // cfg.G) * 4
         wbytes = packed.numel() + d["scales"].numel() * d["scales"].element_size()
         copies = 1 if cfg.M >= 128 else int(max(1, min(8, -(-3 * L2_BYTES // max(wbytes, 1)))))
         W = [packed] + [packed.clone() for _ in range(copies - 1)]
@@ -439,17 +451,18 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
         odt = torch.float32 if cfg.out == "f32" else torch.bfloat16
         o = torch.empty((cfg.M, cfg.N // 2 if fused else cfg.N), dtype=odt, device=dev)
         big = cfg.M >= 128
-        res = gq.gq_bench(cfg.M, cfg.K, cfg.N, cfg.G, prec, d["A"].data_ptr(),
+        res = gq.gq_bench(cfg.M, cfg.K, cfg.N, cfg.G, prec, a_ptr,
                           [w.data_ptr() for w in W], [x.data_ptr() for x in S],
                           [z.data_ptr() for z in Z] if Z else None, o.data_ptr(),
                           warmup=3, iters=10 if big else 200, use_graph=not big,
-                          stream=side.cuda_stream)
+                          stream=side.cuda_stream, a_scales_ptr=as_ptr)
         us = res["us_per_call"]
         gbs = nbytes / (us * 1e-6) / 1e9
         tf = gemm_flops(cfg.M, cfg.K, cfg.N) / (us * 1e-6) / 1e12
         plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
         row = {"workload": name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "G": cfg.G,
                **({"epilogue": "silu(gate) * up, N/2 output columns"} if fused else {}),
+               **({"activations": "int8 codes, fp32 scale per (row, group)"} if a8 else {}),
                "path": plan["path"], "us": us, "GB/s": gbs, "TFLOPS": tf,
                "weight_copies": copies,
                "l2": ("from HBM (rotated copies exceed L2)" if copies * wbytes > L2_BYTES

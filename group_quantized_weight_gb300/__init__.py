@@ -38,7 +38,8 @@ class gq_bench_args(ctypes.Structure):
     _fields_ = [("M", _i), ("K", _i), ("N", _i), ("G", _i), ("prec", _i), ("A", _p),
                 ("Wq", ctypes.POINTER(_p)), ("scales", ctypes.POINTER(_p)),
                 ("zeros", ctypes.POINTER(_p)), ("n_copies", _i), ("out", _p),
-                ("warmup", _i), ("iters", _i), ("use_graph", _i), ("stream", _p)]
+                ("warmup", _i), ("iters", _i), ("use_graph", _i), ("stream", _p),
+                ("a_scales", _p)]
 
 
 class gq_bench_result(ctypes.Structure):
@@ -52,6 +53,8 @@ _SIGS = {
     "gq_set_workspace": [_p, _sz],
     "gq_gemm": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_gemm_static_scratch": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
+    "gq_gemm_a8": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
+    "gq_quantize_act": [_i, _i, _i, _i, _p, _p, _p, _p],
     "gq_bench": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
     "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
@@ -109,6 +112,18 @@ def gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, str
     return _lib.gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream)
 
 
+def gq_gemm_a8(M, K, N, G, prec, Aq_ptr, a_scales_ptr, Wq_ptr, scales_ptr, out_ptr,
+               stream=None) -> int:
+    """W8A8 group GEMM (GQ_ACT_I8).  Raw call; returns the status."""
+    return _lib.gq_gemm_a8(M, K, N, G, prec, Aq_ptr, a_scales_ptr, Wq_ptr, scales_ptr, out_ptr,
+                           stream)
+
+
+def gq_quantize_act(M, K, G, prec, A_ptr, Aq_ptr, a_scales_ptr, stream=None) -> int:
+    """Dynamic per-group INT8 quantization of activations.  Raw call; returns the status."""
+    return _lib.gq_quantize_act(M, K, G, prec, A_ptr, Aq_ptr, a_scales_ptr, stream)
+
+
 def gq_gemm_static_scratch(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr,
                            stream=None) -> int:
     """gq_gemm that never allocates: scratch comes from a fixed array inside the library
@@ -137,12 +152,12 @@ def gq_device_error(clear: bool = False) -> int:
 
 
 def gq_bench(M, K, N, G, prec, A_ptr, Wq_ptrs, scales_ptrs, zeros_ptrs, out_ptr, *, warmup=3,
-             iters=100, use_graph=True, stream=None) -> dict:
+             iters=100, use_graph=True, stream=None, a_scales_ptr=None) -> dict:
     n = len(Wq_ptrs)
     arr = _p * n
     args = gq_bench_args(M, K, N, G, prec, A_ptr, arr(*Wq_ptrs), arr(*scales_ptrs),
                          arr(*zeros_ptrs) if zeros_ptrs else None, n, out_ptr, warmup, iters,
-                         1 if use_graph else 0, stream)
+                         1 if use_graph else 0, stream, a_scales_ptr)
     res = gq_bench_result()
     _check(_lib.gq_bench(ctypes.byref(args), ctypes.byref(res)), "gq_bench")
     return {"us_per_call": res.us_per_call, "launches_per_call": res.launches_per_call}
@@ -163,6 +178,25 @@ def pack_weights_t(codes, K: int, N: int, G: int, prec: int, stream=None):
     _check(gq_pack_weights(K, N, G, prec, codes.data_ptr(), packed.data_ptr(),
                            _stream_ptr(stream)), "gq_pack_weights")
     return packed
+
+
+def quantize_act_t(A, K: int, G: int, prec: int = 0, stream=None):
+    """A [M][K] (bf16 bits as int16/bfloat16, or fp32 with GQ_ACT_F32) -> (Aq int8 [M][K],
+    a_scales fp32 [M][K/G]) on torch's current stream."""
+    import torch
+    M = A.shape[0]
+    Aq = torch.empty((M, K), dtype=torch.int8, device=A.device)
+    As = torch.empty((M, K // G), dtype=torch.float32, device=A.device)
+    _check(gq_quantize_act(M, K, G, prec, A.data_ptr(), Aq.data_ptr(), As.data_ptr(),
+                           _stream_ptr(stream)), "gq_quantize_act")
+    return Aq, As
+
+
+def gemm_a8_t(Aq, As, Wq, scales, out, M: int, K: int, N: int, G: int, prec: int, stream=None):
+    """out <- gq_gemm_a8(...) on torch's current stream; raises GqError on a bad status."""
+    _check(gq_gemm_a8(M, K, N, G, prec, Aq.data_ptr(), As.data_ptr(), Wq.data_ptr(),
+                      scales.data_ptr(), out.data_ptr(), _stream_ptr(stream)), "gq_gemm_a8")
+    return out
 
 
 def gemm_t(A, Wq, scales, zeros, out, M: int, K: int, N: int, G: int, prec: int, stream=None):

@@ -10,6 +10,7 @@ GQ_SC_F32 = 0x10
 GQ_OUT_F32 = 0x20
 GQ_STATIC_W = 0x40
 GQ_GATE_UP = 0x80
+GQ_ACT_I8 = 0x100
 
 GQ_OK = 0
 STATUS_NAMES = {0: "GQ_OK", 1: "GQ_ERR_INVALID_ARG", 2: "GQ_ERR_UNSUPPORTED",

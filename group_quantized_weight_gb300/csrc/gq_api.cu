@@ -17,7 +17,7 @@ static inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 int validate(int M, int K, int N, int G, int prec) {
   if (M < 0 || N < 0 || K <= 0) return GQ_ERR_INVALID_ARG;
   if (prec & ~(GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_SC_BF16 | GQ_SC_F32 | GQ_OUT_F32 | GQ_STATIC_W |
-               GQ_GATE_UP))
+               GQ_GATE_UP | GQ_ACT_I8))
     return GQ_ERR_INVALID_ARG;
   if ((prec & GQ_SC_BF16) && (prec & GQ_SC_F32)) return GQ_ERR_INVALID_ARG;
   if (!(G == 32 || G == 64 || G == 128 || G == 256)) return GQ_ERR_UNSUPPORTED;
@@ -26,6 +26,12 @@ int validate(int M, int K, int N, int G, int prec) {
   if (prec & GQ_GATE_UP) {
     if (!(prec & GQ_W4)) return GQ_ERR_UNSUPPORTED;
     if (N % 16 != 0) return GQ_ERR_INVALID_ARG;
+  }
+  if (prec & GQ_ACT_I8) {                          // W8A8: INT8 codes, fp32 scales
+    if (prec & (GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_GATE_UP)) return GQ_ERR_UNSUPPORTED;
+    if (!(prec & GQ_SC_F32)) return GQ_ERR_UNSUPPORTED;
+    if (K % kChunkK8 != 0) return GQ_ERR_UNSUPPORTED;
+    return GQ_OK;
   }
   if (prec & GQ_W4) {
     if (K % kChunkK != 0) return GQ_ERR_UNSUPPORTED;
@@ -79,6 +85,30 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const int Mc = M > 0 ? M : 1;
   const int Nc = N > 0 ? N : 8;
   const size_t kCtaSmemCap = 227u * 1024u - 1024u;   // minus the static shared memory
+  // W8A8 (GQ_ACT_I8): integer group dots, 64 columns x one K slice x 32 rows per CTA
+  if (prec & GQ_ACT_I8) {
+    const int ks = q8a8_slices(Mc, K, Nc, G, sms, kPartCap);
+    if (ks < 1) return GQ_ERR_UNSUPPORTED;
+    p->path = kPathQ8A8;
+    p->m_tile = Mc < 32 ? Mc : 32;
+    p->n_tile = 64;
+    p->unit_k = G;
+    p->units = K / G;
+    p->nsplit = ks;
+    p->grid_x = ceil_div(Nc, 64) * ks;
+    p->grid_y = 1;
+    p->grid_z = ceil_div(Mc, 32);
+    p->block_threads = 256;
+    p->smem_bytes = q8a8_smem_bytes(Mc, K, G, ks);
+    if (ks > 1) {
+      p->part_bytes = round_up((size_t)ks * Mc * Nc * sizeof(float), 256);
+      p->counter_bytes = kCounterRegionBytes;
+      if ((size_t)p->grid_z * ceil_div(Nc, 64) * sizeof(unsigned) > kCounterRegionBytes)
+        return GQ_ERR_UNSUPPORTED;
+    }
+    p->workspace_bytes = p->part_bytes + p->counter_bytes;
+    return GQ_OK;
+  }
   // striped persistent decode (M <= 8): one CTA of kStrWarps warps per SM over a
   // contiguous range of (tile, 256-k slot) pairs; whole tiles per CTA when that keeps the
   // SMs within 10% of even, else equal slot ranges with a cross-CTA reduction
@@ -460,8 +490,13 @@ int gq_pack_weights(int K, int N, int G, int prec, const void *codes, void *pack
   return e == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
 
+static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,
+                        const void *a_scales, const void *Wq, const void *scales, void *out,
+                        void *stream);
+
 static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
                      const void *scales, const void *zeros, void *out, void *stream) {
+  if (prec & GQ_ACT_I8) return GQ_ERR_INVALID_ARG;   // needs the activation scales: gq_gemm_a8
   int st = validate(M, K, N, G, prec);
   if (st != GQ_OK) return st;
   if (M == 0 || N == 0) return GQ_OK;
@@ -497,13 +532,74 @@ int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
   return gemm_impl(M, K, N, G, prec, A, Wq, scales, zeros, out, stream);
 }
 
+static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,
+                        const void *a_scales, const void *Wq, const void *scales, void *out,
+                        void *stream) {
+  if (!(prec & GQ_ACT_I8)) return GQ_ERR_INVALID_ARG;
+  int st = validate(M, K, N, G, prec);
+  if (st != GQ_OK) return st;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!Aq || !a_scales || !Wq || !scales || !out) return GQ_ERR_INVALID_ARG;
+  if (!aligned16(Aq) || !aligned16(a_scales) || !aligned16(Wq) || !aligned16(scales) ||
+      !aligned16(out))
+    return GQ_ERR_ALIGNMENT;
+  int sms = 0;
+  st = device_sm_count(&sms);
+  if (st != GQ_OK) return st;
+  Plan p;
+  st = make_plan(M, K, N, G, prec, sms, &p);
+  if (st != GQ_OK) return st;
+  void *ws = nullptr;
+  st = get_scratch(p.workspace_bytes, &ws);
+  if (st != GQ_OK) return st;
+  unsigned *counters = (unsigned *)ws;
+  float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
+  const cudaError_t e = launch_q8a8(p, M, K, N, G, prec, (const int8_t *)Aq,
+                                    (const float *)a_scales, Wq, scales, out, part, counters,
+                                    (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    note_cuda_error("launch", e);
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  return GQ_OK;
+}
+
+int gq_gemm_a8(int M, int K, int N, int G, int prec, const void *Aq, const void *a_scales,
+               const void *Wq, const void *scales, void *out, void *stream) {
+  return gemm_a8_impl(M, K, N, G, prec, Aq, a_scales, Wq, scales, out, stream);
+}
+
+int gq_quantize_act(int M, int K, int G, int prec, const void *A, void *Aq, void *a_scales,
+                    void *stream) {
+  if (prec & ~GQ_ACT_F32) return GQ_ERR_INVALID_ARG;
+  if (M < 0 || K <= 0) return GQ_ERR_INVALID_ARG;
+  if (!(G == 32 || G == 64 || G == 128 || G == 256) || K % G != 0 || K % 16 != 0)
+    return GQ_ERR_INVALID_ARG;
+  if (M == 0) return GQ_OK;
+  if (!A || !Aq || !a_scales) return GQ_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Aq) || !aligned16(a_scales)) return GQ_ERR_ALIGNMENT;
+  const cudaError_t e = launch_quantize_act(M, K, G, (prec & GQ_ACT_F32) != 0, A,
+                                            (int8_t *)Aq, (float *)a_scales, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    note_cuda_error("launch", e);
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  return GQ_OK;
+}
+
 int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
   if (!a || !r || a->n_copies < 1 || a->iters < 1 || a->warmup < 0 || !a->Wq || !a->scales)
     return GQ_ERR_INVALID_ARG;
   if ((a->prec & GQ_ZP) && !a->zeros) return GQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)a->stream;
+  if ((a->prec & GQ_ACT_I8) && !a->a_scales) return GQ_ERR_INVALID_ARG;
   auto call = [&](int i) {
     const int c = i % a->n_copies;
+    if (a->prec & GQ_ACT_I8)
+      return gemm_a8_impl(a->M, a->K, a->N, a->G, a->prec, a->A, a->a_scales, a->Wq[c],
+                          a->scales[c], a->out, a->stream);
     return gemm_impl(a->M, a->K, a->N, a->G, a->prec, a->A, a->Wq[c], a->scales[c],
                      (a->prec & GQ_ZP) ? a->zeros[c] : nullptr, a->out, a->stream);
   };

@@ -38,7 +38,7 @@ constexpr int kQ8MaxRows = 32;
 constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
 
 enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3,
-            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6 };
+            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6, kPathQ8A8 = 7 };
 
 struct Plan {
   int path;
@@ -130,6 +130,14 @@ int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap);
 cudaError_t launch_q8_mma(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                           const void *Wq, const void *scales, void *out, float *part,
                           unsigned *counters, cudaStream_t s);
+// INT8-activation variant (W8A8): the dynamic activation quantizer and the integer group GEMM
+cudaError_t launch_quantize_act(int M, int K, int G, bool f32, const void *A, int8_t *Aq,
+                                float *a_scales, cudaStream_t s);
+int q8a8_slices(int M, int K, int N, int G, int sms, size_t part_cap);
+size_t q8a8_smem_bytes(int M, int K, int G, int KS);
+cudaError_t launch_q8a8(const Plan &p, int M, int K, int N, int G, int prec, const int8_t *Aq,
+                        const float *As, const void *Wq, const void *scales, void *out,
+                        float *part, unsigned *counters, cudaStream_t s);
 // Launches the kernel of plan p (any path); part and counters may be NULL when the plan
 // needs no workspace.
 cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, const void *A,

@@ -51,6 +51,7 @@ using namespace gq;
 extern "C" int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, const void *A,
                                       const void *Wq, const void *scales, const void *zeros,
                                       void *out, void *stream) {
+  if (prec & GQ_ACT_I8) return GQ_ERR_INVALID_ARG;   // the W8A8 entry is gq_gemm_a8
   int st = validate(M, K, N, G, prec);
   if (st != GQ_OK) return st;
   if (M == 0 || N == 0) return GQ_OK;

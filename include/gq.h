@@ -54,6 +54,9 @@ typedef enum gq_status {
                             gq_pack_weights must get the flag too (it interleaves gate and up
                             columns tile by tile).  Needs N % 16 == 0 and, in gq_gemm, M <= 8 and
                             K % 256 == 0 (else GQ_ERR_UNSUPPORTED)                            */
+#define GQ_ACT_I8  0x100  /* INT8-activation variant (gq_gemm_a8, and gq_plan / gq_workspace_size
+                            for it): activations are int8 codes with one fp32 scale per (row,
+                            group); W8 codes and GQ_SC_F32 only; gq_gemm refuses it         */
 #define GQ_STATIC_W 0x40 /* Wq, scales and zeros are not written by work still running on the
                             stream (weights loaded once, as in serving): the decode kernels
                             may start streaming them before the preceding kernel has ended;
@@ -161,6 +164,8 @@ typedef struct gq_bench_args {
   void *out;
   int warmup, iters, use_graph;
   void *stream;
+  const void *a_scales;        /* GQ_ACT_I8: device fp32 [M][K/G] activation scales (A holds the
+                                  int8 codes) and each call is gq_gemm_a8; else NULL */
 } gq_bench_args;
 
 typedef struct gq_bench_result {
@@ -169,6 +174,35 @@ typedef struct gq_bench_result {
 } gq_bench_result;
 
 int gq_bench(const gq_bench_args *args, gq_bench_result *result);
+
+/* ---------------------------------------------------------------------------------------
+ * INT8-activation variant: the group-wise GEMM with integer activations of "04 · 分组量化
+ * GEMM 内核" section 2,
+ *     out[m][n] = Σ_g a_scales[m][g] · scales[g][n] · ( Σ_{k ∈ g} Aq[m][k] · q[k][n] ),
+ * the integer dot of a whole group finished exactly (INT32) before either scale.
+ * ------------------------------------------------------------------------------------- */
+
+/* Dynamic per-group INT8 quantization of activations (the absmax reduction and cast of
+ * "量化与融合 kernel" section 四.5, with 127 and one scale per group of G):
+ *   a_scales[m][g] = max_{k in g} |A[m][k]| / 127        (FP32 division)
+ *   Aq[m][k]       = rint(A[m][k] / a_scales[m][g])      (FP32 division, ties to even),
+ *                    clamped to [-127, 127]; a group of zeros gets scale 0 and codes 0.
+ *   A        device [M][K] bf16, or fp32 with GQ_ACT_F32 (prec holds no other flag).
+ *   Aq       device int8 [M][K];  a_scales  device fp32 [M][K/G].
+ * Asynchronous on stream.  Errors: GQ_ERR_INVALID_ARG (M < 0, K % G != 0, G outside
+ * {32, 64, 128, 256}, K % 16 != 0, NULL pointer, other flags), GQ_ERR_ALIGNMENT (a pointer
+ * not 16-byte aligned), GQ_ERR_CUDA. */
+int gq_quantize_act(int M, int K, int G, int prec, const void *A, void *Aq, void *a_scales,
+                    void *stream);
+
+/* The W8A8 group GEMM above.  prec = GQ_ACT_I8 | GQ_SC_F32 [| GQ_OUT_F32] [| GQ_STATIC_W].
+ *   Aq        device int8 [M][K] (e.g. from gq_quantize_act);  a_scales  device fp32 [M][K/G].
+ *   Wq        W8 codes packed by gq_pack_weights (prec without GQ_W4);
+ *   scales    device fp32 [K/G][N];  out  device [M][N] bf16, or fp32 with GQ_OUT_F32.
+ * Shape contract and workspace as gq_gemm (gq_workspace_size with the same prec).
+ * Errors as gq_gemm; GQ_ERR_UNSUPPORTED for GQ_W4, GQ_ZP, GQ_ACT_F32 or GQ_GATE_UP. */
+int gq_gemm_a8(int M, int K, int N, int G, int prec, const void *Aq, const void *a_scales,
+               const void *Wq, const void *scales, void *out, void *stream);
 
 /* Host-only description of the launch gq_gemm would make (for tests and reports).
  * sm_count > 0 overrides the device query, so it works without a GPU. */
@@ -181,7 +215,8 @@ typedef struct gq_plan_t {
                         5 = INT8 CUDA-core kernel for M <= 4 (64 columns x one K slice
                             per CTA, paired FP32 FMAs),
                         6 = INT8 on BF16 tensor cores for 5 <= M <= 32 (codes exact in
-                            BF16, fp32 activations as three exact BF16 parts) */
+                            BF16, fp32 activations as three exact BF16 parts),
+                        7 = W8A8 integer group GEMM (GQ_ACT_I8, dp4a) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
   int n_tile;        /* output columns one CTA covers */

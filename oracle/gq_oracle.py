@@ -28,6 +28,7 @@ __all__ = [
     "f64_to_f32", "unpack_int4_k", "unpack_int4_n", "dequantize", "group_gemm",
     "group_gemm_magnitude", "reference", "tolerance", "check", "quantize_w4_g",
     "bits_per_weight", "dequantize_brute", "silu", "silu_mul_reference",
+    "quantize_act_i8", "group_gemm_a8", "reference_a8",
 ]
 
 
@@ -238,6 +239,64 @@ def silu_mul_reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, a
                       rows=rows, cols=F + jc)
     sg = silu(g)
     return sg * u, 1.1 * mg * np.abs(u) + np.abs(sg) * mu
+
+
+# ---------------------------------------------------------------------------------------
+# INT8-activation variant.  P2 section 2: out[m][n] = Σ_g a_scale[m][g] · b_scale[g][n] ·
+# (Σ_{k ∈ g} Aq[m][k] · Wq[k][n]), the integer dot of a whole group before either scale.
+# The activation codes come from the per-group absmax quantization of P1 section 四.5
+# (s = max|x| / 127, divide, round, saturate, cast).
+# ---------------------------------------------------------------------------------------
+
+def quantize_act_i8(A_raw, G: int, act: str):
+    """Per (row, group of G): s = max|x| / 127 and q = rint(x / s) clamped to [-127, 127];
+    s = 0 and q = 0 for a group of zeros.  Both divisions are IEEE binary32 and the rounding
+    is to nearest, ties to even: the integer each code is decided in the same precision as
+    the GPU kernel.  Returns (Aq int8 [M][K], a_scales float32 [M][K/G])."""
+    A = bf16_bits_to_f64(A_raw) if act == "bf16" else f32_to_f64(A_raw)
+    A32 = A.astype(np.float32)                      # exact: bf16 and fp32 inputs
+    M, K = A32.shape
+    Ag = A32.reshape(M, K // G, G)
+    amax = np.abs(Ag).max(axis=2)                   # exact
+    s = (amax / np.float32(127)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (Ag / s[:, :, None]).astype(np.float32)
+    q = np.where(s[:, :, None] > 0, np.clip(np.rint(r), -127, 127), 0)
+    return q.reshape(M, K).astype(np.int8), s
+
+
+def group_gemm_a8(Aq, a_s, q, s, G: int):
+    """Σ_g a_s[m][g] · s[g][n] · Σ_{k ∈ g} Aq[m][k] · q[k][n], the group dots in exact int64,
+    the scales in float64.  Returns (out, mag) with mag = Σ_g |a_s · s| · Σ_k |Aq · q|."""
+    Aq = np.asarray(Aq, dtype=np.int64)
+    q = np.asarray(q, dtype=np.int64)
+    a_s = np.asarray(a_s, dtype=np.float64)
+    s = np.asarray(s, dtype=np.float64)
+    M, K = Aq.shape
+    N = q.shape[1]
+    out = np.zeros((M, N))
+    mag = np.zeros((M, N))
+    for g in range(K // G):
+        ks = slice(g * G, (g + 1) * G)
+        dot = Aq[:, ks] @ q[ks, :]                  # exact integers
+        adot = np.abs(Aq[:, ks]) @ np.abs(q[ks, :])
+        w = a_s[:, g][:, None] * s[g][None, :]
+        out += w * dot.astype(np.float64)
+        mag += np.abs(w) * adot.astype(np.float64)
+    return out, mag
+
+
+def reference_a8(Aq, a_scales, codes, scales, *, K: int, N: int, G: int, rows=None, cols=None):
+    """(ref, mag) of the W8A8 group GEMM from int8 activation codes [M][K], fp32 activation
+    scales [M][K/G], int8 weight codes [K][N] and fp32 weight scales [K/G][N]."""
+    Aq = np.asarray(Aq)
+    a_s = f32_to_f64(a_scales)
+    if rows is not None:
+        Aq, a_s = Aq[np.asarray(rows)], a_s[np.asarray(rows)]
+    cols_ = np.arange(N) if cols is None else np.asarray(cols)
+    q = np.asarray(codes)[:, cols_]
+    s = f32_to_f64(np.asarray(scales)[:, cols_])
+    return group_gemm_a8(Aq, a_s, q, s, G)
 
 
 # ---------------------------------------------------------------------------------------

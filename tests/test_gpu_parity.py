@@ -421,3 +421,89 @@ def test_pack_gate_up_interleaves_gate_and_up_columns(gq):
     order = np.concatenate([np.r_[8 * t:8 * t + 8, F + 8 * t:F + 8 * t + 8]
                             for t in range(cfg.N // 16)])
     assert np.array_equal(qp, inp["q"].astype(np.int64)[:, order])
+
+
+# ------------------------------------------------------------------ INT8-activation variant
+
+def _a8_inputs(cfg, seed):
+    """W8 weights of cfg plus its fp32 activations, quantized by the oracle."""
+    inp = gq_synth.make_inputs(cfg, seed=seed)
+    Aq, As = oracle.quantize_act_i8(inp["A"], cfg.G, cfg.act)
+    return inp, Aq, As
+
+
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+def test_activation_quantizer_is_bit_exact(gq, act):
+    from group_quantized_weight_gb300.constants import GQ_ACT_F32
+    cfg = gq_synth.Config("aq", M=5, K=1024, N=16, G=32, w4=False, act=act, sc="f32",
+                          outlier_frac=0.01)
+    A = gq_synth.make_activations(cfg, seed=3)
+    A[1, 32:64] = 0                                # a group of zeros
+    if act == "f32":                               # ties: largest magnitude 127, halves
+        A[2, :32] = np.arange(32, dtype=np.float32) + 0.5
+        A[2, 0] = 127.0
+    Aq_ref, As_ref = oracle.quantize_act_i8(A, cfg.G, act)
+    Aq, As = gq.quantize_act_t(np_to_dev(A), cfg.K, cfg.G, GQ_ACT_F32 if act == "f32" else 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(Aq.cpu().numpy(), Aq_ref)
+    assert np.array_equal(As.cpu().numpy().view(np.uint32), As_ref.view(np.uint32))
+
+
+A8_SHAPES = [
+    gq_synth.Config("a8_m1", M=1, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8_m3_g64", M=3, K=512, N=136, G=64, w4=False, act="f32", sc="f32",
+                    out="bf16", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8_m16_split", M=16, K=2048, N=1000, G=32, w4=False, act="f32",
+                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8_m40_rows", M=40, K=1024, N=328, G=128, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8_m32_g256", M=32, K=2048, N=200, G=256, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+]
+
+
+@pytest.mark.parametrize("cfg", A8_SHAPES, ids=lambda c: c.name)
+def test_a8_group_gemm(gq, cfg):
+    from group_quantized_weight_gb300.constants import GQ_ACT_I8, GQ_OUT_F32, GQ_SC_F32
+    inp, Aq, As = _a8_inputs(cfg, seed=9)
+    prec = GQ_ACT_I8 | GQ_SC_F32 | (GQ_OUT_F32 if cfg.out == "f32" else 0)
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    out = alloc_out(cfg.M, cfg.N, cfg.out)
+    gq.gemm_a8_t(np_to_dev(Aq), np_to_dev(As), packed, np_to_dev(inp["scales"]), out,
+                 cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    ref, mag = oracle.reference_a8(Aq, As, inp["codes"], inp["scales"], K=cfg.K, N=cfg.N,
+                                   G=cfg.G)
+    _assert_parity(cfg, out_to_f64(out, cfg.out), ref, mag)
+
+
+def test_a8_quantize_then_gemm_and_integer_exactness(gq):
+    """gq_quantize_act feeding gq_gemm_a8 on the device equals the oracle's chain; with
+    power-of-two scales and integer activations the result is exact and equal bit for bit."""
+    from group_quantized_weight_gb300.constants import GQ_ACT_F32, GQ_ACT_I8, GQ_OUT_F32, GQ_SC_F32
+    cfg = gq_synth.Config("a8_chain", M=4, K=1024, N=264, G=32, w4=False, act="f32", sc="f32",
+                          out="f32", s_lo=1e-3, s_hi=1e-2)
+    inp = gq_synth.make_inputs(cfg, seed=12)
+    prec = GQ_ACT_I8 | GQ_SC_F32 | GQ_OUT_F32
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    Aq, As = gq.quantize_act_t(np_to_dev(inp["A"]), cfg.K, cfg.G, GQ_ACT_F32)
+    out = alloc_out(cfg.M, cfg.N, "f32")
+    gq.gemm_a8_t(Aq, As, packed, np_to_dev(inp["scales"]), out, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    Aq_r, As_r = oracle.quantize_act_i8(inp["A"], cfg.G, "f32")
+    ref, mag = oracle.reference_a8(Aq_r, As_r, inp["codes"], inp["scales"], K=cfg.K, N=cfg.N,
+                                   G=cfg.G)
+    _assert_parity(cfg, out_to_f64(out, "f32"), ref, mag)
+    # exact case: activation codes in [-8, 8], scales 2^-4 or 2^-3 and 2^-6 or 2^-5: every
+    # product and partial sum is a multiple of 2^-10 below 2^11 (21 bits), exact in FP32
+    rng = np.random.default_rng(4)
+    Aq_i = rng.integers(-8, 9, (cfg.M, cfg.K)).astype(np.int8)
+    As_i = np.ldexp(1.0, rng.integers(-4, -2, (cfg.M, cfg.K // cfg.G))).astype(np.float32)
+    S_i = np.ldexp(1.0, rng.integers(-6, -4, (cfg.K // cfg.G, cfg.N))).astype(np.float32)
+    out_i = alloc_out(cfg.M, cfg.N, "f32")
+    gq.gemm_a8_t(np_to_dev(Aq_i), np_to_dev(As_i), packed, np_to_dev(S_i), out_i, cfg.M, cfg.K,
+                 cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    ref_i, _ = oracle.reference_a8(Aq_i, As_i, inp["codes"], S_i, K=cfg.K, N=cfg.N, G=cfg.G)
+    assert np.array_equal(out_to_f64(out_i, "f32"), ref_i)

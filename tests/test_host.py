@@ -232,3 +232,28 @@ def test_gate_up_flag_is_validated_and_planned_on_the_striped_kernel():
         assert e.value.status == 2
     # the packed size does not change
     assert gq.gq_packed_bytes(4096, 28672, 128, gu) == gq.gq_packed_bytes(4096, 28672, 128, C.GQ_W4)
+
+
+def test_int8_activation_variant_validation_and_plan():
+    a8 = C.GQ_ACT_I8 | C.GQ_SC_F32 | C.GQ_OUT_F32
+    assert gq.gq_plan(1, 2048, 12288, 32, a8, sm_count=152)["path"] == 7
+    p = gq.gq_plan(40, 2048, 1000, 32, a8, sm_count=152)
+    assert p["path"] == 7 and p["grid_z"] == 2 and p["m_tile"] == 32
+    assert p["grid_x"] % -(-1000 // 64) == 0 and p["smem_bytes"] <= 113 * 1024
+    for bad in (C.GQ_ACT_I8 | C.GQ_SC_F32 | C.GQ_W4, C.GQ_ACT_I8 | C.GQ_SC_F32 | C.GQ_ACT_F32,
+                C.GQ_ACT_I8):                      # W4, fp32 activations, fp16 scales
+        with pytest.raises(C.GqError) as e:
+            gq.gq_plan(1, 512, 64, 32, bad, sm_count=152)
+        assert e.value.status == 2
+    # gq_gemm and the static-scratch entry refuse the flag: the scales need gq_gemm_a8
+    assert gq.gq_gemm(1, 512, 64, 32, a8, 16, 16, 16, None, 16, None) == 1
+    assert gq.gq_gemm_static_scratch(1, 512, 64, 32, a8, 16, 16, 16, None, 16, None) == 1
+    # gq_gemm_a8 without the flag, a NULL activation scale, a misaligned code pointer
+    assert gq.gq_gemm_a8(1, 512, 64, 32, C.GQ_SC_F32, 16, 16, 16, 16, 16, None) == 1
+    assert gq.gq_gemm_a8(1, 512, 64, 32, a8, 16, None, 16, 16, 16, None) == 1
+    assert gq.gq_gemm_a8(1, 512, 64, 32, a8, 8, 16, 16, 16, 16, None) == 3
+    # the quantizer: shape and flag checks before any launch
+    assert gq.gq_quantize_act(1, 100, 32, 0, 16, 16, 16, None) == 1
+    assert gq.gq_quantize_act(1, 512, 32, C.GQ_W4, 16, 16, 16, None) == 1
+    assert gq.gq_quantize_act(1, 512, 32, 0, 16, 8, 16, None) == 3
+    assert gq.gq_quantize_act(0, 512, 32, 0, None, None, None, None) == 0

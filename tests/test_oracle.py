@@ -393,3 +393,51 @@ def test_silu_mul_takes_gate_from_the_first_half_and_up_from_the_second():
     assert ref.shape == (3, F)
     assert np.array_equal(ref, expect)
     assert (mag >= 0).all() and (mag[:, j0] > 0).all()
+
+
+# ------------------------------------------------------------------ INT8-activation variant
+
+def test_activation_quantizer_special_cases():
+    """A group whose largest magnitude is 127 has scale exactly 1, so codes are the values
+    rounded to nearest with ties to even (2.5 -> 2, 3.5 -> 4, -2.5 -> -2), ±127 map to ±127,
+    and an all-zero group has scale 0 and codes 0."""
+    G = 32
+    row = np.zeros(2 * G, dtype=np.float32)
+    row[:8] = [127.0, -127.0, 2.5, 3.5, -2.5, 0.25, 126.5, 0.0]
+    Aq, s = orc.quantize_act_i8(row[None, :], G, "f32")
+    assert s[0, 0] == 1.0 and s[0, 1] == 0.0
+    assert Aq[0, :8].tolist() == [127, -127, 2, 4, -2, 0, 126, 0]
+    assert (Aq[0, G:] == 0).all()
+
+
+def test_activation_quantizer_error_bound_and_range():
+    """|x − s·q| ≤ s/2 (to float32 rounding of x/s) and |q| ≤ 127, with the group's largest
+    magnitude at ±127, on bf16 N(0,1) activations with outliers."""
+    cfg = gq_synth.Config("aq", M=4, K=1024, N=16, G=64, outlier_frac=0.01)
+    A = gq_synth.make_activations(cfg, seed=5)
+    Aq, s = orc.quantize_act_i8(A, 64, "bf16")
+    x = orc.bf16_bits_to_f64(A).reshape(4, 16, 64)
+    qq = Aq.astype(np.int64).reshape(4, 16, 64)
+    ss = s.astype(np.float64)[:, :, None]
+    assert (np.abs(qq) <= 127).all()
+    assert (np.abs(qq).max(axis=2) == 127).all()
+    assert (np.abs(x - ss * qq) <= ss * (0.5 + 1e-6)).all()
+
+
+def test_a8_group_gemm_matches_brute_force_and_integer_product():
+    rng = np.random.default_rng(8)
+    M, K, N, G = 3, 96, 5, 32
+    Aq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    q = rng.integers(-127, 128, (K, N)).astype(np.int8)
+    a_s = rng.uniform(0.01, 0.1, (M, K // G)).astype(np.float32)
+    s = rng.uniform(1e-3, 1e-2, (K // G, N)).astype(np.float32)
+    out, mag = orc.reference_a8(Aq, a_s, q, s, K=K, N=N, G=G)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(a_s[m, k // G])) * Fraction(float(s[k // G, n])) *
+                        int(Aq[m, k]) * int(q[k, n]) for k in range(K))
+            assert abs(out[m, n] - float(exact)) <= 1e-12 * mag[m, n]
+    # unit scales reduce it to the integer matrix product
+    one_a, one_s = np.ones_like(a_s), np.ones_like(s)
+    out1, _ = orc.reference_a8(Aq, one_a, q, one_s, K=K, N=N, G=G)
+    assert np.array_equal(out1, (Aq.astype(np.int64) @ q.astype(np.int64)).astype(np.float64))
