@@ -563,11 +563,36 @@ def _prefill(gq, torch, dev, peaks, peak_kind):
     torch.cuda.synchronize()
     cublas_us = e0.elapsed_time(e1) * 100.0
     del Wd, Ad
+    # the FP8 W8A8 GEMM with 128 x 128 block scales (gq_gemm_fp8_block) on the same shape:
+    # E4M3 activations and weights, one fp32 scale per (row, 128-k block) and per weight block
+    Af = torch.randn(cfg.M, cfg.K, device=dev).to(torch.float8_e4m3fn).view(torch.uint8)
+    Wf = (0.5 * torch.randn(cfg.N, cfg.K, device=dev)).to(torch.float8_e4m3fn).view(torch.uint8)
+    a_s = torch.rand(cfg.K // 128, cfg.M, device=dev) * 0.09 + 0.01
+    w_s = torch.rand(-(-cfg.N // 128), cfg.K // 128, device=dev) * 0.09 + 0.01
+    of = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        gq.gemm_fp8_t(Af, a_s, Wf, w_s, of, cfg.M, cfg.K, cfg.N)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(10):
+        gq.gemm_fp8_t(Af, a_s, Wf, w_s, of, cfg.M, cfg.K, cfg.N)
+    e1.record()
+    torch.cuda.synchronize()
+    fp8_us = e0.elapsed_time(e1) * 100.0
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    del Af, Wf, a_s, w_s, of
     return {"workload": "prefill: M=4096 K=4096 N=14336 G=128 W4A16 sym", "us": us,
             "tflops": tflops, "peak_tflops": peaks["bf16_tflops"],
             "frac": tflops / peaks["bf16_tflops"], "peak_source": f"bf16_tflops of {peak_kind}",
             "path": plan["path"], "cublas_bf16_dense_us": cublas_us,
-            "cublas_bf16_dense_tflops": flops / (cublas_us * 1e-6) / 1e12}
+            "cublas_bf16_dense_tflops": flops / (cublas_us * 1e-6) / 1e12,
+            "fp8_block": {"workload": "FP8 E4M3 W8A8, 1x128 / 128x128 block scales, "
+                                      "M=4096 K=4096 N=14336, bf16 out",
+                          "us": fp8_us, "tflops": flops / (fp8_us * 1e-6) / 1e12,
+                          "peak_tflops": fp8_peak,
+                          "frac": flops / (fp8_us * 1e-6) / 1e12 / fp8_peak,
+                          "peak_source": f"2 x bf16_tflops of {peak_kind} (nominal FP8/BF16 "
+                                         "ratio)"}}
 
 
 if __name__ == "__main__":

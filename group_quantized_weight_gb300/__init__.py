@@ -55,6 +55,7 @@ _SIGS = {
     "gq_gemm_static_scratch": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_gemm_a8": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_quantize_act": [_i, _i, _i, _i, _p, _p, _p, _p],
+    "gq_gemm_fp8_block": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_bench": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
     "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
@@ -122,6 +123,14 @@ def gq_gemm_a8(M, K, N, G, prec, Aq_ptr, a_scales_ptr, Wq_ptr, scales_ptr, out_p
 def gq_quantize_act(M, K, G, prec, A_ptr, Aq_ptr, a_scales_ptr, stream=None) -> int:
     """Dynamic per-group INT8 quantization of activations.  Raw call; returns the status."""
     return _lib.gq_quantize_act(M, K, G, prec, A_ptr, Aq_ptr, a_scales_ptr, stream)
+
+
+def gq_gemm_fp8_block(M, K, N, prec, A_ptr, a_scales_ptr, W_ptr, w_scales_ptr, out_ptr,
+                      stream=None) -> int:
+    """FP8 W8A8 GEMM with 1 x 128 activation and 128 x 128 weight block scales.  Raw call;
+    returns the status."""
+    return _lib.gq_gemm_fp8_block(M, K, N, prec, A_ptr, a_scales_ptr, W_ptr, w_scales_ptr,
+                                  out_ptr, stream)
 
 
 def gq_gemm_static_scratch(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr,
@@ -196,6 +205,15 @@ def gemm_a8_t(Aq, As, Wq, scales, out, M: int, K: int, N: int, G: int, prec: int
     """out <- gq_gemm_a8(...) on torch's current stream; raises GqError on a bad status."""
     _check(gq_gemm_a8(M, K, N, G, prec, Aq.data_ptr(), As.data_ptr(), Wq.data_ptr(),
                       scales.data_ptr(), out.data_ptr(), _stream_ptr(stream)), "gq_gemm_a8")
+    return out
+
+
+def gemm_fp8_t(A, a_scales, W, w_scales, out, M: int, K: int, N: int, prec: int = 0,
+               stream=None):
+    """out <- gq_gemm_fp8_block(...) on torch's current stream; raises GqError on a bad status."""
+    _check(gq_gemm_fp8_block(M, K, N, prec, A.data_ptr(), a_scales.data_ptr(), W.data_ptr(),
+                             w_scales.data_ptr(), out.data_ptr(), _stream_ptr(stream)),
+           "gq_gemm_fp8_block")
     return out
 
 

@@ -663,7 +663,26 @@ int gq_device_error(int clear) {
   const int v = prefill_read_error(clear);
   const int w = stripe_read_error(clear);
   const int x = batch_read_error(clear);
-  return v != 0 ? v : (w != 0 ? w : x);
+  const int y = fp8_read_error(clear);
+  return v != 0 ? v : (w != 0 ? w : (x != 0 ? x : y));
+}
+
+int gq_gemm_fp8_block(int M, int K, int N, int prec, const void *A, const void *a_scales,
+                      const void *W, const void *w_scales, void *out, void *stream) {
+  if (prec & ~GQ_OUT_F32) return GQ_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 128 || K % 128 != 0 || N % 16 != 0) return GQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!A || !a_scales || !W || !w_scales || !out) return GQ_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(a_scales) || !aligned16(W) || !aligned16(w_scales) ||
+      !aligned16(out))
+    return GQ_ERR_ALIGNMENT;
+  int sms = 0;
+  int st = device_sm_count(&sms);
+  if (st != GQ_OK) return st;
+  int grid = 0;
+  fp8_block_plan(M, N, sms, &grid);
+  return launch_fp8_block(M, K, N, prec, A, a_scales, W, w_scales, out, grid,
+                          (cudaStream_t)stream);
 }
 
 }  // extern "C"

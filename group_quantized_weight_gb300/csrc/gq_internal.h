@@ -138,6 +138,12 @@ size_t q8a8_smem_bytes(int M, int K, int G, int KS);
 cudaError_t launch_q8a8(const Plan &p, int M, int K, int N, int G, int prec, const int8_t *Aq,
                         const float *As, const void *Wq, const void *scales, void *out,
                         float *part, unsigned *counters, cudaStream_t s);
+// FP8 W8A8 block-scaled GEMM (tcgen05 kind::f8f6f4)
+size_t fp8_smem_bytes();
+int fp8_block_plan(int M, int N, int sms, int *grid);
+int launch_fp8_block(int M, int K, int N, int prec, const void *A, const void *a_scales,
+                     const void *W, const void *w_scales, void *out, int grid, cudaStream_t s);
+int fp8_read_error(int clear);
 // Launches the kernel of plan p (any path); part and counters may be NULL when the plan
 // needs no workspace.
 cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, const void *A,

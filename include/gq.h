@@ -204,6 +204,23 @@ int gq_quantize_act(int M, int K, int G, int prec, const void *A, void *Aq, void
 int gq_gemm_a8(int M, int K, int N, int G, int prec, const void *Aq, const void *a_scales,
                const void *Wq, const void *scales, void *out, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * FP8 W8A8 GEMM with block scales ("GPU Kernel 工程（09）：量化与融合 kernel", section 四.3):
+ *     out[m][n] = Σ_b a_scales[b][m] · w_scales[n/128][b] · Σ_{k in block b} A[m][k]·W[n][k]
+ * over 128-k blocks b; each block's tensor-core sum is scaled and added into FP32 inside the
+ * K loop (the scales depend on k, so they cannot wait for the epilogue).
+ *   A         device FP8 E4M3 bytes [M][K];  a_scales  device fp32 [K/128][M] (one per row and
+ *             block, M contiguous);
+ *   W         device FP8 E4M3 bytes [N][K] (k contiguous: row n is output column n);
+ *   w_scales  device fp32 [ceil(N/128)][K/128] (one per 128 x 128 block);
+ *   out       device [M][N] bf16, or fp32 with GQ_OUT_F32 (prec holds no other flag).
+ * Contract: M >= 0, N >= 0 (either 0: nothing launched), K >= 128, K % 128 == 0, N % 16 == 0;
+ * pointers 16-byte aligned.  Needs no workspace.  Asynchronous on stream.  Errors:
+ * GQ_ERR_INVALID_ARG, GQ_ERR_ALIGNMENT, GQ_ERR_CUDA; a bounded device wait that gives up
+ * sets GQ_ERR_TIMEOUT in gq_device_error. */
+int gq_gemm_fp8_block(int M, int K, int N, int prec, const void *A, const void *a_scales,
+                      const void *W, const void *w_scales, void *out, void *stream);
+
 /* Host-only description of the launch gq_gemm would make (for tests and reports).
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {

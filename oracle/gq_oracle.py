@@ -28,7 +28,8 @@ __all__ = [
     "f64_to_f32", "unpack_int4_k", "unpack_int4_n", "dequantize", "group_gemm",
     "group_gemm_magnitude", "reference", "tolerance", "check", "quantize_w4_g",
     "bits_per_weight", "dequantize_brute", "silu", "silu_mul_reference",
-    "quantize_act_i8", "group_gemm_a8", "reference_a8",
+    "quantize_act_i8", "group_gemm_a8", "reference_a8", "e4m3_bits_to_f64",
+    "fp8_block_gemm",
 ]
 
 
@@ -297,6 +298,46 @@ def reference_a8(Aq, a_scales, codes, scales, *, K: int, N: int, G: int, rows=No
     q = np.asarray(codes)[:, cols_]
     s = f32_to_f64(np.asarray(scales)[:, cols_])
     return group_gemm_a8(Aq, a_s, q, s, G)
+
+
+# ---------------------------------------------------------------------------------------
+# FP8 W8A8 GEMM with block scales (P1 section 四.3).  E4M3 ("FN": no infinities): 1 sign bit,
+# 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal (m/8 · 2^-6); the
+# pattern S.1111.111 is NaN, so the largest finite magnitude is 1.75 · 2^8 = 448.
+# ---------------------------------------------------------------------------------------
+
+def e4m3_bits_to_f64(bits) -> np.ndarray:
+    b = np.asarray(bits).astype(np.int64) & 0xFF
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((e == 15) & (m == 7), np.nan, val)
+    return sign * val
+
+
+def fp8_block_gemm(A_bits, a_scales, W_bits, w_scales, block: int = 128):
+    """out[m][n] = Σ_b a_scales[b][m] · w_scales[n // block][b] · Σ_{k ∈ b} A[m][k] · W[n][k]
+    in float64 (each product of two E4M3 values is exact), with mag = the same sum of
+    absolute values for the tolerance.  A_bits [M][K], W_bits [N][K] (E4M3 bytes), a_scales
+    float32 [K/block][M], w_scales float32 [ceil(N/block)][K/block]."""
+    A = e4m3_bits_to_f64(A_bits)
+    W = e4m3_bits_to_f64(W_bits)
+    a_s = f32_to_f64(a_scales)
+    w_s = f32_to_f64(w_scales)
+    M, K = A.shape
+    N = W.shape[0]
+    nrow_blk = np.arange(N) // block
+    out = np.zeros((M, N))
+    mag = np.zeros((M, N))
+    for b in range(K // block):
+        ks = slice(b * block, (b + 1) * block)
+        part = A[:, ks] @ W[:, ks].T
+        apart = np.abs(A[:, ks]) @ np.abs(W[:, ks]).T
+        sc = a_s[b][:, None] * w_s[nrow_blk, b][None, :]
+        out += sc * part
+        mag += np.abs(sc) * apart
+    return out, mag
 
 
 # ---------------------------------------------------------------------------------------

@@ -507,3 +507,38 @@ def test_a8_quantize_then_gemm_and_integer_exactness(gq):
     torch.cuda.synchronize()
     ref_i, _ = oracle.reference_a8(Aq_i, As_i, inp["codes"], S_i, K=cfg.K, N=cfg.N, G=cfg.G)
     assert np.array_equal(out_to_f64(out_i, "f32"), ref_i)
+
+
+# ------------------------------------------------------------------ FP8 block-scaled GEMM
+
+def _fp8_inputs(M, K, N, seed):
+    """E4M3 activations ~N(0, 1) and weights ~N(0, 0.25) as bytes (torch's round to nearest
+    E4M3), activation scales U[0.01, 0.1] per (128-k block, row), weight scales U[0.01, 0.1]
+    per 128 x 128 block."""
+    g = torch.Generator().manual_seed(seed)
+    A = torch.randn(M, K, generator=g).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    W = (0.5 * torch.randn(N, K, generator=g)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    rng = np.random.default_rng(seed)
+    a_s = rng.uniform(0.01, 0.1, (K // 128, M)).astype(np.float32)
+    w_s = rng.uniform(0.01, 0.1, (-(-N // 128), K // 128)).astype(np.float32)
+    return A, a_s, W, w_s
+
+
+@pytest.mark.parametrize("M,K,N,out", [
+    (256, 128, 128, "bf16"),        # one tile, one block
+    (300, 512, 400, "bf16"),        # ragged rows and columns
+    (1, 256, 256, "bf16"),          # a single activation row
+    (1024, 1024, 640, "f32"),       # several tiles per CTA
+    (700, 384, 128, "f32"),
+])
+def test_fp8_block_gemm(gq, M, K, N, out):
+    from group_quantized_weight_gb300.constants import GQ_OUT_F32
+    A, a_s, W, w_s = _fp8_inputs(M, K, N, seed=M + K + N)
+    o = alloc_out(M, N, out)
+    gq.gemm_fp8_t(np_to_dev(A), np_to_dev(a_s), np_to_dev(W), np_to_dev(w_s), o, M, K, N,
+                  GQ_OUT_F32 if out == "f32" else 0)
+    torch.cuda.synchronize()
+    assert gq.gq_device_error(clear=True) == 0
+    ref, mag = oracle.fp8_block_gemm(A, a_s, W, w_s)
+    cfg = gq_synth.Config(f"fp8_{M}x{K}x{N}", M=M, K=K, N=N, G=128, out=out)
+    _assert_parity(cfg, out_to_f64(o, out), ref, mag)

@@ -257,3 +257,13 @@ def test_int8_activation_variant_validation_and_plan():
     assert gq.gq_quantize_act(1, 512, 32, C.GQ_W4, 16, 16, 16, None) == 1
     assert gq.gq_quantize_act(1, 512, 32, 0, 16, 8, 16, None) == 3
     assert gq.gq_quantize_act(0, 512, 32, 0, None, None, None, None) == 0
+
+
+def test_fp8_block_gemm_validation():
+    f = gq.gq_gemm_fp8_block
+    assert f(4, 192, 128, 0, 16, 16, 16, 16, 16, None) == 1      # K % 128 != 0
+    assert f(4, 256, 120, 0, 16, 16, 16, 16, 16, None) == 1      # N % 16 != 0
+    assert f(4, 256, 128, C.GQ_W4, 16, 16, 16, 16, 16, None) == 1
+    assert f(4, 256, 128, 0, 16, None, 16, 16, 16, None) == 1
+    assert f(4, 256, 128, 0, 8, 16, 16, 16, 16, None) == 3       # misaligned
+    assert f(0, 256, 128, 0, None, None, None, None, None, None) == 0

@@ -441,3 +441,39 @@ def test_a8_group_gemm_matches_brute_force_and_integer_product():
     one_a, one_s = np.ones_like(a_s), np.ones_like(s)
     out1, _ = orc.reference_a8(Aq, one_a, q, one_s, K=K, N=N, G=G)
     assert np.array_equal(out1, (Aq.astype(np.int64) @ q.astype(np.int64)).astype(np.float64))
+
+
+# ------------------------------------------------------------------ FP8 block-scaled GEMM
+
+def test_e4m3_decoder_matches_library_on_all_patterns():
+    bits = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = orc.e4m3_bits_to_f64(bits)
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(ours[ok], lib[ok])
+    assert np.nanmax(ours) == 448.0 and orc.e4m3_bits_to_f64(0x01) == 2.0 ** -9
+
+
+def test_fp8_block_gemm_matches_brute_force_and_block_scaling():
+    rng = np.random.default_rng(2)
+    M, K, N = 3, 256, 136                          # two k blocks, two weight row blocks
+    A = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    W = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0x38                   # no NaN patterns (0x38 = 1.0)
+    W[(W & 0x7F) == 0x7F] = 0x38
+    a_s = rng.uniform(0.01, 0.1, (K // 128, M)).astype(np.float32)
+    w_s = rng.uniform(0.01, 0.1, (2, K // 128)).astype(np.float32)
+    out, mag = orc.fp8_block_gemm(A, a_s, W, w_s)
+    Af, Wf = orc.e4m3_bits_to_f64(A), orc.e4m3_bits_to_f64(W)
+    for m in range(M):
+        for n in (0, 7, 127, 128, 135):
+            exact = sum(Fraction(float(a_s[k // 128, m])) * Fraction(float(w_s[n // 128, k // 128])) *
+                        Fraction(Af[m, k]) * Fraction(Wf[n, k]) for k in range(K))
+            assert abs(out[m, n] - float(exact)) <= 1e-12 * mag[m, n]
+    # doubling one block's activation scales doubles exactly that block's share
+    a2 = a_s.copy()
+    a2[1] *= 2
+    out2, _ = orc.fp8_block_gemm(A, a2, W, w_s)
+    one_block, _ = orc.fp8_block_gemm(A[:, 128:], a_s[1:], W[:, 128:], w_s[:, 1:])
+    assert np.allclose(out2 - out, one_block, rtol=1e-12, atol=1e-12)
