@@ -56,6 +56,7 @@ _SIGS = {
     "gq_gemm_a8": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_quantize_act": [_i, _i, _i, _i, _p, _p, _p, _p],
     "gq_gemm_fp8_block": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
+    "gq_quantize_act_fp8": [_i, _i, _i, _p, _p, _p, _p],
     "gq_bench": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
     "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
@@ -133,6 +134,11 @@ def gq_gemm_fp8_block(M, K, N, prec, A_ptr, a_scales_ptr, W_ptr, w_scales_ptr, o
                                   out_ptr, stream)
 
 
+def gq_quantize_act_fp8(M, K, prec, A_ptr, Aq_ptr, a_scales_ptr, stream=None) -> int:
+    """Dynamic FP8 (E4M3) quantization of activations per 1 x 128 block.  Raw call."""
+    return _lib.gq_quantize_act_fp8(M, K, prec, A_ptr, Aq_ptr, a_scales_ptr, stream)
+
+
 def gq_gemm_static_scratch(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr,
                            stream=None) -> int:
     """gq_gemm that never allocates: scratch comes from a fixed array inside the library
@@ -206,6 +212,18 @@ def gemm_a8_t(Aq, As, Wq, scales, out, M: int, K: int, N: int, G: int, prec: int
     _check(gq_gemm_a8(M, K, N, G, prec, Aq.data_ptr(), As.data_ptr(), Wq.data_ptr(),
                       scales.data_ptr(), out.data_ptr(), _stream_ptr(stream)), "gq_gemm_a8")
     return out
+
+
+def quantize_act_fp8_t(A, K: int, prec: int = 0, stream=None):
+    """A [M][K] (bf16 bits, or fp32 with GQ_ACT_F32) -> (Aq uint8 E4M3 [M][K], a_scales fp32
+    [K/128][M]) on torch's current stream."""
+    import torch
+    M = A.shape[0]
+    Aq = torch.empty((M, K), dtype=torch.uint8, device=A.device)
+    As = torch.empty((K // 128, M), dtype=torch.float32, device=A.device)
+    _check(gq_quantize_act_fp8(M, K, prec, A.data_ptr(), Aq.data_ptr(), As.data_ptr(),
+                               _stream_ptr(stream)), "gq_quantize_act_fp8")
+    return Aq, As
 
 
 def gemm_fp8_t(A, a_scales, W, w_scales, out, M: int, K: int, N: int, prec: int = 0,

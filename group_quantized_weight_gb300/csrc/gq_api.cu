@@ -667,6 +667,17 @@ int gq_device_error(int clear) {
   return v != 0 ? v : (w != 0 ? w : (x != 0 ? x : y));
 }
 
+int gq_quantize_act_fp8(int M, int K, int prec, const void *A, void *Aq, void *a_scales,
+                        void *stream) {
+  if (prec & ~GQ_ACT_F32) return GQ_ERR_INVALID_ARG;
+  if (M < 0 || K < 128 || K % 128 != 0) return GQ_ERR_INVALID_ARG;
+  if (M == 0) return GQ_OK;
+  if (!A || !Aq || !a_scales) return GQ_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(Aq) || !aligned16(a_scales)) return GQ_ERR_ALIGNMENT;
+  return launch_quantize_fp8(M, K, (prec & GQ_ACT_F32) != 0, A, Aq, a_scales,
+                             (cudaStream_t)stream);
+}
+
 int gq_gemm_fp8_block(int M, int K, int N, int prec, const void *A, const void *a_scales,
                       const void *W, const void *w_scales, void *out, void *stream) {
   if (prec & ~GQ_OUT_F32) return GQ_ERR_INVALID_ARG;

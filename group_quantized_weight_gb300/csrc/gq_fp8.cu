@@ -371,6 +371,65 @@ fp8_block_gemm_kernel(const __grid_constant__ CUtensorMap map_w,
   }
 }
 
+// ------------------------------------------------------------------ activation quantizer
+
+// Dynamic FP8 quantization of activations ("量化与融合 kernel" section 四.5, with 1 x 128
+// blocks): scale = max_{k in block} |x| / 448 (binary32 division), code = E4M3(x / scale)
+// (binary32 division, then the hardware's round-to-nearest-even conversion with saturation
+// to ±448); a block of zeros gets scale 0 and codes 0.  One warp per (row, block): lane l
+// holds k = 4l .. 4l + 3.
+template <bool F32>
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const void *__restrict__ A,
+                                                           uint8_t *__restrict__ Aq,
+                                                           float *__restrict__ scales, int M,
+                                                           int K) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nb = K / kF8Block;
+  if (wid >= (long long)M * nb) return;
+  const int m = (int)(wid / nb), b = (int)(wid - (long long)m * nb);
+  const size_t base = (size_t)m * K + (size_t)b * kF8Block + 4 * lane;
+  float x[4];
+  if (F32) {
+    const float4 v = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(A) + base);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2 *>(reinterpret_cast<const unsigned short *>(A) + base);
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  }
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float s = __fdiv_rn(amax, 448.f);
+  uint32_t word = 0;
+  if (s > 0.f) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(__fdiv_rn(x[1], s)), "f"(__fdiv_rn(x[0], s)));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(__fdiv_rn(x[3], s)), "f"(__fdiv_rn(x[2], s)));
+    word = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+  *reinterpret_cast<uint32_t *>(Aq + base) = word;
+  if (lane == 0) scales[(size_t)b * M + m] = s;   // [K/128][M], the GEMM's layout
+}
+
+int launch_quantize_fp8(int M, int K, bool f32, const void *A, void *Aq, void *scales,
+                        cudaStream_t s) {
+  const long long warps = (long long)M * (K / kF8Block);
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7FFFFFFFll) return GQ_ERR_INVALID_ARG;
+  if (f32)
+    quantize_fp8_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(A, (uint8_t *)Aq, (float *)scales, M, K);
+  else
+    quantize_fp8_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(A, (uint8_t *)Aq, (float *)scales, M, K);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    note_cuda_error("launch(fp8 quantizer)", e);
+    return GQ_ERR_CUDA;
+  }
+  return GQ_OK;
+}
+
 // ------------------------------------------------------------------ host side
 
 using F8EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

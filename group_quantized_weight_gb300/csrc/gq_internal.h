@@ -144,6 +144,8 @@ int fp8_block_plan(int M, int N, int sms, int *grid);
 int launch_fp8_block(int M, int K, int N, int prec, const void *A, const void *a_scales,
                      const void *W, const void *w_scales, void *out, int grid, cudaStream_t s);
 int fp8_read_error(int clear);
+int launch_quantize_fp8(int M, int K, bool f32, const void *A, void *Aq, void *scales,
+                        cudaStream_t s);
 // Launches the kernel of plan p (any path); part and counters may be NULL when the plan
 // needs no workspace.
 cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, const void *A,

@@ -221,6 +221,18 @@ int gq_gemm_a8(int M, int K, int N, int G, int prec, const void *Aq, const void 
 int gq_gemm_fp8_block(int M, int K, int N, int prec, const void *A, const void *a_scales,
                       const void *W, const void *w_scales, void *out, void *stream);
 
+/* Dynamic FP8 quantization of activations for gq_gemm_fp8_block (the absmax reduction and cast
+ * of "量化与融合 kernel" section 四.5, one scale per row and 128-k block):
+ *   a_scales[b][m] = max_{k in block b} |A[m][k]| / 448         (binary32 division)
+ *   Aq[m][k]       = E4M3(A[m][k] / a_scales[b][m])              (binary32 division, round to
+ *                    nearest even, saturated to ±448); a block of zeros: scale 0, codes 0.
+ *   A         device [M][K] bf16, or fp32 with GQ_ACT_F32 (prec holds no other flag);
+ *   Aq        device E4M3 bytes [M][K];  a_scales  device fp32 [K/128][M].
+ * Contract: M >= 0, K >= 128, K % 128 == 0; pointers 16-byte aligned.  Asynchronous.
+ * Errors: GQ_ERR_INVALID_ARG, GQ_ERR_ALIGNMENT, GQ_ERR_CUDA. */
+int gq_quantize_act_fp8(int M, int K, int prec, const void *A, void *Aq, void *a_scales,
+                        void *stream);
+
 /* Host-only description of the launch gq_gemm would make (for tests and reports).
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {

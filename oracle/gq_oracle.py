@@ -29,7 +29,7 @@ __all__ = [
     "group_gemm_magnitude", "reference", "tolerance", "check", "quantize_w4_g",
     "bits_per_weight", "dequantize_brute", "silu", "silu_mul_reference",
     "quantize_act_i8", "group_gemm_a8", "reference_a8", "e4m3_bits_to_f64",
-    "fp8_block_gemm",
+    "fp8_block_gemm", "f64_to_e4m3_bits", "quantize_act_fp8",
 ]
 
 
@@ -314,6 +314,37 @@ def e4m3_bits_to_f64(bits) -> np.ndarray:
     val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
     val = np.where((e == 15) & (m == 7), np.nan, val)
     return sign * val
+
+
+def f64_to_e4m3_bits(x) -> np.ndarray:
+    """Nearest E4M3 value, ties to the even code, finite values beyond ±448 saturated to ±448
+    (the "satfinite" conversion); the sign of a zero is kept.  Written from the format: the
+    finite magnitudes are the 127 codes 0x00 .. 0x7E in increasing order."""
+    x = np.asarray(x, dtype=np.float64)
+    grid = e4m3_bits_to_f64(np.arange(0x7F))       # increasing, 0 .. 448
+    a = np.minimum(np.abs(x), 448.0)
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_lo, d_hi = a - grid[lo], grid[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(take_hi, hi, lo)
+    code = np.where(a == grid[hi], hi, code)       # exact grid values
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_act_fp8(A_raw, act: str, block: int = 128):
+    """Per (row, block of 128 k): s = max|x| / 448 and code = E4M3(x / s), both divisions in
+    binary32 as on the GPU (the code is decided in the kernel's precision); s = 0 and codes 0
+    for a block of zeros.  Returns (Aq uint8 [M][K], a_scales float32 [K/block][M])."""
+    A = bf16_bits_to_f64(A_raw) if act == "bf16" else f32_to_f64(A_raw)
+    A32 = A.astype(np.float32)
+    M, K = A32.shape
+    Ag = A32.reshape(M, K // block, block)
+    s = (np.abs(Ag).max(axis=2) / np.float32(448)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (Ag / s[:, :, None]).astype(np.float32)
+    codes = np.where(s[:, :, None] > 0, f64_to_e4m3_bits(r.astype(np.float64)), 0)
+    return codes.reshape(M, K).astype(np.uint8), np.ascontiguousarray(s.T)
 
 
 def fp8_block_gemm(A_bits, a_scales, W_bits, w_scales, block: int = 128):

@@ -542,3 +542,35 @@ def test_fp8_block_gemm(gq, M, K, N, out):
     ref, mag = oracle.fp8_block_gemm(A, a_s, W, w_s)
     cfg = gq_synth.Config(f"fp8_{M}x{K}x{N}", M=M, K=K, N=N, G=128, out=out)
     _assert_parity(cfg, out_to_f64(o, out), ref, mag)
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_fp8_activation_quantizer_is_bit_exact(gq, act):
+    from group_quantized_weight_gb300.constants import GQ_ACT_F32
+    cfg = gq_synth.Config("q8f", M=7, K=1024, N=16, G=128, w4=False, act=act, sc="f32",
+                          outlier_frac=0.01)
+    A = gq_synth.make_activations(cfg, seed=8)
+    A[2, 128:256] = 0                              # a block of zeros
+    if act == "f32":
+        A[3, 0] = -0.0
+    Aq_ref, s_ref = oracle.quantize_act_fp8(A, act)
+    Aq, s = gq.quantize_act_fp8_t(np_to_dev(A), cfg.K, GQ_ACT_F32 if act == "f32" else 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(Aq.cpu().numpy(), Aq_ref)
+
+
+def test_fp8_quantize_then_gemm(gq):
+    """bf16 activations quantized on the device, then the block-scaled FP8 GEMM, against the
+    oracle's quantizer and GEMM."""
+    M, K, N = 200, 512, 384
+    cfg = gq_synth.Config("fp8chain", M=M, K=K, N=N, G=128)
+    A = gq_synth.make_activations(cfg, seed=10)
+    _, _, W, w_s = _fp8_inputs(M, K, N, seed=10)
+    Aq, a_s = gq.quantize_act_fp8_t(np_to_dev(A), K, 0)
+    o = alloc_out(M, N, "bf16")
+    gq.gemm_fp8_t(Aq, a_s, np_to_dev(W), np_to_dev(w_s), o, M, K, N, 0)
+    torch.cuda.synchronize()
+    Aq_r, a_s_r = oracle.quantize_act_fp8(A, "bf16")
+    ref, mag = oracle.fp8_block_gemm(Aq_r, a_s_r, W, w_s)
+    _assert_parity(cfg, out_to_f64(o, "bf16"), ref, mag)

@@ -267,3 +267,11 @@ def test_fp8_block_gemm_validation():
     assert f(4, 256, 128, 0, 16, None, 16, 16, 16, None) == 1
     assert f(4, 256, 128, 0, 8, 16, 16, 16, 16, None) == 3       # misaligned
     assert f(0, 256, 128, 0, None, None, None, None, None, None) == 0
+
+
+def test_fp8_activation_quantizer_validation():
+    f = gq.gq_quantize_act_fp8
+    assert f(2, 192, 0, 16, 16, 16, None) == 1                # K % 128 != 0
+    assert f(2, 256, C.GQ_W4, 16, 16, 16, None) == 1
+    assert f(2, 256, 0, 16, 8, 16, None) == 3
+    assert f(0, 256, 0, None, None, None, None) == 0

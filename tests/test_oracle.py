@@ -477,3 +477,33 @@ def test_fp8_block_gemm_matches_brute_force_and_block_scaling():
     out2, _ = orc.fp8_block_gemm(A, a2, W, w_s)
     one_block, _ = orc.fp8_block_gemm(A[:, 128:], a_s[1:], W[:, 128:], w_s[:, 1:])
     assert np.allclose(out2 - out, one_block, rtol=1e-12, atol=1e-12)
+
+
+def test_e4m3_encoder_matches_library_rounding_and_saturates():
+    """Inside ±448 the encoder is torch's round-to-nearest-even cast; beyond, it saturates;
+    every code decodes back to itself."""
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.normal(0, 30, 20000), rng.uniform(-448, 448, 20000),
+                        orc.e4m3_bits_to_f64(np.arange(0x7F))])
+    # midpoints between neighbouring codes: ties go to the even code
+    grid = orc.e4m3_bits_to_f64(np.arange(0x7F))
+    x = np.concatenate([x, (grid[1:] + grid[:-1]) / 2, -(grid[1:] + grid[:-1]) / 2])
+    ours = orc.f64_to_e4m3_bits(x)
+    lib = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, lib)
+    assert orc.f64_to_e4m3_bits(np.array([1000.0, -1e6]))[0] == 0x7E
+    assert orc.f64_to_e4m3_bits(np.array([-1e6]))[0] == 0xFE
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(orc.f64_to_e4m3_bits(orc.e4m3_bits_to_f64(codes)), codes)
+
+
+def test_fp8_activation_quantizer_block_maximum_and_error_bound():
+    cfg = gq_synth.Config("q8f", M=3, K=512, N=16, G=128, outlier_frac=0.01)
+    A = gq_synth.make_activations(cfg, seed=6)
+    Aq, s = orc.quantize_act_fp8(A, "bf16")
+    x = orc.bf16_bits_to_f64(A).reshape(3, 4, 128)
+    q = orc.e4m3_bits_to_f64(Aq).reshape(3, 4, 128)
+    ss = s.T.astype(np.float64)[:, :, None]
+    assert (np.abs(q).max(axis=2) == 448.0).all()        # each block's largest element
+    # E4M3 has 3 mantissa bits: the relative error of a normal code is at most 2^-4
+    assert (np.abs(x - ss * q) <= np.abs(x) * 2.0 ** -4 + ss * 2.0 ** -10).all()
