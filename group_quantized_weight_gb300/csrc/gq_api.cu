@@ -218,7 +218,10 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   if (Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)) {
     const int ksl = batch_slice_k(Mc, K);
     const int slots = batch_slots_for(Mc, ksl, G, prec, kCtaSmemCap);
-    if (slots >= 2) {
+    // split K needs one arrival counter per (row block, 16-column tile)
+    const bool ctr_ok = K == ksl || (size_t)ceil_div(Mc, 32) * ceil_div(Nc, kTileN) *
+                                            sizeof(unsigned) <= kCounterRegionBytes;
+    if (slots >= 2 && ctr_ok) {
       const int ks = K / ksl, rb = ceil_div(Mc, 32);
       int cps = sms / (ks * rb);
       if (cps < 1) cps = 1;
@@ -234,12 +237,11 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       p->grid_x = ks * cps;
       p->grid_y = 1;
       p->grid_z = rb;
-      p->block_threads = 16 * 32;
+      p->block_threads = batch_threads(Mc);
       p->smem_bytes = batch_smem_bytes(Mc, ksl, G, prec, slots);
       if (ks > 1) {
         p->part_bytes = round_up((size_t)ks * Mc * Nc * sizeof(float), 256);
         p->counter_bytes = kCounterRegionBytes;
-        if ((size_t)rb * cps * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
       }
       p->workspace_bytes = p->part_bytes + p->counter_bytes;
       return GQ_OK;

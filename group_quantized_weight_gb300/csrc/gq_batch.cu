@@ -12,8 +12,8 @@
 // Grid: (K slice, tile range) pairs x row blocks of 32 activation rows.  CTA (s, c) holds
 // activation rows m0 .. m0 + 31 of K slice s in shared memory (bf16, permuted so that a lane
 // reads the B operands of four 16-k MMA steps with two 16-byte loads) and computes the
-// slice's partial sums for tile range c.  Its 16 warps split the tile range into whole
-// tiles.  Each warp streams its tiles' slots (256 k, 2 KB of codes) through a shared-memory
+// slice's partial sums for tile range c.  Its warps (32, 24 or 16 as the rows grow) split
+// the tile range into whole tiles.  Each warp streams its tiles' slots (256 k, 2 KB of codes) through a shared-memory
 // ring: lane 0 issues a cp.async.bulk copy of the codes, lanes 0 .. NL-1 copy the group
 // scales with cp.async, and both report on the slot's mbarrier.
 //
@@ -25,8 +25,8 @@
 // columns on activation rows.  Each group's FP32 result is multiplied by its scale after the
 // whole group (the group-wise GEMM of "04 · 分组量化 GEMM 内核", section 2).
 //
-// Slices are combined by the split-K of the same page, section 3.3: every CTA writes its
-// FP32 partial sums, and the last of the K slices' CTAs to finish a tile range adds them in
+// Slices are combined by the split-K of the same page, section 3.3: every warp writes its
+// tile's FP32 partial sums, and the last of the K slices' warps to finish a tile adds them in
 // slice order 0, 1, ... (a fixed order: bitwise reproducible).
 #include <type_traits>
 
@@ -34,7 +34,6 @@
 
 namespace gq {
 
-constexpr int kBtWarps = 16;                         // warps per CTA
 constexpr int kBtSlotK = 256;                        // k per slot (four 64-k chunks)
 constexpr int kBtSlotCodes = 2048;                   // bytes of codes per slot
 constexpr int kBtMaxSlots = 4;                       // ring slots per warp
@@ -115,7 +114,7 @@ struct BtParams {
   const uint32_t *zeros;      // [K/G][N/8] or NULL
   void *out;                  // [M][N]
   float *part;                // [KS][M][N] FP32 slice partial sums (KS > 1)
-  unsigned *counters;         // per (row block, tile range) arrival counters (KS > 1)
+  unsigned *counters;         // per (row block, tile) arrival counters (KS > 1)
   int M, K, N;
   int T;                      // 16-column tiles
   int KS, KSL;                // K slices and k per slice
@@ -125,6 +124,14 @@ struct BtParams {
   int static_w;               // weights may be read before the preceding kernel ends
 };
 
+// Warps per CTA for MT 8-row MMA blocks of activations: as many as the registers allow
+// without spills (64 registers a thread for MT = 1, 80 for MT = 2, 128 above).  The kernel
+// is latency-bound (no pipe near saturation), so more warps per SM is what speeds it up.
+__host__ __device__ constexpr int batch_warps(int MT) { return MT == 1 ? 32 : MT == 2 ? 24 : 16; }
+__host__ __device__ constexpr int batch_mt(int M) {
+  return ((M < kBtRows ? M : kBtRows) + 7) / 8;
+}
+
 __host__ __device__ constexpr int batch_groups_per_slot(int G) { return kBtSlotK / G; }
 __host__ __device__ constexpr int batch_slot_bytes(int G, int es) {
   return kBtSlotCodes + batch_groups_per_slot(G) * 16 * es;
@@ -133,7 +140,7 @@ __host__ __device__ constexpr int batch_slot_bytes(int G, int es) {
 // Shared memory (dynamic): [activation slice: min(M, 32) rows x act_row_words(KSL / 64)]
 // [rings]
 template <int G, int SC, bool ZP, int MT>
-__global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtParams p) {
+__global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const BtParams p) {
   using namespace bt;
   constexpr int ES = SC == kScF32 ? 4 : 2;          // bytes per scale
   constexpr int GPS = batch_groups_per_slot(G);     // groups per slot
@@ -145,7 +152,8 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
   typedef typename std::conditional<SC == kScF32, uint32_t, unsigned short>::type sc_t;
 
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kBtWarps][kBtMaxSlots];
+  constexpr int NWARP = batch_warps(MT);
+  __shared__ __align__(8) uint64_t bars[NWARP][kBtMaxSlots];
   asm volatile("griddepcontrol.launch_dependents;");
 
   const int M = p.M, K = p.K, N = p.N, S = p.S;
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
   int tb, te;                                       // this CTA's tiles
   zsplit_dev(p.T, p.cps, c, tb, te);
   int wtb, wte;                                     // this warp's tiles
-  zsplit_dev(te - tb, kBtWarps, warp, wtb, wte);
+  zsplit_dev(te - tb, NWARP, warp, wtb, wte);
   wtb += tb;
   wte += tb;
   const int nloads = (wte - wtb) * SPS;
@@ -190,16 +198,13 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
     const uint32_t bar = saddr(&bars[warp][hs]);
     const uint32_t dst = saddr(ring + hs * SLOTB);
     const uint8_t *src = p.Wp + ((size_t)ht * SPT + j) * kBtSlotCodes;
-    const uint32_t ubar = __shfl_sync(0xffffffffu, bar, 0);
-    const uint32_t udst = __shfl_sync(0xffffffffu, dst, 0);
-    const unsigned long long usrc = __shfl_sync(0xffffffffu, (unsigned long long)src, 0);
-    if (lane == 0) {
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(ubar),
+    if (lane == 0) {                                // ht, hj, hs are uniform across the warp
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                    "n"(kBtSlotCodes)
                    : "memory");
       asm volatile(
-          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(udst),
-          "l"(usrc), "n"(kBtSlotCodes), "r"(ubar)
+          "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+          "l"(src), "n"(kBtSlotCodes), "r"(bar)
           : "memory");
     }
     if (lane < NL) {
@@ -225,16 +230,33 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
   // ---- the activation slice: rows m0 .. m0 + Mb - 1, k = ks KSL .. (ks + 1) KSL - 1, as
   // 16-byte pieces (8 k); the four words of piece pc go to base(pc) + 0, 4, 8, 12 of the row
   {
-    const int ppr = p.KSL >> 3;
+    // eight pieces per thread in flight at once: one global round trip per batch
+    constexpr int kU = 8;
+    const int ppr = p.KSL >> 3, npc = Mb * ppr;
     const uint4 *A4 = reinterpret_cast<const uint4 *>(p.A32);
-    for (int idx = threadIdx.x; idx < Mb * ppr; idx += blockDim.x) {
-      const int m = idx / ppr, pc = idx - m * ppr;
-      const uint4 v = A4[((size_t)(m0 + m) * K + (size_t)ks * p.KSL) / 8 + pc];
-      uint32_t *dst = sA + m * RS + (pc >> 3) * 32 + ((pc & 7) >> 2) * 16 + ((pc >> 1) & 1) * 2 + (pc & 1);
-      dst[0] = v.x;
-      dst[4] = v.y;
-      dst[8] = v.z;
-      dst[12] = v.w;
+    for (int base = threadIdx.x; base < npc; base += kU * blockDim.x) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < npc) {
+          const int m = idx / ppr, pc = idx - m * ppr;
+          v[u] = __ldg(A4 + ((size_t)(m0 + m) * K + (size_t)ks * p.KSL) / 8 + pc);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < npc) {
+          const int m = idx / ppr, pc = idx - m * ppr;
+          uint32_t *dst = sA + m * RS + (pc >> 3) * 32 + ((pc & 7) >> 2) * 16 +
+                          ((pc >> 1) & 1) * 2 + (pc & 1);
+          dst[0] = v[u].x;
+          dst[4] = v[u].y;
+          dst[8] = v[u].z;
+          dst[12] = v[u].w;
+        }
+      }
     }
   }
   __syncthreads();
@@ -260,14 +282,12 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
   };
   if (ZP && nloads > 0) load_zeros(wtb, 0);
 
-  // B operands: activation row m0 + r0 + 8 mt of the slice, this lane's 8 words of a chunk
+  // B operands: activation row m0 + r0 + 8 mt of the slice, this lane's 8 words of a chunk.
+  // A row past the block's last reads row 0 instead: B column r0 only reaches D column r0,
+  // an output row that is never stored, so no zero fill is needed.
   const uint32_t *brow[MT];
-  bool bval[MT];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    bval[mt] = r0 + 8 * mt < Mb;
-    brow[mt] = sA + (bval[mt] ? r0 + 8 * mt : 0) * RS + q * 4;
-  }
+  for (int mt = 0; mt < MT; ++mt) brow[mt] = sA + (r0 + 8 * mt < Mb ? r0 + 8 * mt : 0) * RS + q * 4;
   const bool split = p.KS > 1;
 
   // ---- main loop: this warp's tiles, each over the slice's slots
@@ -299,16 +319,11 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
         uint32_t bq[MT][8];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          if (bval[mt]) {
-            const uint32_t *bp = brow[mt] + (j * 4 + ch) * 32;
-            const uint4 lo = *reinterpret_cast<const uint4 *>(bp);
-            const uint4 hi = *reinterpret_cast<const uint4 *>(bp + 16);
-            bq[mt][0] = lo.x; bq[mt][1] = lo.y; bq[mt][2] = lo.z; bq[mt][3] = lo.w;
-            bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) bq[mt][e] = 0u;
-          }
+          const uint32_t *bp = brow[mt] + (j * 4 + ch) * 32;
+          const uint4 lo = *reinterpret_cast<const uint4 *>(bp);
+          const uint4 hi = *reinterpret_cast<const uint4 *>(bp + 16);
+          bq[mt][0] = lo.x; bq[mt][1] = lo.y; bq[mt][2] = lo.z; bq[mt][3] = lo.w;
+          bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
         }
         const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
         float d[MT][4];
@@ -357,6 +372,39 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
     }
     // D fragment: e = 0, 1 -> column 16 t + r0, e = 2, 3 -> column 16 t + r0 + 8; rows
     // m0 + 8 mt + 2 q + (e & 1)
+    if (!split) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int n = t * kTileN + r0 + 8 * (e >> 1);
+          const int ml = 8 * mt + 2 * q + (e & 1);
+          if (n < N && ml < Mb)
+            store_out_rt(p.out, (size_t)(m0 + ml) * N + n, acc[mt][e], p.out_f32 != 0);
+        }
+      continue;
+    }
+    // split K: write this slice's partial sums of tile t; the last of the KS warps (one per
+    // K slice) to finish the tile adds the slices in the fixed order 0, 1, ..., so the
+    // reduction is spread over the run instead of forming a tail at its end
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int n = t * kTileN + r0 + 8 * (e >> 1);
+        const int ml = 8 * mt + 2 * q + (e & 1);
+        if (n < N && ml < Mb) p.part[(size_t)ks * M * N + (size_t)(m0 + ml) * N + n] = acc[mt][e];
+      }
+    __threadfence();                // this lane's partials visible device-wide
+    __syncwarp();
+    unsigned last = 0u;
+    if (lane == 0) {
+      unsigned *ctr = p.counters + (size_t)blockIdx.y * p.T + t;
+      last = atomicAdd(ctr, 1u) == (unsigned)(p.KS - 1) ? 1u : 0u;
+      if (last) *ctr = 0u;          // every slice of this tile has arrived: reset
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+    __threadfence();
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -365,25 +413,13 @@ __global__ void __launch_bounds__(kBtWarps * 32, 1) w4_batch_kernel(const BtPara
         const int ml = 8 * mt + 2 * q + (e & 1);
         if (n < N && ml < Mb) {
           const size_t o = (size_t)(m0 + ml) * N + n;
-          if (split)
-            p.part[(size_t)ks * M * N + o] = acc[mt][e];
-          else
-            store_out_rt(p.out, o, acc[mt][e], p.out_f32 != 0);
+          float sum = 0.f;
+#pragma unroll 4
+          for (int s2 = 0; s2 < p.KS; ++s2)
+            sum += s2 == ks ? acc[mt][e] : __ldcg(p.part + (size_t)s2 * M * N + o);
+          store_out_rt(p.out, o, sum, p.out_f32 != 0);
         }
       }
-  }
-
-  if (!split) return;
-  // the last CTA of this (row block, tile range) to finish adds the slices in order
-  if (!last_arriver(p.counters + blockIdx.y * p.cps + c, p.KS)) return;
-  const int n_lo = tb * kTileN, n_hi = min(te * kTileN, N);
-  const int W = n_hi - n_lo;
-  for (int idx = threadIdx.x; idx < Mb * W; idx += blockDim.x) {
-    const int ml = idx / W, n = n_lo + idx - ml * W;
-    const size_t o = (size_t)(m0 + ml) * N + n;
-    float sum = 0.f;
-    for (int s2 = 0; s2 < p.KS; ++s2) sum += __ldcg(p.part + (size_t)s2 * M * N + o);
-    store_out_rt(p.out, o, sum, p.out_f32 != 0);
   }
 }
 
@@ -397,7 +433,7 @@ static cudaError_t launch_bt_t(const Plan &pl, const BtParams &bp, cudaStream_t 
   // runs; this kernel touches its inputs and outputs only after griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid_x, pl.grid_z);
-  cfg.blockDim = dim3(pl.block_threads);
+  cfg.blockDim = dim3(batch_warps(MT) * 32);     // the kernel's own warp count
   cfg.dynamicSmemBytes = pl.smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -462,8 +498,10 @@ size_t batch_smem_bytes(int M, int K_slice, int G, int prec, int slots) {
   const int es = (prec & GQ_SC_F32) ? 4 : 2;
   const int rows = M < kBtRows ? M : kBtRows;
   const size_t act = ((size_t)rows * act_row_words(K_slice / kChunkK) * 4 + 127) & ~(size_t)127;
-  return act + (size_t)kBtWarps * slots * batch_slot_bytes(G, es);
+  return act + (size_t)batch_warps(batch_mt(M)) * slots * batch_slot_bytes(G, es);
 }
+
+int batch_threads(int M) { return batch_warps(batch_mt(M)) * 32; }
 
 int batch_slots_for(int M, int K_slice, int G, int prec, size_t smem_cap) {
   for (int s = kBtMaxSlots; s >= 2; --s)

@@ -94,6 +94,7 @@ bool batch_supported(int M, int K, int G, int prec);
 int batch_slice_k(int M, int K);
 size_t batch_smem_bytes(int M, int K_slice, int G, int prec, int slots);
 int batch_slots_for(int M, int K_slice, int G, int prec, size_t smem_cap);
+int batch_threads(int M);
 cudaError_t launch_batch(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                          const void *Wq, const void *scales, const void *zeros, void *out,
                          float *part, unsigned *counters, cudaStream_t s);

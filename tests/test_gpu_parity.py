@@ -57,6 +57,9 @@ W4_SHAPES = [
     gq_synth.Config("w4_out_f32", M=7, K=1024, N=80, G=128, out="f32"),
     gq_synth.Config("w4_outliers", M=1, K=4096, N=2048, G=128, outlier_frac=0.001),
     gq_synth.Config("w4_asym_m16", M=16, K=8192, N=512, G=128, zp=True, sc="bf16"),
+    # small-batch kernel with split K: two row blocks and a ragged last tile; eight slices
+    gq_synth.Config("w4_m40_g32_split", M=40, K=4096, N=264, G=32, zp=True),
+    gq_synth.Config("w4_m24_split_ragged", M=24, K=8192, N=136, G=64, sc="f32", out="f32"),
 ]
 
 
