@@ -41,6 +41,7 @@ class Config:
     G: int
     w4: bool = True
     zp: bool = False            # per-group packed INT4 zero points (else z = 8 for W4, 0 for W8)
+    zf: bool = False            # per-group float zero points [K/G][N] in the scales' format
     act: str = "bf16"           # "bf16" | "f32"
     sc: str = "fp16"            # "fp16" | "bf16" | "f32"
     out: str = "bf16"           # "bf16" | "f32"
@@ -164,6 +165,21 @@ def make_weights(cfg: Config, seed: int = 0) -> dict:
     else:
         scales = s
     z = zeros = None
+    if cfg.zf:
+        # float zero points near s·z for z in [z_lo, z_hi] (a real z; an integer one with
+        # power-of-two scales, so that s·z is exact in every format)
+        assert cfg.w4 and not cfg.zp, "float zero points replace the packed INT4 ones"
+        if cfg.pow2_scales:
+            zr = rz.integers(cfg.z_lo, cfg.z_hi + 1, size=(ng, N)).astype(np.float64)
+        else:
+            zr = rz.uniform(cfg.z_lo, cfg.z_hi, size=(ng, N))
+        zf = (s.astype(np.float64) * zr).astype(np.float32)
+        if cfg.sc == "fp16":
+            zeros = f32_to_fp16_bits(zf)
+        elif cfg.sc == "bf16":
+            zeros = f32_to_bf16_bits(zf)
+        else:
+            zeros = zf
     if cfg.zp:
         assert cfg.w4, "zero points are INT4-packed"
         z = rz.integers(cfg.z_lo, cfg.z_hi + 1, size=(ng, N), dtype=np.uint8)

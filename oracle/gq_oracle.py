@@ -29,7 +29,7 @@ __all__ = [
     "group_gemm_magnitude", "reference", "tolerance", "check", "quantize_w4_g",
     "bits_per_weight", "dequantize_brute", "silu", "silu_mul_reference",
     "quantize_act_i8", "group_gemm_a8", "reference_a8", "e4m3_bits_to_f64",
-    "fp8_block_gemm", "f64_to_e4m3_bits", "quantize_act_fp8",
+    "fp8_block_gemm", "f64_to_e4m3_bits", "quantize_act_fp8", "group_gemm_zf",
 ]
 
 
@@ -178,8 +178,25 @@ def group_gemm_magnitude(A, q, z, s, G) -> np.ndarray:
     return out
 
 
+def group_gemm_zf(A: np.ndarray, q: np.ndarray, zf: np.ndarray, s: np.ndarray, G: int):
+    """Float zero points: out = A @ W_hat with W_hat[k][n] = q[k][n] · s[g][n] − zf[g][n],
+    g = k // G (P1 section 3.4: Machete's out = (w_q · w_s − w_z) @ a, the zero point a float
+    in the scale type, subtracted after scaling rather than from the code).  Returns
+    (out, mag) with mag[m][n] = Σ_k |A[m][k] · W_hat[k][n]|.
+
+    A [M][K] float64, q [K][N] integer codes, zf and s [K/G][N] float64.  The dequantized
+    weights are formed first, as the formula is written, then one library matmul.
+    """
+    A = np.asarray(A, np.float64)
+    K, N = q.shape
+    assert K % G == 0 and A.shape[1] == K
+    W = (q.astype(np.float64).reshape(K // G, G, N) * np.asarray(s, np.float64)[:, None, :]
+         - np.asarray(zf, np.float64)[:, None, :]).reshape(K, N)
+    return A @ W, np.abs(A) @ np.abs(W)
+
+
 def reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, w4: bool,
-              act: str, sc: str, rows=None, cols=None):
+              act: str, sc: str, rows=None, cols=None, zp_float: bool = False):
     """Decode canonical inputs with this module's own codecs and return (ref, mag), both
     float64 [len(rows)][len(cols)].
 
@@ -187,7 +204,8 @@ def reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, w4: bool,
     codes:  W4: uint32 [K/8][N]; W8: int8 [K][N] (zero point 0).
     scales: [K/G][N] fp16 / bf16 bits (uint16) or float32, per ``sc``.
     zeros:  W4 only: uint32 [K/G][N/8] or None (then z = 8, the symmetric point of the
-            INT4 teaching kernel, P1 section 9.4).
+            INT4 teaching kernel, P1 section 9.4); with ``zp_float``, float zero points
+            [K/G][N] in the scales' format, subtracted after scaling (``group_gemm_zf``).
     """
     A_raw = np.asarray(A_raw)
     if rows is not None:
@@ -197,20 +215,24 @@ def reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, w4: bool,
     cols_ = np.arange(N) if cols is None else np.asarray(cols)
     if w4:
         q = unpack_int4_k(np.asarray(codes)[:, cols_])
-        if zeros is None:
+        if zeros is None or zp_float:
             z = np.full((ng, len(cols_)), 8, dtype=np.int64)
         else:
             z = unpack_int4_n(np.asarray(zeros))[:, cols_]
     else:
         q = np.asarray(codes)[:, cols_].astype(np.int64)
         z = np.zeros((ng, len(cols_)), dtype=np.int64)
-    sraw = np.asarray(scales)[:, cols_]
-    if sc == "fp16":
-        s = fp16_bits_to_f64(sraw)
-    elif sc == "bf16":
-        s = bf16_bits_to_f64(sraw)
-    else:
-        s = f32_to_f64(sraw)
+    def dec(raw):
+        raw = np.asarray(raw)[:, cols_]
+        if sc == "fp16":
+            return fp16_bits_to_f64(raw)
+        if sc == "bf16":
+            return bf16_bits_to_f64(raw)
+        return f32_to_f64(raw)
+    s = dec(scales)
+    if zp_float:
+        assert w4
+        return group_gemm_zf(A, unpack_int4_k(np.asarray(codes)[:, cols_]), dec(zeros), s, G)
     return group_gemm(A, q, z, s, G), group_gemm_magnitude(A, q, z, s, G)
 
 

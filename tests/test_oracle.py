@@ -443,6 +443,81 @@ def test_a8_group_gemm_matches_brute_force_and_integer_product():
     assert np.array_equal(out1, (Aq.astype(np.int64) @ q.astype(np.int64)).astype(np.float64))
 
 
+# ------------------------------------------------------------------ float zero points
+
+def _lib_decode(bits, fmt):
+    """Scale-format bits -> float64 with library routines (numpy fp16, torch bf16)."""
+    if fmt == "fp16":
+        return np.asarray(bits).view(np.float16).astype(np.float64)
+    if fmt == "bf16":
+        return torch.from_numpy(np.asarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+    return np.asarray(bits).astype(np.float64)
+
+
+ZF_SMALL = [
+    gq_synth.Config("zf_bf16", M=2, K=64, N=5, G=32, zf=True, sc="bf16"),
+    gq_synth.Config("zf_fp16_g128", M=3, K=256, N=8, G=128, zf=True),
+    gq_synth.Config("zf_f32", M=1, K=96, N=16, G=32, zf=True, sc="f32", out="f32"),
+]
+
+
+@pytest.mark.parametrize("cfg", ZF_SMALL, ids=lambda c: c.name)
+def test_float_zero_oracle_matches_exact_rational_sum(cfg):
+    """Σ_k A·(q·s − zf) in exact rationals from the generator's raw codes and library-decoded
+    scales, zero points and activations (nothing shared with the oracle's decoders)."""
+    inp = gq_synth.make_inputs(cfg, seed=5)
+    ref, mag = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                             N=cfg.N, G=cfg.G, w4=True, act=cfg.act, sc=cfg.sc, zp_float=True)
+    s, zf = _lib_decode(inp["scales"], cfg.sc), _lib_decode(inp["zeros"], cfg.sc)
+    A = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    q = inp["q"]
+    for m in range(A.shape[0]):
+        for n in range(cfg.N):
+            exact = sum(Fraction(float(A[m, k])) * (int(q[k, n]) * Fraction(float(s[k // cfg.G, n]))
+                                                     - Fraction(float(zf[k // cfg.G, n])))
+                        for k in range(cfg.K))
+            assert abs(ref[m, n] - float(exact)) <= 1e-13 * mag[m, n] + 1e-300
+    assert (mag >= np.abs(ref) * (1 - 1e-12)).all()
+
+
+def test_float_zero_equal_to_scaled_integer_zero_gives_the_integer_form():
+    """With power-of-two scales and zf = s·z for integer z (exact), W_hat = q·s − zf equals
+    s·(q − z): the float form must agree with the integer-zero group GEMM."""
+    cfg = gq_synth.Config("zf_int", M=3, K=256, N=24, G=64, zf=True, sc="bf16", pow2_scales=True)
+    inp = gq_synth.make_inputs(cfg, seed=2)
+    s, zf = _lib_decode(inp["scales"], "bf16"), _lib_decode(inp["zeros"], "bf16")
+    z = zf / s
+    assert np.array_equal(z, np.round(z)) and z.min() >= cfg.z_lo and z.max() <= cfg.z_hi
+    assert len(np.unique(z)) > 3                     # zero points vary over groups and columns
+    A = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    out_f, _ = orc.group_gemm_zf(A, inp["q"].astype(np.int64), zf, s, cfg.G)
+    out_i = orc.group_gemm(A, inp["q"].astype(np.int64), z.astype(np.int64), s, cfg.G)
+    mag = orc.group_gemm_magnitude(A, inp["q"].astype(np.int64), z.astype(np.int64), s, cfg.G)
+    assert np.allclose(out_f, out_i, rtol=0, atol=1e-12 * float(mag.max()))
+
+
+def test_float_zero_enters_through_the_group_sums_of_the_activations():
+    """out(zf) − out(0) = −Σ_g (Σ_{k∈g} A[m][k]) · zf[g][n]: the sign, the group of each k and
+    the column of each zero point (group sums by a numpy reshape)."""
+    rng = np.random.default_rng(4)
+    M, K, N, G = 3, 128, 6, 32
+    A = rng.standard_normal((M, K))
+    q = rng.integers(0, 16, (K, N))
+    s = rng.uniform(0.005, 0.02, (K // G, N))
+    zf = rng.uniform(-0.2, 0.2, (K // G, N))
+    out, _ = orc.group_gemm_zf(A, q, zf, s, G)
+    out0, _ = orc.group_gemm_zf(A, q, np.zeros_like(zf), s, G)
+    gsum = A.reshape(M, K // G, G).sum(axis=2)
+    assert np.allclose(out - out0, -(gsum @ zf), rtol=1e-12, atol=1e-12)
+
+
+def test_float_zero_pins_catch_a_planted_sign_error(monkeypatch):
+    real = orc.group_gemm_zf
+    monkeypatch.setattr(orc, "group_gemm_zf", lambda A, q, zf, s, G: real(A, q, -np.asarray(zf), s, G))
+    with pytest.raises(AssertionError):
+        test_float_zero_enters_through_the_group_sums_of_the_activations()
+
+
 # ------------------------------------------------------------------ FP8 block-scaled GEMM
 
 def test_e4m3_decoder_matches_library_on_all_patterns():
