@@ -417,22 +417,27 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
     out = []
     side = torch.cuda.Stream()           # graph capture needs a stream other than the legacy one
     for name in ("tiny_gemv", "decode_gateup", "decode_gateup_silu", "q8_m1", "q8_m32",
-                 "q8a8_m1", "q8a8_m32", "asym_m16", "prefill"):
+                 "q8a8_m1", "q8a8_m32", "asym_m16", "asym_m16_zf", "prefill"):
         # decode_gateup_silu: the gate+up GEMV with the fused SiLU-and-mul epilogue
         # (GQ_GATE_UP): the same weights, an output of N/2 columns.  q8a8_*: the Q8_0 shapes
         # with int8 activation codes and per-group scales (GQ_ACT_I8), quantized on the device
-        # by gq_quantize_act before the timed calls
+        # by gq_quantize_act before the timed calls.  asym_m16_zf: the asymmetric shape with
+        # bf16 float zero points subtracted after scaling (GQ_ZP_FLOAT) in place of packed ones
         fused = name == "decode_gateup_silu"
         a8 = name.startswith("q8a8")
-        cfg = gq_synth.CONFIGS["decode_gateup" if fused else name.replace("q8a8", "q8")]
-        prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out) | GQ_STATIC_W
+        if name == "asym_m16_zf":
+            cfg = gq_synth.CONFIGS["asym_m16"].replace(name=name, zp=False, zf=True)
+        else:
+            cfg = gq_synth.CONFIGS["decode_gateup" if fused else name.replace("q8a8", "q8")]
+        prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out, zf=cfg.zf) | GQ_STATIC_W
         if fused:
             prec |= GQ_GATE_UP
         if a8:
             prec = (prec & ~GQ_ACT_F32) | GQ_ACT_I8
         d = _dev_inputs(torch, dev, gq_synth.make_inputs(cfg, seed=0))
         packed = gq.pack_weights_t(d["codes"], cfg.K, cfg.N, cfg.G, prec)
-        nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+        nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc,
+                                   cfg.out, zf=cfg.zf)
         if fused:
             nbytes -= cfg.M * (cfg.N // 2) * 2        # half the bf16 output columns
         a_ptr, as_ptr = d["A"].data_ptr(), None
@@ -463,6 +468,7 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
         row = {"workload": name, "M": cfg.M, "K": cfg.K, "N": cfg.N, "G": cfg.G,
                **({"epilogue": "silu(gate) * up, N/2 output columns"} if fused else {}),
                **({"activations": "int8 codes, fp32 scale per (row, group)"} if a8 else {}),
+               **({"zero_points": "bf16 float zero points, W = q*s - zf"} if cfg.zf else {}),
                "path": plan["path"], "us": us, "GB/s": gbs, "TFLOPS": tf,
                "weight_copies": copies,
                "l2": ("from HBM (rotated copies exceed L2)" if copies * wbytes > L2_BYTES

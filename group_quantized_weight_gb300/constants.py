@@ -11,6 +11,7 @@ GQ_OUT_F32 = 0x20
 GQ_STATIC_W = 0x40
 GQ_GATE_UP = 0x80
 GQ_ACT_I8 = 0x100
+GQ_ZP_FLOAT = 0x200
 
 GQ_OK = 0
 STATUS_NAMES = {0: "GQ_OK", 1: "GQ_ERR_INVALID_ARG", 2: "GQ_ERR_UNSUPPORTED",
@@ -26,8 +27,8 @@ class GqError(RuntimeError):
         self.status = status
 
 
-def prec_flags(w4: bool, zp: bool, act: str, sc: str, out: str) -> int:
-    p = 0
+def prec_flags(w4: bool, zp: bool, act: str, sc: str, out: str, zf: bool = False) -> int:
+    p = GQ_ZP_FLOAT if zf else 0
     if w4:
         p |= GQ_W4
     if zp:
@@ -44,16 +45,16 @@ def prec_flags(w4: bool, zp: bool, act: str, sc: str, out: str) -> int:
 
 
 def algorithmic_bytes(M: int, K: int, N: int, G: int, w4: bool, zp: bool, act: str, sc: str,
-                      out: str) -> int:
+                      out: str, zf: bool = False) -> int:
     """Bytes the GEMM must move at least once: the codes (0.5 or 1 byte per weight), one
-    scale and (optionally) one INT4 zero point per group and column, the activations read
+    scale and (optionally) one INT4 or float zero point per group and column, the activations read
     once and the output written once.  This is the memory term of the weight-only GEMM
     roofline of "GPU Kernel 工程（09）：量化与融合 kernel", section 3.2 (weights K·N·b_w plus
     activations M·K and outputs M·N), with the group metadata of section 3.1 added."""
     ng = K // G
     codes = K * N // 2 if w4 else K * N
     scales = ng * N * _SIZE[sc]
-    zeros = ng * (N // 8) * 4 if zp else 0
+    zeros = ng * (N // 8) * 4 if zp else ng * N * _SIZE[sc] if zf else 0
     return codes + scales + zeros + M * K * _SIZE[act] + M * N * _SIZE[out]
 
 

@@ -17,8 +17,11 @@ static inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 int validate(int M, int K, int N, int G, int prec) {
   if (M < 0 || N < 0 || K <= 0) return GQ_ERR_INVALID_ARG;
   if (prec & ~(GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_SC_BF16 | GQ_SC_F32 | GQ_OUT_F32 | GQ_STATIC_W |
-               GQ_GATE_UP | GQ_ACT_I8))
+               GQ_GATE_UP | GQ_ACT_I8 | GQ_ZP_FLOAT))
     return GQ_ERR_INVALID_ARG;
+  if ((prec & GQ_ZP_FLOAT) && (prec & GQ_ZP)) return GQ_ERR_INVALID_ARG;   // one zero-point form
+  if ((prec & GQ_ZP_FLOAT) && (!(prec & GQ_W4) || (prec & (GQ_GATE_UP | GQ_ACT_I8))))
+    return GQ_ERR_UNSUPPORTED;
   if ((prec & GQ_SC_BF16) && (prec & GQ_SC_F32)) return GQ_ERR_INVALID_ARG;
   if (!(G == 32 || G == 64 || G == 128 || G == 256)) return GQ_ERR_UNSUPPORTED;
   if (K < G || K % G != 0) return GQ_ERR_INVALID_ARG;
@@ -85,6 +88,9 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const int Mc = M > 0 ? M : 1;
   const int Nc = N > 0 ? N : 8;
   const size_t kCtaSmemCap = 227u * 1024u - 1024u;   // minus the static shared memory
+  // float zero points: the small-batch kernel only
+  if ((prec & GQ_ZP_FLOAT) && !(Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)))
+    return GQ_ERR_UNSUPPORTED;
   // W8A8 (GQ_ACT_I8): integer group dots, 64 columns x one K slice x 32 rows per CTA
   if (prec & GQ_ACT_I8) {
     const int ks = q8a8_slices(Mc, K, Nc, G, sms, kPartCap);
@@ -112,7 +118,9 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   // striped persistent decode (M <= 8): one CTA of kStrWarps warps per SM over a
   // contiguous range of (tile, 256-k slot) pairs; whole tiles per CTA when that keeps the
   // SMs within 10% of even, else equal slot ranges with a cross-CTA reduction
-  const int slots = stripe_supported(Mc, K, G, prec) ? stripe_slots_for(Mc, K, G, prec, kCtaSmemCap) : 0;
+  const int slots = stripe_supported(Mc, K, G, prec) && !(prec & GQ_ZP_FLOAT)
+                        ? stripe_slots_for(Mc, K, G, prec, kCtaSmemCap)
+                        : 0;
   if ((prec & GQ_GATE_UP) && slots < 2) return GQ_ERR_UNSUPPORTED;   // striped kernel only
   if (slots >= 2) {
     p->path = kPathStripe;
@@ -196,7 +204,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       return GQ_OK;
     }
   }
-  if (M >= kPrefillMinM && prefill_supported(M, K, N, G, prec)) {
+  if (M >= kPrefillMinM && !(prec & GQ_ZP_FLOAT) && prefill_supported(M, K, N, G, prec)) {
     // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
     p->path = kPathPrefill;
     p->m_tile = 256;
@@ -247,6 +255,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       return GQ_OK;
     }
   }
+  if (prec & GQ_ZP_FLOAT) return GQ_ERR_UNSUPPORTED;
   if (prec & GQ_W4) {
     p->path = kPathMmaDecode;
     const int rows = Mc < 8 * kDecMaxMT ? Mc : 8 * kDecMaxMT;
@@ -503,7 +512,7 @@ static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const 
   if (st != GQ_OK) return st;
   if (M == 0 || N == 0) return GQ_OK;
   if (!A || !Wq || !scales || !out) return GQ_ERR_INVALID_ARG;
-  if (((prec & GQ_ZP) != 0) != (zeros != nullptr)) return GQ_ERR_INVALID_ARG;
+  if (((prec & (GQ_ZP | GQ_ZP_FLOAT)) != 0) != (zeros != nullptr)) return GQ_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(Wq) || !aligned16(scales) || !aligned16(out) ||
       (zeros && !aligned16(zeros)))
     return GQ_ERR_ALIGNMENT;
@@ -594,7 +603,7 @@ int gq_quantize_act(int M, int K, int G, int prec, const void *A, void *Aq, void
 int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
   if (!a || !r || a->n_copies < 1 || a->iters < 1 || a->warmup < 0 || !a->Wq || !a->scales)
     return GQ_ERR_INVALID_ARG;
-  if ((a->prec & GQ_ZP) && !a->zeros) return GQ_ERR_INVALID_ARG;
+  if ((a->prec & (GQ_ZP | GQ_ZP_FLOAT)) && !a->zeros) return GQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)a->stream;
   if ((a->prec & GQ_ACT_I8) && !a->a_scales) return GQ_ERR_INVALID_ARG;
   auto call = [&](int i) {
@@ -603,7 +612,8 @@ int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
       return gemm_a8_impl(a->M, a->K, a->N, a->G, a->prec, a->A, a->a_scales, a->Wq[c],
                           a->scales[c], a->out, a->stream);
     return gemm_impl(a->M, a->K, a->N, a->G, a->prec, a->A, a->Wq[c], a->scales[c],
-                     (a->prec & GQ_ZP) ? a->zeros[c] : nullptr, a->out, a->stream);
+                     (a->prec & (GQ_ZP | GQ_ZP_FLOAT)) ? a->zeros[c] : nullptr, a->out,
+                     a->stream);
   };
   int st = GQ_OK;
   for (int i = 0; i < a->warmup && st == GQ_OK; ++i) st = call(i);

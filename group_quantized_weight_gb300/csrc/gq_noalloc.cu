@@ -56,7 +56,7 @@ extern "C" int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, cons
   if (st != GQ_OK) return st;
   if (M == 0 || N == 0) return GQ_OK;
   if (!A || !Wq || !scales || !out) return GQ_ERR_INVALID_ARG;
-  if (((prec & GQ_ZP) != 0) != (zeros != nullptr)) return GQ_ERR_INVALID_ARG;
+  if (((prec & (GQ_ZP | GQ_ZP_FLOAT)) != 0) != (zeros != nullptr)) return GQ_ERR_INVALID_ARG;
   const uintptr_t mis = (uintptr_t)A | (uintptr_t)Wq | (uintptr_t)scales | (uintptr_t)out |
                         (uintptr_t)zeros;
   if (mis & 15u) return GQ_ERR_ALIGNMENT;

@@ -57,6 +57,12 @@ typedef enum gq_status {
 #define GQ_ACT_I8  0x100  /* INT8-activation variant (gq_gemm_a8, and gq_plan / gq_workspace_size
                             for it): activations are int8 codes with one fp32 scale per (row,
                             group); W8 codes and GQ_SC_F32 only; gq_gemm refuses it         */
+#define GQ_ZP_FLOAT 0x200 /* W4 float zero points ("GPU Kernel 工程（09）：量化与融合 kernel",
+                            section 3.4, Machete's form out = (w_q * w_s - w_z) @ a): zeros is
+                            [K/G][N] in the scales' format and W_hat = q * s - zf, the zero
+                            subtracted after scaling.  Excludes GQ_ZP, GQ_GATE_UP, GQ_ACT_I8;
+                            needs bf16 activations, K % 256 == 0 and M <= 64 (the small-batch
+                            kernel), else GQ_ERR_UNSUPPORTED                                  */
 #define GQ_STATIC_W 0x40 /* Wq, scales and zeros are not written by work still running on the
                             stream (weights loaded once, as in serving): the decode kernels
                             may start streaming them before the preceding kernel has ended;
@@ -115,7 +121,8 @@ int gq_set_workspace(void *dev_ptr, size_t bytes);
  *   A       device [M][K], bf16 (or fp32 with GQ_ACT_F32).
  *   Wq      device, packed by gq_pack_weights with the same (K, N, G, prec).
  *   scales  device [K/G][N].
- *   zeros   device [K/G][N/8] uint32 with GQ_ZP, else must be NULL.
+ *   zeros   device [K/G][N/8] uint32 with GQ_ZP, [K/G][N] in the scales' format with
+ *           GQ_ZP_FLOAT, else must be NULL.
  *   out     device [M][N], fully overwritten.
  * Path choice depends only on (M, K, N, G, prec) and the device's SM count, so a given
  * problem on a given device always produces the same bits.  Scratch comes from the
@@ -159,7 +166,7 @@ typedef struct gq_bench_args {
   const void *A;
   const void *const *Wq;       /* n_copies device pointers (host array) */
   const void *const *scales;   /* n_copies device pointers (host array) */
-  const void *const *zeros;    /* n_copies device pointers, or NULL without GQ_ZP */
+  const void *const *zeros;    /* n_copies device pointers, or NULL without GQ_ZP / GQ_ZP_FLOAT */
   int n_copies;
   void *out;
   int warmup, iters, use_graph;

@@ -26,7 +26,7 @@ def load():
 
 def prec_of(cfg) -> int:
     from group_quantized_weight_gb300.constants import prec_flags
-    return prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    return prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out, zf=cfg.zf)
 
 
 def np_to_dev(a: np.ndarray):

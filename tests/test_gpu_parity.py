@@ -28,7 +28,7 @@ def gq():
 def _oracle(cfg, inp, rows=None, cols=None):
     return oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
                             N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc, rows=rows,
-                            cols=cols)
+                            cols=cols, zp_float=cfg.zf)
 
 
 def _assert_parity(cfg, got, ref, mag):
@@ -167,6 +167,52 @@ def test_prefill_integer_inputs_are_bit_exact(gq):
     ref, _ = _oracle(cfg, inp)
     h = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(h, oracle.f64_to_bf16_bits(ref))
+
+
+# ------------------------------------------------------------------ float zero points
+
+ZF_SHAPES = [
+    gq_synth.Config("zf_m1", M=1, K=512, N=264, G=128, zf=True, sc="bf16"),
+    gq_synth.Config("zf_m5_g32", M=5, K=1024, N=136, G=32, zf=True),
+    gq_synth.Config("zf_m16_split", M=16, K=8192, N=512, G=128, zf=True, sc="bf16"),
+    gq_synth.Config("zf_m24_f32", M=24, K=2048, N=200, G=64, zf=True, sc="f32", out="f32"),
+    gq_synth.Config("zf_m32_g256", M=32, K=4096, N=152, G=256, zf=True),
+    gq_synth.Config("zf_m40_rows", M=40, K=2048, N=264, G=128, zf=True, sc="bf16"),
+    gq_synth.Config("zf_m64_g32", M=64, K=1024, N=128, G=32, zf=True, sc="f32", out="f32"),
+    gq_synth.Config("zf_outliers", M=8, K=4096, N=512, G=128, zf=True, outlier_frac=0.001),
+]
+
+
+@pytest.mark.parametrize("cfg", ZF_SHAPES, ids=lambda c: c.name)
+def test_float_zero_points(gq, cfg):
+    _full_case(gq, cfg)
+
+
+def test_float_zero_points_integer_inputs_are_bit_exact(gq):
+    """Integer activations, power-of-two scales and zf = s·z: every group dot, product and
+    sum is exact in FP32, so the output equals the oracle bit for bit."""
+    cfg = gq_synth.Config("zf_exact", M=16, K=1024, N=128, G=64, zf=True, sc="bf16",
+                          a_kind="int", pow2_scales=True, out="f32")
+    inp = gq_synth.make_inputs(cfg, seed=3)
+    out, _ = run_gemm(gq, cfg, inp)
+    ref, _ = _oracle(cfg, inp)
+    assert np.array_equal(out.cpu().numpy(), ref.astype(np.float32))
+
+
+def test_float_zero_points_full_size_sampled_and_repeatable(gq):
+    cfg = gq_synth.CONFIGS["asym_m16"].replace(name="asym_m16_zf", zp=False, zf=True)
+    inp = gq_synth.make_inputs(cfg, seed=0)
+    out, packed = run_gemm(gq, cfg, inp)
+    rng = np.random.default_rng(9)
+    rows = np.arange(cfg.M)
+    cols = np.unique(np.concatenate([[0, 1, 15, 16, cfg.N - 1], rng.choice(cfg.N, 512, replace=False)]))
+    ref, mag = _oracle(cfg, inp, rows=rows, cols=cols)
+    _assert_parity(cfg, out_to_f64(out, cfg.out)[np.ix_(rows, cols)], ref, mag)
+    out2 = alloc_out(cfg.M, cfg.N, cfg.out)
+    gq.gemm_t(np_to_dev(inp["A"]), packed, np_to_dev(inp["scales"]), np_to_dev(inp["zeros"]),
+              out2, cfg.M, cfg.K, cfg.N, cfg.G, prec_of(cfg))
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
 # ------------------------------------------------------------------ the workloads

@@ -259,6 +259,30 @@ def test_int8_activation_variant_validation_and_plan():
     assert gq.gq_quantize_act(0, 512, 32, 0, None, None, None, None) == 0
 
 
+def test_float_zero_points_validation_and_plan():
+    zf = C.GQ_W4 | C.GQ_ZP_FLOAT | C.GQ_SC_BF16
+    # one zero-point form at a time; W4 only; no fused epilogue; the zeros pointer is required
+    assert gq.gq_gemm(1, 512, 64, 128, zf | C.GQ_ZP, 16, 16, 16, 16, 16, None) == 1
+    assert gq.gq_gemm(1, 512, 64, 32, C.GQ_ZP_FLOAT | C.GQ_ACT_F32 | C.GQ_SC_F32,
+                      16, 16, 16, 16, 16, None) == 2
+    assert gq.gq_gemm(1, 512, 64, 128, zf | C.GQ_GATE_UP, 16, 16, 16, 16, 16, None) == 2
+    assert gq.gq_gemm(1, 512, 64, 128, zf, 16, 16, 16, None, 16, None) == 1
+    # every M up to 64 runs on the small-batch kernel (not the striped or prefill ones), with
+    # room for the slice's activation group sums
+    for M, K, N, G in ((1, 4096, 28672, 128), (16, 8192, 28672, 128), (40, 2048, 264, 128),
+                       (64, 1024, 128, 32)):
+        p = gq.gq_plan(M, K, N, G, zf, sm_count=152)
+        assert p["path"] == 4
+        assert p["smem_bytes"] <= 226 * 1024
+    for M, K in ((65, 1024), (4096, 4096), (1, 320)):
+        with pytest.raises(C.GqError) as e:
+            gq.gq_plan(M, K, 512, 64, zf, sm_count=152)
+        assert e.value.status == 2
+    # bytes: one float zero point per group and column in the scales' format
+    assert C.algorithmic_bytes(1, 4096, 1024, 128, True, False, "bf16", "bf16", "bf16", zf=True) == \
+        C.algorithmic_bytes(1, 4096, 1024, 128, True, False, "bf16", "bf16", "bf16") + 32 * 1024 * 2
+
+
 def test_fp8_block_gemm_validation():
     f = gq.gq_gemm_fp8_block
     assert f(4, 192, 128, 0, 16, 16, 16, 16, 16, None) == 1      # K % 128 != 0
