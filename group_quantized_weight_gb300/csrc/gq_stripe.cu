@@ -3,7 +3,7 @@
 // Work partition.  The packed weights are a sequence of 16-column tiles, each tile's K
 // contiguous, so the flattened sequence of (tile, slot) pairs — a slot is 256 consecutive k
 // of one tile, 2 KB of codes — is one contiguous byte stream.  CTA c (one per SM) owns a
-// contiguous range of slots and its 16 warps split that range into contiguous sub-ranges
+// contiguous range of slots and its 24 warps split that range into contiguous sub-ranges
 // (the striped partitioning of "GPU Kernel 工程（09）：量化与融合 kernel", section 3.3 item 4:
 // every SM gets the same amount of work for any shape).  When there are enough tiles the
 // CTA ranges are whole tiles, so no tile is shared between SMs; otherwise they are equal

@@ -30,6 +30,7 @@ def gq():
     gq_synth.Config("nsa_asym_m3", M=3, K=2048, N=1032, G=128, zp=True, sc="bf16"),
     gq_synth.Config("nsa_q8_m16", M=16, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),        # INT8 CUDA-core kernel, K split
+    gq_synth.Config("nsa_zf_m12", M=12, K=4096, N=520, G=64, zf=True, sc="bf16"),  # float zeros, K split
 ], ids=lambda c: c.name)
 def test_static_scratch_matches_gq_gemm_twice(gq, cfg):
     inp = gq_synth.make_inputs(cfg, seed=4)
@@ -43,7 +44,8 @@ def test_static_scratch_matches_gq_gemm_twice(gq, cfg):
     gq.gemm_t(A, packed, S, Z, ref, cfg.M, cfg.K, cfg.N, cfg.G, prec)
     stream = torch.cuda.current_stream().cuda_stream
     _, mag = oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
-                              N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc)
+                              N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc,
+                              zp_float=cfg.zf)
     ref64 = out_to_f64(ref, cfg.out)
     for _ in range(2):
         got = alloc_out(cfg.M, cfg.N, cfg.out)
