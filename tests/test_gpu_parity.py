@@ -238,7 +238,8 @@ def test_workload_sampled(gq, name):
     _assert_parity(cfg, got, ref, mag)
 
 
-@pytest.mark.parametrize("name", ["decode_gateup", "asym_m16", "q8_m1"])
+@pytest.mark.parametrize("name", ["tiny_gemv", "decode_gateup", "asym_m16", "q8_m1", "q8_m32",
+                                  "prefill"])
 def test_bitwise_deterministic(gq, name):
     cfg = gq_synth.CONFIGS[name]
     inp = gq_synth.make_inputs(cfg, seed=0)
@@ -591,6 +592,34 @@ def test_fp8_block_gemm(gq, M, K, N, out):
     ref, mag = oracle.fp8_block_gemm(A, a_s, W, w_s)
     cfg = gq_synth.Config(f"fp8_{M}x{K}x{N}", M=M, K=K, N=N, G=128, out=out)
     _assert_parity(cfg, out_to_f64(o, out), ref, mag)
+
+
+def test_a8_and_fp8_paths_are_bitwise_repeatable(gq):
+    """The W8A8 group GEMM at the Q8_0 M=32 workload (split K, fixed-order reduction) and the
+    FP8 block-scaled GEMM on a multi-tile shape give the same bits call after call."""
+    from group_quantized_weight_gb300.constants import GQ_ACT_I8, GQ_OUT_F32, GQ_SC_F32
+    cfg = gq_synth.CONFIGS["q8_m32"]
+    inp, Aq, As = _a8_inputs(cfg, seed=0)
+    prec = GQ_ACT_I8 | GQ_SC_F32 | GQ_OUT_F32
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    Aq_d, As_d, S = np_to_dev(Aq), np_to_dev(As), np_to_dev(inp["scales"])
+    outs = []
+    for _ in range(3):
+        o = alloc_out(cfg.M, cfg.N, "f32")
+        gq.gemm_a8_t(Aq_d, As_d, packed, S, o, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+        outs.append(o.view(torch.int32))
+    M, K, N = 1024, 4096, 4096
+    A, a_s, W, w_s = _fp8_inputs(M, K, N, seed=21)
+    A_d, as_d, W_d, ws_d = np_to_dev(A), np_to_dev(a_s), np_to_dev(W), np_to_dev(w_s)
+    f8 = []
+    for _ in range(3):
+        o = alloc_out(M, N, "bf16")
+        gq.gemm_fp8_t(A_d, as_d, W_d, ws_d, o, M, K, N, 0)
+        f8.append(o.view(torch.int16))
+    torch.cuda.synchronize()
+    assert gq.gq_device_error(clear=True) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    assert torch.equal(f8[0], f8[1]) and torch.equal(f8[0], f8[2])
 
 
 @pytest.mark.parametrize("act", ["bf16", "f32"])
