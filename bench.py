@@ -153,6 +153,21 @@ def _sample_bytes(cfg, n_cols):
     return algorithmic_bytes(cfg.M, cfg.K, n_cols, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
 
 
+def slowest_rank_ms(ms: float, world: int, dist, device="cpu") -> float:
+    """The timed region's length on the slowest rank (every rank receives it)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_call: int, calls: int, ms: float) -> float:
+    """Whole-job throughput: the bytes of every rank's calls over the slowest rank's time."""
+    return world * bytes_per_call * calls / (ms * 1e-3) / 1e9
+
+
 def run_reference(args):
     """The reference arm: the float64 CPU oracle on a bounded column sample per step."""
     rank = int(os.environ.get("RANK", "0"))
@@ -290,15 +305,11 @@ def main():
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(e0.elapsed_time(e1), world, dist, dev)
     nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
     launches = args.steps * calls_per_step
     kernel_us = 1e3 * ms / launches
-    value = world * nbytes * launches / (ms * 1e-3) / 1e9
+    value = job_gbs(world, nbytes, launches, ms)
     peaks, peak_kind = _peaks()
     achieved = nbytes / (kernel_us * 1e-6) / 1e9
 
