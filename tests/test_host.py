@@ -28,6 +28,23 @@ def test_library_exports_every_declared_function():
     assert set(names) == set(gq.EXPORTED)
 
 
+def test_binding_flags_and_statuses_match_the_header():
+    """Every GQ_* constant the binding defines has the header's value, and the reverse."""
+    src = open(os.path.join(ROOT, "include", "gq.h"), encoding="utf-8").read()
+    flags = {m.group(1): int(m.group(2), 16)
+             for m in re.finditer(r"#define\s+(GQ_\w+)\s+0x([0-9a-fA-F]+)", src)}
+    statuses = {m.group(1): int(m.group(2))
+                for m in re.finditer(r"\b(GQ_(?:OK|ERR_\w+))\s*=\s*(\d+)", src)}
+    assert len(flags) >= 10 and "GQ_ZP_FLOAT" in flags
+    for name, val in flags.items():
+        assert getattr(C, name) == val, name
+    for name, val in statuses.items():
+        assert C.STATUS_NAMES[val] == name
+    binding = {n for n in dir(C) if n.startswith("GQ_") and isinstance(getattr(C, n), int)
+               and n not in ("GQ_OK",)}
+    assert binding <= set(flags), binding - set(flags)
+
+
 def test_status_strings():
     assert gq.gq_status_string(0) == "ok"
     for s in range(1, 8):
