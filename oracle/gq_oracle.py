@@ -13,7 +13,13 @@ P1 section 8 rule 2, compare against the dequantized weights, not the unquantize
     out[m][n] = Σ_g s[g][n] · Σ_{k ∈ group g} A[m][k] · (q[k][n] − z[g][n])
 
 with activation scale 1 (float activations).  The per-group integer-weighted dot is
-finished before the scale is applied, exactly as the formula states.  All arithmetic is
+finished before the scale is applied, exactly as the formula states.  The variants the
+library also computes have their own functions here: float zero points subtracted after
+scaling (``group_gemm_zf``, P1 section 3.4), the fused SiLU-and-mul epilogue
+(``silu_mul_reference``, P1 section 5.2), int8 activations with per-group scales
+(``quantize_act_i8``, ``group_gemm_a8``; P2 section 2, P1 section 4.5) and the FP8
+block-scaled GEMM with its activation quantizer (``quantize_act_fp8``, ``fp8_block_gemm``;
+P1 section 4.3).  All arithmetic is
 float64; products of a bf16/fp32 activation and a small integer are exact in float64 and
 sums of at most a few thousand such terms lose at most a few ulps of float64, far below
 every tolerance used against the GPU.
