@@ -213,6 +213,24 @@ def test_decode_plan_fills_the_machine():
     assert p["workspace_bytes"] == 0
 
 
+def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
+    """The small-batch kernel runs as many warps as its registers allow without spills (32 up
+    to 8 rows, 24 up to 16, 16 above), one CTA per SM, K slices x tile ranges = #SM."""
+    zp = C.GQ_W4 | C.GQ_ZP | C.GQ_SC_BF16
+    for M, warps in ((9, 24), (16, 24), (17, 16), (32, 16)):
+        p = gq.gq_plan(M, 8192, 28672, 128, zp, sm_count=152)
+        assert p["path"] == 4 and p["block_threads"] == 32 * warps, (M, p)
+        assert p["grid_x"] * p["grid_z"] <= 152 and p["grid_x"] >= 150
+        assert p["smem_bytes"] <= 226 * 1024
+    # float zero points take the same kernel from one row: 32 warps up to 8 rows
+    p = gq.gq_plan(1, 4096, 28672, 128, zp & ~C.GQ_ZP | C.GQ_ZP_FLOAT, sm_count=152)
+    assert p["path"] == 4 and p["block_threads"] == 32 * 32
+    # the asymmetric M=16 workload: 4 K slices of 2048 x 38 tile ranges, split-K scratch
+    p = gq.gq_plan(16, 8192, 28672, 128, zp, sm_count=152)
+    assert (p["nsplit"], p["grid_x"]) == (4, 152)
+    assert p["workspace_bytes"] >= 4 * 16 * 28672 * 4
+
+
 def test_small_decode_plan_splits_slots_between_ctas():
     p = gq.gq_plan(1, 4096, 1024, 128, C.GQ_W4, sm_count=152)
     assert p["path"] == 3
