@@ -70,7 +70,8 @@ typedef enum gq_status {
 
 /*
  * Supported operand combinations (anything else returns GQ_ERR_UNSUPPORTED):
- *   W4 : activations bf16; scales fp16, bf16 or fp32; zero points optional; out bf16 or fp32.
+ *   W4 : activations bf16; scales fp16, bf16 or fp32; zero points optional (packed INT4 with
+ *        GQ_ZP, or float in the scales' format with GQ_ZP_FLOAT); out bf16 or fp32.
  *   W8 : activations fp32; scales fp32; no zero points; out fp32 or bf16.
  * Shape contract: M ≥ 0, N ≥ 0 (either 0 is a valid empty call), N % 8 == 0, G in
  * {32, 64, 128, 256}, K ≥ G, K % G == 0, and K % 64 == 0 for W4 (K % 16 == 0 for W8).
