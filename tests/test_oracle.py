@@ -582,3 +582,194 @@ def test_fp8_activation_quantizer_block_maximum_and_error_bound():
     assert (np.abs(q).max(axis=2) == 448.0).all()        # each block's largest element
     # E4M3 has 3 mantissa bits: the relative error of a normal code is at most 2^-4
     assert (np.abs(x - ss * q) <= np.abs(x) * 2.0 ** -4 + ss * 2.0 ** -10).all()
+
+
+# ------------------------------------------------------------------ the tolerance's magnitude term
+#
+# Every GPU parity bound is 2^-8·|ref| + 1e-4·mag (bf16) or 1e-5·|ref| + 1e-6·mag (fp32), so an
+# inflated mag would silently loosen every parity test.  These pins compute mag term by term
+# (exact rational sums of |A[m][k]·W_hat[k][n]| from the generator's raw codes and library
+# decoders) and require equality to float64 rounding: a mag that is too large fails as surely
+# as one that is too small.  P1 section 8: the error of the K-term sum scales with the size of
+# the terms it adds, not with the size of the result.
+
+def _lib_act(inp, act):
+    if act == "bf16":
+        return torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16).double().numpy()
+    return inp["A"].astype(np.float64)
+
+
+def _exact_abs_sum(terms):
+    return float(sum((abs(Fraction(float(t))) for t in terms), Fraction(0)))
+
+
+def _brute_mag(cfg, inp):
+    s = _lib_decode(inp["scales"], cfg.sc)
+    A = _lib_act(inp, cfg.act)
+    q = inp["q"].astype(np.int64)
+    z = inp["z"] if inp["z"] is not None else None
+    z0 = 8 if cfg.w4 else 0
+    M = A.shape[0]
+    mag = np.zeros((M, cfg.N))
+    for m in range(M):
+        for n in range(cfg.N):
+            terms = []
+            for k in range(cfg.K):
+                g = k // cfg.G
+                zz = int(z[g, n]) if z is not None else z0
+                # A·s and the integer (q − z) are exact in float64; |·| of their product is
+                # formed as an exact rational
+                terms.append(Fraction(float(A[m, k])) * Fraction(float(s[g, n])) * (int(q[k, n]) - zz))
+            mag[m, n] = float(sum((abs(t) for t in terms), Fraction(0)))
+    return mag
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_magnitude_equals_the_exact_sum_of_absolute_terms(cfg):
+    inp = gq_synth.make_inputs(cfg, seed=11)
+    _, mag = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                           N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc)
+    exact = _brute_mag(cfg, inp)
+    assert np.allclose(mag, exact, rtol=1e-13, atol=0)
+
+
+def _mutant_mag_doubled(A, q, z, s, G):
+    return 2.0 * _REAL_MAG(A, q, z, s, G)
+
+
+def _mutant_mag_abs_code(A, q, z, s, G):
+    # |q| in place of |q − z|
+    return _REAL_MAG(A, q, np.zeros_like(z), s, G)
+
+
+def _mutant_mag_abs_after_sum(A, q, z, s, G):
+    # |Σ| in place of Σ|·|: the magnitude collapses to |ref| where the terms cancel
+    return np.abs(orc.group_gemm(A, q, z, s, G))
+
+
+_REAL_MAG = orc.gq_oracle.group_gemm_magnitude
+
+
+@pytest.mark.parametrize("mutant", [_mutant_mag_doubled, _mutant_mag_abs_code,
+                                    _mutant_mag_abs_after_sum])
+def test_magnitude_pin_catches_planted_mistakes(mutant, monkeypatch):
+    cfg = SMALL[1]                                  # asymmetric zero points, several groups
+    inp = gq_synth.make_inputs(cfg, seed=11)
+    exact = _brute_mag(cfg, inp)
+    monkeypatch.setattr(orc.gq_oracle, "group_gemm_magnitude", mutant)
+    _, mag = orc.gq_oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"],
+                                     K=cfg.K, N=cfg.N, G=cfg.G, w4=True, act=cfg.act, sc=cfg.sc)
+    assert not np.allclose(mag, exact, rtol=1e-6, atol=0)
+
+
+def test_a8_magnitude_equals_the_exact_sum_of_absolute_terms():
+    rng = np.random.default_rng(12)
+    M, K, N, G = 3, 96, 7, 32
+    Aq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    q = rng.integers(-127, 128, (K, N)).astype(np.int8)
+    a_s = rng.uniform(0.01, 0.1, (M, K // G)).astype(np.float32)
+    s = rng.uniform(1e-3, 1e-2, (K // G, N)).astype(np.float32)
+    _, mag = orc.reference_a8(Aq, a_s, q, s, K=K, N=N, G=G)
+    for m in range(M):
+        for n in range(N):
+            exact = _exact_abs_sum(
+                float(Fraction(float(a_s[m, k // G])) * Fraction(float(s[k // G, n])) *
+                      int(Aq[m, k]) * int(q[k, n])) for k in range(K))
+            assert mag[m, n] == pytest.approx(exact, rel=1e-13)
+    # planted: the magnitude of the group sums (|Σ|) is not the sum of magnitudes
+    out, _ = orc.reference_a8(Aq, a_s, q, s, K=K, N=N, G=G)
+    assert (mag > np.abs(out) * (1 + 1e-3)).any()
+
+
+@pytest.mark.parametrize("cfg", ZF_SMALL, ids=lambda c: c.name)
+def test_float_zero_magnitude_equals_the_exact_sum_of_absolute_terms(cfg):
+    inp = gq_synth.make_inputs(cfg, seed=5)
+    _, mag = orc.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                           N=cfg.N, G=cfg.G, w4=True, act=cfg.act, sc=cfg.sc, zp_float=True)
+    s, zf = _lib_decode(inp["scales"], cfg.sc), _lib_decode(inp["zeros"], cfg.sc)
+    A = _lib_act(inp, cfg.act)
+    q = inp["q"]
+    for m in range(A.shape[0]):
+        for n in range(cfg.N):
+            exact = sum((abs(Fraction(float(A[m, k])) *
+                             (int(q[k, n]) * Fraction(float(s[k // cfg.G, n])) -
+                              Fraction(float(zf[k // cfg.G, n]))))
+                         for k in range(cfg.K)), Fraction(0))
+            # W_hat = q·s − zf is formed in float64 first (one rounding per weight)
+            assert mag[m, n] == pytest.approx(float(exact), rel=1e-13)
+
+
+def test_fp8_magnitude_equals_the_exact_sum_of_absolute_terms():
+    rng = np.random.default_rng(21)
+    M, K, N = 2, 256, 136
+    A = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    W = rng.integers(0, 256, (N, K)).astype(np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0x38
+    W[(W & 0x7F) == 0x7F] = 0x38
+    a_s = rng.uniform(0.01, 0.1, (K // 128, M)).astype(np.float32)
+    w_s = rng.uniform(0.01, 0.1, (2, K // 128)).astype(np.float32)
+    _, mag = orc.fp8_block_gemm(A, a_s, W, w_s)
+    Af = torch.from_numpy(A).view(torch.float8_e4m3fn).double().numpy()
+    Wf = torch.from_numpy(W).view(torch.float8_e4m3fn).double().numpy()
+    for m in range(M):
+        for n in (0, 1, 127, 128, 135):
+            exact = sum((abs(Fraction(float(a_s[k // 128, m])) * Fraction(float(w_s[n // 128, k // 128])) *
+                             Fraction(float(Af[m, k])) * Fraction(float(Wf[n, k])))
+                         for k in range(K)), Fraction(0))
+            assert mag[m, n] == pytest.approx(float(exact), rel=1e-13)
+
+
+def test_silu_derivative_bound_is_tight():
+    """|silu'(x)| = |σ(x)·(1 + x·(1 − σ(x)))| peaks just below 1.1 (about 1.0998 near x ≈ 2.4),
+    so the factor 1.1 of the SiLU-and-mul magnitude is an upper bound, and 1.0 would not be.
+    The derivative is taken by central differences of silu itself."""
+    x = np.linspace(-30, 30, 600001)
+    h = 1e-6
+    d = (orc.silu(x + h) - orc.silu(x - h)) / (2 * h)
+    assert np.max(np.abs(d)) < 1.1
+    assert np.max(np.abs(d)) > 1.099
+
+
+def test_silu_mul_magnitude_bounds_the_propagated_gemm_error(monkeypatch):
+    """First-order propagation: if gate and up each carry an error up to ε·(their own mag),
+    silu(gate)·up moves by at most ε·mag_out (+ O(ε²)).  The gate and up values are planted
+    through a stand-in for the GEMM: worst-case signs, gate at the steepest point of silu."""
+    gvals = np.array([[2.3994, -1.0, 0.5, 8.0]])
+    uvals = np.array([[3.0, -2.0, 7.0, 0.25]])
+    mg = np.array([[40.0, 5.0, 2.0, 1.0]])
+    mu = np.array([[10.0, 3.0, 30.0, 2.0]])
+
+    def fake_reference(A_raw, codes, scales, zeros, *, K, N, G, w4, act, sc, rows=None, cols=None,
+                       zp_float=False):
+        cols = np.asarray(cols)
+        if cols[0] < N // 2:
+            return gvals[:, cols], mg[:, cols]
+        return uvals[:, cols - N // 2], mu[:, cols - N // 2]
+
+    monkeypatch.setattr(orc.gq_oracle, "reference", fake_reference)
+    ref, mag = orc.gq_oracle.silu_mul_reference(None, None, None, None, K=128, N=8, G=128,
+                                                act="bf16", sc="fp16")
+    eps = 1e-7
+    worst = np.zeros_like(ref)
+    for sg in (-1, 1):
+        for su in (-1, 1):
+            g2 = gvals + sg * eps * mg
+            u2 = uvals + su * eps * mu
+            worst = np.maximum(worst, np.abs(orc.silu(g2) * u2 - ref))
+    assert (worst <= eps * mag * (1 + 1e-4)).all()
+    # planted: without the 1.1 the bound fails at the steepest point of silu
+    mag_no_factor = mg * np.abs(uvals) + np.abs(orc.silu(gvals)) * mu
+    assert (worst > eps * mag_no_factor * (1 + 1e-4)).any()
+
+
+def test_dequantize_matches_the_element_by_element_loop():
+    cfg = gq_synth.Config("dq", M=1, K=128, N=16, G=32, zp=True, sc="bf16")
+    inp = gq_synth.make_weights(cfg, seed=3)
+    s = _lib_decode(inp["scales"], "bf16")
+    W = orc.dequantize(inp["q"].astype(np.int64), inp["z"].astype(np.int64), s, cfg.G)
+    brute = np.array(orc.dequantize_brute(inp["q"], inp["z"], s, cfg.G, cfg.K, cfg.N))
+    assert np.array_equal(W, brute)
+    # and the group GEMM is A @ W_hat (one product per weight, no reassociation in W_hat)
+    A = np.random.default_rng(1).standard_normal((3, cfg.K))
+    out = orc.group_gemm(A, inp["q"].astype(np.int64), inp["z"].astype(np.int64), s, cfg.G)
+    assert np.allclose(out, A @ W, rtol=1e-12, atol=1e-12)

@@ -1,7 +1,8 @@
 """gq_gemm_static_scratch: the entry point for callers that cannot allocate device memory
 (serving runtimes that reserve all memory up front, latency-critical loops, embedders with
 their own allocator).  It must give the same result as gq_gemm, call after call, while its
-scratch comes from a fixed array inside the library.
+scratch comes from a fixed array inside the library; both are checked against the float64
+oracle.
 
 This file is collected last on purpose, so that a run stopping at the first failure has
 already run every other test.
@@ -43,10 +44,11 @@ def test_static_scratch_matches_gq_gemm_twice(gq, cfg):
     ref = alloc_out(cfg.M, cfg.N, cfg.out)
     gq.gemm_t(A, packed, S, Z, ref, cfg.M, cfg.K, cfg.N, cfg.G, prec)
     stream = torch.cuda.current_stream().cuda_stream
-    _, mag = oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
-                              N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc,
-                              zp_float=cfg.zf)
-    ref64 = out_to_f64(ref, cfg.out)
+    want, mag = oracle.reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"], K=cfg.K,
+                                 N=cfg.N, G=cfg.G, w4=cfg.w4, act=cfg.act, sc=cfg.sc,
+                                 zp_float=cfg.zf)
+    bad, ratio = oracle.check(out_to_f64(ref, cfg.out), want, mag, cfg.out)
+    assert bad == 0, f"gq_gemm: {bad} elements out of tolerance against the oracle ({ratio:.3g})"
     for _ in range(2):
         got = alloc_out(cfg.M, cfg.N, cfg.out)
         st = gq.gq_gemm_static_scratch(cfg.M, cfg.K, cfg.N, cfg.G, prec, A.data_ptr(),
@@ -55,10 +57,12 @@ def test_static_scratch_matches_gq_gemm_twice(gq, cfg):
                                        got.data_ptr(), stream)
         assert st == 0, gq.gq_status_string(st)
         torch.cuda.synchronize()
-        bad, ratio = oracle.check(out_to_f64(got, cfg.out), ref64, mag, cfg.out)
-        assert bad == 0, f"{bad} elements differ from gq_gemm beyond tolerance ({ratio:.3g})"
+        # against the oracle first (a fault shared by both entry points must not pass), then
+        # bit for bit against gq_gemm (the same kernels, so the same bits)
+        bad, ratio = oracle.check(out_to_f64(got, cfg.out), want, mag, cfg.out)
+        assert bad == 0, f"{bad} elements out of tolerance against the oracle ({ratio:.3g})"
         view = torch.int16 if cfg.out == "bf16" else torch.int32
-        assert torch.equal(got.view(view), ref.view(view))      # same kernels, same bits
+        assert torch.equal(got.view(view), ref.view(view))
 
 
 def test_static_scratch_rejects_problems_larger_than_the_array(gq):
