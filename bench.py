@@ -148,9 +148,36 @@ print(json.dumps({{"calls": n, "seconds": time.perf_counter() - t0}}))
     return d, cores, None
 
 
+def _constants():
+    """The package's host-side constants module, loaded from its file: importing the package
+    itself would map libgq.so, which the oracle-timed arm must not load."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_gq_constants", os.path.join(ROOT, "group_quantized_weight_gb300", "constants.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
 def _sample_bytes(cfg, n_cols):
-    from group_quantized_weight_gb300.constants import algorithmic_bytes
-    return algorithmic_bytes(cfg.M, cfg.K, n_cols, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
+    return _constants().algorithmic_bytes(cfg.M, cfg.K, n_cols, cfg.G, cfg.w4, cfg.zp, cfg.act,
+                                          cfg.sc, cfg.out)
+
+
+def _pct(xs, q):
+    """Percentile q (0..100) of xs by linear interpolation between order statistics."""
+    ys = sorted(xs)
+    if not ys:
+        return None
+    pos = (len(ys) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
+def _copies_for(nbytes: int, l2_bytes: int, cap: int = 16) -> int:
+    """Rotated copies so that one round of them overflows L2 twice over: ceil(2·L2/bytes) + 1."""
+    return int(min(cap, -(-2 * l2_bytes // max(nbytes, 1)) + 1))
 
 
 def slowest_rank_ms(ms: float, world: int, dist, device="cpu") -> float:
@@ -295,17 +322,34 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
         graph.replay()
-    e1.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = slowest_rank_ms(e0.elapsed_time(e1), world, dist, dev)
+    ms = slowest_rank_ms(ev[0].elapsed_time(ev[-1]), world, dist, dev)
+    step_us = [1e3 * ev[i].elapsed_time(ev[i + 1]) / calls_per_step for i in range(args.steps)]
+    # five equal blocks of the timed steps: the median block and the spread of the steps
+    blocks = [statistics.fmean(step_us[i * len(step_us) // 5:(i + 1) * len(step_us) // 5])
+              for i in range(5)] if len(step_us) >= 5 else step_us
+    dist_us = {"median_of_5_blocks": statistics.median(blocks), "p10": _pct(step_us, 10),
+               "p90": _pct(step_us, 90), "unit": "us per gq_gemm call (graph-replayed)"}
+    # one host-launched call at a time (no graph, no overlap with a previous call)
+    single = []
+    for i in range(30):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s0.record(stream)
+        call(i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 5:
+            single.append(1e3 * s0.elapsed_time(s1))
+    dist_us["single_call_us"] = statistics.median(single)
     nbytes = algorithmic_bytes(cfg.M, cfg.K, cfg.N, cfg.G, cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out)
     launches = args.steps * calls_per_step
     kernel_us = 1e3 * ms / launches
@@ -342,7 +386,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": "w4_stripe_kernel", "peak_source": f"hbm_gbs of {peak_kind}",
-                     "kernel_us": kernel_us},
+                     "kernel_us": kernel_us, "kernel_us_distribution": dist_us},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -428,18 +472,18 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
     out = []
     side = torch.cuda.Stream()           # graph capture needs a stream other than the legacy one
     for name in ("tiny_gemv", "decode_gateup", "decode_gateup_silu", "q8_m1", "q8_m32",
-                 "q8a8_m1", "q8a8_m32", "asym_m16", "asym_m16_zf", "prefill"):
-        # decode_gateup_silu: the gate+up GEMV with the fused SiLU-and-mul epilogue
-        # (GQ_GATE_UP): the same weights, an output of N/2 columns.  q8a8_*: the Q8_0 shapes
+                 "q8a8_m1", "q8a8_m32", "asym_m16", "asym_m16_silu", "asym_m16_zf", "prefill"):
+        # decode_gateup_silu, asym_m16_silu: the gate+up shapes with the fused SiLU-and-mul
+        # epilogue (GQ_GATE_UP): the same weights, an output of N/2 columns.  q8a8_*: the Q8_0 shapes
         # with int8 activation codes and per-group scales (GQ_ACT_I8), quantized on the device
         # by gq_quantize_act before the timed calls.  asym_m16_zf: the asymmetric shape with
         # bf16 float zero points subtracted after scaling (GQ_ZP_FLOAT) in place of packed ones
-        fused = name == "decode_gateup_silu"
+        fused = name.endswith("_silu")
         a8 = name.startswith("q8a8")
         if name == "asym_m16_zf":
             cfg = gq_synth.CONFIGS["asym_m16"].replace(name=name, zp=False, zf=True)
         else:
-            cfg = gq_synth.CONFIGS["decode_gateup" if fused else name.replace("q8a8", "q8")]
+            cfg = gq_synth.CONFIGS[name[:-len("_silu")] if fused else name.replace("q8a8", "q8")]
         prec = prec_flags(cfg.w4, cfg.zp, cfg.act, cfg.sc, cfg.out, zf=cfg.zf) | GQ_STATIC_W
         if fused:
             prec |= GQ_GATE_UP
@@ -458,7 +502,7 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
             a_ptr, as_ptr = Aq.data_ptr(), As.data_ptr()
             nbytes += cfg.M * cfg.K * (1 - 4) + cfg.M * (cfg.K // cfg.G) * 4
         wbytes = packed.numel() + d["scales"].numel() * d["scales"].element_size()
-        copies = 1 if cfg.M >= 128 else int(max(1, min(8, -(-3 * L2_BYTES // max(wbytes, 1)))))
+        copies = 1 if cfg.M >= 128 else _copies_for(wbytes, L2_BYTES)
         W = [packed] + [packed.clone() for _ in range(copies - 1)]
         S = [d["scales"]] + [d["scales"].clone() for _ in range(copies - 1)]
         Z = None
@@ -467,7 +511,7 @@ def _all_configs(gq, torch, dev, peaks, peak_kind):
         odt = torch.float32 if cfg.out == "f32" else torch.bfloat16
         o = torch.empty((cfg.M, cfg.N // 2 if fused else cfg.N), dtype=odt, device=dev)
         big = cfg.M >= 128
-        res = gq.gq_bench(cfg.M, cfg.K, cfg.N, cfg.G, prec, a_ptr,
+        res = gq.gq_bench_calls(cfg.M, cfg.K, cfg.N, cfg.G, prec, a_ptr,
                           [w.data_ptr() for w in W], [x.data_ptr() for x in S],
                           [z.data_ptr() for z in Z] if Z else None, o.data_ptr(),
                           warmup=3, iters=10 if big else 200, use_graph=not big,
@@ -507,10 +551,13 @@ def _m_sweep(gq, torch, dev, peaks):
     packed = gq.pack_weights_t(codes, base.K, base.N, base.G, prec)
     S = torch.from_numpy(w["scales"].view(np.int16)).to(dev)
     del codes
-    copies = 4
+    # both sides rotate enough copies that each round of them overflows L2 twice over, so
+    # every call of either streams its weights from HBM
+    copies = _copies_for(packed.numel() + S.numel() * 2, L2_BYTES)
+    copies_d = _copies_for(base.N * base.K * 2, L2_BYTES)
     W = [packed] + [packed.clone() for _ in range(copies - 1)]
     Ss = [S] + [S.clone() for _ in range(copies - 1)]
-    Wd = [torch.randn(base.N, base.K, device=dev).to(torch.bfloat16) for _ in range(copies)]
+    Wd = [torch.randn(base.N, base.K, device=dev).to(torch.bfloat16) for _ in range(copies_d)]
     rows = []
     crossover = None
     stream = torch.cuda.Stream()         # graph capture needs a stream other than the legacy one
@@ -520,17 +567,17 @@ def _m_sweep(gq, torch, dev, peaks):
         A = torch.from_numpy(a.view(np.int16)).to(dev)
         o = torch.empty((M, base.N), dtype=torch.bfloat16, device=dev)
         iters = 200 if M <= 64 else (50 if M <= 512 else 10)
-        res = gq.gq_bench(M, base.K, base.N, base.G, prec, A.data_ptr(), [x.data_ptr() for x in W],
+        res = gq.gq_bench_calls(M, base.K, base.N, base.G, prec, A.data_ptr(), [x.data_ptr() for x in W],
                           [x.data_ptr() for x in Ss], None, o.data_ptr(), warmup=3, iters=iters,
                           use_graph=M < 128, stream=stream.cuda_stream)
         Ad = A.view(torch.bfloat16)
         for i in range(3):
-            torch.matmul(Ad, Wd[i % copies].t())
+            torch.matmul(Ad, Wd[i % copies_d].t())
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record()
         for i in range(iters):
-            torch.matmul(Ad, Wd[i % copies].t())
+            torch.matmul(Ad, Wd[i % copies_d].t())
         e1.record()
         torch.cuda.synchronize()
         dense_us = e0.elapsed_time(e1) * 1e3 / iters
@@ -542,8 +589,9 @@ def _m_sweep(gq, torch, dev, peaks):
     del W, Ss, Wd
     torch.cuda.empty_cache()
     return {"shape": "K=4096 N=14336 G=128 W4A16 sym fp16 scales vs torch.matmul bf16",
-            "weights": f"{copies} rotated copies of each (INT4 {copies * 29.4:.0f} MB, "
-                       f"BF16 {copies * 117.4:.0f} MB)",
+            "weights": f"rotated copies, ceil(2*L2/bytes)+1 of each: INT4 {copies} x 30.3 MB "
+                       f"= {copies * 30.3:.0f} MB, BF16 {copies_d} x 117.4 MB = "
+                       f"{copies_d * 117.4:.0f} MB (L2 {L2_BYTES / 2**20:.0f} MiB)",
             "crossover_M": crossover, "rows": rows}
 
 
@@ -559,7 +607,7 @@ def _prefill(gq, torch, dev, peaks, peak_kind):
     S = torch.from_numpy(w["scales"].view(np.int16)).to(dev)
     A = torch.from_numpy(a.view(np.int16)).to(dev)
     out = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
-    res = gq.gq_bench(cfg.M, cfg.K, cfg.N, cfg.G, prec, A.data_ptr(), [packed.data_ptr()],
+    res = gq.gq_bench_calls(cfg.M, cfg.K, cfg.N, cfg.G, prec, A.data_ptr(), [packed.data_ptr()],
                       [S.data_ptr()], None, out.data_ptr(), warmup=3, iters=10,
                       use_graph=False, stream=torch.cuda.current_stream().cuda_stream)
     us = res["us_per_call"]

@@ -57,9 +57,11 @@ _SIGS = {
     "gq_quantize_act": [_i, _i, _i, _i, _p, _p, _p, _p],
     "gq_gemm_fp8_block": [_i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_quantize_act_fp8": [_i, _i, _i, _p, _p, _p, _p],
-    "gq_bench": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
+    "gq_bench_calls": [ctypes.POINTER(gq_bench_args), ctypes.POINTER(gq_bench_result)],
+    "gq_bench": [ctypes.c_char_p, ctypes.c_char_p, _sz],
     "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
+    "gq_set_split_override": [_i],
     "gq_device_error": [_i],
     "gq_status_string": [_i],
     "gq_last_error_detail": [],
@@ -162,19 +164,34 @@ def gq_zsplit(units: int, nsplit: int, z: int):
     return b.value, e.value
 
 
+def gq_set_split_override(n: int) -> int:
+    """Force the K-slice count of the split-K paths (0 = planner's choice, -1 = the largest);
+    returns the previous setting."""
+    return _lib.gq_set_split_override(n)
+
+
 def gq_device_error(clear: bool = False) -> int:
     return _lib.gq_device_error(1 if clear else 0)
 
 
-def gq_bench(M, K, N, G, prec, A_ptr, Wq_ptrs, scales_ptrs, zeros_ptrs, out_ptr, *, warmup=3,
-             iters=100, use_graph=True, stream=None, a_scales_ptr=None) -> dict:
+def gq_bench(config: str, cap: int = 1 << 16):
+    """Self-contained benchmark of a named workload ("all" for every one); returns the parsed
+    JSON the library writes (a dict, or a list for "all")."""
+    import json
+    buf = ctypes.create_string_buffer(cap)
+    _check(_lib.gq_bench(config.encode(), buf, cap), "gq_bench")
+    return json.loads(buf.value.decode())
+
+
+def gq_bench_calls(M, K, N, G, prec, A_ptr, Wq_ptrs, scales_ptrs, zeros_ptrs, out_ptr, *,
+                   warmup=3, iters=100, use_graph=True, stream=None, a_scales_ptr=None) -> dict:
     n = len(Wq_ptrs)
     arr = _p * n
     args = gq_bench_args(M, K, N, G, prec, A_ptr, arr(*Wq_ptrs), arr(*scales_ptrs),
                          arr(*zeros_ptrs) if zeros_ptrs else None, n, out_ptr, warmup, iters,
                          1 if use_graph else 0, stream, a_scales_ptr)
     res = gq_bench_result()
-    _check(_lib.gq_bench(ctypes.byref(args), ctypes.byref(res)), "gq_bench")
+    _check(_lib.gq_bench_calls(ctypes.byref(args), ctypes.byref(res)), "gq_bench_calls")
     return {"us_per_call": res.us_per_call, "launches_per_call": res.launches_per_call}
 
 

@@ -279,16 +279,21 @@ __global__ void __launch_bounds__(kA8Threads, 2) q8a8_kernel(const A8Params p) {
 // K slices: up to 8 rows the fewest whose shared memory fits two CTAs per SM (load-latency
 // bound); above, the fewest waves of two CTAs per SM with 5% charged per slice.  Every warp of
 // a split CTA keeps a group.
-int q8a8_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
+int q8a8_slices(int M, int K, int N, int G, int sms, size_t part_cap, int forced) {
   const int Mb = M < kA8MaxRows ? M : kA8MaxRows;
   const int groups = K / G, kp = kA8Warps / a8_rb(Mb);
   const long ctas1 = (long)((N + kA8Cols - 1) / kA8Cols) * ((M + kA8MaxRows - 1) / kA8MaxRows);
-  int best = 0;
+  int best = 0, largest = 0;
   double best_cost = 0.0;
   for (int ks = 1; ks <= groups; ++ks) {
     if (ks > 1 && groups / ks < kp) break;
     if (ks > 1 && (size_t)ks * M * N * 4 > part_cap) break;
     if (a8_smem_bytes(Mb, K, G, ks) > kA8SmemCap) continue;
+    largest = ks;
+    if (forced != 0) {
+      if (forced == ks) return ks;
+      continue;
+    }
     if (Mb <= 8) return ks;
     const long waves = (ctas1 * ks + 2L * sms - 1) / (2L * sms);
     const double cost = (double)waves / ks * (1.0 + 0.05 * ks);
@@ -297,7 +302,8 @@ int q8a8_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
       best_cost = cost;
     }
   }
-  return best;
+  if (forced == -1) return largest;
+  return forced != 0 ? 0 : best;
 }
 
 size_t q8a8_smem_bytes(int M, int K, int G, int KS) {

@@ -1,5 +1,6 @@
 // C ABI of libgq: argument validation, the launch plan (path choice, split-K), scratch
 // management and the timing harness.  The compute itself lives in the kernel files.
+#include <atomic>
 #include <mutex>
 #include <string.h>
 #include <vector>
@@ -11,6 +12,10 @@
 namespace gq {
 
 static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// gq_set_split_override: process-wide, read at plan time
+static std::atomic<int> g_split_override{0};
+int split_override() { return g_split_override.load(std::memory_order_relaxed); }
 static inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -93,7 +98,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     return GQ_ERR_UNSUPPORTED;
   // W8A8 (GQ_ACT_I8): integer group dots, 64 columns x one K slice x 32 rows per CTA
   if (prec & GQ_ACT_I8) {
-    const int ks = q8a8_slices(Mc, K, Nc, G, sms, kPartCap);
+    const int ks = q8a8_slices(Mc, K, Nc, G, sms, kPartCap, split_override());
     if (ks < 1) return GQ_ERR_UNSUPPORTED;
     p->path = kPathQ8A8;
     p->m_tile = Mc < 32 ? Mc : 32;
@@ -115,13 +120,56 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->workspace_bytes = p->part_bytes + p->counter_bytes;
     return GQ_OK;
   }
+  // warp-specialized decode (M <= 4): one CTA per SM (a producer warp streaming stages of
+  // slots, consumer warps decoding them) over equal slot ranges with a cross-CTA reduction,
+  // for problems with fewer 16-column tiles than SMs (latency-bound: its shorter prologue and
+  // two CTAs per SM make it the faster there); larger ones stay on the striped kernel below
+  int gv_nc = 0, gv_stages = 0, gv_cps = 0;
+  const bool gv_whole = ceil_div(Nc, kTileN) >= sms;
+  if (!gv_whole && gemv_supported(Mc, K, G, prec) &&
+      gemv_config(Mc, K, G, prec, kCtaSmemCap, &gv_nc, &gv_stages, &gv_cps) == GQ_OK) {
+    {
+      p->path = kPathGemv;
+      p->mt = 1;
+      p->m_tile = 4;
+      p->n_tile = kTileN;
+      p->unit_k = stripe_slot_k();
+      const int T = ceil_div(Nc, kTileN), spt = K / p->unit_k;
+      p->units = T * spt;
+      p->slots = gv_stages;
+      p->ctas_per_sm = gv_cps;
+      p->consumers = gv_nc;
+      p->block_threads = (gv_nc + 1) * 32;
+      p->smem_bytes = gemv_smem_bytes(Mc, K, G, prec, gv_nc, gv_stages);
+      p->grid_y = p->grid_z = 1;
+      const int per = ceil_div(T, sms);
+      if (T >= sms && (double)T >= 0.9 * (double)sms * per) {
+        p->grid_x = sms;
+        p->split_count = T;
+        p->split_mult = spt;
+        p->workspace_bytes = 0;
+      } else {
+        // equal slot ranges: at least two slots per consumer warp, at most one CTA per SM
+        int grid = ceil_div(p->units, 2 * gv_nc);
+        if (grid > sms) grid = sms;
+        p->grid_x = grid;
+        p->split_count = p->units;
+        p->split_mult = 1;
+        p->part_bytes = round_up((size_t)grid * 2 * 4 * kTileN * sizeof(float), 256);
+        p->counter_bytes = kCounterRegionBytes;
+        if ((size_t)T * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
+        p->workspace_bytes = p->part_bytes + p->counter_bytes;
+      }
+      p->nsplit = p->grid_x;
+      return GQ_OK;
+    }
+  }
   // striped persistent decode (M <= 8): one CTA of kStrWarps warps per SM over a
   // contiguous range of (tile, 256-k slot) pairs; whole tiles per CTA when that keeps the
   // SMs within 10% of even, else equal slot ranges with a cross-CTA reduction
   const int slots = stripe_supported(Mc, K, G, prec) && !(prec & GQ_ZP_FLOAT)
                         ? stripe_slots_for(Mc, K, G, prec, kCtaSmemCap)
                         : 0;
-  if ((prec & GQ_GATE_UP) && slots < 2) return GQ_ERR_UNSUPPORTED;   // striped kernel only
   if (slots >= 2) {
     p->path = kPathStripe;
     p->mt = Mc <= 4 ? 1 : 2;   // MMA blocks
@@ -146,7 +194,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       p->grid_x = grid;
       p->split_count = p->units;
       p->split_mult = 1;
-      p->part_bytes = round_up((size_t)grid * 8 * kTileN * sizeof(float), 256);
+      p->part_bytes = round_up((size_t)grid * 2 * 8 * kTileN * sizeof(float), 256);
       p->counter_bytes = kCounterRegionBytes;
       if ((size_t)T * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
       p->workspace_bytes = p->part_bytes + p->counter_bytes;
@@ -156,9 +204,11 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   }
   // INT8 codes, 5 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 4
   // rows the CUDA-core kernel below is faster: it is load-latency-bound there)
-  if (Mc > 4 && Mc <= 32 && q8_mma_supported(Mc, K, G, prec)) {
-    const int ks = q8_mma_slices(Mc, K, Nc, G, sms, kPartCap);
-    if (ks >= 1) {
+  if (Mc > 4 && Mc <= 32 && q8_mma_supported(Mc, K, G, prec) &&
+      q8_mma_slices(Mc, K, Nc, G, sms, kPartCap, 0) >= 1) {
+    const int ks = q8_mma_slices(Mc, K, Nc, G, sms, kPartCap, split_override());
+    if (ks < 1) return GQ_ERR_UNSUPPORTED;   // a forced count this kernel cannot take
+    {
       p->path = kPathQ8Mma;
       p->m_tile = (Mc + 7) / 8 * 8;
       p->mt = (Mc + 7) / 8;
@@ -181,9 +231,11 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     }
   }
   // INT8 codes, M <= 32: CUDA-core FP32 kernel, 64 columns x one K slice per CTA
-  if (Mc <= kQ8BlockMaxM && q8_block_supported(Mc, K, G, prec)) {
-    const int ks = q8_block_slices(Mc, K, Nc, G, sms, kPartCap);
-    if (ks >= 1) {
+  if (Mc <= kQ8BlockMaxM && q8_block_supported(Mc, K, G, prec) &&
+      q8_block_slices(Mc, K, Nc, G, sms, kPartCap, 0) >= 1) {
+    const int ks = q8_block_slices(Mc, K, Nc, G, sms, kPartCap, split_override());
+    if (ks < 1) return GQ_ERR_UNSUPPORTED;   // a forced count this kernel cannot take
+    {
       p->path = kPathQ8Block;
       p->m_tile = Mc;
       p->n_tile = q8_block_cols();
@@ -204,7 +256,10 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       return GQ_OK;
     }
   }
-  if (M >= kPrefillMinM && !(prec & GQ_ZP_FLOAT) && prefill_supported(M, K, N, G, prec)) {
+  // the fused gate+up epilogue lives in the decode and small-batch kernels only
+  const bool gate_up = (prec & GQ_GATE_UP) != 0;
+  if (!gate_up && M >= kPrefillMinM && !(prec & GQ_ZP_FLOAT) &&
+      prefill_supported(M, K, N, G, prec)) {
     // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
     p->path = kPathPrefill;
     p->m_tile = 256;
@@ -224,7 +279,16 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   // range) pairs, activation
   // slices in shared memory, slices added by the last CTA of each tile range
   if (Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)) {
-    const int ksl = batch_slice_k(Mc, K);
+    int ksl = batch_slice_k(Mc, K);
+    const int forced = split_override();
+    if (forced != 0 && batch_slots_for(Mc, ksl, G, prec, kCtaSmemCap) >= 2) {
+      // a forced slice count: K/forced must be a whole number of 256-k slots
+      const int slots_k = K / 256, fs = forced == -1 ? slots_k : forced;
+      if (fs < 1 || fs > slots_k || slots_k % fs != 0) return GQ_ERR_UNSUPPORTED;
+      ksl = K / fs;
+      if (batch_slots_for(Mc, ksl, G, prec, kCtaSmemCap) < 2) return GQ_ERR_UNSUPPORTED;
+      if (fs > 1 && (size_t)fs * Mc * Nc * 4 > kPartCap) return GQ_ERR_UNSUPPORTED;
+    }
     const int slots = batch_slots_for(Mc, ksl, G, prec, kCtaSmemCap);
     // split K needs one arrival counter per (row block, 16-column tile)
     const bool ctr_ok = K == ksl || (size_t)ceil_div(Mc, 32) * ceil_div(Nc, kTileN) *
@@ -255,7 +319,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
       return GQ_OK;
     }
   }
-  if (prec & GQ_ZP_FLOAT) return GQ_ERR_UNSUPPORTED;
+  if (prec & (GQ_ZP_FLOAT | GQ_GATE_UP)) return GQ_ERR_UNSUPPORTED;
   if (prec & GQ_W4) {
     p->path = kPathMmaDecode;
     const int rows = Mc < 8 * kDecMaxMT ? Mc : 8 * kDecMaxMT;
@@ -270,6 +334,13 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     const int rows_staged = Mc < p->m_tile ? Mc : p->m_tile;
     p->nsplit = choose_nsplit(p->grid_x * p->grid_z, p->units, p->unit_k, target,
                               (size_t)rows_staged * 2, kSmemCap, (size_t)Mc * Nc * 4, kPartCap);
+    if (split_override() != 0) {
+      const int fs = split_override() == -1 ? p->units : split_override();
+      if (fs < 1 || fs > p->units || (size_t)fs * Mc * Nc * 4 > kPartCap ||
+          (size_t)ceil_div(p->units, fs) * p->unit_k * rows_staged * 2 > kSmemCap)
+        return GQ_ERR_UNSUPPORTED;
+      p->nsplit = fs;
+    }
     const int widest = ceil_div(p->units, p->nsplit) * p->unit_k;
     p->smem_bytes = (size_t)rows_staged * (widest / kChunkK * 32 + 16) * 4;
   } else {
@@ -290,6 +361,13 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     if (cap > kPartCap) cap = kPartCap;
     p->nsplit = choose_nsplit(p->grid_x * p->grid_z, p->units, p->unit_k, target,
                               (size_t)rows_staged * 4, kSmemCap, (size_t)Mc * Nc * 4, cap);
+    if (split_override() != 0) {
+      const int fs = split_override() == -1 ? p->units : split_override();
+      if (fs < 1 || fs > p->units || (size_t)fs * Mc * Nc * 4 > kPartCap ||
+          (size_t)ceil_div(p->units, fs) * p->unit_k * rows_staged * 4 > kSmemCap)
+        return GQ_ERR_UNSUPPORTED;
+      p->nsplit = fs;
+    }
     const int widest = ceil_div(p->units, p->nsplit) * p->unit_k;
     p->smem_bytes = (size_t)rows_staged * widest * 4;
   }
@@ -303,6 +381,25 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   }
   p->workspace_bytes = p->part_bytes + p->counter_bytes;
   return GQ_OK;
+}
+
+// Bytes of arrival counters the kernels of plan p index (a prefix of the counter region);
+// 0 when the plan uses none.
+size_t plan_counter_bytes_used(const Plan &p, int N) {
+  if (p.counter_bytes == 0) return 0;
+  const int Nc = N > 0 ? N : 8;
+  size_t n = 0;
+  switch (p.path) {
+    case kPathQ8A8: n = (size_t)p.grid_z * ceil_div(Nc, 64); break;
+    case kPathStripe:
+    case kPathGemv: n = (size_t)ceil_div(Nc, kTileN); break;
+    case kPathQ8Mma: n = (size_t)ceil_div(Nc, 64); break;
+    case kPathQ8Block: n = (size_t)ceil_div(Nc, p.n_tile); break;
+    case kPathBatch: n = (size_t)p.grid_z * ceil_div(Nc, kTileN); break;
+    default: n = (size_t)p.grid_x * p.grid_z; break;
+  }
+  const size_t b = round_up(n * sizeof(unsigned), 16);
+  return b < p.counter_bytes ? b : p.counter_bytes;
 }
 
 // ------------------------------------------------------------------ scratch per device
@@ -358,6 +455,8 @@ cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, con
   switch (p.path) {
     case kPathPrefill:
       return launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
+    case kPathGemv:
+      return launch_gemv(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
     case kPathStripe:
       return launch_stripe_decode(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part,
                                   counters, s);
@@ -405,6 +504,11 @@ const char *gq_status_string(int status) {
     case GQ_ERR_NO_DEVICE: return "no usable CUDA device";
     default: return "unknown status";
   }
+}
+
+int gq_set_split_override(int n) {
+  if (n < -1) return -2;
+  return g_split_override.exchange(n);
 }
 
 int gq_zsplit(int units, int nsplit, int z, int *begin, int *end) {
@@ -505,8 +609,10 @@ static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,
                         const void *a_scales, const void *Wq, const void *scales, void *out,
                         void *stream);
 
-static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
-                     const void *scales, const void *zeros, void *out, void *stream) {
+}  // extern "C"
+
+int gq::gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
+                  const void *scales, const void *zeros, void *out, void *stream) {
   if (prec & GQ_ACT_I8) return GQ_ERR_INVALID_ARG;   // needs the activation scales: gq_gemm_a8
   int st = validate(M, K, N, G, prec);
   if (st != GQ_OK) return st;
@@ -537,6 +643,8 @@ static int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const 
   }
   return GQ_OK;
 }
+
+extern "C" {
 
 int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
             const void *scales, const void *zeros, void *out, void *stream) {
@@ -600,7 +708,7 @@ int gq_quantize_act(int M, int K, int G, int prec, const void *A, void *Aq, void
   return GQ_OK;
 }
 
-int gq_bench(const gq_bench_args *a, gq_bench_result *r) {
+int gq_bench_calls(const gq_bench_args *a, gq_bench_result *r) {
   if (!a || !r || a->n_copies < 1 || a->iters < 1 || a->warmup < 0 || !a->Wq || !a->scales)
     return GQ_ERR_INVALID_ARG;
   if ((a->prec & (GQ_ZP | GQ_ZP_FLOAT)) && !a->zeros) return GQ_ERR_INVALID_ARG;
@@ -676,7 +784,8 @@ int gq_device_error(int clear) {
   const int w = stripe_read_error(clear);
   const int x = batch_read_error(clear);
   const int y = fp8_read_error(clear);
-  return v != 0 ? v : (w != 0 ? w : (x != 0 ? x : y));
+  const int g = gemv_read_error(clear);
+  return v != 0 ? v : (w != 0 ? w : (x != 0 ? x : (y != 0 ? y : g)));
 }
 
 int gq_quantize_act_fp8(int M, int K, int prec, const void *A, void *Aq, void *a_scales,

@@ -84,6 +84,7 @@ cudaError_t launch_batch(const Plan &pl, int M, int K, int N, int G, int prec, c
   bp.S = pl.slots;
   bp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   bp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
+  bp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
   if (prec & GQ_ZP_FLOAT) return launch_batch_zf(pl, prec, G, bp, s);
   switch (G) {
     case 32: return launch_bt_g<32>(pl, prec, bp, s);

@@ -132,6 +132,8 @@ struct BtParams {
   int S;                      // ring slots per warp
   int out_f32;
   int static_w;               // weights may be read before the preceding kernel ends
+  int gate_up;                // fused gate+up: tile t holds gate columns 8t.. and up columns
+                              // N/2 + 8t..; out[m][8t + r] = silu(gate) * up, [M][N/2]
 };
 
 // Warps per CTA for MT 8-row MMA blocks of activations: as many as the registers allow
@@ -235,11 +237,17 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
     if (lane < NL) {
       // 16 bytes of group (j * GPS + lg)'s scales of the tile's columns; a ragged last tile
       // (8 columns) copies only the parts inside its columns
+      // (gate+up: the first 8 columns' parts from the gate columns 8 ht.., the others from
+      // the up columns N/2 + 8 ht..)
+      const size_t col_bytes =
+          !p.gate_up ? (size_t)ht * kTileN * ES + lp * 16
+          : lp * 16 < 8 * ES ? (size_t)8 * ht * ES + lp * 16
+                             : (size_t)(N / 2 + 8 * ht) * ES + (lp * 16 - 8 * ES);
       if (lp * 16 < min(kTileN, N - ht * kTileN) * ES)
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                          dst + kBtSlotCodes + lg * 16 * ES + lp * 16),
                      "l"(reinterpret_cast<const uint8_t *>(p.scales) + (size_t)(j * GPS + lg) * srow +
-                         (size_t)ht * kTileN * ES + lp * 16)
+                         col_bytes)
                      : "memory");
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
     }
@@ -327,8 +335,10 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
 #pragma unroll
     for (int gi = 0; gi < GPS; ++gi) {
       const uint32_t *row = p.zeros + (size_t)((ks * SPS + jz) * GPS + gi) * NW;
-      zn[gi][0] = __ldg(row + min(2 * tz, NW - 1));
-      zn[gi][1] = __ldg(row + min(2 * tz + 1, NW - 1));
+      // the words of the tile's columns r0 and r0 + 8 (gate+up: gate word tz, up word
+      // N/16 + tz)
+      zn[gi][0] = __ldg(row + min(p.gate_up ? tz : 2 * tz, NW - 1));
+      zn[gi][1] = __ldg(row + min(p.gate_up ? NW / 2 + tz : 2 * tz + 1, NW - 1));
     }
   };
   // float zero points of slot jz (of the slice) of tile tz: the raw bits for this lane's
@@ -455,7 +465,24 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
     }
     // D fragment: e = 0, 1 -> column 16 t + r0, e = 2, 3 -> column 16 t + r0 + 8; rows
     // m0 + 8 mt + 2 q + (e & 1)
+    // gate+up: e = 0, 1 hold gate column 8 t + r0 of rows 2 q, 2 q + 1 and e = 2, 3 the matching
+    // up column, so each lane stores silu(gate) * up for two rows of out [M][N/2]
+    auto store_pairs = [&](const float (&v)[MT][4]) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ml = 8 * mt + 2 * q + e;
+          if (ml < Mb)
+            store_out_rt(p.out, (size_t)(m0 + ml) * (N / 2) + 8 * t + r0,
+                         silu_mul(v[mt][e], v[mt][e + 2]), p.out_f32 != 0);
+        }
+    };
     if (!split) {
+      if (p.gate_up) {
+        store_pairs(acc);
+        continue;
+      }
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -488,21 +515,24 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
     }
     if (!__shfl_sync(0xffffffffu, last, 0)) continue;
     __threadfence();
+    float tot[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int n = t * kTileN + r0 + 8 * (e >> 1);
         const int ml = 8 * mt + 2 * q + (e & 1);
+        float sum = 0.f;
         if (n < N && ml < Mb) {
           const size_t o = (size_t)(m0 + ml) * N + n;
-          float sum = 0.f;
 #pragma unroll 4
           for (int s2 = 0; s2 < p.KS; ++s2)
             sum += s2 == ks ? acc[mt][e] : __ldcg(p.part + (size_t)s2 * M * N + o);
-          store_out_rt(p.out, o, sum, p.out_f32 != 0);
+          if (!p.gate_up) store_out_rt(p.out, o, sum, p.out_f32 != 0);
         }
+        tot[mt][e] = sum;
       }
+    if (p.gate_up) store_pairs(tot);
   }
 }
 

@@ -127,6 +127,60 @@ __device__ __forceinline__ void store_out_rt(void *out, size_t idx, float v, boo
     reinterpret_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
 }
 
+// ------------------------------------------------------------------ FP16 decode and MMA
+// (the striped and warp-specialized small-M kernels)
+
+__device__ __forceinline__ void mma_16816_f16(float d[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// the same MMA with a zero accumulator input (the first step of a group)
+__device__ __forceinline__ void mma_16816_f16_zc(float d[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// (a & MASK) | c in one LOP3: the mask is an immediate of the instruction and c a register
+// (with both constants taken from memory operands the compiler emits two instructions)
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(c));
+  return r;
+}
+
+// x * 2^e for e in [-174, 127], rounded once.  2^e is a normal float for e >= -126; below
+// that, x is first scaled by 2^-64 (exact unless |x| < 2^-62, in which case the result is
+// below 2^-188 and rounds to zero either way) and then by 2^(e + 64).
+__device__ __forceinline__ float scale_pow2(float x, int e) {
+  if (e >= -126) return x * __int_as_float((127 + e) << 23);
+  return x * __int_as_float((127 - 64) << 23) * __int_as_float((127 + 64 + e) << 23);
+}
+
+// silu(g) * u = g / (1 + e^-g) * u in FP32 (CUDA's expf and IEEE division)
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
 // Shared-memory image of the CTA's activation slice, permuted so that lane (m, q) gets
 // the B operands of four consecutive 16-k MMA steps with two 16-byte loads:
 //   word(m, chunk c, half h2, q, e) = A[m][kb + 64c + 16(2*h2 + e/2) + 8(e%2) + 2q .. +1]

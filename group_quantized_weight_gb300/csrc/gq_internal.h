@@ -38,7 +38,7 @@ constexpr int kQ8MaxRows = 32;
 constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
 
 enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3,
-            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6, kPathQ8A8 = 7 };
+            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6, kPathQ8A8 = 7, kPathGemv = 8 };
 
 struct Plan {
   int path;
@@ -55,14 +55,24 @@ struct Plan {
   size_t counter_bytes;  // arrival counters
   size_t workspace_bytes;
   int split_count, split_mult;   // path 3: CTA c owns slots zsplit(split_count, grid, c) * split_mult
-  int slots;                     // path 3: ring slots per warp
+  int slots;                     // path 3: ring slots per warp; path 8: ring stages
+  int ctas_per_sm;               // path 8: CTAs that fit on one SM (2 lets calls overlap)
+  int consumers;                 // path 8: consumer warps per CTA
 };
 
 // scale / output type codes used as template parameters
 enum ScaleType { kScF16 = 0, kScBF16 = 1, kScF32 = 2 };
 
 int validate(int M, int K, int N, int G, int prec);
+// The K-slice count forced by gq_set_split_override (0 = the planner's own choice, -1 = the
+// largest count the path supports, n > 0 = exactly n).  The slice choosers take it as
+// `forced` and return 0 when the path cannot take that count.
+int split_override();
 int make_plan(int M, int K, int N, int G, int prec, int sm_count, Plan *p);
+size_t plan_counter_bytes_used(const Plan &p, int N);
+// the body of gq_gemm (validation, plan, scratch, launch)
+int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
+              const void *scales, const void *zeros, void *out, void *stream);
 size_t packed_bytes(int K, int N, int prec);
 int device_sm_count(int *sms);
 
@@ -75,6 +85,16 @@ cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int pre
                               const void *A, const void *Wq, const void *scales,
                               const void *zeros, void *out, float *part,
                               unsigned *counters, cudaStream_t s);
+// warp-specialized small-M decode kernel (M <= 4): a producer warp and kGemvConsumers
+// consumer warps per CTA
+bool gemv_supported(int M, int K, int G, int prec);
+int gemv_config(int M, int K, int G, int prec, size_t smem_cap, int *consumers, int *stages,
+                int *ctas_per_sm);
+size_t gemv_smem_bytes(int M, int K, int G, int prec, int consumers, int stages);
+cudaError_t launch_gemv(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                        const void *Wq, const void *scales, const void *zeros, void *out,
+                        float *part, unsigned *counters, cudaStream_t s);
+int gemv_read_error(int clear);
 bool stripe_supported(int M, int K, int G, int prec);
 size_t stripe_smem_bytes(int M, int K, int G, int prec, int slots);
 int stripe_slots_for(int M, int K, int G, int prec, size_t smem_cap);
@@ -118,7 +138,7 @@ cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec
 constexpr int kQ8BlockMaxM = 32;
 bool q8_block_supported(int M, int K, int G, int prec);
 size_t q8_block_smem_bytes(int M, int K, int G, int KS);
-int q8_block_slices(int M, int K, int N, int G, int sms, size_t part_cap);
+int q8_block_slices(int M, int K, int N, int G, int sms, size_t part_cap, int forced);
 int q8_block_cols();
 int q8_block_threads();
 cudaError_t launch_q8_block(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
@@ -127,14 +147,14 @@ cudaError_t launch_q8_block(const Plan &p, int M, int K, int N, int G, int prec,
 // INT8 on BF16 tensor cores (codes exact, fp32 activations as three exact BF16 parts)
 bool q8_mma_supported(int M, int K, int G, int prec);
 size_t q8_mma_smem_bytes(int M, int K, int G, int KS);
-int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap);
+int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap, int forced);
 cudaError_t launch_q8_mma(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                           const void *Wq, const void *scales, void *out, float *part,
                           unsigned *counters, cudaStream_t s);
 // INT8-activation variant (W8A8): the dynamic activation quantizer and the integer group GEMM
 cudaError_t launch_quantize_act(int M, int K, int G, bool f32, const void *A, int8_t *Aq,
                                 float *a_scales, cudaStream_t s);
-int q8a8_slices(int M, int K, int N, int G, int sms, size_t part_cap);
+int q8a8_slices(int M, int K, int N, int G, int sms, size_t part_cap, int forced);
 size_t q8a8_smem_bytes(int M, int K, int G, int KS);
 cudaError_t launch_q8a8(const Plan &p, int M, int K, int N, int G, int prec, const int8_t *Aq,
                         const float *As, const void *Wq, const void *scales, void *out,

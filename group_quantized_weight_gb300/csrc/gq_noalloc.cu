@@ -76,8 +76,11 @@ extern "C" int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, cons
   cudaStream_t s = (cudaStream_t)stream;
   unsigned *counters = (unsigned *)ws;
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
-  // the arrival counters must start at zero; the array keeps the previous call's contents
-  if (ws && cudaMemsetAsync(counters, 0, p.counter_bytes, s) != cudaSuccess) {
+  // the arrival counters this plan indexes must start at zero; the array keeps the previous
+  // call's contents (the kernels leave their counters at zero, but a call cut short by a
+  // device-side timeout may not)
+  const size_t ctr = plan_counter_bytes_used(p, N);
+  if (ctr && cudaMemsetAsync(counters, 0, ctr, s) != cudaSuccess) {
     cudaGetLastError();
     return GQ_ERR_CUDA;
   }

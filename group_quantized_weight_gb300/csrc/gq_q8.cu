@@ -553,15 +553,20 @@ size_t q8_mma_smem_bytes(int M, int K, int G, int KS) {
 
 // K slices: as for the CUDA-core kernel, counted against this kernel's shared memory and
 // its two K parts per CTA.
-int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
+int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap, int forced) {
   const int groups = K / G;
   const int nb = (N + 63) / 64;
-  int best = 0;
+  int best = 0, largest = 0;
   double best_cost = 0.0;
   for (int ks = 1; ks <= groups; ++ks) {
     if (ks > 1 && groups / ks < 2) break;          // both K parts keep a group
     if (ks > 1 && (size_t)ks * M * N * 4 > part_cap) break;
     if (q8_mma_smem_bytes(M, K, G, ks) > kQbSmemCap) continue;
+    largest = ks;
+    if (forced != 0) {
+      if (forced == ks) return ks;
+      continue;
+    }
     if (M <= 8) return ks;
     const long waves = ((long)nb * ks + 2L * sms - 1) / (2L * sms);
     const double cost = (double)waves / ks * (1.0 + 0.05 * ks);
@@ -570,7 +575,8 @@ int q8_mma_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
       best_cost = cost;
     }
   }
-  return best;
+  if (forced == -1) return largest;
+  return forced != 0 ? 0 : best;
 }
 
 cudaError_t launch_q8_mma(const Plan &pl, int M, int K, int N, int G, int prec, const void *A,
@@ -624,15 +630,20 @@ int q8_block_threads() { return kQbThreads; }
 // extra wave of CTAs pays again: the fewest slices that fit.  Above 8 rows it is bound by
 // the FP32 pipes: the count with the least work per SM counted in waves of two CTAs per SM,
 // each slice charged 5% for its partial sums and its CTAs' fixed costs (fewer on ties).
-int q8_block_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
+int q8_block_slices(int M, int K, int N, int G, int sms, size_t part_cap, int forced) {
   const int groups = K / G, rb = q8_rb(M), kp = kQbWarps / rb;
   const int nb = (N + kQbCols - 1) / kQbCols;
-  int best = 0;
+  int best = 0, largest = 0;
   double best_cost = 0.0;
   for (int ks = 1; ks <= groups; ++ks) {
     if (ks > 1 && groups / ks < kp) break;        // a CTA's warps would run out of groups
     if (ks > 1 && (size_t)ks * M * N * 4 > part_cap) break;
     if (q8_block_smem_bytes(M, K, G, ks) > kQbSmemCap) continue;
+    largest = ks;
+    if (forced != 0) {
+      if (forced == ks) return ks;
+      continue;
+    }
     if (M <= 8) return ks;
     const long waves = ((long)nb * ks + 2L * sms - 1) / (2L * sms);
     const double cost = (double)waves / ks * (1.0 + 0.05 * ks);
@@ -641,7 +652,8 @@ int q8_block_slices(int M, int K, int N, int G, int sms, size_t part_cap) {
       best_cost = cost;
     }
   }
-  return best;
+  if (forced == -1) return largest;
+  return forced != 0 ? 0 : best;
 }
 
 cudaError_t launch_q8_block(const Plan &pl, int M, int K, int N, int G, int prec, const void *A,

@@ -52,54 +52,6 @@ constexpr long long kStripeWaitCycles = 4000000000ll;   // bounded waits: about 
 // read by the host through stripe_read_error.
 static __device__ int g_stripe_error;
 
-__device__ __forceinline__ void mma_16816_f16(float d[4], uint32_t a0, uint32_t a1,
-                                              uint32_t a2, uint32_t a3, uint32_t b0,
-                                              uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// the same MMA with a zero accumulator input (the first step of a group)
-__device__ __forceinline__ void mma_16816_f16_zc(float d[4], uint32_t a0, uint32_t a1,
-                                                 uint32_t a2, uint32_t a3, uint32_t b0,
-                                                 uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
-}
-
-__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
-// (a & MASK) | c in one LOP3: the mask is an immediate of the instruction and c a register
-// (with both constants taken from memory operands the compiler emits two instructions)
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t c) {
-  uint32_t r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "r"(c));
-  return r;
-}
-
-// x * 2^e for e in [-174, 127], rounded once.  2^e is a normal float for e >= -126; below
-// that, x is first scaled by 2^-64 (exact unless |x| < 2^-62, in which case the result is
-// below 2^-188 and rounds to zero either way) and then by 2^(e + 64).
-__device__ __forceinline__ float scale_pow2(float x, int e) {
-  if (e >= -126) return x * __int_as_float((127 + e) << 23);
-  return x * __int_as_float((127 - 64) << 23) * __int_as_float((127 + 64 + e) << 23);
-}
-
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -127,9 +79,6 @@ __device__ __forceinline__ bool slot_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// silu(g) * u = g / (1 + e^-g) * u in FP32 (CUDA's expf and IEEE division)
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
-
 // decode constants (fp16x2 bit patterns)
 constexpr uint32_t kMagic = 0x64006400u;       // 1024 in both halves
 constexpr uint32_t kSixteenth = 0x2C002C00u;   // 1/16
@@ -142,7 +91,8 @@ struct StripeParams {
   const void *scales;         // [K/G][N]
   const uint32_t *zeros;      // [K/G][N/8] or NULL
   void *out;                  // [M][N]
-  float *part;                // [gridDim.x][8][16] per-CTA partial sums (shared tiles only)
+  float *part;                // [gridDim.x][2][8][16] per-CTA partial sums of the tile a CTA
+                              // starts inside and the tile it ends inside (shared tiles only)
   unsigned *counters;         // per-tile arrival counters (shared tiles only)
   int M, K, N;
   int split_count, split_mult;   // CTA c owns slots zsplit(split_count, grid, c) * split_mult
@@ -533,6 +483,7 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
   // A tile is reduced by the lowest warp of the CTA that holds part of it: this warp for its
   // first tile unless a lower warp ends inside that tile, and for its last tile when that
   // differs from its first.  A share that covers a whole tile was stored already.
+  __shared__ int s_last[kStrWarps];
   for (int pass = 0; pass < 2 && n > 0; ++pass) {
     const int tt = pass == 0 ? t_first : (we - 1) / SPT;
     if (pass == 1 && tt == t_first) break;
@@ -540,7 +491,9 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
     if (max(tb, wb) == tb && min(te, we) == te) continue;          // stored directly
     if (pass == 0 && wb > cb && wb % SPT != 0) continue;          // a lower warp reduces it
     const bool cta_whole = tb >= cb && te <= ce;
-    const bool cta_first = tb >= cb;               // the CTA holds the tile's first slot
+    // region of this CTA's share of tile tt in the partial-sum buffer: one per CTA for the
+    // tile it starts inside and one for the tile it ends inside
+    const int region = tb < cb ? 0 : 1;
     for (int base = 0; base < M * kTileN; base += 32) {
       const int idx = base + lane;
       const int m = idx / kTileN, nl = idx - m * kTileN;
@@ -558,45 +511,53 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
       }
       if (cta_whole) {
         store_tile_value(tt, idx, m, nl, sum);
-      } else if (!cta_first) {
-        // a contributor: publish this CTA's share (counted in below)
-        if (idx < M * kTileN) p.part[(size_t)blockIdx.x * (8 * kTileN) + m * kTileN + nl] = sum;
-      } else {
-        // the reducer: wait for the CTAs after this one, then add their shares in order
-        if (base == 0 && lane == 0) {
-          const unsigned target = (unsigned)(te - ce);
-          const long long c0 = clock64();
-          for (;;) {
-            unsigned v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.counters + tt) : "memory");
-            if (v == target) break;
-            if (clock64() - c0 > kStripeWaitCycles) {
-              atomicExch(&g_stripe_error, GQ_ERR_TIMEOUT);
-              break;
-            }
-            __nanosleep(64);
-          }
-          p.counters[tt] = 0u;                     // every contributor has arrived
-        }
-        __syncwarp();
-        if (idx < M * kTileN) {
-          for (int c2 = blockIdx.x + 1; c2 < (int)gridDim.x; ++c2) {
-            int b2, e2;
-            zsplit_dev(p.split_count, gridDim.x, c2, b2, e2);
-            if (b2 * p.split_mult >= te) break;
-            sum += __ldcg(p.part + (size_t)c2 * (8 * kTileN) + m * kTileN + nl);
-          }
-        }
-        store_tile_value(tt, idx, m, nl, sum);
+      } else if (idx < M * kTileN) {
+        __stcg(p.part + ((size_t)blockIdx.x * 2 + region) * (8 * kTileN) + m * kTileN + nl, sum);
       }
     }
-    if (!cta_whole && !cta_first) {
-      // __syncwarp orders the lanes' stores before lane 0's release, which publishes them
-      __syncwarp();
-      if (lane == 0)
-        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p.counters + tt),
-                     "r"((unsigned)(min(te, ce) - max(tb, cb)))
-                     : "memory");
+    if (cta_whole) continue;
+    // Last arriver: every CTA holding part of the tile publishes its share, then adds its slot
+    // count to the tile's counter; the CTA whose addition completes the tile's SPT slots adds
+    // all shares in CTA order (the same order whichever CTA arrives last), stores the tile
+    // and resets the counter.  No CTA waits for another.
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+      const unsigned mine = (unsigned)(min(te, ce) - max(tb, cb));
+      const unsigned prev = atomicAdd(p.counters + tt, mine);
+      const bool last = prev + mine == (unsigned)SPT;
+      if (last) p.counters[tt] = 0u;
+      s_last[warp] = last ? 1 : 0;
+    }
+    __syncwarp();
+    if (!s_last[warp]) continue;
+    __threadfence();
+    // the CTAs holding slots of the tile: a contiguous run of block indices around this one
+    int c_lo = blockIdx.x;
+    for (;;) {
+      if (c_lo == 0) break;
+      int b2, e2;
+      zsplit_dev(p.split_count, gridDim.x, c_lo - 1, b2, e2);
+      if (e2 * p.split_mult <= tb) break;
+      --c_lo;
+    }
+    for (int base = 0; base < M * kTileN; base += 32) {
+      const int idx = base + lane;
+      const int m = idx / kTileN, nl = idx - m * kTileN;
+      float sum = 0.f;
+      if (idx < M * kTileN) {
+        for (int c2 = c_lo; c2 < (int)gridDim.x; ++c2) {
+          int b2, e2;
+          zsplit_dev(p.split_count, gridDim.x, c2, b2, e2);
+          b2 *= p.split_mult;
+          e2 *= p.split_mult;
+          if (b2 >= te) break;
+          if (e2 <= b2) continue;                    // a CTA without slots
+          const int r2 = tb < b2 ? 0 : 1;           // the region that CTA wrote
+          sum += __ldcg(p.part + ((size_t)c2 * 2 + r2) * (8 * kTileN) + m * kTileN + nl);
+        }
+      }
+      store_tile_value(tt, idx, m, nl, sum);
     }
   }
 }

@@ -52,8 +52,9 @@ typedef enum gq_status {
                             then F up columns, and out is [M][F] = silu(gate) * up (silu(x) =
                             x / (1 + e^-x), in FP32 on the FP32 GEMM results, then rounded).
                             gq_pack_weights must get the flag too (it interleaves gate and up
-                            columns tile by tile).  Needs N % 16 == 0 and, in gq_gemm, M <= 8 and
-                            K % 256 == 0 (else GQ_ERR_UNSUPPORTED)                            */
+                            columns tile by tile).  Needs N % 16 == 0 and, in gq_gemm,
+                            K % 256 == 0 and M <= 64: the decode and small-batch kernels
+                            (else GQ_ERR_UNSUPPORTED)                                         */
 #define GQ_ACT_I8  0x100  /* INT8-activation variant (gq_gemm_a8, and gq_plan / gq_workspace_size
                             for it): activations are int8 codes with one fp32 scale per (row,
                             group); W8 codes and GQ_SC_F32 only; gq_gemm refuses it         */
@@ -146,8 +147,8 @@ int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
  * (gq_workspace_size) exceeds it returns GQ_ERR_WORKSPACE and launches nothing.
  *   The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call before any
- * stream capture.  Every call clears the arrival counters it uses (an asynchronous memset
- * on `stream`).  All calls on a device share the one array, which keeps the last call's
+ * stream capture.  Every call that splits K clears the arrival counters its plan indexes (an
+ * asynchronous memset of 4 bytes per output tile on `stream`, a few KiB at most).  All calls on a device share the one array, which keeps the last call's
  * contents, so calls that overlap on the GPU — different streams, or host threads without
  * ordering between them — race on it and must be serialized by the caller. */
 #define GQ_STATIC_SCRATCH_BYTES (4u << 20)
@@ -155,7 +156,7 @@ int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, const void *A,
                            const void *Wq, const void *scales, const void *zeros, void *out,
                            void *stream);
 
-/* Timing harness.  Runs `warmup` untimed and then `iters` timed gq_gemm calls back to back
+/* Timing harness over caller buffers.  Runs `warmup` untimed and then `iters` timed gq_gemm calls back to back
  * on `stream`, call i reading weight copy i % n_copies (so that copies larger than L2 in
  * total make every call read from HBM), and reports the mean time per call from CUDA
  * events recorded on `stream`.  With use_graph != 0 the `iters` calls are captured once
@@ -181,7 +182,35 @@ typedef struct gq_bench_result {
   int launches_per_call;       /* kernels one gq_gemm call launches for this problem */
 } gq_bench_result;
 
-int gq_bench(const gq_bench_args *args, gq_bench_result *result);
+int gq_bench_calls(const gq_bench_args *args, gq_bench_result *result);
+
+/* Self-contained benchmark of a named workload (the measured-data section, 四, of "04 · 分组量化
+ * GEMM 内核" reports time per call per shape; its tables did not survive, so the workloads are
+ * the library's five configurations):
+ *   "tiny_gemv"     M=1    K=512  N=512   G=128  W4 sym, fp16 scales, bf16 act/out
+ *   "decode_gateup" M=1    K=4096 N=28672 G=128  W4 sym, fp16 scales, 0.1% x50 activations
+ *   "q8_m1"/"q8_m32" M=1/32 K=2048 N=12288 G=32  INT8 codes, fp32 scales/act/out
+ *   "asym_m16"      M=16   K=8192 N=28672 G=128  W4 with INT4 zero points, bf16 scales
+ *   "prefill"       M=4096 K=4096 N=14336 G=128  W4 sym, fp16 scales
+ *   "all"           every one of the above, in that order (a JSON array).
+ * It allocates the workload on the current device, fills it on the device from a
+ * counter-based hash with the stated distributions (codes uniform, scales uniform in
+ * [0.005, 0.02] or [1e-3, 1e-2], zero points uniform in [4, 11], activations N(0, 1) by
+ * Box-Muller), packs the weights into enough rotated copies that one round of them exceeds
+ * twice the L2 (decode shapes), and times gq_gemm with CUDA events: five repeats of a CUDA
+ * graph of back-to-back calls (host-launched calls from M = 128), reporting the median, 10th
+ * and 90th percentile microseconds per call, the median latency of single host-launched
+ * calls, GB/s of the algorithmic bytes (codes, scales, zero points, activations once, output
+ * once), TFLOPS (2·M·N·K), the roofline fraction — against the library's own 1 GiB copy kernel
+ * (read + write bytes) for M < 128, against the nominal 2250 TFLOPS dense BF16 above — the
+ * kernels launched per call, and whether two calls gave identical bits.  Synchronizes the
+ * device and frees everything it allocated before returning.
+ *   json_out  host buffer of `cap` bytes; receives one NUL-terminated JSON object (an array
+ *             for "all").
+ * Errors: GQ_ERR_INVALID_ARG (unknown name, NULL json_out, or cap too small for the result:
+ * then json_out holds ""), GQ_ERR_NO_DEVICE, GQ_ERR_CUDA (an allocation or launch failed),
+ * and any status of gq_gemm. */
+int gq_bench(const char *config, char *json_out, size_t cap);
 
 /* ---------------------------------------------------------------------------------------
  * INT8-activation variant: the group-wise GEMM with integer activations of "04 · 分组量化
@@ -240,6 +269,19 @@ int gq_gemm_fp8_block(int M, int K, int N, int prec, const void *A, const void *
  * Errors: GQ_ERR_INVALID_ARG, GQ_ERR_ALIGNMENT, GQ_ERR_CUDA. */
 int gq_quantize_act_fp8(int M, int K, int prec, const void *A, void *Aq, void *a_scales,
                         void *stream);
+
+/* Testing and diagnostics: force the number of K slices (split-K over whole groups, summed in
+ * slice order) that the planner gives the kernels that split K — paths 0, 1, 4, 5, 6 and 7 of
+ * gq_plan_t below.  n >= 1 asks for exactly n slices, n = -1 for the largest count the path
+ * supports, n = 0 restores the planner's own choice (the default).  Process-wide; it changes
+ * what gq_plan, gq_workspace_size, gq_gemm, gq_gemm_a8 and gq_gemm_static_scratch do until it
+ * is reset, and a count that the chosen path cannot take makes them return
+ * GQ_ERR_UNSUPPORTED.  The path itself and paths that do not split K are unaffected.  Every
+ * count gives results within the tolerance of the group GEMM; the bits may differ between
+ * counts (another summation order) but never between runs at one count ("分组量化 GEMM 内核"
+ * section 3.3: the z-split and its fixed-order reduction).  Host only; returns the previous
+ * setting, or -2 (and changes nothing) for n < -1. */
+int gq_set_split_override(int n);
 
 /* Host-only description of the launch gq_gemm would make (for tests and reports).
  * sm_count > 0 overrides the device query, so it works without a GPU. */

@@ -257,6 +257,50 @@ def test_bitwise_deterministic(gq, name):
     assert torch.equal(b[0], b[1]) and torch.equal(b[0], b[2])
 
 
+# ------------------------------------------------------------------ forced split counts
+#
+# The z-split of "分组量化 GEMM 内核" section 3.3 partitions K into slices of whole groups and
+# adds the slices' partial sums in slice order.  The same problem at one slice, two slices and
+# the largest count each path supports must stay within the tolerance of the oracle.
+
+SPLIT_SHAPES = [
+    gq_synth.Config("split_w4_batch", M=16, K=2048, N=1032, G=128, zp=True, sc="bf16"),
+    gq_synth.Config("split_w4_mma_decode", M=3, K=1088, N=264, G=64),        # K % 256 != 0
+    gq_synth.Config("split_w8_block", M=2, K=2048, N=1000, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("split_w8_mma", M=12, K=512, N=520, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("split_w8_decode", M=40, K=512, N=264, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+]
+
+
+@pytest.mark.parametrize("cfg", SPLIT_SHAPES, ids=lambda c: c.name)
+def test_forced_split_counts_one_two_and_max_match_the_oracle(gq, cfg):
+    inp = gq_synth.make_inputs(cfg, seed=7)
+    ref, mag = _oracle(cfg, inp)
+    prec = prec_of(cfg)
+    path = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)["path"]
+    counts = []
+    try:
+        for n in (1, 2, -1):
+            gq.gq_set_split_override(n)
+            plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
+            assert plan["path"] == path
+            if n > 0:
+                assert plan["nsplit"] == n
+            counts.append(plan["nsplit"])
+            out, _ = run_gemm(gq, cfg, inp)
+            _assert_parity(cfg.replace(name=f"{cfg.name}_nsplit{plan['nsplit']}"),
+                           out_to_f64(out, cfg.out), ref, mag)
+            again, _ = run_gemm(gq, cfg, inp)
+            view = torch.int16 if cfg.out == "bf16" else torch.int32
+            assert torch.equal(out.view(view), again.view(view))
+    finally:
+        gq.gq_set_split_override(0)
+    assert counts[0] == 1 and counts[1] == 2 and counts[2] > 2
+
+
 # ------------------------------------------------------------------ layout, API edges
 
 def _unpack_w4_device_layout(packed: np.ndarray, K: int, N: int) -> np.ndarray:
@@ -418,6 +462,11 @@ GATE_UP_SHAPES = [
     # 128 tiles on 152 SMs: CTAs split tiles, so the cross-CTA reduction stores the epilogue
     gq_synth.Config("gu_m1_split", M=1, K=4096, N=2048, G=128, outlier_frac=0.001),
     gq_synth.Config("gu_m5_g32", M=5, K=1024, N=320, G=32, zp=True),
+    # the small-batch kernel: one slice, K split into slices, two row blocks, fp32 scales
+    gq_synth.Config("gu_m16_zp", M=16, K=2048, N=1056, G=128, zp=True, sc="bf16"),
+    gq_synth.Config("gu_m12_split_f32", M=12, K=8192, N=288, G=64, sc="f32", out="f32"),
+    gq_synth.Config("gu_m40_g32_split", M=40, K=4096, N=544, G=32, zp=True),
+    gq_synth.Config("gu_m33_g64", M=33, K=1024, N=160, G=64),
 ]
 
 
@@ -451,6 +500,22 @@ def test_gate_up_full_size_sampled_and_repeatable(gq):
     cfg = gq_synth.CONFIGS["decode_gateup"]
     cols = np.random.default_rng(11).choice(cfg.N // 2, 512, replace=False)
     _, (A, packed, S, Z, prec) = _gate_up_case(gq, cfg, seed=0, cols=cols)
+    o1 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+    o2 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+    gq.gemm_t(A, packed, S, Z, o1, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    gq.gemm_t(A, packed, S, Z, o2, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_gate_up_small_batch_full_size_sampled_and_repeatable(gq):
+    """The fused gate+up GEMM at the asymmetric small-batch size (M = 16, K = 8192,
+    N = 2·14336, INT4 zero points), 384 sampled output columns of every row against the
+    oracle; a second call gives the same bits."""
+    cfg = gq_synth.CONFIGS["asym_m16"]
+    cols = np.random.default_rng(12).choice(cfg.N // 2, 384, replace=False)
+    _, (A, packed, S, Z, prec) = _gate_up_case(gq, cfg, seed=0, cols=cols)
+    assert gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)["path"] == 4
     o1 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
     o2 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
     gq.gemm_t(A, packed, S, Z, o1, cfg.M, cfg.K, cfg.N, cfg.G, prec)

@@ -147,6 +147,21 @@ def test_plan_is_a_pure_function_of_shape(name):
         else:
             assert tiles >= 152
         return
+    if p1["path"] == 8:
+        # warp-specialized decode (M <= 4): a producer warp and eight consumer warps per CTA,
+        # at most one CTA per SM in the grid; two fit on an SM where the shape allows, so the
+        # next call's CTAs can start while this call's finish
+        tiles = (cfg.N + 15) // 16
+        assert cfg.M <= 4 and cfg.K % 256 == 0
+        assert p1["block_threads"] == 9 * 32
+        assert 1 <= p1["grid_x"] <= min(152, tiles * cfg.K // 256)
+        assert p1["nsplit"] == p1["grid_x"]
+        assert p1["smem_bytes"] <= 227 * 1024
+        if p1["workspace_bytes"]:
+            assert p1["workspace_bytes"] >= p1["grid_x"] * 2 * 4 * 16 * 4 + 4 * tiles
+        else:
+            assert tiles >= 152
+        return
     if p1["path"] == 4:
         # small-batch kernel: (K slice, tile range) CTAs x 32-row blocks, at most one wave
         assert 1 <= cfg.M <= 64 and cfg.K % 256 == 0
@@ -211,6 +226,10 @@ def test_decode_plan_fills_the_machine():
     assert p["grid_x"] == 152
     # 1792 tiles over 152 SMs: whole tiles per CTA (11 or 12), no scratch
     assert p["workspace_bytes"] == 0
+    # fewer tiles than SMs, up to four rows: the warp-specialized kernel, two CTAs per SM
+    p = gq.gq_plan(1, 512, 512, 128, C.GQ_W4, sm_count=152)
+    assert p["path"] == 8 and p["smem_bytes"] <= 113 * 1024
+    assert gq.gq_plan(5, 512, 512, 128, C.GQ_W4, sm_count=152)["path"] == 3
 
 
 def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
@@ -233,9 +252,13 @@ def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
 
 def test_small_decode_plan_splits_slots_between_ctas():
     p = gq.gq_plan(1, 4096, 1024, 128, C.GQ_W4, sm_count=152)
+    assert p["path"] == 8
+    assert p["grid_x"] == -(-64 * 16 // 16)      # 64 tiles x 16 slots, two slots per consumer
+    assert p["workspace_bytes"] > 0
+    p = gq.gq_plan(6, 4096, 1024, 128, C.GQ_W4, sm_count=152)
     assert p["path"] == 3
     warps = p["block_threads"] // 32
-    assert p["grid_x"] == -(-64 * 16 // warps)   # 64 tiles x 16 slots, one slot per warp or more
+    assert p["grid_x"] == -(-64 * 16 // warps)   # one slot per warp or more
     assert p["workspace_bytes"] > 0
 
 
@@ -252,18 +275,26 @@ def test_algorithmic_bytes_match_the_worked_figures():
     assert C.gemm_flops(4096, 4096, 14336) == 481036337152
 
 
-def test_gate_up_flag_is_validated_and_planned_on_the_striped_kernel():
+def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     gu = C.GQ_W4 | C.GQ_GATE_UP
     # N must hold whole 16-column tiles of 8 gate and 8 up columns; INT8 has no fused epilogue
     assert gq.gq_gemm(1, 512, 24, 128, gu, 16, 16, 16, None, 16, None) == 1
     assert gq.gq_gemm(1, 512, 32, 32, C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_GATE_UP,
                       16, 16, 16, None, 16, None) == 2
-    # only the striped decode kernel (M <= 8, K % 256 == 0) carries the epilogue
+    # the decode and small-batch kernels (K % 256 == 0) carry the epilogue: the
+    # warp-specialized one up to four rows, the striped one to eight, the small-batch one to
+    # 64 rows; not the prefill kernel, which would take 33 rows and more without it
     assert gq.gq_plan(1, 4096, 28672, 128, gu, sm_count=152)["path"] == 3
+    assert gq.gq_plan(1, 4096, 2048, 128, gu, sm_count=152)["path"] == 8
     assert gq.gq_plan(8, 1024, 512, 64, gu | C.GQ_ZP, sm_count=152)["path"] == 3
-    for M, K in ((9, 4096), (1, 320)):
+    assert gq.gq_plan(16, 8192, 28672, 128, gu | C.GQ_ZP, sm_count=152)["path"] == 4
+    assert gq.gq_plan(9, 4096, 1024, 64, gu, sm_count=152)["path"] == 4
+    assert gq.gq_plan(64, 4096, 1024, 32, gu, sm_count=152)["path"] == 4
+    assert gq.gq_plan(33, 4096, 1024, 64, gu, sm_count=152)["path"] == 4
+    assert gq.gq_plan(33, 4096, 1024, 64, C.GQ_W4, sm_count=152)["path"] == 2
+    for M, K, G in ((1, 320, 64), (65, 4096, 32), (65, 4096, 128)):
         with pytest.raises(C.GqError) as e:
-            gq.gq_plan(M, K, 1024, 64, gu, sm_count=152)
+            gq.gq_plan(M, K, 1024, G, gu, sm_count=152)
         assert e.value.status == 2
     # the packed size does not change
     assert gq.gq_packed_bytes(4096, 28672, 128, gu) == gq.gq_packed_bytes(4096, 28672, 128, C.GQ_W4)
@@ -334,3 +365,57 @@ def test_fp8_activation_quantizer_validation():
     assert f(2, 256, C.GQ_W4, 16, 16, 16, None) == 1
     assert f(2, 256, 0, 16, 8, 16, None) == 3
     assert f(0, 256, 0, None, None, None, None) == 0
+
+
+def test_split_override_forces_the_slice_count_and_rejects_counts_a_path_cannot_take():
+    """gq_set_split_override: n slices exactly, -1 the largest count, 0 the planner's own
+    choice again; the path never changes; a count the path cannot take is GQ_ERR_UNSUPPORTED."""
+    from group_quantized_weight_gb300.constants import GqError
+    W4ZP = C.GQ_W4 | C.GQ_ZP | C.GQ_SC_BF16
+    W8 = C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_OUT_F32
+    shapes = [((16, 2048, 1032, 128, W4ZP), 4, 8),     # K / 256 slots
+              ((3, 1088, 264, 64, C.GQ_W4), 0, 17),    # K / 64 units
+              ((2, 2048, 1000, 32, W8), 5, 8),         # groups / 8 warps
+              ((40, 512, 264, 32, W8), 1, 16)]         # K / G units
+    try:
+        for args, path, largest in shapes:
+            base = gq.gq_plan(*args, sm_count=152)
+            assert base["path"] == path
+            for n, want in ((1, 1), (2, 2), (-1, largest)):
+                assert gq.gq_set_split_override(n) in (0, 1, 2, -1)
+                p = gq.gq_plan(*args, sm_count=152)
+                assert p["path"] == path and p["nsplit"] == want, (args, n, p)
+                assert (p["workspace_bytes"] > 0) == (want > 1)
+            gq.gq_set_split_override(largest + 1)
+            with pytest.raises(GqError) as e:
+                gq.gq_plan(*args, sm_count=152)
+            assert e.value.status == 2
+            gq.gq_set_split_override(0)
+            assert gq.gq_plan(*args, sm_count=152) == base
+        # the batch kernel needs K / n to be a whole number of 256-k slots
+        gq.gq_set_split_override(3)
+        with pytest.raises(GqError):
+            gq.gq_plan(16, 2048, 1032, 128, W4ZP, sm_count=152)
+        assert gq.gq_set_split_override(-5) == -2                  # rejected, unchanged
+        assert gq.gq_set_split_override(0) == 3
+    finally:
+        gq.gq_set_split_override(0)
+
+
+def test_config_benchmark_validates_its_arguments_before_touching_a_device():
+    """gq_bench(config, json_out, cap): an unknown workload name or a NULL buffer is
+    GQ_ERR_INVALID_ARG; a known name needs a device (GQ_ERR_NO_DEVICE here, on a machine
+    without one).  The buffer holds "" after any error."""
+    import ctypes
+    lib = gq._lib
+    buf = ctypes.create_string_buffer(64)
+    buf.value = b"junk"
+    assert lib.gq_bench(b"no_such_workload", buf, 64) == 1
+    assert buf.value == b""
+    assert lib.gq_bench(b"tiny_gemv", None, 64) == 1
+    assert lib.gq_bench(None, buf, 64) == 1
+    assert lib.gq_bench(b"tiny_gemv", buf, 0) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.gq_bench(b"tiny_gemv", buf, 64) == 7
+        assert lib.gq_bench(b"all", buf, 64) == 7
