@@ -62,6 +62,8 @@ _SIGS = {
     "gq_plan": [_i, _i, _i, _i, _i, _i, ctypes.POINTER(gq_plan_t)],
     "gq_zsplit": [_i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)],
     "gq_set_split_override": [_i],
+    "gq_set_wait_limit": [ctypes.c_longlong],
+    "gq_set_fault_injection": [_i],
     "gq_device_error": [_i],
     "gq_status_string": [_i],
     "gq_last_error_detail": [],
@@ -168,6 +170,17 @@ def gq_set_split_override(n: int) -> int:
     """Force the K-slice count of the split-K paths (0 = planner's choice, -1 = the largest);
     returns the previous setting."""
     return _lib.gq_set_split_override(n)
+
+
+def gq_set_wait_limit(cycles: int) -> int:
+    """SM clock cycles after which a bounded device-side wait gives up (0 = the default);
+    returns the status."""
+    return _lib.gq_set_wait_limit(cycles)
+
+
+def gq_set_fault_injection(fault: int) -> int:
+    """Inject a failure (GQ_FAULT_* of gq.h; 0 = none); returns the previous setting."""
+    return _lib.gq_set_fault_injection(fault)
 
 
 def gq_device_error(clear: bool = False) -> int:

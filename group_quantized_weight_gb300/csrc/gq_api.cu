@@ -16,6 +16,8 @@ static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; 
 // gq_set_split_override: process-wide, read at plan time
 static std::atomic<int> g_split_override{0};
 int split_override() { return g_split_override.load(std::memory_order_relaxed); }
+// gq_set_fault_injection: process-wide
+static std::atomic<int> g_fault{GQ_FAULT_NONE};
 static inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 static inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -120,46 +122,48 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->workspace_bytes = p->part_bytes + p->counter_bytes;
     return GQ_OK;
   }
-  // warp-specialized decode (M <= 4): one CTA per SM (a producer warp streaming stages of
-  // slots, consumer warps decoding them) over equal slot ranges with a cross-CTA reduction,
-  // for problems with fewer 16-column tiles than SMs (latency-bound: its shorter prologue and
-  // two CTAs per SM make it the faster there); larger ones stay on the striped kernel below
-  int gv_nc = 0, gv_stages = 0, gv_cps = 0;
-  const bool gv_whole = ceil_div(Nc, kTileN) >= sms;
-  if (!gv_whole && gemv_supported(Mc, K, G, prec) &&
-      gemv_config(Mc, K, G, prec, kCtaSmemCap, &gv_nc, &gv_stages, &gv_cps) == GQ_OK) {
-    {
+  // warp-specialized decode (M <= 4): one CTA per SM (a producer warp streaming 2 KB slots
+  // for sixteen consumer warps that decode them) over a contiguous range of (tile, 256-k slot)
+  // pairs; whole tiles per CTA when that keeps the SMs within 10% of even, else equal slot
+  // ranges with a cross-CTA reduction.  Shapes whose activations and tables do not fit the
+  // shared memory take the striped kernel below.
+  if (gemv_supported(Mc, K, G, prec)) {
+    const int T = ceil_div(Nc, kTileN), spt = K / stripe_slot_k();
+    const int units = T * spt, per = ceil_div(T, sms);
+    int grid, split_count, split_mult;
+    if (T >= sms && (double)T >= 0.9 * (double)sms * per) {
+      grid = sms;
+      split_count = T;
+      split_mult = spt;
+    } else {
+      // equal slot ranges: at least two slots per consumer warp, at most one CTA per SM
+      grid = ceil_div(units, 32);
+      if (grid > sms) grid = sms;
+      split_count = units;
+      split_mult = 1;
+    }
+    const int max_cta_slots = ceil_div(split_count, grid) * split_mult;
+    const size_t smem = gemv_smem_bytes(Mc, K, G, prec, max_cta_slots);
+    if (smem <= kCtaSmemCap) {
       p->path = kPathGemv;
       p->mt = 1;
       p->m_tile = 4;
       p->n_tile = kTileN;
       p->unit_k = stripe_slot_k();
-      const int T = ceil_div(Nc, kTileN), spt = K / p->unit_k;
-      p->units = T * spt;
-      p->slots = gv_stages;
-      p->ctas_per_sm = gv_cps;
-      p->consumers = gv_nc;
-      p->block_threads = (gv_nc + 1) * 32;
-      p->smem_bytes = gemv_smem_bytes(Mc, K, G, prec, gv_nc, gv_stages);
+      p->units = units;
+      p->table_bytes = gemv_table_bytes(G, prec, max_cta_slots);
+      p->block_threads = gemv_threads();
+      p->smem_bytes = smem;
+      p->grid_x = grid;
       p->grid_y = p->grid_z = 1;
-      const int per = ceil_div(T, sms);
-      if (T >= sms && (double)T >= 0.9 * (double)sms * per) {
-        p->grid_x = sms;
-        p->split_count = T;
-        p->split_mult = spt;
-        p->workspace_bytes = 0;
-      } else {
-        // equal slot ranges: at least two slots per consumer warp, at most one CTA per SM
-        int grid = ceil_div(p->units, 2 * gv_nc);
-        if (grid > sms) grid = sms;
-        p->grid_x = grid;
-        p->split_count = p->units;
-        p->split_mult = 1;
+      p->split_count = split_count;
+      p->split_mult = split_mult;
+      if (split_mult == 1) {
         p->part_bytes = round_up((size_t)grid * 2 * 4 * kTileN * sizeof(float), 256);
         p->counter_bytes = kCounterRegionBytes;
         if ((size_t)T * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
-        p->workspace_bytes = p->part_bytes + p->counter_bytes;
       }
+      p->workspace_bytes = p->part_bytes + p->counter_bytes;
       p->nsplit = p->grid_x;
       return GQ_OK;
     }
@@ -425,6 +429,10 @@ static int get_scratch(size_t need, void **out) {
     *out = d.ptr;
     return GQ_OK;
   }
+  if (g_fault.load(std::memory_order_relaxed) == GQ_FAULT_WORKSPACE) {
+    note_cuda_error_code("workspace allocation (injected)", 0);
+    return GQ_ERR_CUDA;
+  }
   if (d.bytes < need) {
     if (d.ptr) {
       if (cudaDeviceSynchronize() != cudaSuccess || cudaFree(d.ptr) != cudaSuccess) {
@@ -476,6 +484,13 @@ cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, con
   }
 }
 
+// true (and the detail noted) when gq_set_fault_injection asked launches to fail
+bool launch_fault_injected() {
+  if (g_fault.load(std::memory_order_relaxed) != GQ_FAULT_LAUNCH) return false;
+  note_cuda_error_code("launch (injected)", 0);
+  return true;
+}
+
 static thread_local char g_detail[160];
 void note_cuda_error(const char *where, cudaError_t e) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorName(e));
@@ -504,6 +519,35 @@ const char *gq_status_string(int status) {
     case GQ_ERR_NO_DEVICE: return "no usable CUDA device";
     default: return "unknown status";
   }
+}
+
+int gq_set_wait_limit(long long cycles) {
+  if (cycles != 0 && (cycles < 10000ll || cycles > 100000000000ll)) return GQ_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GQ_ERR_NO_DEVICE; }
+  const long long v = cycles == 0 ? 4000000000ll : cycles;
+  const int r = gemv_set_wait_limit(v) | stripe_set_wait_limit(v) | batch_set_wait_limit(v) |
+                prefill_set_wait_limit(v) | fp8_set_wait_limit(v);
+  if (r != 0) {
+    note_cuda_error_code("gq_set_wait_limit", r);
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  return GQ_OK;
+}
+
+int gq_set_fault_injection(int fault) {
+  if (fault < GQ_FAULT_NONE || fault > GQ_FAULT_DEVICE_WAIT) return -1;
+  const int prev = g_fault.load();
+  // the device-side form lives in the warp-specialized decode kernel's translation unit; a
+  // machine without a device keeps the host-side forms only
+  if ((fault == GQ_FAULT_DEVICE_WAIT) != (prev == GQ_FAULT_DEVICE_WAIT)) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) gemv_set_withhold(fault == GQ_FAULT_DEVICE_WAIT);
+    cudaGetLastError();
+  }
+  g_fault.store(fault);
+  return prev;
 }
 
 int gq_set_split_override(int n) {
@@ -634,6 +678,7 @@ int gq::gemm_impl(int M, int K, int N, int G, int prec, const void *A, const voi
   unsigned *counters = (unsigned *)ws;
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
+  if (launch_fault_injected()) return GQ_ERR_CUDA;
   const cudaError_t e = launch_plan(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part,
                                     counters, s);
   if (e != cudaSuccess) {
@@ -673,6 +718,7 @@ static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,
   if (st != GQ_OK) return st;
   unsigned *counters = (unsigned *)ws;
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
+  if (launch_fault_injected()) return GQ_ERR_CUDA;
   const cudaError_t e = launch_q8a8(p, M, K, N, G, prec, (const int8_t *)Aq,
                                     (const float *)a_scales, Wq, scales, out, part, counters,
                                     (cudaStream_t)stream);

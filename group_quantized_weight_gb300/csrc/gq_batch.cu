@@ -17,6 +17,12 @@ static cudaError_t launch_bt_g(const Plan &pl, int prec, const BtParams &bp, cud
   return launch_bt_z<G, kScF16>(pl, prec, bp, s);
 }
 
+int batch_set_wait_limit(long long cycles) {
+  const int a = cudaMemcpyToSymbol(g_batch_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? 0 : -1;
+  const int b = batch_zf_set_wait_limit(cycles);
+  return a != 0 ? a : b;
+}
+
 int batch_read_error(int clear) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_batch_error, sizeof(int)) != cudaSuccess) {

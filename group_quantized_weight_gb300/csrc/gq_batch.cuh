@@ -45,7 +45,9 @@ constexpr int kBtSlotK = 256;                        // k per slot (four 64-k ch
 constexpr int kBtSlotCodes = 2048;                   // bytes of codes per slot
 constexpr int kBtMaxSlots = 4;                       // ring slots per warp
 constexpr int kBtRows = 32;                          // activation rows per CTA
-constexpr long long kBtWaitCycles = 4000000000ll;    // bounded waits: about two seconds
+// bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
+// gq_set_wait_limit changes it); one copy per translation unit, like the error word
+static __device__ long long g_batch_wait_limit = 4000000000ll;
 
 // Sticky device-side status of this kernel (GQ_ERR_TIMEOUT after a bounded wait gave up); one
 // word per translation unit that instantiates the kernel (gq_batch.cu: symmetric and INT4
@@ -104,7 +106,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
     if (done) return true;
     if (it == 0) {
       t0 = clock64();
-    } else if ((it & 63u) == 0u && clock64() - t0 > kBtWaitCycles) {
+    } else if ((it & 63u) == 0u && clock64() - t0 > g_batch_wait_limit) {
       atomicExch(&g_batch_error, GQ_ERR_TIMEOUT);
       return false;
     }
@@ -569,5 +571,6 @@ static cudaError_t launch_bt_m(const Plan &pl, const BtParams &bp, cudaStream_t 
 // float zero points (GQ_ZP_FLOAT): instantiated in their own translation unit
 cudaError_t launch_batch_zf(const Plan &pl, int prec, int G, const BtParams &bp, cudaStream_t s);
 int batch_zf_read_error(int clear);
+int batch_zf_set_wait_limit(long long cycles);
 
 }  // namespace gq

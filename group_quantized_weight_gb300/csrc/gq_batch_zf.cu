@@ -27,6 +27,10 @@ cudaError_t launch_batch_zf(const Plan &pl, int prec, int G, const BtParams &bp,
   }
 }
 
+int batch_zf_set_wait_limit(long long cycles) {
+  return cudaMemcpyToSymbol(g_batch_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? 0 : -1;
+}
+
 int batch_zf_read_error(int clear) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_batch_error, sizeof(int)) != cudaSuccess) {

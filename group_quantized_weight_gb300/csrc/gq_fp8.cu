@@ -40,7 +40,9 @@ constexpr int kF8SumWarps = 16;              // warpgroups 1-4
 constexpr uint32_t kF8WBytes = kF8TileN * kF8Block;          // 16 KB per stage
 constexpr uint32_t kF8ABytes = kF8TileM * kF8Block;          // 32 KB per stage
 constexpr uint32_t kF8StageBytes = kF8ABytes + kF8WBytes;    // 48 KB
-constexpr long long kF8WaitCycles = 4000000000ll;            // bounded waits (~2 s)
+// bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
+// gq_set_wait_limit changes it)
+static __device__ long long g_f8_wait_limit = 4000000000ll;
 
 static __device__ int g_fp8_error;           // sticky status (GQ_ERR_TIMEOUT), read by the host
 static __device__ unsigned g_fp8_abort;      // token of the launch that gave up
@@ -62,7 +64,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 // Bounded wait for phase `parity`: false once another role of this launch gave up, or after
-// kF8WaitCycles SM clock cycles, recording GQ_ERR_TIMEOUT and this launch's token.
+// g_f8_wait_limit SM clock cycles, recording GQ_ERR_TIMEOUT and this launch's token.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned token) {
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
@@ -77,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     if (done) return true;
     if ((it & 255u) == 0u) {
       if (*(volatile unsigned *)&g_fp8_abort == token) return false;
-      if (clock64() - t0 > kF8WaitCycles) {
+      if (clock64() - t0 > g_f8_wait_limit) {
         atomicExch(&g_fp8_abort, token);
         atomicExch(&g_fp8_error, GQ_ERR_TIMEOUT);
         return false;
@@ -530,6 +532,10 @@ int launch_fp8_block(int M, int K, int N, int prec, const void *A, const void *a
     return GQ_ERR_CUDA;
   }
   return GQ_OK;
+}
+
+int fp8_set_wait_limit(long long cycles) {
+  return cudaMemcpyToSymbol(g_f8_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? 0 : -1;
 }
 
 int fp8_read_error(int clear) {

@@ -34,7 +34,6 @@
 #include <type_traits>
 
 #include "gq_device.cuh"
-#include "gq_tma_host.h"
 
 namespace gq {
 
@@ -42,9 +41,6 @@ namespace gv {
 constexpr int kSlotChunks = 4;                          // 64-k chunks per slot
 constexpr int kSlotK = kSlotChunks * kChunkK;           // 256 k
 constexpr int kSlotCodes = kSlotChunks * 512;           // 2 KB of codes per slot
-constexpr int kMaxStages = 8;
-constexpr int kMaxConsumers = 16;
-constexpr long long kWaitCycles = 4000000000ll;         // bounded waits: about two seconds
 constexpr uint32_t kMagic = 0x64006400u;                // fp16 1024 in both halves
 constexpr uint32_t kSixteenth = 0x2C002C00u;            // fp16 1/16
 constexpr uint32_t kLoSym = 0x64086408u;                // fp16 1024 + 8
@@ -53,6 +49,12 @@ constexpr uint32_t kHiSym = 0xD480D480u;                // fp16 -(64 + 8)
 
 // Sticky device-side status (GQ_ERR_TIMEOUT after a bounded wait gave up).
 static __device__ int g_gemv_error;
+// bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
+// gq_set_wait_limit changes it)
+static __device__ long long g_gemv_wait_limit = 4000000000ll;
+// Failure-path test (gq_set_fault_injection(GQ_FAULT_DEVICE_WAIT)): when set, every producer
+// withholds consumer 0's first slot, so that consumer's bounded wait runs out.
+static __device__ int g_gemv_withhold;
 
 namespace gv {
 
@@ -79,7 +81,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (try_phase(bar, parity)) return true;
-    if ((it & 63u) == 0u && clock64() - t0 > kWaitCycles) {
+    if ((it & 63u) == 0u && clock64() - t0 > g_gemv_wait_limit) {
       atomicExch(&g_gemv_error, GQ_ERR_TIMEOUT);
       return false;
     }
@@ -94,59 +96,60 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
       : "memory");
 }
 
-__device__ __forceinline__ void tensor_copy_2d(uint32_t dst, const CUtensorMap *map,
-                                               uint32_t bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
 }  // namespace gv
 
 struct GemvParams {
   const uint8_t *Wp;          // packed codes
   const uint16_t *A;          // activations, bf16 [M][K]
+  const void *scales;         // [K/G][N]
   const uint32_t *zeros;      // [K/G][N/8] or NULL
   void *out;                  // [M][N] (gate+up: [M][N/2])
   float *part;                // [gridDim.x][2][4][16] per-CTA partial sums (shared tiles only)
   unsigned *counters;         // per-tile arrival counters (shared tiles only)
   int M, K, N;
   int split_count, split_mult;   // CTA c owns slots zsplit(split_count, grid, c) * split_mult
-  int S;                         // ring stages
-  int slot_bytes;                // codes + scale regions of one slot in the ring
-  int scale_b_off;               // byte offset of the scales of the tile's columns 8..15
+  int table_bytes;               // bytes of one consumer warp's scale / zero-point table
   int out_f32;
   int static_w;                  // weights may be read before the preceding kernel ends
   int gate_up;                   // fused gate+up: out[m][j] = silu(col j) * (col N/2 + j)
 };
 
-// Shared memory (dynamic): [bands][ring][pieces]
+namespace gv {
+constexpr int kConsumers = 16;                          // consumer warps per CTA
+constexpr int kStages = 4;                              // ring stages (one slot per consumer each)
+}  // namespace gv
+
+// Shared memory (dynamic, base rounded up to 128 bytes): [bands][ring][tables][pieces]
 //   bands   (1 + 2M) rows of act_row_words(K / 64) words: a zero row, then the two exponent
 //           bands of each activation row, permuted for the B operands
-//   ring    S stages x NC slots x slot_bytes: 2 KB of codes, then the slot's group scales
-//   pieces  NC x 2 x M x 16 floats: a warp's partial sums of its first and last tile
-template <int G, int SC, bool ZP, int NC>
-__global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
-    w4_gemv_kernel(const __grid_constant__ CUtensorMap smap, const GemvParams p) {
+//   ring    kStages x kConsumers slots of 2 KB of codes
+//   tables  per consumer warp, for each of its slots in order: the slot's group scales of the
+//           tile's 16 columns [G rows][16], then (INT4 zero points) the two zero-point words of
+//           each group row — loaded once, before the main loop
+//   pieces  kConsumers x 2 x M x 16 floats: a warp's partial sums of its first and last tile
+template <int G, int SC, bool ZP>
+__global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
+    w4_gemv_kernel(const GemvParams p) {
   using namespace gv;
+  constexpr int NC = kConsumers, S = kStages;
   constexpr int ES = SC == kScF32 ? 4 : 2;          // bytes per scale
   constexpr int GPS = kSlotK / G;                   // groups per slot
   constexpr int SPG = G / 16;                       // 16-k MMA steps per group
+  constexpr int SCB = GPS * 16 * ES;                // table bytes of a slot's scales
+  // table bytes per slot, a multiple of 16 so that every slot's scales start 16-byte aligned
+  constexpr int TSB = (SCB + (ZP ? GPS * 2 * 4 : 0) + 15) & ~15;
   typedef typename std::conditional<SC == kScF32, uint32_t, unsigned short>::type sc_t;
 
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  // the tensor copies of the scales land at 128-byte aligned addresses
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  // full_bar[stage][w]: consumer w's slot of the stage landed; empty_bar[stage]: every consumer
-  // released the stage
-  __shared__ __align__(8) uint64_t full_bar[kMaxStages][kMaxConsumers], empty_bar[kMaxStages];
+  // full_bar[stage][w]: consumer w's slot of the stage landed; empty_bar[stage][w]: consumer
+  // w released it.  Each consumer and its producer lane form an independent pipeline.
+  __shared__ __align__(8) uint64_t full_bar[S][NC], empty_bar[S][NC];
   __shared__ int s_emax[4], s_emin[4];
-  __shared__ int s_last[kMaxConsumers];
+  __shared__ int s_last[NC];
   asm volatile("griddepcontrol.launch_dependents;");
 
-  const int M = p.M, K = p.K, N = p.N, S = p.S;
+  const int M = p.M, K = p.K, N = p.N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = K / kChunkK;                        // chunks per tile
   const int SPT = K / kSlotK;                       // slots per tile
@@ -157,15 +160,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
   const int RS = act_row_words(C);
   uint32_t *bands = reinterpret_cast<uint32_t *>(smem);
   uint8_t *ring = smem + (((size_t)(1 + 2 * M) * RS * 4 + 127) & ~(size_t)127);
-  float *pieces = reinterpret_cast<float *>(ring + (size_t)S * NC * p.slot_bytes);
+  uint8_t *tables = ring + (size_t)S * NC * kSlotCodes;
+  float *pieces = reinterpret_cast<float *>(tables + (size_t)NC * p.table_bytes);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      for (int w = 0; w < NC; ++w)
+    for (int s = 0; s < S; ++s)
+      for (int w = 0; w < NC; ++w) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full_bar[s][w])) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(&empty_bar[s])), "r"(NC)
-                   : "memory");
-    }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&empty_bar[s][w])) : "memory");
+      }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (threadIdx.x < 4) {
@@ -177,44 +180,37 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
   // ================================================================ producer warp
   if (warp == NC) {
     if (!p.static_w) asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&smap) : "memory");
-    // lane w < NC feeds consumer w: slots [wb, we) of the CTA's range
-    int wb = 0, we = 0;
+    // lane w < NC streams consumer w's slots [wb, we) through ring slot (stage, w), refilling a
+    // stage as soon as that consumer released it
     if (lane < NC) {
+      int wb, we;
       zsplit_dev(ce - cb, NC, lane, wb, we);
       wb += cb;
       we += cb;
-    }
-    int n0, e0;                                     // consumer 0 has the most slots
-    zsplit_dev(ce - cb, NC, 0, n0, e0);
-    const int nmax = e0 - n0;
-    const int full_bytes_slot = kSlotCodes + 16 * GPS * ES;
-    int st = 0;
-    for (int j = 0; j < nmax; ++j) {
-      if (j >= S) {
-        // fill j of stage st reuses it after fill j - S: wait until every consumer released
-        // that one (empty phase j / S - 1)
-        bool ok = true;
-        if (lane == 0) ok = wait_phase(saddr(&empty_bar[st]), (uint32_t)((j / S + 1) & 1));
-        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      }
-      // lane w fills consumer w's slot of the stage, if it still has one
-      if (lane < NC && wb + j < we) {
-        const uint32_t fb = saddr(&full_bar[st][lane]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                     "r"(full_bytes_slot)
-                     : "memory");
-        const int slot = wb + j, t = slot / SPT, js = slot - t * SPT;
-        const uint32_t dst = saddr(ring + ((size_t)st * NC + lane) * p.slot_bytes);
-        bulk_copy(dst, p.Wp + (size_t)slot * kSlotCodes, kSlotCodes, fb);
-        if (p.gate_up) {                            // gate columns 8t.., up columns N/2 + 8t..
-          tensor_copy_2d(dst + kSlotCodes, &smap, fb, 8 * t, js * GPS);
-          tensor_copy_2d(dst + p.scale_b_off, &smap, fb, N / 2 + 8 * t, js * GPS);
-        } else {
-          tensor_copy_2d(dst + kSlotCodes, &smap, fb, 16 * t, js * GPS);
+      const int mine = we - wb;
+      const bool withhold = lane == 0 && *(volatile int *)&g_gemv_withhold != 0;
+      int issued = 0;
+      for (int j = 0; j < mine; ++j) {
+        const int st = j % S;
+        if (j >= S && !wait_phase(saddr(&empty_bar[st][lane]), (uint32_t)((j / S + 1) & 1))) break;
+        if (!(withhold && j == 0)) {
+          const uint32_t fb = saddr(&full_bar[st][lane]);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                       "n"(kSlotCodes)
+                       : "memory");
+          bulk_copy(saddr(ring + ((size_t)st * NC + lane) * kSlotCodes),
+                    p.Wp + (size_t)(wb + j) * kSlotCodes, kSlotCodes, fb);
         }
+        issued = j + 1;
       }
-      if (++st == S) st = 0;
+      // Before the producer leaves, every copy it issued has landed: the CTA's shared memory
+      // must not be written after all of its warps are gone (a consumer that gave up never
+      // waits for its later slots).  Fill f completed phase f / S of full_bar[f % S][w]; the
+      // last fill of each stage is the latest phase that barrier saw.
+      for (int f = max(0, issued - S); f < issued; ++f) {
+        if (withhold && f == 0) continue;
+        if (!wait_phase(saddr(&full_bar[f % S][lane]), (uint32_t)((f / S) & 1))) break;
+      }
     }
     return;
   }
@@ -226,7 +222,45 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
   wb += cb;
   we += cb;
   const int n = we - wb;
+
+  // ---- this warp's table: for each of its slots, the group scales of the tile's columns (16
+  // bytes per cp.async; gate+up: the gate columns 8t.. then the up columns N/2 + 8t..) and the
+  // zero-point words; static weights (GQ_STATIC_W) are read before the preceding kernel ends
+  uint8_t *tbl = tables + (size_t)warp * p.table_bytes;
+  auto load_table = [&]() {
+    const size_t srow = (size_t)N * ES;
+    const uint8_t *sbase = reinterpret_cast<const uint8_t *>(p.scales);
+    constexpr int PPS = GPS * ES;                  // 16-byte scale parts per slot
+    for (int e = lane; e < n * PPS; e += 32) {
+      const int i = e / PPS, pr = e - i * PPS, g = pr / ES, lp = pr - g * ES;
+      const int slot = wb + i, t = slot / SPT, js = slot - t * SPT;
+      size_t col_bytes = (size_t)t * kTileN * ES + lp * 16;
+      if (p.gate_up)
+        col_bytes = lp * 16 < 8 * ES ? (size_t)8 * t * ES + lp * 16
+                                     : (size_t)(N / 2 + 8 * t) * ES + (lp * 16 - 8 * ES);
+      if (lp * 16 < min(kTileN, N - t * kTileN) * ES)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                         saddr(tbl + (size_t)i * TSB + g * 16 * ES + lp * 16)),
+                     "l"(sbase + (size_t)(js * GPS + g) * srow + col_bytes)
+                     : "memory");
+    }
+    if (ZP) {
+      const int NW = N >> 3;
+      for (int e = lane; e < n * GPS * 2; e += 32) {
+        const int i = e / (GPS * 2), pr = e - i * (GPS * 2), g = pr >> 1, h = pr & 1;
+        const int slot = wb + i, t = slot / SPT, js = slot - t * SPT;
+        const int word = p.gate_up ? (h ? NW / 2 + t : t) : min(2 * t + h, NW - 1);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                         saddr(tbl + (size_t)i * TSB + SCB + (g * 2 + h) * 4)),
+                     "l"(p.zeros + (size_t)(js * GPS + g) * NW + word)
+                     : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  if (p.static_w) load_table();
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!p.static_w) load_table();
 
   // ---- exponent bands (the consumer warps only; the producer is already streaming)
   const int nth = NC * 32, tid = threadIdx.x;
@@ -297,6 +331,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
       }
     }
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's table copies landed
   asm volatile("bar.sync 1, %0;" ::"r"(nth) : "memory");
 
   // B-operand row of this lane: MMA column r0 = band r0 % 2 of activation row r0 / 2, or the
@@ -312,32 +347,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
     }
     brow = bands + row * RS + q * 4;
   }
-  auto zlo_of = [&](uint32_t zw) -> uint32_t {     // fp16(1024 + z) in both halves
-    return (0x6400u | ((zw >> (4 * r0)) & 0xFu)) * 0x00010001u;
-  };
-  auto zhi_of = [&](uint32_t zw) -> uint32_t {     // fp16(-(64 + z)) in both halves
-    return (0xD400u | (((zw >> (4 * r0)) & 0xFu) << 4)) * 0x00010001u;
-  };
   auto scale_f = [&](uint32_t bits) -> float {
     if (SC == kScF32) return __uint_as_float(bits);
     if (SC == kScBF16) return __uint_as_float(bits << 16);
     return __half2float(__ushort_as_half((unsigned short)bits));
   };
-  const int NW = N >> 3;
-  auto load_zeros = [&](int tz, int jz, uint32_t (&z)[GPS][2]) {
-#pragma unroll
-    for (int gi = 0; gi < GPS; ++gi) {
-      const uint32_t *zr = p.zeros + (size_t)(jz * GPS + gi) * NW;
-      z[gi][0] = __ldg(zr + min(p.gate_up ? tz : 2 * tz, NW - 1));
-      z[gi][1] = __ldg(zr + min(p.gate_up ? NW / 2 + tz : 2 * tz + 1, NW - 1));
-    }
-  };
   const int t_first = wb / SPT;
   int t = t_first, j = wb - t_first * SPT;
   int j0 = j;                                      // first slot of this warp's share of t
-  uint32_t zcur[GPS][2], znext[GPS][2];
-  if (ZP && n > 0) load_zeros(t, j, znext);
-  const int scale_row = p.gate_up ? 8 : 16;        // scale elements per group row in a slot
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   // end of the warp's share of tile t (slots j0 .. j1 - 1): combine the bands, then store a
@@ -364,25 +381,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
     }
   };
 
-  int st = 0;
-  uint32_t ph = 0;
+  const uint8_t *ringw = ring + (size_t)warp * kSlotCodes;
+  const uint8_t *ts = tbl;                         // the current slot's table entry
+  const uint32_t *bslot = brow + j * (kSlotChunks * 32);
   for (int i = 0; i < n; ++i) {
-    if (!wait_phase(saddr(&full_bar[st][warp]), ph)) break;
-    if (ZP) {
-#pragma unroll
-      for (int gi = 0; gi < GPS; ++gi) {
-        zcur[gi][0] = znext[gi][0];
-        zcur[gi][1] = znext[gi][1];
-      }
-      if (i + 1 < n) {
-        if (j + 1 < SPT) load_zeros(t, j + 1, znext);
-        else load_zeros(t + 1, 0, znext);
-      }
-    }
-    const uint8_t *slot = ring + ((size_t)st * NC + warp) * p.slot_bytes;
-    const sc_t *sca = reinterpret_cast<const sc_t *>(slot + kSlotCodes);
-    const sc_t *scb = reinterpret_cast<const sc_t *>(slot + p.scale_b_off);
-    const uint32_t *bslot = brow + j * (kSlotChunks * 32);
+    const int st = i % S;
+    if (!wait_phase(saddr(&full_bar[st][warp]), (uint32_t)((i / S) & 1))) break;
+    const uint8_t *slot = ringw + (size_t)st * (NC * kSlotCodes);
+    const sc_t *sg = reinterpret_cast<const sc_t *>(ts);
+    const uint32_t *zt = reinterpret_cast<const uint32_t *>(ts + SCB);
 #pragma unroll
     for (int ch = 0; ch < kSlotChunks; ++ch) {
       const uint4 wv = *reinterpret_cast<const uint4 *>(slot + ch * 512 + lane * 16);
@@ -395,8 +402,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
       for (int jj = 0; jj < 4; ++jj) {
         const int stp = ch * 4 + jj;                 // compile-time 16-k step of the slot
         const int gi = stp / SPG;
-        const uint32_t zl = ZP ? zlo_of(zcur[gi][0]) : kLoSym;
-        const uint32_t zh = ZP ? zhi_of(zcur[gi][1]) : kHiSym;
+        // fp16(1024 + z) and fp16(-(64 + z)) in both halves, z of the tile's columns r0 and
+        // r0 + 8 (nibble r0 of the group's two zero-point words)
+        const uint32_t zl = ZP ? (0x6400u | ((zt[2 * gi] >> (4 * r0)) & 0xFu)) * 0x00010001u : kLoSym;
+        const uint32_t zh = ZP ? (0xD400u | (((zt[2 * gi + 1] >> (4 * r0)) & 0xFu) << 4)) * 0x00010001u
+                               : kHiSym;
         const uint32_t w = words[jj], w8 = w >> 8;
         const uint32_t a0 = hsub2_u(lop3_and_or<0x000F000Fu>(w, kMagic), zl);
         const uint32_t a1 = hfma2_u(lop3_and_or<0x00F000F0u>(w, kMagic), kSixteenth, zh);
@@ -407,8 +417,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
         else
           mma_16816_f16(d, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
         if ((stp + 1) % SPG == 0) {                 // a whole group: scale it in
-          const float fa = scale_f((uint32_t)sca[gi * scale_row + r0]);
-          const float fb = scale_f((uint32_t)scb[gi * scale_row + r0]);
+          const float fa = scale_f((uint32_t)sg[gi * 16 + r0]);
+          const float fb = scale_f((uint32_t)sg[gi * 16 + r0 + 8]);
           acc[0] = fmaf(fa, d[0], acc[0]);
           acc[1] = fmaf(fa, d[1], acc[1]);
           acc[2] = fmaf(fb, d[2], acc[2]);
@@ -416,20 +426,22 @@ __global__ void __launch_bounds__((NC + 1) * 32, NC <= 8 ? 2 : 1)
         }
       }
     }
-    // every lane has read the slot (its values fed the instructions above): one arrival per
-    // warp releases it
+    // every lane has read the slot (its values fed the instructions above): one arrival
+    // releases it to the producer lane
     __syncwarp();
-    if (lane == 0)
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&empty_bar[st])) : "memory");
-    if (++st == S) {
-      st = 0;
-      ph ^= 1u;
-    }
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %1, 0;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(saddr(&empty_bar[st][warp])),
+        "r"(lane)
+        : "memory");
+    ts += TSB;
+    bslot += kSlotChunks * 32;
     if (++j == SPT) {
       flush(SPT);
       ++t;
       j = 0;
       j0 = 0;
+      bslot = brow;
     }
   }
   if (n > 0 && j != 0) flush(j);
@@ -528,10 +540,9 @@ namespace {
 
 size_t round128(size_t x) { return (x + 127) & ~(size_t)127; }
 
-int scale_region_bytes(int G, int prec) {
+int table_slot_bytes(int G, int prec) {
   const int es = (prec & GQ_SC_F32) ? 4 : 2, gps = gv::kSlotK / G;
-  if (prec & GQ_GATE_UP) return 2 * (int)round128((size_t)gps * 8 * es);
-  return (int)round128((size_t)gps * 16 * es);
+  return (gps * 16 * es + ((prec & GQ_ZP) ? gps * 2 * 4 : 0) + 15) & ~15;
 }
 
 }  // namespace
@@ -541,48 +552,33 @@ bool gemv_supported(int M, int K, int G, int prec) {
          K % gv::kSlotK == 0 && G <= gv::kSlotK;
 }
 
-int gemv_slot_bytes(int G, int prec) { return gv::kSlotCodes + scale_region_bytes(G, prec); }
+// Bytes of one consumer warp's table for a CTA holding at most max_cta_slots slots.
+int gemv_table_bytes(int G, int prec, int max_cta_slots) {
+  const int per_warp = (max_cta_slots + gv::kConsumers - 1) / gv::kConsumers;
+  return (int)(((size_t)per_warp * table_slot_bytes(G, prec) + 15) & ~(size_t)15);
+}
 
-size_t gemv_smem_bytes(int M, int K, int G, int prec, int consumers, int stages) {
+size_t gemv_smem_bytes(int M, int K, int G, int prec, int max_cta_slots) {
   const size_t bands = round128((size_t)(1 + 2 * M) * act_row_words(K / kChunkK) * 4);
-  const size_t ring = (size_t)stages * consumers * gemv_slot_bytes(G, prec);
-  const size_t pieces = (size_t)consumers * 2 * M * kTileN * 4;
-  return 128 + bands + ring + pieces;                // 128: alignment of the dynamic base
+  const size_t ring = (size_t)gv::kStages * gv::kConsumers * gv::kSlotCodes;
+  const size_t tables = (size_t)gv::kConsumers * gemv_table_bytes(G, prec, max_cta_slots);
+  const size_t pieces = (size_t)gv::kConsumers * 2 * M * kTileN * 4;
+  return 128 + bands + ring + tables + pieces;       // 128: alignment of the dynamic base
 }
 
-// Consumer warps and ring depth.  Eight consumers and the deepest ring of four to six
-// stages that keeps two CTAs on an SM (so that consecutive calls overlap); where that does
-// not fit, sixteen consumers and the deepest ring that fits one CTA.
-int gemv_config(int M, int K, int G, int prec, size_t smem_cap, int *consumers, int *stages,
-                int *ctas_per_sm) {
-  const size_t half = 113u * 1024u;                // two CTAs per SM (228 KB less 1 KB each)
-  for (int s = 6; s >= 4; --s)
-    if (gemv_smem_bytes(M, K, G, prec, 8, s) <= half) {
-      *consumers = 8;
-      *stages = s;
-      *ctas_per_sm = 2;
-      return GQ_OK;
-    }
-  for (int s = gv::kMaxStages; s >= 3; --s)
-    if (gemv_smem_bytes(M, K, G, prec, 16, s) <= smem_cap) {
-      *consumers = 16;
-      *stages = s;
-      *ctas_per_sm = 1;
-      return GQ_OK;
-    }
-  return GQ_ERR_UNSUPPORTED;
-}
+int gemv_threads() { return (gv::kConsumers + 1) * 32; }
 
-template <int G, int SC, bool ZP, int NC>
-static cudaError_t launch_gemv_t(const Plan &pl, const CUtensorMap &map, const GemvParams &gp,
-                                 cudaStream_t s) {
-  auto kern = w4_gemv_kernel<G, SC, ZP, NC>;
+template <int G, int SC, bool ZP>
+static cudaError_t launch_gemv_t(const Plan &pl, const GemvParams &gp, cudaStream_t s) {
+  auto kern = w4_gemv_kernel<G, SC, ZP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem_bytes);
   if (e != cudaSuccess) return e;
+  // programmatic stream serialization: the next kernel may begin launching while this one
+  // runs; this kernel reads activations and writes outputs only after griddepcontrol.wait
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid_x);
-  cfg.blockDim = dim3(pl.block_threads);
+  cfg.blockDim = dim3(gemv_threads());
   cfg.dynamicSmemBytes = pl.smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -590,57 +586,29 @@ static cudaError_t launch_gemv_t(const Plan &pl, const CUtensorMap &map, const G
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map, gp);
+  return cudaLaunchKernelEx(&cfg, kern, gp);
 }
 
 template <int G, int SC>
-static cudaError_t launch_gemv_z(const Plan &pl, int prec, const CUtensorMap &map,
-                                 const GemvParams &gp, cudaStream_t s) {
-  if (pl.consumers == 16) {
-    if (prec & GQ_ZP) return launch_gemv_t<G, SC, true, 16>(pl, map, gp, s);
-    return launch_gemv_t<G, SC, false, 16>(pl, map, gp, s);
-  }
-  if (prec & GQ_ZP) return launch_gemv_t<G, SC, true, 8>(pl, map, gp, s);
-  return launch_gemv_t<G, SC, false, 8>(pl, map, gp, s);
+static cudaError_t launch_gemv_z(const Plan &pl, int prec, const GemvParams &gp, cudaStream_t s) {
+  if (prec & GQ_ZP) return launch_gemv_t<G, SC, true>(pl, gp, s);
+  return launch_gemv_t<G, SC, false>(pl, gp, s);
 }
 
 template <int G>
-static cudaError_t launch_gemv_g(const Plan &pl, int prec, const CUtensorMap &map,
-                                 const GemvParams &gp, cudaStream_t s) {
-  if (prec & GQ_SC_F32) return launch_gemv_z<G, kScF32>(pl, prec, map, gp, s);
-  if (prec & GQ_SC_BF16) return launch_gemv_z<G, kScBF16>(pl, prec, map, gp, s);
-  return launch_gemv_z<G, kScF16>(pl, prec, map, gp, s);
+static cudaError_t launch_gemv_g(const Plan &pl, int prec, const GemvParams &gp, cudaStream_t s) {
+  if (prec & GQ_SC_F32) return launch_gemv_z<G, kScF32>(pl, prec, gp, s);
+  if (prec & GQ_SC_BF16) return launch_gemv_z<G, kScBF16>(pl, prec, gp, s);
+  return launch_gemv_z<G, kScF16>(pl, prec, gp, s);
 }
 
 cudaError_t launch_gemv(const Plan &pl, int M, int K, int N, int G, int prec, const void *A,
                         const void *Wq, const void *scales, const void *zeros, void *out,
                         float *part, unsigned *counters, cudaStream_t s) {
-  // the canonical scale matrix [K/G][N] as a 2-D tensor: 16 columns (8 for gate+up halves) x
-  // the slot's groups per box
-  const EncodeTiledFn enc = tensor_map_encoder();
-  if (!enc) {
-    note_cuda_error_code("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1);
-    return cudaErrorInvalidValue;
-  }
-  const bool f32 = (prec & GQ_SC_F32) != 0;
-  const int es = f32 ? 4 : 2;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)(K / G)};
-  const cuuint64_t strides[1] = {(cuuint64_t)N * es};
-  const cuuint32_t box[2] = {(cuuint32_t)((prec & GQ_GATE_UP) ? 8 : 16),
-                             (cuuint32_t)(gv::kSlotK / G)};
-  const cuuint32_t ones[2] = {1, 1};
-  const CUresult r = enc(&map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16,
-                         2, const_cast<void *>(scales), dims, strides, box, ones,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    note_cuda_error_code("cuTensorMapEncodeTiled(scales)", (int)r);
-    return cudaErrorInvalidValue;
-  }
   GemvParams gp;
   gp.Wp = reinterpret_cast<const uint8_t *>(Wq);
   gp.A = reinterpret_cast<const uint16_t *>(A);
+  gp.scales = scales;
   gp.zeros = reinterpret_cast<const uint32_t *>(zeros);
   gp.out = out;
   gp.part = part;
@@ -650,20 +618,26 @@ cudaError_t launch_gemv(const Plan &pl, int M, int K, int N, int G, int prec, co
   gp.N = N;
   gp.split_count = pl.split_count;
   gp.split_mult = pl.split_mult;
-  gp.S = pl.slots;
-  gp.slot_bytes = gemv_slot_bytes(G, prec);
-  gp.scale_b_off = (prec & GQ_GATE_UP) ? gv::kSlotCodes + scale_region_bytes(G, prec) / 2
-                                       : gv::kSlotCodes + 8 * es;
+  gp.table_bytes = pl.table_bytes;
   gp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   gp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   gp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
   switch (G) {
-    case 32: return launch_gemv_g<32>(pl, prec, map, gp, s);
-    case 64: return launch_gemv_g<64>(pl, prec, map, gp, s);
-    case 128: return launch_gemv_g<128>(pl, prec, map, gp, s);
-    case 256: return launch_gemv_g<256>(pl, prec, map, gp, s);
+    case 32: return launch_gemv_g<32>(pl, prec, gp, s);
+    case 64: return launch_gemv_g<64>(pl, prec, gp, s);
+    case 128: return launch_gemv_g<128>(pl, prec, gp, s);
+    case 256: return launch_gemv_g<256>(pl, prec, gp, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int gemv_set_wait_limit(long long cycles) {
+  return cudaMemcpyToSymbol(g_gemv_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? 0 : -1;
+}
+
+int gemv_set_withhold(bool on) {
+  const int v = on ? 1 : 0;
+  return cudaMemcpyToSymbol(g_gemv_withhold, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
 }
 
 int gemv_read_error(int clear) {

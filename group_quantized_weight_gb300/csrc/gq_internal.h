@@ -55,9 +55,8 @@ struct Plan {
   size_t counter_bytes;  // arrival counters
   size_t workspace_bytes;
   int split_count, split_mult;   // path 3: CTA c owns slots zsplit(split_count, grid, c) * split_mult
-  int slots;                     // path 3: ring slots per warp; path 8: ring stages
-  int ctas_per_sm;               // path 8: CTAs that fit on one SM (2 lets calls overlap)
-  int consumers;                 // path 8: consumer warps per CTA
+  int slots;                     // path 3: ring slots per warp
+  int table_bytes;               // path 8: bytes of a consumer warp's scale table
 };
 
 // scale / output type codes used as template parameters
@@ -85,16 +84,27 @@ cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int pre
                               const void *A, const void *Wq, const void *scales,
                               const void *zeros, void *out, float *part,
                               unsigned *counters, cudaStream_t s);
-// warp-specialized small-M decode kernel (M <= 4): a producer warp and kGemvConsumers
-// consumer warps per CTA
+// warp-specialized small-M decode kernel (M <= 4): a producer warp and sixteen consumer
+// warps per CTA
 bool gemv_supported(int M, int K, int G, int prec);
-int gemv_config(int M, int K, int G, int prec, size_t smem_cap, int *consumers, int *stages,
-                int *ctas_per_sm);
-size_t gemv_smem_bytes(int M, int K, int G, int prec, int consumers, int stages);
+int gemv_table_bytes(int G, int prec, int max_cta_slots);
+size_t gemv_smem_bytes(int M, int K, int G, int prec, int max_cta_slots);
+int gemv_threads();
 cudaError_t launch_gemv(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                         const void *Wq, const void *scales, const void *zeros, void *out,
                         float *part, unsigned *counters, cudaStream_t s);
 int gemv_read_error(int clear);
+// per translation unit: the SM clock cycles after which a bounded device-side wait gives up
+int gemv_set_wait_limit(long long cycles);
+// GQ_FAULT_DEVICE_WAIT: the producer warps withhold one slot (device flag of the current device)
+int gemv_set_withhold(bool on);
+// gq_set_fault_injection(GQ_FAULT_LAUNCH): true, with the error detail noted, when the next
+// launch is to fail
+bool launch_fault_injected();
+int stripe_set_wait_limit(long long cycles);
+int batch_set_wait_limit(long long cycles);
+int prefill_set_wait_limit(long long cycles);
+int fp8_set_wait_limit(long long cycles);
 bool stripe_supported(int M, int K, int G, int prec);
 size_t stripe_smem_bytes(int M, int K, int G, int prec, int slots);
 int stripe_slots_for(int M, int K, int G, int prec, size_t smem_cap);

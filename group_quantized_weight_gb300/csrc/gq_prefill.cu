@@ -42,7 +42,9 @@ constexpr uint32_t kPfPackedBytes = 8 * 512;                  // packed codes pe
 constexpr uint32_t kPfActBytes = kPfTileM * 64 * 2;           // activations per stage
 constexpr uint32_t kPfDqBytes = kPfTileN * 64 * 2;            // dequantized weights per stage
 constexpr uint32_t kPfStageBytes = kPfActBytes + kPfPackedBytes;   // 36864: one TMA stage
-constexpr long long kPfWaitCycles = 4000000000ll;              // bounded waits (~2 s)
+// bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
+// gq_set_wait_limit changes it)
+static __device__ long long g_pf_wait_limit = 4000000000ll;
 
 static __device__ int g_prefill_error;        // sticky status (GQ_ERR_TIMEOUT), read by the host
 static __device__ unsigned g_prefill_abort;     // token of the launch that gave up
@@ -68,7 +70,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Wait for the phase of parity `parity` to complete.  Bounded: gives up (false) once another
-// role of the same launch gave up, or after kPfWaitCycles SM clock cycles (about two
+// role of the same launch gave up, or after g_pf_wait_limit SM clock cycles (about two
 // seconds), recording GQ_ERR_TIMEOUT (sticky) and this launch's token.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned token) {
   const long long t0 = clock64();
@@ -84,7 +86,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     if (done) return true;
     if ((it & 255u) == 0u) {
       if (*(volatile unsigned *)&g_prefill_abort == token) return false;   // this launch gave up
-      if (clock64() - t0 > kPfWaitCycles) {
+      if (clock64() - t0 > g_pf_wait_limit) {
         atomicExch(&g_prefill_abort, token);
         atomicExch(&g_prefill_error, GQ_ERR_TIMEOUT);
         return false;
@@ -618,6 +620,10 @@ cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, 
     case 256: return launch_pf_s<4>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int prefill_set_wait_limit(long long cycles) {
+  return cudaMemcpyToSymbol(g_pf_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? 0 : -1;
 }
 
 int prefill_read_error(int clear) {

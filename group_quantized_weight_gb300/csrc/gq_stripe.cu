@@ -46,7 +46,9 @@ namespace gq {
 constexpr int kSlotChunks = 4;                          // 64-k chunks per slot
 constexpr int kSlotK = kSlotChunks * kChunkK;           // 256 k
 constexpr int kMaxSlots = 3;                            // ring slots per warp
-constexpr long long kStripeWaitCycles = 4000000000ll;   // bounded waits: about two seconds
+// bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
+// gq_set_wait_limit changes it)
+static __device__ long long g_stripe_wait_limit = 4000000000ll;
 
 // Sticky device-side status of this kernel (GQ_ERR_TIMEOUT after a bounded wait gave up),
 // read by the host through stripe_read_error.
@@ -72,7 +74,7 @@ __device__ __forceinline__ bool slot_wait(uint32_t bar, uint32_t parity) {
     if (done) return true;
     if (it == 0) {
       t0 = clock64();
-    } else if ((it & 63u) == 0u && clock64() - t0 > kStripeWaitCycles) {
+    } else if ((it & 63u) == 0u && clock64() - t0 > g_stripe_wait_limit) {
       atomicExch(&g_stripe_error, GQ_ERR_TIMEOUT);
       return false;
     }
@@ -600,6 +602,10 @@ static cudaError_t launch_stripe_g(const Plan &pl, int prec, const StripeParams 
   if (prec & GQ_SC_F32) return launch_stripe_z<G, kScF32>(pl, prec, sp, s);
   if (prec & GQ_SC_BF16) return launch_stripe_z<G, kScBF16>(pl, prec, sp, s);
   return launch_stripe_z<G, kScF16>(pl, prec, sp, s);
+}
+
+int stripe_set_wait_limit(long long cycles) {
+  return cudaMemcpyToSymbol(g_stripe_wait_limit, &cycles, sizeof(cycles)) == cudaSuccess ? 0 : -1;
 }
 
 int stripe_read_error(int clear) {

@@ -283,6 +283,35 @@ int gq_quantize_act_fp8(int M, int K, int prec, const void *A, void *Aq, void *a
  * setting, or -2 (and changes nothing) for n < -1. */
 int gq_set_split_override(int n);
 
+/* Testing and diagnostics: the SM clock cycles after which every bounded device-side wait in
+ * the library's kernels gives up (it records GQ_ERR_TIMEOUT, which gq_device_error reports,
+ * and the kernel leaves early; nothing traps or hangs).  cycles = 0 restores the default,
+ * 4e9 cycles (about two seconds at 2 GHz); otherwise 1e4 <= cycles <= 1e11.  Applies to the
+ * current device from the next launch on; synchronous.  Errors: GQ_ERR_INVALID_ARG,
+ * GQ_ERR_NO_DEVICE, GQ_ERR_CUDA. */
+int gq_set_wait_limit(long long cycles);
+
+/* Testing: injected failures, to check that each one surfaces as the documented status.
+ *   GQ_FAULT_NONE         no injection (the default).
+ *   GQ_FAULT_WORKSPACE    the library-owned scratch cannot be had: a gq_gemm or gq_gemm_a8
+ *                         that needs it returns GQ_ERR_CUDA ("workspace allocation
+ *                         (injected)" in gq_last_error_detail) and launches nothing.
+ *   GQ_FAULT_LAUNCH       the kernel launch fails: gq_gemm, gq_gemm_a8 and
+ *                         gq_gemm_static_scratch return GQ_ERR_CUDA ("launch (injected)") and
+ *                         launch nothing.
+ *   GQ_FAULT_DEVICE_WAIT  on the device: in the warp-specialized decode kernel (gq_plan path 8)
+ *                         the producer warp of every CTA withholds its first consumer's first
+ *                         slot, so that consumer's bounded wait runs out (gq_set_wait_limit
+ *                         shortens it); the call ends early with an output that is not valid
+ *                         and gq_device_error reports GQ_ERR_TIMEOUT.  Other paths ignore it.
+ * Process-wide; the device-side form is set on the current device (synchronous).  Returns the
+ * previous setting, or -1 (and changes nothing) for an unknown value. */
+#define GQ_FAULT_NONE 0
+#define GQ_FAULT_WORKSPACE 1
+#define GQ_FAULT_LAUNCH 2
+#define GQ_FAULT_DEVICE_WAIT 3
+int gq_set_fault_injection(int fault);
+
 /* Host-only description of the launch gq_gemm would make (for tests and reports).
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {

@@ -153,7 +153,7 @@ def test_plan_is_a_pure_function_of_shape(name):
         # next call's CTAs can start while this call's finish
         tiles = (cfg.N + 15) // 16
         assert cfg.M <= 4 and cfg.K % 256 == 0
-        assert p1["block_threads"] == 9 * 32
+        assert p1["block_threads"] == 17 * 32
         assert 1 <= p1["grid_x"] <= min(152, tiles * cfg.K // 256)
         assert p1["nsplit"] == p1["grid_x"]
         assert p1["smem_bytes"] <= 227 * 1024
@@ -222,14 +222,14 @@ def test_plan_is_a_pure_function_of_shape(name):
 def test_decode_plan_fills_the_machine():
     cfg = gq_synth.CONFIGS["decode_gateup"]
     p = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, C.GQ_W4, sm_count=152)
-    assert p["path"] == 3
+    assert p["path"] == 8 and p["block_threads"] == 17 * 32
     assert p["grid_x"] == 152
     # 1792 tiles over 152 SMs: whole tiles per CTA (11 or 12), no scratch
     assert p["workspace_bytes"] == 0
-    # fewer tiles than SMs, up to four rows: the warp-specialized kernel, two CTAs per SM
-    p = gq.gq_plan(1, 512, 512, 128, C.GQ_W4, sm_count=152)
-    assert p["path"] == 8 and p["smem_bytes"] <= 113 * 1024
-    assert gq.gq_plan(5, 512, 512, 128, C.GQ_W4, sm_count=152)["path"] == 3
+    # five to eight rows take the striped kernel
+    assert gq.gq_plan(5, cfg.K, cfg.N, cfg.G, C.GQ_W4, sm_count=152)["path"] == 3
+    # activations too large for the decode kernels' shared memory: the small-batch kernel
+    assert gq.gq_plan(4, 32768, 28672, 128, C.GQ_W4, sm_count=152)["path"] == 4
 
 
 def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
@@ -253,7 +253,7 @@ def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
 def test_small_decode_plan_splits_slots_between_ctas():
     p = gq.gq_plan(1, 4096, 1024, 128, C.GQ_W4, sm_count=152)
     assert p["path"] == 8
-    assert p["grid_x"] == -(-64 * 16 // 16)      # 64 tiles x 16 slots, two slots per consumer
+    assert p["grid_x"] == -(-64 * 16 // 32)      # 64 tiles x 16 slots, two slots per consumer
     assert p["workspace_bytes"] > 0
     p = gq.gq_plan(6, 4096, 1024, 128, C.GQ_W4, sm_count=152)
     assert p["path"] == 3
@@ -284,7 +284,7 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     # the decode and small-batch kernels (K % 256 == 0) carry the epilogue: the
     # warp-specialized one up to four rows, the striped one to eight, the small-batch one to
     # 64 rows; not the prefill kernel, which would take 33 rows and more without it
-    assert gq.gq_plan(1, 4096, 28672, 128, gu, sm_count=152)["path"] == 3
+    assert gq.gq_plan(1, 4096, 28672, 128, gu, sm_count=152)["path"] == 8
     assert gq.gq_plan(1, 4096, 2048, 128, gu, sm_count=152)["path"] == 8
     assert gq.gq_plan(8, 1024, 512, 64, gu | C.GQ_ZP, sm_count=152)["path"] == 3
     assert gq.gq_plan(16, 8192, 28672, 128, gu | C.GQ_ZP, sm_count=152)["path"] == 4
@@ -419,3 +419,24 @@ def test_config_benchmark_validates_its_arguments_before_touching_a_device():
     if not torch.cuda.is_available():
         assert lib.gq_bench(b"tiny_gemv", buf, 64) == 7
         assert lib.gq_bench(b"all", buf, 64) == 7
+
+
+def test_fault_injection_and_wait_limit_settings_are_validated():
+    """gq_set_fault_injection takes the four documented values (returning the previous one)
+    and refuses others; gq_set_wait_limit refuses limits outside [1e4, 1e11] cycles before it
+    touches a device."""
+    lib = gq._lib
+    assert lib.gq_set_fault_injection(7) == -1 and lib.gq_set_fault_injection(-1) == -1
+    try:
+        assert lib.gq_set_fault_injection(2) == 0
+        assert lib.gq_set_fault_injection(1) == 2
+        assert lib.gq_set_fault_injection(0) == 1
+    finally:
+        lib.gq_set_fault_injection(0)
+    import ctypes
+    f = lib.gq_set_wait_limit
+    f.argtypes = [ctypes.c_longlong]
+    assert f(5) == 1 and f(10 ** 12) == 1 and f(-3) == 1
+    import torch
+    if not torch.cuda.is_available():
+        assert f(0) == 7 and f(2_000_000) == 7            # no device: GQ_ERR_NO_DEVICE
