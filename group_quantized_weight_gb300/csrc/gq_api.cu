@@ -34,8 +34,8 @@ int validate(int M, int K, int N, int G, int prec) {
   if (K < G || K % G != 0) return GQ_ERR_INVALID_ARG;
   if (N % 8 != 0) return GQ_ERR_INVALID_ARG;
   if (prec & GQ_GATE_UP) {
-    if (!(prec & GQ_W4)) return GQ_ERR_UNSUPPORTED;
-    if (N % 16 != 0) return GQ_ERR_INVALID_ARG;
+    // W4: whole 16-column tiles of 8 gate and 8 up columns; W8: whole 64-column blocks of 32
+    if (N % ((prec & GQ_W4) ? 16 : 64) != 0) return GQ_ERR_INVALID_ARG;
   }
   if (prec & GQ_ACT_I8) {                          // W8A8: INT8 codes, fp32 scales
     if (prec & (GQ_W4 | GQ_ZP | GQ_ACT_F32 | GQ_GATE_UP)) return GQ_ERR_UNSUPPORTED;
@@ -264,19 +264,49 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   const bool gate_up = (prec & GQ_GATE_UP) != 0;
   if (!gate_up && M >= kPrefillMinM && !(prec & GQ_ZP_FLOAT) &&
       prefill_supported(M, K, N, G, prec)) {
-    // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM, no scratch
+    // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM.  Activation tiles of 64,
+    // 128 or 256 rows (the MMA's N) so that few rows do not pay for a 256-row product, the
+    // deepest TMA ring that fits, and a K split of whole groups when the 128-column tiles are
+    // too few to keep every SM busy: the count that minimises the waves of (tile, slice)
+    // units per slice, among those whose FP32 partial sums (written and read once) stay
+    // within the packed weight bytes
     p->path = kPathPrefill;
-    p->m_tile = 256;
+    const int BM = M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    p->m_tile = BM;
     p->n_tile = 128;
     p->unit_k = G;
     p->units = K / G;
-    const int tiles = ceil_div(N, 128) * ceil_div(M, 256);
-    p->grid_x = tiles < sms ? tiles : sms;
+    const int tiles = ceil_div(N, 128) * ceil_div(M, BM);
+    int ks = 1;
+    double best = 1.0;
+    for (int k2 = 2; k2 <= 16 && k2 <= p->units; ++k2) {
+      if ((double)k2 * M * N * 8.0 > (double)K * N / 2.0) break;
+      if ((size_t)k2 * M * N * 4 > kPartCap) break;
+      const double cost = (double)ceil_div(tiles * k2, sms) / k2 /
+                          (double)ceil_div(tiles, sms);
+      if (cost < best * (1.0 - 1e-9)) {
+        best = cost;
+        ks = k2;
+      }
+    }
+    if (split_override() != 0) {
+      const int fs = split_override() == -1 ? (p->units < 16 ? p->units : 16) : split_override();
+      if (fs < 1 || fs > p->units || (fs > 1 && (size_t)fs * M * N * 4 > kPartCap))
+        return GQ_ERR_UNSUPPORTED;
+      ks = fs;
+    }
+    p->nsplit = ks;
+    p->grid_x = tiles * ks < sms ? tiles * ks : sms;
     p->grid_y = p->grid_z = 1;
-    p->nsplit = 1;
     p->block_threads = kPrefillThreads;
-    p->smem_bytes = prefill_smem_bytes();
-    p->workspace_bytes = 0;
+    p->slots = prefill_stages(BM, kCtaSmemCap);
+    p->smem_bytes = prefill_smem_bytes(BM, p->slots);
+    if (ks > 1) {
+      p->part_bytes = round_up((size_t)ks * M * N * sizeof(float), 256);
+      p->counter_bytes = kCounterRegionBytes;
+      if ((size_t)tiles * 8 * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
+    }
+    p->workspace_bytes = p->part_bytes + p->counter_bytes;
     return GQ_OK;
   }
   // small batch (M <= 32, or up to 64 with G = 32): persistent CTAs over (K slice, tile
@@ -389,7 +419,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
 
 // Bytes of arrival counters the kernels of plan p index (a prefix of the counter region);
 // 0 when the plan uses none.
-size_t plan_counter_bytes_used(const Plan &p, int N) {
+size_t plan_counter_bytes_used(const Plan &p, int M, int N) {
   if (p.counter_bytes == 0) return 0;
   const int Nc = N > 0 ? N : 8;
   size_t n = 0;
@@ -397,6 +427,7 @@ size_t plan_counter_bytes_used(const Plan &p, int N) {
     case kPathQ8A8: n = (size_t)p.grid_z * ceil_div(Nc, 64); break;
     case kPathStripe:
     case kPathGemv: n = (size_t)ceil_div(Nc, kTileN); break;
+    case kPathPrefill: n = (size_t)ceil_div(Nc, 128) * ceil_div(M > 0 ? M : 1, p.m_tile) * 8; break;
     case kPathQ8Mma: n = (size_t)ceil_div(Nc, 64); break;
     case kPathQ8Block: n = (size_t)ceil_div(Nc, p.n_tile); break;
     case kPathBatch: n = (size_t)p.grid_z * ceil_div(Nc, kTileN); break;
@@ -462,7 +493,7 @@ cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, con
                         float *part, unsigned *counters, cudaStream_t s) {
   switch (p.path) {
     case kPathPrefill:
-      return launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, s);
+      return launch_prefill(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
     case kPathGemv:
       return launch_gemv(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part, counters, s);
     case kPathStripe:
@@ -645,7 +676,8 @@ int gq_pack_weights(int K, int N, int G, int prec, const void *codes, void *pack
     e = launch_pack_w4(K, N, (const uint32_t *)codes, (uint32_t *)packed,
                        (prec & GQ_GATE_UP) != 0, s);
   else
-    e = launch_pack_w8(K, N, (const int8_t *)codes, (uint8_t *)packed, s);
+    e = launch_pack_w8(K, N, (const int8_t *)codes, (uint8_t *)packed,
+                       (prec & GQ_GATE_UP) != 0, s);
   return e == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
 

@@ -394,6 +394,8 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
       }
       const uint8_t *slot = ring + rs * SLOTB;
       const uint8_t *ssc = slot + kBtSlotCodes;
+      // a group's MMA accumulators (a group may span chunks; never a slot: G <= 256)
+      float d[MT][4];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         const uint4 wv = *reinterpret_cast<const uint4 *>(slot + ch * 512 + lane * 16);
@@ -407,7 +409,6 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
           bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
         }
         const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-        float d[MT][4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const int stp = ch * 4 + jj;               // 16-k step of the slot

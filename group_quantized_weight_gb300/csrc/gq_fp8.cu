@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 
 #include "gq_internal.h"
+#include "gq_tma_host.h"
 
 namespace gq {
 
@@ -434,32 +435,10 @@ int launch_quantize_fp8(int M, int K, bool f32, const void *A, void *Aq, void *s
 
 // ------------------------------------------------------------------ host side
 
-using F8EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static F8EncodeFn f8_encode_fn() {
-  static std::atomic<F8EncodeFn> fn{nullptr};
-  F8EncodeFn f = fn.load();
-  if (f) return f;
-  void *p = nullptr;
-  cudaDriverEntryPointQueryResult q{};
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                       &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || !p) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  f = reinterpret_cast<F8EncodeFn>(p);
-  fn.store(f);
-  return f;
-}
-
 // rows x K bytes, K contiguous: boxes of 128 k x box_rows rows, 128-byte swizzle
 static int f8_encode(CUtensorMap *map, const void *base, int rows, int K, int box_rows,
                      const char *what) {
-  const F8EncodeFn enc = f8_encode_fn();
+  const EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) {
     note_cuda_error_code("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1);
     return GQ_ERR_CUDA;

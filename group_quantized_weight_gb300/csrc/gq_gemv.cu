@@ -5,19 +5,18 @@
 // instructions per byte as possible.  One CTA per SM, two roles:
 //   producer warp   streams this CTA's slots (256 k of one 16-column tile: 2 KB of codes, a
 //                   contiguous piece of the packed layout) into a ring of S stages.  A stage
-//                   holds one slot per consumer warp: lane w issues consumer w's cp.async.bulk
-//                   of codes and one TMA tensor copy of the slot's group scales (a 16-column x
-//                   G-row box of the canonical [K/G][N] scale matrix); everything completes on
-//                   the stage's "full" mbarrier.
-//   consumer warps  wait for a stage, decode their slot's codes in registers (the FP16
-//                   magic-number trick of section 2.4 of the same page), multiply on tensor
-//                   cores (mma.sync m16n8k16, the 16 MMA rows on the tile's columns) and
-//                   release the stage on its "empty" mbarrier.
+//                   holds one slot per consumer warp: lane w issues consumer w's
+//                   cp.async.bulk of codes, completing on that consumer's own "full" mbarrier.
+//   consumer warps  first copy the group scales (and zero points) of every slot they own into
+//                   a table of their own in shared memory (cp.async, once per call), then wait
+//                   for a slot, decode its codes in registers (the FP16 magic-number trick of
+//                   section 2.4 of the same page), multiply on tensor cores (mma.sync
+//                   m16n8k16, the 16 MMA rows on the tile's columns) and release the slot on
+//                   their "empty" mbarrier.
 // A consumer's only per-slot bookkeeping is one wait and one arrive; address arithmetic for
-// the copies lives in the producer.  The shared memory (activations in exponent bands, the
-// ring, and the consumers' partial sums) is sized so that two CTAs fit on an SM where the
-// shape allows: the next call's CTA then starts streaming its weights (GQ_STATIC_W) while
-// this one finishes, so consecutive calls overlap on every SM.
+// the copies lives in the producer.  One CTA per SM.  With GQ_STATIC_W the weight stream and the
+// scale tables start before the wait on the previous kernel in the stream (programmatic
+// dependent launch), so they overlap the previous call's tail.
 //
 // Work partition (the striped partitioning of section 3.3 item 4 of the same page): the
 // packed codes are a sequence of 16-column tiles with K contiguous, so the (tile, slot) pairs
@@ -262,23 +261,44 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!p.static_w) load_table();
 
-  // ---- exponent bands (the consumer warps only; the producer is already streaming)
+  // ---- exponent bands (the consumer warps only; the producer is already streaming).  Each
+  // thread reads its 16-byte pieces of A (8 consecutive k of one row) once: for the row's
+  // exponent range, then, after one barrier, to convert them (held in registers when every
+  // row has at most two pieces per thread, read again from L1 otherwise).
   const int nth = NC * 32, tid = threadIdx.x;
   for (int idx = tid; idx < RS; idx += nth) bands[idx] = 0u;   // zero row 0
   const int ppr = K >> 3;                          // 16-byte pieces per row
+  const int per = (ppr + nth - 1) / nth;           // pieces per thread and row
   const uint4 *A4 = reinterpret_cast<const uint4 *>(p.A);
-  for (int m = 0; m < M; ++m) {
-    unsigned mx = 0u, mn = 0xFFFFu;
-    for (int pc = tid; pc < ppr; pc += nth) {
-      const uint4 v = A4[(size_t)m * ppr + pc];
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  const bool held_all = per <= 2;
+  uint4 held[4][2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t mag = wv[e] & 0x7FFF7FFFu;
-        const uint32_t lo = mag & 0xFFFFu, hi = mag >> 16;
-        mx = max(mx, max(lo, hi));
-        mn = min(mn, min(lo ? lo : 0xFFFFu, hi ? hi : 0xFFFFu));   // smallest non-zero
-      }
+  for (int m = 0; m < 4; ++m)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int pc = tid + i * nth;
+      held[m][i] = make_uint4(0u, 0u, 0u, 0u);
+      if (held_all && m < M && i < per && pc < ppr) held[m][i] = A4[(size_t)m * ppr + pc];
+    }
+  auto range_of = [&](const uint4 v, unsigned &mx, unsigned &mn) {
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t mag = wv[e] & 0x7FFF7FFFu;
+      const uint32_t lo = mag & 0xFFFFu, hi = mag >> 16;
+      mx = max(mx, max(lo, hi));
+      mn = min(mn, min(lo ? lo : 0xFFFFu, hi ? hi : 0xFFFFu));   // smallest non-zero
+    }
+  };
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    if (m >= M) break;
+    unsigned mx = 0u, mn = 0xFFFFu;
+    if (held_all) {
+      range_of(held[m][0], mx, mn);
+      range_of(held[m][1], mx, mn);
+    } else {
+      for (int pc = tid; pc < ppr; pc += nth) range_of(A4[(size_t)m * ppr + pc], mx, mn);
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
     mn = __reduce_min_sync(0xffffffffu, mn);
@@ -288,46 +308,62 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
     }
   }
   asm volatile("bar.sync 1, %0;" ::"r"(nth) : "memory");
-  for (int v = 0; v < 2 * M; ++v) {
-    const int m = v >> 1, b = v & 1;
+  // piece pc (k = 8 pc .. 8 pc + 7) of row m, band b: its four words go to base(pc) + 0, 4,
+  // 8, 12 of the band row
+  auto convert = [&](const uint4 vv, int m, int b, int pc) {
     const int emax = s_emax[m], emin = s_emin[m];
     const int nbu = emin > emax ? 0 : min(2, ((emax - emin) >> 5) + 1);
-    if (b >= nbu) continue;
     const int sb_ = 142 - emax + 32 * b;           // scale exponent of band b
-    uint32_t *brw = bands + (1 + v) * RS;
+    uint32_t *brw = bands + (1 + 2 * m + b) * RS;
     const bool fast = nbu == 1 && emax < 255;
     const int s1 = sb_ / 2, s2 = sb_ - s1;
     const float c1 = __int_as_float((127 + s1) << 23), c2 = __int_as_float((127 + s2) << 23);
-    for (int pc = tid; pc < ppr; pc += nth) {
-      const uint4 vv = A4[(size_t)m * ppr + pc];
-      const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
-      uint32_t *dst = brw + (pc >> 3) * 32 + ((pc & 7) >> 2) * 16 + ((pc >> 1) & 1) * 2 + (pc & 1);
+    const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
+    uint32_t *dst = brw + (pc >> 3) * 32 + ((pc & 7) >> 2) * 16 + ((pc >> 1) & 1) * 2 + (pc & 1);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t raw = wv[e];
-        uint32_t pair = 0u;
-        if (fast) {
-          const __half2 h = __floats2half2_rn(__uint_as_float(raw << 16) * c1 * c2,
-                                              __uint_as_float(raw & 0xFFFF0000u) * c1 * c2);
-          pair = *reinterpret_cast<const uint32_t *>(&h);
-        } else {
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t raw = wv[e];
+      uint32_t pair = 0u;
+      if (fast) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(raw << 16) * c1 * c2,
+                                            __uint_as_float(raw & 0xFFFF0000u) * c1 * c2);
+        pair = *reinterpret_cast<const uint32_t *>(&h);
+      } else {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t bits = (raw >> (16 * h)) & 0xFFFFu;
-            const int ex = (bits >> 7) & 0xFF;
-            if ((bits & 0x7FFFu) && ((emax - ex) >> 5) == b) {
-              float f;
-              if (ex == 255)
-                f = __uint_as_float(bits << 16);                        // inf / nan stay so
-              else if (ex == 0)
-                f = ldexpf(__uint_as_float(bits << 16), sb_);           // bf16 subnormal
-              else
-                f = __uint_as_float((bits << 16) + ((uint32_t)sb_ << 23));  // exponent + sb
-              pair |= (uint32_t)__half_as_ushort(__float2half_rn(f)) << (16 * h);
-            }
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t bits = (raw >> (16 * h)) & 0xFFFFu;
+          const int ex = (bits >> 7) & 0xFF;
+          if ((bits & 0x7FFFu) && ((emax - ex) >> 5) == b) {
+            float f;
+            if (ex == 255)
+              f = __uint_as_float(bits << 16);                        // inf / nan stay so
+            else if (ex == 0)
+              f = ldexpf(__uint_as_float(bits << 16), sb_);           // bf16 subnormal
+            else
+              f = __uint_as_float((bits << 16) + ((uint32_t)sb_ << 23));  // exponent + sb
+            pair |= (uint32_t)__half_as_ushort(__float2half_rn(f)) << (16 * h);
           }
         }
-        dst[4 * e] = pair;
+      }
+      dst[4 * e] = pair;
+    }
+  };
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    if (m >= M) break;
+    const int emax = s_emax[m], emin = s_emin[m];
+    const int nbu = emin > emax ? 0 : min(2, ((emax - emin) >> 5) + 1);
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      if (b >= nbu) break;
+      if (held_all) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int pc = tid + i * nth;
+          if (i < per && pc < ppr) convert(held[m][i], m, b, pc);
+        }
+      } else {
+        for (int pc = tid; pc < ppr; pc += nth) convert(A4[(size_t)m * ppr + pc], m, b, pc);
       }
     }
   }
@@ -384,6 +420,10 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
   const uint8_t *ringw = ring + (size_t)warp * kSlotCodes;
   const uint8_t *ts = tbl;                         // the current slot's table entry
   const uint32_t *bslot = brow + j * (kSlotChunks * 32);
+  // A group's 16-k steps alternate between two MMA accumulators (even and odd steps), so
+  // that two independent dependency chains are in flight; the group's dot is their sum.
+  // Groups never straddle a slot (G <= 256 = one slot), so both start afresh in every slot.
+  float d[2][4];
   for (int i = 0; i < n; ++i) {
     const int st = i % S;
     if (!wait_phase(saddr(&full_bar[st][warp]), (uint32_t)((i / S) & 1))) break;
@@ -397,7 +437,6 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
       const uint4 bhi = *reinterpret_cast<const uint4 *>(bslot + ch * 32 + 16);
       const uint32_t bq[8] = {blo.x, blo.y, blo.z, blo.w, bhi.x, bhi.y, bhi.z, bhi.w};
       const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-      float d[4];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int stp = ch * 4 + jj;                 // compile-time 16-k step of the slot
@@ -412,17 +451,18 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
         const uint32_t a1 = hfma2_u(lop3_and_or<0x00F000F0u>(w, kMagic), kSixteenth, zh);
         const uint32_t a2 = hsub2_u(lop3_and_or<0x000F000Fu>(w8, kMagic), zl);
         const uint32_t a3 = hfma2_u(lop3_and_or<0x00F000F0u>(w8, kMagic), kSixteenth, zh);
-        if (stp % SPG == 0)
-          mma_16816_f16_zc(d, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
+        float *dd = d[stp & 1];
+        if (stp % SPG < 2)
+          mma_16816_f16_zc(dd, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
         else
-          mma_16816_f16(d, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
+          mma_16816_f16(dd, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
         if ((stp + 1) % SPG == 0) {                 // a whole group: scale it in
           const float fa = scale_f((uint32_t)sg[gi * 16 + r0]);
           const float fb = scale_f((uint32_t)sg[gi * 16 + r0 + 8]);
-          acc[0] = fmaf(fa, d[0], acc[0]);
-          acc[1] = fmaf(fa, d[1], acc[1]);
-          acc[2] = fmaf(fb, d[2], acc[2]);
-          acc[3] = fmaf(fb, d[3], acc[3]);
+          acc[0] = fmaf(fa, d[0][0] + d[1][0], acc[0]);
+          acc[1] = fmaf(fa, d[0][1] + d[1][1], acc[1]);
+          acc[2] = fmaf(fb, d[0][2] + d[1][2], acc[2]);
+          acc[3] = fmaf(fb, d[0][3] + d[1][3], acc[3]);
         }
       }
     }

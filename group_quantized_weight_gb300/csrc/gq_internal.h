@@ -55,7 +55,7 @@ struct Plan {
   size_t counter_bytes;  // arrival counters
   size_t workspace_bytes;
   int split_count, split_mult;   // path 3: CTA c owns slots zsplit(split_count, grid, c) * split_mult
-  int slots;                     // path 3: ring slots per warp
+  int slots;                     // path 3: ring slots per warp; path 2: TMA ring stages
   int table_bytes;               // path 8: bytes of a consumer warp's scale table
 };
 
@@ -68,7 +68,7 @@ int validate(int M, int K, int N, int G, int prec);
 // `forced` and return 0 when the path cannot take that count.
 int split_override();
 int make_plan(int M, int K, int N, int G, int prec, int sm_count, Plan *p);
-size_t plan_counter_bytes_used(const Plan &p, int N);
+size_t plan_counter_bytes_used(const Plan &p, int M, int N);
 // the body of gq_gemm (validation, plan, scratch, launch)
 int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
               const void *scales, const void *zeros, void *out, void *stream);
@@ -78,7 +78,7 @@ int device_sm_count(int *sms);
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed, bool gate_up,
                            cudaStream_t s);
-cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed,
+cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed, bool gate_up,
                            cudaStream_t s);
 cudaError_t launch_mma_decode(const Plan &p, int M, int K, int N, int G, int prec,
                               const void *A, const void *Wq, const void *scales,
@@ -113,11 +113,12 @@ cudaError_t launch_stripe_decode(const Plan &p, int M, int K, int N, int G, int 
                                 const void *A, const void *Wq, const void *scales,
                                 const void *zeros, void *out, float *part,
                                 unsigned *counters, cudaStream_t s);
-size_t prefill_smem_bytes();
+size_t prefill_smem_bytes(int BM, int stages);
+int prefill_stages(int BM, size_t smem_cap);
 bool prefill_supported(int M, int K, int N, int G, int prec);
 cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                            const void *Wq, const void *scales, const void *zeros, void *out,
-                           cudaStream_t s);
+                           float *part, unsigned *counters, cudaStream_t s);
 int prefill_read_error(int clear);
 int stripe_read_error(int clear);
 bool batch_supported(int M, int K, int G, int prec);

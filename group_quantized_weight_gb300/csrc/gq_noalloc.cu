@@ -80,7 +80,7 @@ extern "C" int gq_gemm_static_scratch(int M, int K, int N, int G, int prec, cons
   // call's contents (the kernels leave their counters at zero, but a call cut short by a
   // device-side timeout may not)
   if (launch_fault_injected()) return GQ_ERR_CUDA;
-  const size_t ctr = plan_counter_bytes_used(p, N);
+  const size_t ctr = plan_counter_bytes_used(p, M, N);
   if (ctr && cudaMemsetAsync(counters, 0, ctr, s) != cudaSuccess) {
     cudaGetLastError();
     return GQ_ERR_CUDA;

@@ -50,8 +50,10 @@ __global__ void pack_w4_kernel(int K, int N, const uint32_t *__restrict__ codes,
   }
 }
 
+// gate_up: block b holds gate columns 32b .. 32b + 31 then up columns N/2 + 32b .. + 31 (the
+// canonical column of packed column n)
 __global__ void pack_w8_kernel(int K, int N, const int8_t *__restrict__ codes,
-                               uint8_t *__restrict__ packed, size_t total_vecs) {
+                               uint8_t *__restrict__ packed, size_t total_vecs, bool gate_up) {
   const size_t per_block = (size_t)(kColBlock8 / kChunkK8) * K;   // 16-byte vectors
   for (size_t o = blockIdx.x * (size_t)blockDim.x + threadIdx.x; o < total_vecs;
        o += (size_t)gridDim.x * blockDim.x) {
@@ -59,11 +61,12 @@ __global__ void pack_w8_kernel(int K, int N, const int8_t *__restrict__ codes,
     const size_t rem = o - (size_t)b * per_block;
     const int wb = N - b * kColBlock8 < kColBlock8 ? N - b * kColBlock8 : kColBlock8;
     const size_t c = rem / wb;
-    const int n = b * kColBlock8 + (int)(rem - c * wb);
+    const int j = (int)(rem - c * wb), n = b * kColBlock8 + j;
+    const int src = !gate_up ? n : j < 32 ? 32 * b + j : N / 2 + 32 * b + (j - 32);
     uint32_t w[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const uint32_t v = (uint8_t)codes[(c * 16 + e) * (size_t)N + n];
+      const uint32_t v = (uint8_t)codes[(c * 16 + e) * (size_t)N + src];
       w[e >> 2] |= v << (8 * (e & 3));
     }
     reinterpret_cast<uint4 *>(packed)[o] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -85,10 +88,10 @@ cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed,
+cudaError_t launch_pack_w8(int K, int N, const int8_t *codes, uint8_t *packed, bool gate_up,
                            cudaStream_t s) {
   const size_t total = (size_t)(K / kChunkK8) * N;
-  pack_w8_kernel<<<grid_for(total, 256), 256, 0, s>>>(K, N, codes, packed, total);
+  pack_w8_kernel<<<grid_for(total, 256), 256, 0, s>>>(K, N, codes, packed, total, gate_up);
   return cudaGetLastError();
 }
 

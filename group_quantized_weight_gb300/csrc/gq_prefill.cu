@@ -27,21 +27,23 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include "gq_internal.h"
+#include "gq_device.cuh"
+#include "gq_tma_host.h"
 
 namespace gq {
 
-constexpr int kPfStages = 4;                 // TMA ring depth (64-k stages)
+constexpr int kPfMaxStages = 12;             // TMA ring depth (64-k stages), at most
 constexpr int kPfDqBufs = 4;                 // dequantized-operand buffers
 constexpr int kPfTileN = 128;                // weight columns per tile (TMEM lanes)
-constexpr int kPfTileM = 256;                // activation rows per tile (TMEM columns)
+constexpr int kPfMaxTileM = 256;             // activation rows per tile (TMEM columns), at most
+static_assert(2 * kPfMaxTileM <= 512, "two accumulators of the tallest tile fill TMEM");
 constexpr int kPfThreads = 512;              // 16 warps = 4 warpgroups
 constexpr int kPfDqWarps = 4;                // warpgroup 1
 constexpr int kPfSumWarps = 8;               // warpgroups 2 and 3
 constexpr uint32_t kPfPackedBytes = 8 * 512;                  // packed codes per stage
-constexpr uint32_t kPfActBytes = kPfTileM * 64 * 2;           // activations per stage
 constexpr uint32_t kPfDqBytes = kPfTileN * 64 * 2;            // dequantized weights per stage
-constexpr uint32_t kPfStageBytes = kPfActBytes + kPfPackedBytes;   // 36864: one TMA stage
+// one TMA stage: the BM x 64 bf16 activation box, then the 128 x 64 packed codes
+__host__ __device__ constexpr uint32_t pf_stage_bytes(int BM) { return (uint32_t)BM * 128 + kPfPackedBytes; }
 // bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
 // gq_set_wait_limit changes it)
 static __device__ long long g_pf_wait_limit = 4000000000ll;
@@ -229,6 +231,25 @@ struct PrefillConsts {
   uint32_t sym;       // 0x43084308: bf16 (128 + 8)
 };
 
+// Tile height, ring depth and K split of a launch.
+struct PrefillShape {
+  int BM;             // activation rows per tile: 64, 128 or 256 (the MMA's N, TMEM columns)
+  int S;              // TMA ring stages
+  int KS;             // K slices of whole groups (1 = no split)
+  float *part;        // [KS][M][N] FP32 slice partial sums (KS > 1)
+  unsigned *counters; // [tiles][8] arrival counters, one per promotion warp's part of a tile
+};
+
+// The groups of a work unit (g0 .. g1 - 1) are visited starting at a rotation that depends
+// on the tile's column index: the CTAs working on one row block of activations then read
+// different 64-k boxes of it at any moment, instead of all of them the same box (an L2 hot
+// spot that held every CTA to one stage per half microsecond).  The i-th group visited:
+__device__ __forceinline__ int pf_group(int g0, int g1, int tn, int i) {
+  const int n = g1 - g0;
+  int g = g0 + i + (tn * 5) % n;
+  return g >= g1 ? g - n : g;
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int SPG, int SC, bool ZP>
@@ -237,28 +258,31 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                   const void *__restrict__ scales, const uint32_t *__restrict__ zeros,
                   __nv_bfloat16 *__restrict__ out_bf16, float *__restrict__ out_f32,
                   int M, int K, int N, int out_f32_flag, const PrefillConsts pc,
-                  unsigned token) {
+                  const PrefillShape sh, unsigned token) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[kPfStages], bar_empty[kPfStages],
+  __shared__ __align__(8) uint64_t bar_full[kPfMaxStages], bar_empty[kPfMaxStages],
       bar_dq[kPfDqBufs], bar_dq_empty[kPfDqBufs], bar_acc_full[2], bar_acc_empty[2];
   __shared__ uint32_t s_tmem;
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // stage layout: [activations 32 KB][dequantized weights 16 KB][packed codes 4 KB]
-  // TMA stage s: [activations 32 KB][packed codes 4 KB]; then kPfDqBufs dequantized
-  // operand buffers of 16 KB
-  auto act_at = [&](int s) { return smem + (size_t)s * kPfStageBytes; };
-  auto pk_at = [&](int s) { return smem + (size_t)s * kPfStageBytes + kPfActBytes; };
-  auto dq_at = [&](int d) { return smem + (size_t)kPfStages * kPfStageBytes + (size_t)d * kPfDqBytes; };
+  // TMA stage s: [activations BM x 128 bytes][packed codes 4 KB] (a multiple of 1 KB, as the
+  // 128-byte swizzle wants); then kPfDqBufs dequantized operand buffers of 16 KB
+  const int BM = sh.BM, S = sh.S, KS = sh.KS;
+  const uint32_t stage_bytes = pf_stage_bytes(BM), act_bytes = (uint32_t)BM * 128;
+  auto act_at = [&](int s) { return smem + (size_t)s * stage_bytes; };
+  auto pk_at = [&](int s) { return smem + (size_t)s * stage_bytes + act_bytes; };
+  auto dq_at = [&](int d) { return smem + (size_t)S * stage_bytes + (size_t)d * kPfDqBytes; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wg = warp >> 2;                        // warpgroup: role and register budget
   const int ng = K / (SPG * 64);                   // groups (K / G)
   const int tiles_n = (N + kPfTileN - 1) / kPfTileN;
-  const int tiles_m = (M + kPfTileM - 1) / kPfTileM;
+  const int tiles_m = (M + BM - 1) / BM;
   const int tiles = tiles_n * tiles_m;
+  // work units: (tile, K slice) pairs, tile fastest; slice z covers groups zsplit(ng, KS, z)
+  const int units = tiles * KS;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
       // a stage is free once the MMA read its activations (commit) and every dequant warp
       // read its codes
@@ -295,18 +319,23 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_w) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
-      uint32_t i = 0;
+      int s = 0;                                     // ring stage and its phase parity
+      uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int tile = u % tiles, z = u / tiles;
         const int tn = tile % tiles_n, tm = tile / tiles_n;
-        for (int kc = 0; kc < K / 64 && ok; ++kc, ++i) {
-          const int s = i % kPfStages;
-          ok = mbar_wait(smem_u32(&bar_empty[s]), ((i / kPfStages) & 1) ^ 1, token);
+        int g0, g1;
+        zsplit_dev(ng, KS, z, g0, g1);
+        for (int kk = 0; kk < (g1 - g0) * SPG && ok; ++kk, s = s + 1 == S ? 0 : s + 1,
+                 ph ^= (s == 0 ? 1u : 0u)) {
+          const int kc = pf_group(g0, g1, tn, kk / SPG) * SPG + kk % SPG;
+          ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, token);
           if (!ok) break;
           const uint32_t fb = smem_u32(&bar_full[s]);
-          mbar_expect_tx(fb, kPfActBytes + kPfPackedBytes);
+          mbar_expect_tx(fb, stage_bytes);
           tma_load_3d(smem_u32(pk_at(s)), &map_w, fb, 0, kc, tn * 8);
-          tma_load_2d(smem_u32(act_at(s)), &map_a, fb, kc * 64, tm * kPfTileM);
+          tma_load_2d(smem_u32(act_at(s)), &map_a, fb, kc * 64, tm * BM);
         }
       }
     }
@@ -314,18 +343,23 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
    } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kPfTileN, kPfTileM);
+      const uint32_t idesc = umma_idesc_bf16(kPfTileN, BM);
       uint32_t i = 0, gg = 0;
+      int s = 0;                                     // ring stage and its phase parity
+      uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-        for (int g = 0; g < ng && ok; ++g, ++gg) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        int g0, g1;
+        zsplit_dev(ng, KS, u / tiles, g0, g1);
+        for (int g = g0; g < g1 && ok; ++g, ++gg) {
           const int b = gg & 1;
           ok = mbar_wait(smem_u32(&bar_acc_empty[b]), ((gg >> 1) & 1) ^ 1, token);
           if (!ok) break;
           tc_fence_after();
-          for (int st = 0; st < SPG; ++st, ++i) {
-            const int s = i % kPfStages, dbuf = i % kPfDqBufs;
-            const uint32_t ph = (i / kPfStages) & 1, dph = (i / kPfDqBufs) & 1;
+          for (int st = 0; st < SPG; ++st, ++i, s = s + 1 == S ? 0 : s + 1,
+                   ph ^= (s == 0 ? 1u : 0u)) {
+            const int dbuf = i % kPfDqBufs;
+            const uint32_t dph = (i / kPfDqBufs) & 1;
             ok = mbar_wait(smem_u32(&bar_full[s]), ph, token) &&
                  mbar_wait(smem_u32(&bar_dq[dbuf]), dph, token);
             if (!ok) break;
@@ -336,7 +370,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             const uint64_t db = umma_desc_sw128(smem_u32(act_at(s)));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              umma_bf16(tmem + (uint32_t)b * kPfTileM, da + 16 * k, db + 2 * k, idesc,
+              umma_bf16(tmem + (uint32_t)b * BM, da + 16 * k, db + 2 * k, idesc,
                         (st | k) != 0 ? 1u : 0u);
             umma_commit(smem_u32(&bar_empty[s]));        // activations consumed
             umma_commit(smem_u32(&bar_dq_empty[dbuf]));  // dequantized operand consumed
@@ -361,10 +395,15 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     const int r0 = lane >> 2;
     const int NW = N >> 3;
     uint32_t i = 0;
+    int s = 0;                                       // ring stage and its phase parity
+    uint32_t ph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      const int tn = tile % tiles_n;
-      for (int g = 0; g < ng && ok; ++g) {
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int tn = (u % tiles) % tiles_n;
+      int g0, g1;
+      zsplit_dev(ng, KS, u / tiles, g0, g1);
+      for (int gi = 0; gi < g1 - g0 && ok; ++gi) {
+        const int g = pf_group(g0, g1, tn, gi);
         uint32_t zl[2] = {pc.sym, pc.sym}, zh[2] = {pc.sym, pc.sym};
         if (ZP) {
 #pragma unroll
@@ -376,9 +415,10 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             zh[u] = (0x4300u | ((wb >> (4 * ((n + 8) & 7))) & 0xFu)) * 0x00010001u;
           }
         }
-        for (int st = 0; st < SPG; ++st, ++i) {
-          const int s = i % kPfStages, dbuf = i % kPfDqBufs;
-          const uint32_t ph = (i / kPfStages) & 1, dph = (i / kPfDqBufs) & 1;
+        for (int st = 0; st < SPG; ++st, ++i, s = s + 1 == S ? 0 : s + 1,
+                 ph ^= (s == 0 ? 1u : 0u)) {
+          const int dbuf = i % kPfDqBufs;
+          const uint32_t dph = (i / kPfDqBufs) & 1;
           // the buffer was read by the MMA of stage i - kPfDqBufs; the codes of stage i arrived
           ok = mbar_wait(smem_u32(&bar_dq_empty[dbuf]), dph ^ 1, token) &&
                mbar_wait(smem_u32(&bar_full[s]), ph, token);
@@ -430,56 +470,104 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     float sum[128];
     uint32_t gg = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    const int hb = BM / 2;                         // activation rows of this warp's half
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int tile = u % tiles, z = u / tiles;
       const int tn = tile % tiles_n, tm = tile / tiles_n;
+      int g0, g1;
+      zsplit_dev(ng, KS, z, g0, g1);
       const int ncol = min(tn * kPfTileN + row, N - 1);
 #pragma unroll
       for (int c = 0; c < 128; ++c) sum[c] = 0.f;
-      float sc_next = load_scale(ncol, 0);
-      for (int g = 0; g < ng; ++g, ++gg) {
-        const float sc = sc_next;
-        if (g + 1 < ng) sc_next = load_scale(ncol, g + 1);   // one group ahead
+      // the group scales, four groups ahead of their use: a group's MMAs take only a few
+      // hundred cycles with 64- and 128-row tiles, less than a load's latency
+      const int ngu = g1 - g0;
+      float sc1 = load_scale(ncol, pf_group(g0, g1, tn, 0));
+      float sc2 = 1 < ngu ? load_scale(ncol, pf_group(g0, g1, tn, 1)) : 0.f;
+      float sc3 = 2 < ngu ? load_scale(ncol, pf_group(g0, g1, tn, 2)) : 0.f;
+      float sc4 = 3 < ngu ? load_scale(ncol, pf_group(g0, g1, tn, 3)) : 0.f;
+      for (int gi = 0; gi < ngu; ++gi, ++gg) {
+        const float sc = sc1;
+        sc1 = sc2;
+        sc2 = sc3;
+        sc3 = sc4;
+        if (gi + 4 < ngu) sc4 = load_scale(ncol, pf_group(g0, g1, tn, gi + 4));
         const int b = gg & 1;
         ok = mbar_wait(smem_u32(&bar_acc_full[b]), (gg >> 1) & 1, token);
         ok = __all_sync(0xffffffffu, ok);         // tcgen05.ld below is warp-collective
         if (!ok) break;
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)b * kPfTileM +
-                               (uint32_t)half * 128;
+        const uint32_t taddr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)b * BM +
+                               (uint32_t)half * hb;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          float v[32];
-          tmem_ld32(taddr + c4 * 32, v);
-          tmem_wait_ld();
+          if (c4 * 32 < hb) {                       // BM / 64 loads of 32 columns
+            float v[32];
+            tmem_ld32(taddr + c4 * 32, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            ffma2_bcast(sum[c4 * 32 + c], sum[c4 * 32 + c + 1], v[c], v[c + 1], sc);
+            for (int c = 0; c < 32; c += 2)
+              ffma2_bcast(sum[c4 * 32 + c], sum[c4 * 32 + c + 1], v[c], v[c + 1], sc);
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_acc_empty[b]));
       }
       if (!ok) break;
-      // the tile's output: column n = tn * 128 + row, rows m = tm * 256 + half * 128 + c.
+      const int n = tn * kPfTileN + row;
+      const int mb = tm * BM + half * hb;
+      if (KS > 1) {
+        // K split: publish this slice's partial sums of the warp's part of the tile (32
+        // columns x BM / 2 rows); the warp that adds the last of the KS slices to the part's
+        // counter sums them in slice order 0, 1, ... (the same order whichever arrives last)
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int m = mb + c;
+          if (c < hb && m < M && n < N) __stcg(sh.part + ((size_t)z * M + m) * N + n, sum[c]);
+        }
+        __threadfence();
+        __syncwarp();
+        unsigned last = 0u;
+        if (lane == 0) {
+          unsigned *ctr = sh.counters + (size_t)tile * kPfSumWarps + wq;
+          last = atomicAdd(ctr, 1u) == (unsigned)(KS - 1) ? 1u : 0u;
+          if (last) *ctr = 0u;                      // every slice has arrived: reset
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        __threadfence();
+        // every slice's partial, this warp's own included, read back in slice order
+#pragma unroll
+        for (int c = 0; c < 128; ++c) sum[c] = 0.f;
+        for (int z2 = 0; z2 < KS; ++z2) {
+          const float *pz = sh.part + (size_t)z2 * M * N + n;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int m = mb + c;
+            if (c < hb && m < M && n < N) sum[c] += __ldcg(pz + (size_t)m * N);
+          }
+        }
+      }
+      // the tile's output: column n = tn * 128 + row, rows m = tm * BM + half * BM / 2 + c.
       // Lanes pair up (lane, lane ^ 1) to write two adjacent columns per store: for rows
       // (m, m + 1) the even lane writes row m, columns (n, n + 1), the odd lane row m + 1,
       // columns (n - 1, n).  N is even, so both columns of a pair are in or out of range.
-      const int n = tn * kPfTileN + row;
-      const int mb = tm * kPfTileM + half * 128;
       const int ncol0 = n - (odd ? 1 : 0);
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float mine_keep = odd ? sum[c + 1] : sum[c];
-        const float mine_send = odd ? sum[c] : sum[c + 1];
-        const float other = __shfl_xor_sync(0xffffffffu, mine_send, 1);
-        const float lo = odd ? other : mine_keep, hi = odd ? mine_keep : other;
-        const int m = mb + c + (odd ? 1 : 0);
-        if (m < M && ncol0 < N) {
-          if (out_f32_flag) {
-            *reinterpret_cast<float2 *>(out_f32 + (size_t)m * N + ncol0) = make_float2(lo, hi);
-          } else {
-            *reinterpret_cast<__nv_bfloat162 *>(out_bf16 + (size_t)m * N + ncol0) =
-                __floats2bfloat162_rn(lo, hi);
+        if (c < hb) {
+          const float mine_keep = odd ? sum[c + 1] : sum[c];
+          const float mine_send = odd ? sum[c] : sum[c + 1];
+          const float other = __shfl_xor_sync(0xffffffffu, mine_send, 1);
+          const float lo = odd ? other : mine_keep, hi = odd ? mine_keep : other;
+          const int m = mb + c + (odd ? 1 : 0);
+          if (m < M && ncol0 < N) {
+            if (out_f32_flag) {
+              *reinterpret_cast<float2 *>(out_f32 + (size_t)m * N + ncol0) = make_float2(lo, hi);
+            } else {
+              *reinterpret_cast<__nv_bfloat162 *>(out_bf16 + (size_t)m * N + ncol0) =
+                  __floats2bfloat162_rn(lo, hi);
+            }
           }
         }
       }
@@ -496,38 +584,14 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
 
 // ------------------------------------------------------------------ host side
 
-// cuTensorMapEncodeTiled is a driver-API call; it is fetched through the runtime so that the
-// library does not link libcuda directly (it then loads on machines without a driver).
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static std::atomic<EncodeTiledFn> fn{nullptr};
-  EncodeTiledFn f = fn.load();
-  if (f) return f;
-  void *p = nullptr;
-  cudaDriverEntryPointQueryResult q{};
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                       &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || !p) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  f = reinterpret_cast<EncodeTiledFn>(p);
-  fn.store(f);
-  return f;
-}
-
-static int encode_maps(int M, int K, int N, const void *A, const void *Wq, CUtensorMap *mw,
-                       CUtensorMap *ma) {
+static int encode_maps(int M, int K, int N, int BM, const void *A, const void *Wq,
+                       CUtensorMap *mw, CUtensorMap *ma) {
   // packed codes as uint32 [tiles][K/64 chunks][128 words]
   const cuuint64_t wdims[3] = {128, (cuuint64_t)(K / 64), (cuuint64_t)((N + 15) / 16)};
   const cuuint64_t wstr[2] = {512, (cuuint64_t)(K / 64) * 512};
   const cuuint32_t wbox[3] = {128, 1, 8};
   const cuuint32_t ones[3] = {1, 1, 1};
-  const EncodeTiledFn enc = encode_fn();
+  const EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) {
     note_cuda_error_code("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", -1);
     return GQ_ERR_CUDA;
@@ -541,10 +605,10 @@ static int encode_maps(int M, int K, int N, const void *A, const void *Wq, CUten
     note_cuda_error_code("cuTensorMapEncodeTiled(packed codes)", (int)r);
     return GQ_ERR_CUDA;
   }
-  // activations bf16 [M][K], 256 rows x 64 k per box, 128-byte swizzle
+  // activations bf16 [M][K], BM rows x 64 k per box, 128-byte swizzle
   const cuuint64_t adims[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t astr[1] = {(cuuint64_t)K * 2};
-  const cuuint32_t abox[2] = {64, (cuuint32_t)kPfTileM};
+  const cuuint32_t abox[2] = {64, (cuuint32_t)BM};
   r = enc(ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(A), adims,
                              astr, abox, ones, CU_TENSOR_MAP_INTERLEAVE_NONE,
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -562,8 +626,15 @@ static unsigned next_token() {
   return t.fetch_add(1u) + 1u;
 }
 
-size_t prefill_smem_bytes() {
-  return (size_t)kPfStages * kPfStageBytes + (size_t)kPfDqBufs * kPfDqBytes + 1024;
+size_t prefill_smem_bytes(int BM, int stages) {
+  return (size_t)stages * pf_stage_bytes(BM) + (size_t)kPfDqBufs * kPfDqBytes + 1024;
+}
+
+// The deepest ring (at most kPfMaxStages) of BM-row stages that fits smem_cap bytes.
+int prefill_stages(int BM, size_t smem_cap) {
+  for (int s = kPfMaxStages; s >= 2; --s)
+    if (prefill_smem_bytes(BM, s) <= smem_cap) return s;
+  return 0;
 }
 
 bool prefill_supported(int M, int K, int N, int G, int prec) {
@@ -575,7 +646,7 @@ bool prefill_supported(int M, int K, int N, int G, int prec) {
 template <int SPG, int SC, bool ZP>
 static cudaError_t launch_pf(const Plan &p, int M, int K, int N, int prec, const CUtensorMap &mw,
                              const CUtensorMap &ma, const void *scales, const void *zeros,
-                             void *out, cudaStream_t s) {
+                             void *out, float *part, unsigned *counters, cudaStream_t s) {
   auto kern = w4_prefill_kernel<SPG, SC, ZP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)p.smem_bytes);
@@ -588,36 +659,39 @@ static cudaError_t launch_pf(const Plan &p, int M, int K, int N, int prec, const
       mw, ma, scales, reinterpret_cast<const uint32_t *>(zeros),
       f32 ? nullptr : reinterpret_cast<__nv_bfloat16 *>(out), f32 ? reinterpret_cast<float *>(out) : nullptr,
       M, K, N, f32 ? 1 : 0, PrefillConsts{0x43004300u, 0x43084308u},
-      next_token());
+      PrefillShape{p.m_tile, p.slots, p.nsplit, part, counters}, next_token());
   return cudaGetLastError();
 }
 
 template <int SPG, int SC>
 static cudaError_t launch_pf_z(const Plan &p, int M, int K, int N, int prec, const CUtensorMap &mw,
                                const CUtensorMap &ma, const void *scales, const void *zeros,
-                               void *out, cudaStream_t s) {
-  if (prec & GQ_ZP) return launch_pf<SPG, SC, true>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
-  return launch_pf<SPG, SC, false>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+                               void *out, float *part, unsigned *counters, cudaStream_t s) {
+  if (prec & GQ_ZP)
+    return launch_pf<SPG, SC, true>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
+  return launch_pf<SPG, SC, false>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
 }
 
 template <int SPG>
 static cudaError_t launch_pf_s(const Plan &p, int M, int K, int N, int prec, const CUtensorMap &mw,
                                const CUtensorMap &ma, const void *scales, const void *zeros,
-                               void *out, cudaStream_t s) {
-  if (prec & GQ_SC_F32) return launch_pf_z<SPG, kScF32>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
-  if (prec & GQ_SC_BF16) return launch_pf_z<SPG, kScBF16>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
-  return launch_pf_z<SPG, kScF16>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+                               void *out, float *part, unsigned *counters, cudaStream_t s) {
+  if (prec & GQ_SC_F32)
+    return launch_pf_z<SPG, kScF32>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
+  if (prec & GQ_SC_BF16)
+    return launch_pf_z<SPG, kScBF16>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
+  return launch_pf_z<SPG, kScF16>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
 }
 
 cudaError_t launch_prefill(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
                            const void *Wq, const void *scales, const void *zeros, void *out,
-                           cudaStream_t s) {
+                           float *part, unsigned *counters, cudaStream_t s) {
   CUtensorMap mw, ma;
-  if (encode_maps(M, K, N, A, Wq, &mw, &ma) != GQ_OK) return cudaErrorInvalidValue;
+  if (encode_maps(M, K, N, p.m_tile, A, Wq, &mw, &ma) != GQ_OK) return cudaErrorInvalidValue;
   switch (G) {
-    case 64: return launch_pf_s<1>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
-    case 128: return launch_pf_s<2>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
-    case 256: return launch_pf_s<4>(p, M, K, N, prec, mw, ma, scales, zeros, out, s);
+    case 64: return launch_pf_s<1>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
+    case 128: return launch_pf_s<2>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
+    case 256: return launch_pf_s<4>(p, M, K, N, prec, mw, ma, scales, zeros, out, part, counters, s);
     default: return cudaErrorInvalidValue;
   }
 }

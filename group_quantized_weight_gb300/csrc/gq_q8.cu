@@ -85,6 +85,8 @@ struct QbParams {
   int KS;                     // K slices (groups split as evenly as possible)
   int NB;                     // column blocks of 64
   int out_f32;
+  int gate_up;                // fused gate+up: block b = gate columns 32b.. then up N/2 + 32b..;
+                              // out [M][N/2] = silu(gate) * up
 };
 
 // Rows per warp RT (1, 2, 4 or 8) and row blocks RB (1, 2 or 4) for M rows.
@@ -142,7 +144,9 @@ __global__ void __launch_bounds__(kQbThreads, 2) q8_block_kernel(const QbParams 
   const int c0 = gp0 * cpg, nch = (gp1 - gp0) * cpg;
   const uint4 *blk = p.Wp + (size_t)nb * (kQbCols / kChunkK8) * K + (size_t)c0 * wb;
   const uint4 *wa = blk + ja, *wc = blk + jc;
-  const float *sca = p.S + n0 + ja, *scc = p.S + n0 + jc;
+  // scales of this lane's two columns (gate+up: gate column 32 nb + lane, up N/2 + 32 nb + lane)
+  const float *sca = p.S + (p.gate_up ? 32 * nb + ja : n0 + ja);
+  const float *scc = p.S + (p.gate_up ? N / 2 + 32 * nb + (jc - 32) : n0 + jc);
 
   // the first PD chunk pairs (and the scales of the groups they open) go out before the
   // activations are staged.  Ring slot j of this warp: [2 columns][32 lanes][16 bytes] after
@@ -254,6 +258,19 @@ __global__ void __launch_bounds__(kQbThreads, 2) q8_block_kernel(const QbParams 
   }
   __syncthreads();
   const bool split = p.KS > 1;
+  if (p.gate_up && !split) {
+    // gate column c < 32 of the block and its up column c + 32: out[m][32 nb + c]
+    for (int idx = threadIdx.x; idx < M * 32; idx += blockDim.x) {
+      const int m = idx >> 5, c = idx & 31;
+      float g = 0.f, u = 0.f;
+      for (int q = 0; q < KP; ++q) {
+        g += red[((size_t)q * MR + m) * kQbCols + c];
+        u += red[((size_t)q * MR + m) * kQbCols + 32 + c];
+      }
+      store_out_rt(p.out, (size_t)m * (N / 2) + 32 * nb + c, silu_mul(g, u), p.out_f32 != 0);
+    }
+    return;
+  }
   for (int idx = threadIdx.x; idx < M * kQbCols; idx += blockDim.x) {
     const int m = idx / kQbCols, c = idx - m * kQbCols, n = n0 + c;
     float sum = 0.f;
@@ -268,6 +285,18 @@ __global__ void __launch_bounds__(kQbThreads, 2) q8_block_kernel(const QbParams 
   if (!split) return;
   // the last CTA of this column block adds the K slices in slice order
   if (!last_arriver(p.counters + nb, p.KS)) return;
+  if (p.gate_up) {
+    for (int idx = threadIdx.x; idx < M * 32; idx += blockDim.x) {
+      const int m = idx >> 5, c = idx & 31;
+      float g = 0.f, u = 0.f;
+      for (int s2 = 0; s2 < p.KS; ++s2) {
+        g += __ldcg(p.part + ((size_t)s2 * M + m) * N + n0 + c);
+        u += __ldcg(p.part + ((size_t)s2 * M + m) * N + n0 + 32 + c);
+      }
+      store_out_rt(p.out, (size_t)m * (N / 2) + 32 * nb + c, silu_mul(g, u), p.out_f32 != 0);
+    }
+    return;
+  }
   for (int idx = threadIdx.x; idx < M * kQbCols; idx += blockDim.x) {
     const int m = idx / kQbCols, n = n0 + idx - m * kQbCols;
     if (n >= N) continue;
@@ -308,6 +337,7 @@ struct QmParams {
   int M, K, N, G;
   int KS, NB;
   int out_f32;
+  int gate_up;                // fused gate+up (as QbParams)
 };
 
 __host__ __device__ inline int q8m_rows8(int M) { return (M + 7) / 8 * 8; }
@@ -386,7 +416,9 @@ __global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p)
   const float *ssm = reinterpret_cast<const float *>(smq + area);
   for (int idx = threadIdx.x; idx < (gs1 - gs0) * 16; idx += blockDim.x) {
     const int gr = idx >> 4, q = idx & 15, col = min(q * 4, wb - 4);
-    cp16(smq_s + (uint32_t)(area + gr * 256 + q * 16), p.S + (size_t)(gs0 + gr) * N + n0 + col);
+    // gate+up: block columns 0 .. 31 are gate columns 32 nb.., 32 .. 63 up columns N/2 + 32 nb..
+    const int src = !p.gate_up ? n0 + col : col < 32 ? 32 * nb + col : N / 2 + 32 * nb + (col - 32);
+    cp16(smq_s + (uint32_t)(area + gr * 256 + q * 16), p.S + (size_t)(gs0 + gr) * N + src);
   }
   cp_commit();
   const uint32_t ring_s = smq_s + (uint32_t)(area + sbytes) + (uint32_t)(warp * kQmPD * 512);
@@ -521,6 +553,16 @@ __global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p)
     }
   __syncthreads();
   const bool split = p.KS > 1;
+  if (p.gate_up && !split) {
+    // gate column c < 32 of the block and its up column c + 32: out[m][32 nb + c]
+    for (int idx = threadIdx.x; idx < M * 32; idx += blockDim.x) {
+      const int m = idx >> 5, c = idx & 31;
+      const float g = red[(size_t)m * 64 + c] + red[((size_t)MR8 + m) * 64 + c];
+      const float u = red[(size_t)m * 64 + 32 + c] + red[((size_t)MR8 + m) * 64 + 32 + c];
+      store_out_rt(p.out, (size_t)m * (N / 2) + 32 * nb + c, silu_mul(g, u), p.out_f32 != 0);
+    }
+    return;
+  }
   for (int idx = threadIdx.x; idx < M * 64; idx += blockDim.x) {
     const int m = idx >> 6, c = idx & 63, n = n0 + c;
     const float sum = red[(size_t)m * 64 + c] + red[((size_t)MR8 + m) * 64 + c];
@@ -533,6 +575,18 @@ __global__ void __launch_bounds__(kQmThreads, 2) q8_mma_kernel(const QmParams p)
   }
   if (!split) return;
   if (!last_arriver(p.counters + nb, p.KS)) return;
+  if (p.gate_up) {
+    for (int idx = threadIdx.x; idx < M * 32; idx += blockDim.x) {
+      const int m = idx >> 5, c = idx & 31;
+      float g = 0.f, u = 0.f;
+      for (int s2 = 0; s2 < p.KS; ++s2) {
+        g += __ldcg(p.part + ((size_t)s2 * M + m) * N + n0 + c);
+        u += __ldcg(p.part + ((size_t)s2 * M + m) * N + n0 + 32 + c);
+      }
+      store_out_rt(p.out, (size_t)m * (N / 2) + 32 * nb + c, silu_mul(g, u), p.out_f32 != 0);
+    }
+    return;
+  }
   for (int idx = threadIdx.x; idx < M * 64; idx += blockDim.x) {
     const int m = idx >> 6, c = idx & 63, n = n0 + c;
     if (c >= wb) continue;
@@ -586,6 +640,7 @@ cudaError_t launch_q8_mma(const Plan &pl, int M, int K, int N, int G, int prec, 
   qp.Wp = reinterpret_cast<const uint4 *>(Wq);
   qp.A = reinterpret_cast<const float *>(A);
   qp.S = reinterpret_cast<const float *>(scales);
+  qp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
   qp.out = out;
   qp.part = part;
   qp.counters = counters;
@@ -662,6 +717,7 @@ cudaError_t launch_q8_block(const Plan &pl, int M, int K, int N, int G, int prec
   QbParams qp;
   qp.Wp = reinterpret_cast<const uint4 *>(Wq);
   qp.A = reinterpret_cast<const float *>(A);
+  qp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
   qp.S = reinterpret_cast<const float *>(scales);
   qp.out = out;
   qp.part = part;

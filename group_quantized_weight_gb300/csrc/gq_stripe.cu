@@ -400,6 +400,8 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
     }
     const uint8_t *slot = ring + (size_t)s * SLOTB;
     const uint8_t *ssc = slot + kSlotChunks * 512;          // the slot's scales
+    // a group's MMA accumulators (a group may span chunks; never a slot: G <= 256)
+    float d[MT][4];
 #pragma unroll
     for (int ch = 0; ch < kSlotChunks; ++ch) {
       const uint4 wv = *reinterpret_cast<const uint4 *>(slot + ch * 512 + lane * 16);
@@ -413,7 +415,6 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
         bq[mt][4] = hi.x; bq[mt][5] = hi.y; bq[mt][6] = hi.z; bq[mt][7] = hi.w;
       }
       const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-      float d[MT][4];
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int stp = ch * 4 + jj;                 // compile-time 16-k step of the slot

@@ -48,13 +48,14 @@ typedef enum gq_status {
 #define GQ_SC_BF16 0x08  /* scales bf16                                                        */
 #define GQ_SC_F32  0x10  /* scales fp32; neither SC flag = fp16                                */
 #define GQ_OUT_F32 0x20  /* output fp32; clear = bf16 (round to nearest even)                  */
-#define GQ_GATE_UP  0x80 /* W4 fused gate+up projection: the N = 2F columns are F gate columns
+#define GQ_GATE_UP  0x80 /* fused gate+up projection: the N = 2F columns are F gate columns
                             then F up columns, and out is [M][F] = silu(gate) * up (silu(x) =
                             x / (1 + e^-x), in FP32 on the FP32 GEMM results, then rounded).
                             gq_pack_weights must get the flag too (it interleaves gate and up
-                            columns tile by tile).  Needs N % 16 == 0 and, in gq_gemm,
-                            K % 256 == 0 and M <= 64: the decode and small-batch kernels
-                            (else GQ_ERR_UNSUPPORTED)                                         */
+                            columns: W4 tile by tile, W8 64-column block by block).  W4: N % 16
+                            == 0 and, in gq_gemm, K % 256 == 0 and M <= 64 (the decode and
+                            small-batch kernels); W8: N % 64 == 0 and M <= 32 (the INT8 CUDA-
+                            core and tensor-core kernels); else GQ_ERR_UNSUPPORTED          */
 #define GQ_ACT_I8  0x100  /* INT8-activation variant (gq_gemm_a8, and gq_plan / gq_workspace_size
                             for it): activations are int8 codes with one fp32 scale per (row,
                             group); W8 codes and GQ_SC_F32 only; gq_gemm refuses it         */

@@ -254,17 +254,17 @@ def silu(x) -> np.ndarray:
 
 
 def silu_mul_reference(A_raw, codes, scales, zeros, *, K: int, N: int, G: int, act: str,
-                       sc: str, rows=None, cols=None):
+                       sc: str, rows=None, cols=None, w4: bool = True):
     """out[m][j] = silu(gate[m][j]) · up[m][j] with gate = column j < F = N/2 and up = column
-    F + j of the group GEMM (W4 codes).  Returns (ref, mag) over output columns ``cols``
+    F + j of the group GEMM (W4 or W8 codes).  Returns (ref, mag) over output columns ``cols``
     (default all F).  mag carries the GEMM's own error bound through the product to first
     order: max|silu'| · mag_gate · |up| + |silu(gate)| · mag_up, where |silu'(x)| =
     |σ(x)·(1 + x·(1 − σ(x)))| < 1.1 for every x, so ``tolerance``/``check`` apply unchanged."""
     F = N // 2
     jc = np.arange(F) if cols is None else np.asarray(cols)
-    g, mg = reference(A_raw, codes, scales, zeros, K=K, N=N, G=G, w4=True, act=act, sc=sc,
+    g, mg = reference(A_raw, codes, scales, zeros, K=K, N=N, G=G, w4=w4, act=act, sc=sc,
                       rows=rows, cols=jc)
-    u, mu = reference(A_raw, codes, scales, zeros, K=K, N=N, G=G, w4=True, act=act, sc=sc,
+    u, mu = reference(A_raw, codes, scales, zeros, K=K, N=N, G=G, w4=w4, act=act, sc=sc,
                       rows=rows, cols=F + jc)
     sg = silu(g)
     return sg * u, 1.1 * mg * np.abs(u) + np.abs(sg) * mu

@@ -147,6 +147,13 @@ PREFILL_SHAPES = [
     # the smallest row counts the prefill kernel takes: one 256-row tile, mostly past M
     gq_synth.Config("pf_m33", M=33, K=512, N=136, G=128),
     gq_synth.Config("pf_m64_zp", M=64, K=1024, N=256, G=64, zp=True, sc="bf16", out="f32"),
+    # the mid-M tiles: 64- and 128-row activation tiles, split K over whole groups with a
+    # ragged last 128-column tile, rows past M in the last tile
+    gq_synth.Config("pf_m33_split", M=33, K=4096, N=1032, G=128, zp=True),
+    gq_synth.Config("pf_m64_split", M=64, K=4096, N=2056, G=128, outlier_frac=0.001),
+    gq_synth.Config("pf_m100_bm128", M=100, K=2048, N=520, G=64, sc="bf16"),
+    gq_synth.Config("pf_m128_f32", M=128, K=1024, N=392, G=128, sc="f32", out="f32"),
+    gq_synth.Config("pf_m300_ragged", M=300, K=1024, N=392, G=256, zp=True),
 ]
 
 
@@ -159,14 +166,39 @@ def test_prefill_shapes(gq, cfg):
     assert gq.gq_device_error() == 0
 
 
-def test_prefill_integer_inputs_are_bit_exact(gq):
-    cfg = gq_synth.Config("pf_exact", M=384, K=1024, N=256, G=128, zp=True, a_kind="int",
+@pytest.mark.parametrize("M,K,N", [(384, 1024, 256), (64, 4096, 1032), (128, 2048, 264)])
+def test_prefill_integer_inputs_are_bit_exact(gq, M, K, N):
+    """Integer activations and power-of-two scales: every partial sum is exact in FP32, so the
+    output equals the oracle bit for bit, the split-K slices' sums included."""
+    cfg = gq_synth.Config("pf_exact", M=M, K=K, N=N, G=128, zp=True, a_kind="int",
                           pow2_scales=True)
     inp = gq_synth.make_inputs(cfg, seed=2)
     out, _ = run_gemm(gq, cfg, inp)
     ref, _ = _oracle(cfg, inp)
     h = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(h, oracle.f64_to_bf16_bits(ref))
+
+
+def test_prefill_forced_split_counts_match_the_oracle(gq):
+    """The tcgen05 kernel's K split at one, two and the largest slice count (16 here), on a
+    64-row problem with a ragged last tile."""
+    cfg = gq_synth.Config("pf_split", M=64, K=4096, N=392, G=128, zp=True, sc="bf16")
+    inp = gq_synth.make_inputs(cfg, seed=9)
+    ref, mag = _oracle(cfg, inp)
+    prec = prec_of(cfg)
+    counts = []
+    try:
+        for n in (1, 2, -1):
+            gq.gq_set_split_override(n)
+            plan = gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)
+            assert plan["path"] == 2
+            counts.append(plan["nsplit"])
+            out, _ = run_gemm(gq, cfg, inp)
+            _assert_parity(cfg, out_to_f64(out, cfg.out), ref, mag)
+    finally:
+        gq.gq_set_split_override(0)
+    assert counts == [1, 2, 16]
+    assert gq.gq_device_error() == 0
 
 
 # ------------------------------------------------------------------ float zero points
@@ -467,6 +499,16 @@ GATE_UP_SHAPES = [
     gq_synth.Config("gu_m12_split_f32", M=12, K=8192, N=288, G=64, sc="f32", out="f32"),
     gq_synth.Config("gu_m40_g32_split", M=40, K=4096, N=544, G=32, zp=True),
     gq_synth.Config("gu_m33_g64", M=33, K=1024, N=160, G=64),
+    # INT8 codes (Q8_0 form): the CUDA-core kernel (M <= 4) and the tensor-core one, with and
+    # without a K split, fp32 and bf16 output
+    gq_synth.Config("gu_q8_m1", M=1, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("gu_q8_m3_split", M=3, K=2048, N=128, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("gu_q8_m12", M=12, K=1024, N=640, G=32, w4=False, act="f32", sc="f32",
+                    out="bf16", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("gu_q8_m32_g64", M=32, K=2048, N=256, G=64, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
 ]
 
 
@@ -483,7 +525,7 @@ def _gate_up_case(gq, cfg, seed, cols=None):
     got = out_to_f64(out, cfg.out)
     ref, mag = oracle.silu_mul_reference(inp["A"], inp["codes"], inp["scales"], inp["zeros"],
                                          K=cfg.K, N=cfg.N, G=cfg.G, act=cfg.act, sc=cfg.sc,
-                                         cols=cols)
+                                         cols=cols, w4=cfg.w4)
     if cols is not None:
         got = got[:, cols]
     return _assert_parity(cfg, got, ref, mag), (A, packed, S, Z, prec)
@@ -522,6 +564,21 @@ def test_gate_up_small_batch_full_size_sampled_and_repeatable(gq):
     gq.gemm_t(A, packed, S, Z, o2, cfg.M, cfg.K, cfg.N, cfg.G, prec)
     torch.cuda.synchronize()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_gate_up_q8_full_size_sampled_and_repeatable(gq):
+    """The fused gate+up Q8_0 GEMM at its full size (K = 2048, N = 2·6144, G = 32) for one and
+    32 rows, 512 sampled output columns against the oracle; a second call gives the same bits."""
+    for name in ("q8_m1", "q8_m32"):
+        cfg = gq_synth.CONFIGS[name]
+        cols = np.random.default_rng(13).choice(cfg.N // 2, 512, replace=False)
+        _, (A, packed, S, Z, prec) = _gate_up_case(gq, cfg, seed=0, cols=cols)
+        o1 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+        o2 = alloc_out(cfg.M, cfg.N // 2, cfg.out)
+        gq.gemm_t(A, packed, S, Z, o1, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+        gq.gemm_t(A, packed, S, Z, o2, cfg.M, cfg.K, cfg.N, cfg.G, prec)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2)
 
 
 def test_pack_gate_up_interleaves_gate_and_up_columns(gq):

@@ -126,11 +126,13 @@ def test_plan_is_a_pure_function_of_shape(name):
     assert p1 == p2
     units = cfg.K // max(cfg.G, 64 if cfg.w4 else cfg.G)
     if p1["path"] == 2:
-        # tcgen05 prefill: persistent, at most one CTA per SM, no scratch; one CTA holds the
-        # shared-memory ring (at most 227 KiB per CTA on sm_103a)
+        # tcgen05 prefill: persistent, at most one CTA per SM; one CTA holds the shared-memory
+        # ring (at most 227 KiB per CTA on sm_103a); activation tiles of 64, 128 or 256 rows;
+        # scratch only with a K split
         assert cfg.M >= 33 and cfg.w4
         assert 1 <= p1["grid_x"] <= 152
-        assert p1["workspace_bytes"] == 0
+        assert p1["m_tile"] == (64 if cfg.M <= 64 else 128 if cfg.M <= 128 else 256)
+        assert (p1["workspace_bytes"] > 0) == (p1["nsplit"] > 1)
         assert p1["smem_bytes"] <= 227 * 1024
         return
     if p1["path"] == 3:
@@ -277,10 +279,17 @@ def test_algorithmic_bytes_match_the_worked_figures():
 
 def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     gu = C.GQ_W4 | C.GQ_GATE_UP
-    # N must hold whole 16-column tiles of 8 gate and 8 up columns; INT8 has no fused epilogue
+    # N must hold whole 16-column tiles of 8 gate and 8 up columns (W4) or whole 64-column
+    # blocks of 32 and 32 (W8)
+    W8GU = C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_GATE_UP
     assert gq.gq_gemm(1, 512, 24, 128, gu, 16, 16, 16, None, 16, None) == 1
-    assert gq.gq_gemm(1, 512, 32, 32, C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_GATE_UP,
-                      16, 16, 16, None, 16, None) == 2
+    assert gq.gq_gemm(1, 512, 32, 32, W8GU, 16, 16, 16, None, 16, None) == 1
+    # INT8: the CUDA-core kernel up to four rows, the tensor-core one to 32; not above
+    assert gq.gq_plan(1, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 5
+    assert gq.gq_plan(32, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 6
+    with pytest.raises(C.GqError) as e:
+        gq.gq_plan(33, 2048, 12288, 32, W8GU, sm_count=152)
+    assert e.value.status == 2
     # the decode and small-batch kernels (K % 256 == 0) carry the epilogue: the
     # warp-specialized one up to four rows, the striped one to eight, the small-batch one to
     # 64 rows; not the prefill kernel, which would take 33 rows and more without it
@@ -440,3 +449,17 @@ def test_fault_injection_and_wait_limit_settings_are_validated():
     import torch
     if not torch.cuda.is_available():
         assert f(0) == 7 and f(2_000_000) == 7            # no device: GQ_ERR_NO_DEVICE
+
+
+def test_prefill_plan_tiles_and_split_follow_the_rows():
+    """Few rows: 64-row activation tiles and a K split of whole groups that keeps every SM
+    busy (112 tiles x 4 slices = 448 units, about three waves of 152), while the partial sums
+    stay within the packed weight bytes; from 65 rows 128-row tiles, from 129 rows 256."""
+    W4 = C.GQ_W4
+    p = gq.gq_plan(64, 4096, 14336, 128, W4, sm_count=152)
+    assert (p["path"], p["m_tile"], p["nsplit"], p["grid_x"]) == (2, 64, 4, 152)
+    assert p["workspace_bytes"] >= 4 * 64 * 14336 * 4
+    p = gq.gq_plan(128, 4096, 14336, 128, W4, sm_count=152)
+    assert (p["path"], p["m_tile"], p["nsplit"]) == (2, 128, 1)
+    p = gq.gq_plan(4096, 4096, 14336, 128, W4, sm_count=152)
+    assert (p["path"], p["m_tile"], p["nsplit"], p["workspace_bytes"]) == (2, 256, 1, 0)
