@@ -265,11 +265,12 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   if (!gate_up && M >= kPrefillMinM && !(prec & GQ_ZP_FLOAT) &&
       prefill_supported(M, K, N, G, prec)) {
     // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM.  Activation tiles of 64,
-    // 128 or 256 rows (the MMA's N) so that few rows do not pay for a 256-row product, the
-    // deepest TMA ring that fits, and a K split of whole groups when the 128-column tiles are
-    // too few to keep every SM busy: the count that minimises the waves of (tile, slice)
-    // units per slice, among those whose FP32 partial sums (written and read once) stay
-    // within the packed weight bytes
+    // 128 or 256 rows (the MMA's N) so that few rows do not pay for a 256-row product, and
+    // the deepest TMA ring that fits.  The kernel can also split K into slices of whole
+    // groups (a last-arriver reduction of FP32 partials), but on GB300 every split measured
+    // slower than none: a slice's fixed costs (pipeline start, partial sums out and back)
+    // are worth more than the SMs the unsplit grid leaves idle, so the split is only taken
+    // when a caller forces it
     p->path = kPathPrefill;
     const int BM = M <= 64 ? 64 : M <= 128 ? 128 : 256;
     p->m_tile = BM;
@@ -278,17 +279,6 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->units = K / G;
     const int tiles = ceil_div(N, 128) * ceil_div(M, BM);
     int ks = 1;
-    double best = 1.0;
-    for (int k2 = 2; k2 <= 16 && k2 <= p->units; ++k2) {
-      if ((double)k2 * M * N * 8.0 > (double)K * N / 2.0) break;
-      if ((size_t)k2 * M * N * 4 > kPartCap) break;
-      const double cost = (double)ceil_div(tiles * k2, sms) / k2 /
-                          (double)ceil_div(tiles, sms);
-      if (cost < best * (1.0 - 1e-9)) {
-        best = cost;
-        ks = k2;
-      }
-    }
     if (split_override() != 0) {
       const int fs = split_override() == -1 ? (p->units < 16 ? p->units : 16) : split_override();
       if (fs < 1 || fs > p->units || (fs > 1 && (size_t)fs * M * N * 4 > kPartCap))

@@ -3,15 +3,16 @@
 // Where the path is a dense contraction ("GPU Kernel 工程（09）：量化与融合 kernel", section 3.2:
 // at prefill both BF16 and INT4 GEMMs are compute-bound), the dequantized weights feed the
 // 5th-generation tensor cores.  Roles inside one persistent CTA per SM (16 warps):
-//   warp 0        TMA producer: per 64-k stage, the packed codes of a 128-column tile (one
-//                 3-D box of 8 x 512 bytes) and the 256 x 64 bf16 activation tile (128-byte
-//                 swizzle) into a 4-stage shared-memory ring.
+//   warps 0, 2, 3 TMA producers, taking the stages in turn: per 64-k stage, the packed codes
+//                 of a 128-column tile (one 3-D box of 8 x 512 bytes) and the BM x 64 bf16
+//                 activation tile (BM = 64, 128 or 256 rows, 128-byte swizzle) into a ring
+//                 of up to 12 stages.
 //   warp 1        TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
-//                 M = 128 (weight columns n) x N = 256 (activation rows m) x K = 16, BF16 x
+//                 M = 128 (weight columns n) x N = BM (activation rows m) x K = 16, BF16 x
 //                 BF16 -> FP32, into one of two TMEM accumulators (one per group parity).
-//   warpgroup 1   dequantization of each stage's codes into one of four K-major operand
-//                 buffers (exact bf16 integers q - z), so it can run up to three stages
-//                 ahead of the MMA.
+//   warpgroup 1   dequantization: warp i mod 4 turns stage i's codes into operand buffer
+//                 i mod 4 (K-major, exact bf16 integers q - z), so up to four stages are
+//                 being dequantized at once.
 //   warpgroups 2-3  promotion: tcgen05.ld of a finished group, times its scale (one per
 //                 thread: a TMEM lane is one column n), into FP32 running sums; epilogue.
 // The operand tiles hold the exact integers q - z (bf16 represents |q - z| <= 15 exactly);
@@ -34,11 +35,15 @@ namespace gq {
 
 constexpr int kPfMaxStages = 12;             // TMA ring depth (64-k stages), at most
 constexpr int kPfDqBufs = 4;                 // dequantized-operand buffers
+constexpr int kPfDqWarps = 4;                // warpgroup 1
+static_assert(kPfDqWarps == kPfDqBufs, "dequant warp d fills operand buffer d");
+constexpr int kPfProducers = 3;              // TMA-issuing warps (0, 2 and 3)
+// ring depth at least: the producers' and the dequant warps' waits rely on it (see the roles)
+constexpr int kPfMinStages = kPfDqBufs > kPfProducers ? kPfDqBufs : kPfProducers;
 constexpr int kPfTileN = 128;                // weight columns per tile (TMEM lanes)
 constexpr int kPfMaxTileM = 256;             // activation rows per tile (TMEM columns), at most
 static_assert(2 * kPfMaxTileM <= 512, "two accumulators of the tallest tile fill TMEM");
 constexpr int kPfThreads = 512;              // 16 warps = 4 warpgroups
-constexpr int kPfDqWarps = 4;                // warpgroup 1
 constexpr int kPfSumWarps = 8;               // warpgroups 2 and 3
 constexpr uint32_t kPfPackedBytes = 8 * 512;                  // packed codes per stage
 constexpr uint32_t kPfDqBytes = kPfTileN * 64 * 2;            // dequantized weights per stage
@@ -261,7 +266,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                   const PrefillShape sh, unsigned token) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kPfMaxStages], bar_empty[kPfMaxStages],
-      bar_dq[kPfDqBufs], bar_dq_empty[kPfDqBufs], bar_acc_full[2], bar_acc_empty[2];
+      bar_dq[kPfDqBufs], bar_acc_full[2], bar_acc_empty[2];
   __shared__ uint32_t s_tmem;
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // TMA stage s: [activations BM x 128 bytes][packed codes 4 KB] (a multiple of 1 KB, as the
@@ -284,14 +289,12 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
-      // a stage is free once the MMA read its activations (commit) and every dequant warp
-      // read its codes
-      mbar_init(smem_u32(&bar_empty[s]), 1 + kPfDqWarps);
+      // a stage is free once the MMA read its activations and the dequantized operand made
+      // from it (commit) and its dequant warp read its codes
+      mbar_init(smem_u32(&bar_empty[s]), 2);
     }
-    for (int d = 0; d < kPfDqBufs; ++d) {
-      mbar_init(smem_u32(&bar_dq[d]), kPfDqWarps);        // one arrival per dequant warp
-      mbar_init(smem_u32(&bar_dq_empty[d]), 1);           // the MMA's commit
-    }
+    for (int d = 0; d < kPfDqBufs; ++d)
+      mbar_init(smem_u32(&bar_dq[d]), 1);                 // the stage's dequant warp
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_acc_full[b]), 1);
       mbar_init(smem_u32(&bar_acc_empty[b]), kPfSumWarps);  // one per promotion warp
@@ -314,24 +317,31 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   // 63,488 registers in total, within the launch's 65,536.
   if (wg == 0) {
    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
-   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+   if (warp != 1) {
+    // ---------------------------------------------------------------- TMA producers
+    // Warps 0, 2 and 3 take the stages in turn (stage i: warp i mod 3).  One issuing thread
+    // gets about one stage per memory round trip on this GPU whatever the ring depth, so the
+    // stages of one ring are spread over three.  A producer's successive stages are three
+    // apart and the ring is at least three deep, so the empty barrier it waits on is never
+    // more than one phase behind the phase it waits for.
     if (lane == 0) {
+      const int pid = warp == 0 ? 0 : warp - 1;
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_w) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_a) : "memory");
-      int s = 0;                                     // ring stage and its phase parity
-      uint32_t ph = 0;
+      uint32_t i = 0;                                // stage number within this CTA
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const int tile = u % tiles, z = u / tiles;
         const int tn = tile % tiles_n, tm = tile / tiles_n;
         int g0, g1;
         zsplit_dev(ng, KS, z, g0, g1);
-        for (int kk = 0; kk < (g1 - g0) * SPG && ok; ++kk, s = s + 1 == S ? 0 : s + 1,
-                 ph ^= (s == 0 ? 1u : 0u)) {
-          const int kc = pf_group(g0, g1, tn, kk / SPG) * SPG + kk % SPG;
-          ok = mbar_wait(smem_u32(&bar_empty[s]), ph ^ 1, token);
+        const int nk = (g1 - g0) * SPG;
+        for (int kk = 0; kk < nk && ok; ++kk, ++i) {
+          if (i % kPfProducers != (uint32_t)pid) continue;
+          const int s = (int)(i % (uint32_t)S);
+          ok = mbar_wait(smem_u32(&bar_empty[s]), ((i / (uint32_t)S) & 1u) ^ 1u, token);
           if (!ok) break;
+          const int kc = pf_group(g0, g1, tn, kk / SPG) * SPG + kk % SPG;
           const uint32_t fb = smem_u32(&bar_full[s]);
           mbar_expect_tx(fb, stage_bytes);
           tma_load_3d(smem_u32(pk_at(s)), &map_w, fb, 0, kc, tn * 8);
@@ -342,11 +352,14 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     __syncwarp();
    } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // Per stage one wait (the dequantized operand; its warp saw the stage's copies land, so
+    // the activations are there too), four MMAs and one commit, which frees both the stage
+    // and the operand buffer: each of these costs the single issuing thread 60 to 150 cycles,
+    // as much as a 64-row stage's MMAs take.
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(kPfTileN, BM);
       uint32_t i = 0, gg = 0;
-      int s = 0;                                     // ring stage and its phase parity
-      uint32_t ph = 0;
+      int s = 0;                                     // ring stage
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         int g0, g1;
@@ -356,14 +369,12 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           ok = mbar_wait(smem_u32(&bar_acc_empty[b]), ((gg >> 1) & 1) ^ 1, token);
           if (!ok) break;
           tc_fence_after();
-          for (int st = 0; st < SPG; ++st, ++i, s = s + 1 == S ? 0 : s + 1,
-                   ph ^= (s == 0 ? 1u : 0u)) {
+          for (int st = 0; st < SPG; ++st, ++i, s = s + 1 == S ? 0 : s + 1) {
             const int dbuf = i % kPfDqBufs;
-            const uint32_t dph = (i / kPfDqBufs) & 1;
-            ok = mbar_wait(smem_u32(&bar_full[s]), ph, token) &&
-                 mbar_wait(smem_u32(&bar_dq[dbuf]), dph, token);
+            ok = mbar_wait(smem_u32(&bar_dq[dbuf]), (i / kPfDqBufs) & 1, token);
             if (!ok) break;
             tc_fence_after();
+
             // weights: core matrices, 16 k = two of them = 256 bytes = 16 descriptor units;
             // activations: 128-byte swizzle, 16 k = 32 bytes = 2 descriptor units
             const uint64_t da = umma_desc_plain(smem_u32(dq_at(dbuf)), 128, 1024);
@@ -372,8 +383,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
             for (int k = 0; k < 4; ++k)
               umma_bf16(tmem + (uint32_t)b * BM, da + 16 * k, db + 2 * k, idesc,
                         (st | k) != 0 ? 1u : 0u);
-            umma_commit(smem_u32(&bar_empty[s]));        // activations consumed
-            umma_commit(smem_u32(&bar_dq_empty[dbuf]));  // dequantized operand consumed
+            umma_commit(smem_u32(&bar_empty[s]));        // stage and operand buffer consumed
           }
           if (!ok) break;
           umma_commit(smem_u32(&bar_acc_full[b]));       // group finished
@@ -391,12 +401,21 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     // matrices (8 rows x 16 bytes), core matrix (8-row group rg, 8-k group kg) at
     // rg * 1024 + kg * 128; pair p of word j of a fragment is core matrix
     // (2 sub + (p & 1), 2j + (p >> 1)), byte 16 r0 + 4 (lane % 4) = 4 lane inside it.
+    // Stage i goes to operand buffer i mod 4, last read by the MMA of stage i - 4, whose
+    // commit completed that stage's empty barrier (the ring is at least four deep, so that
+    // barrier is never more than one phase away from the phase waited for).
+    // Stage i is dequantized whole by warp i mod 4 into operand buffer i mod 4, so that each
+    // warp's two waits per stage cover a whole stage of work (four warps sharing every stage
+    // measured slower: their waits, not the conversion, set the pace).  Lane `lane` of
+    // sub-tile u (columns 16u .. 16u + 15 of the tile) holds the 16-byte fragment: rows
+    // r0 = lane / 4 and r0 + 8 of the sub-tile, k = 16j + 2(lane % 4) + 8h + {0,1}.  The
+    // dequantized operand is K-major core matrices (8 rows x 16 bytes), core matrix (8-row
+    // group rg, 8-k group kg) at rg * 1024 + kg * 128; pair p of word j of a fragment is core
+    // matrix (2u + (p & 1), 2j + (p >> 1)), byte 16 r0 + 4 (lane % 4) = 4 lane inside it.
     const int d = warp & 3;
     const int r0 = lane >> 2;
     const int NW = N >> 3;
     uint32_t i = 0;
-    int s = 0;                                       // ring stage and its phase parity
-    uint32_t ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const int tn = (u % tiles) % tiles_n;
@@ -404,38 +423,40 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
       zsplit_dev(ng, KS, u / tiles, g0, g1);
       for (int gi = 0; gi < g1 - g0 && ok; ++gi) {
         const int g = pf_group(g0, g1, tn, gi);
-        uint32_t zl[2] = {pc.sym, pc.sym}, zh[2] = {pc.sym, pc.sym};
-        if (ZP) {
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int n = tn * kPfTileN + (2 * d + u) * 16 + r0;
-            const uint32_t wa = __ldg(zeros + (size_t)g * NW + min(n >> 3, NW - 1));
-            const uint32_t wb = __ldg(zeros + (size_t)g * NW + min((n + 8) >> 3, NW - 1));
-            zl[u] = (0x4300u | ((wa >> (4 * (n & 7))) & 0xFu)) * 0x00010001u;
-            zh[u] = (0x4300u | ((wb >> (4 * ((n + 8) & 7))) & 0xFu)) * 0x00010001u;
-          }
-        }
-        for (int st = 0; st < SPG; ++st, ++i, s = s + 1 == S ? 0 : s + 1,
-                 ph ^= (s == 0 ? 1u : 0u)) {
-          const int dbuf = i % kPfDqBufs;
-          const uint32_t dph = (i / kPfDqBufs) & 1;
-          // the buffer was read by the MMA of stage i - kPfDqBufs; the codes of stage i arrived
-          ok = mbar_wait(smem_u32(&bar_dq_empty[dbuf]), dph ^ 1, token) &&
-               mbar_wait(smem_u32(&bar_full[s]), ph, token);
+        for (int st = 0; st < SPG; ++st, ++i) {
+          if ((int)(i % kPfDqBufs) != d) continue;
+          const int s = (int)(i % (uint32_t)S);
+          // the buffer was last read by the MMA of stage i - 4, whose commit completed that
+          // stage's empty barrier; the ring is at least four deep, so that barrier is never
+          // more than one phase away from the phase waited for
+          const uint32_t pi = i - kPfDqBufs;
+          ok = (i < (uint32_t)kPfDqBufs ||
+                mbar_wait(smem_u32(&bar_empty[pi % (uint32_t)S]), (pi / (uint32_t)S) & 1, token)) &&
+               mbar_wait(smem_u32(&bar_full[s]), (i / (uint32_t)S) & 1, token);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint4 f =
-                *reinterpret_cast<const uint4 *>(pk_at(s) + (2 * d + u) * 512 + lane * 16);
+          uint8_t *dqb = dq_at(d);
+          // (with zero points the loop is kept rolled: fully unrolled, their loads are all
+          // hoisted and spill)
+#pragma unroll (ZP ? 1 : 8)
+          for (int sub = 0; sub < 8; ++sub) {
+            uint32_t zl = pc.sym, zh = pc.sym;
+            if (ZP) {
+              const int n = tn * kPfTileN + sub * 16 + r0;
+              const uint32_t wa = __ldg(zeros + (size_t)g * NW + min(n >> 3, NW - 1));
+              const uint32_t wb = __ldg(zeros + (size_t)g * NW + min((n + 8) >> 3, NW - 1));
+              zl = (0x4300u | ((wa >> (4 * (n & 7))) & 0xFu)) * 0x00010001u;
+              zh = (0x4300u | ((wb >> (4 * ((n + 8) & 7))) & 0xFu)) * 0x00010001u;
+            }
+            const uint4 f = *reinterpret_cast<const uint4 *>(pk_at(s) + sub * 512 + lane * 16);
             const uint32_t words[4] = {f.x, f.y, f.z, f.w};
-            uint8_t *dq = dq_at(dbuf) + (2 * d + u) * 2048 + lane * 4;
+            uint8_t *dq = dqb + sub * 2048 + lane * 4;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
 #pragma unroll
               for (int p = 0; p < 4; ++p) {        // pair p: bits 4p and 4p + 16
                 const uint32_t v = bsub2(lo_nibbles(words[j] >> (4 * p), pc.magic),
-                                         (p & 1) ? zh[u] : zl[u]);
+                                         (p & 1) ? zh : zl);
                 *reinterpret_cast<uint32_t *>(dq + (p & 1) * 1024 + (2 * j + (p >> 1)) * 128) = v;
               }
             }
@@ -443,7 +464,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic -> tensor core
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&bar_dq[dbuf]));
+            mbar_arrive(smem_u32(&bar_dq[d]));
             mbar_arrive(smem_u32(&bar_empty[s]));          // this warp is done with the codes
           }
         }
@@ -632,7 +653,7 @@ size_t prefill_smem_bytes(int BM, int stages) {
 
 // The deepest ring (at most kPfMaxStages) of BM-row stages that fits smem_cap bytes.
 int prefill_stages(int BM, size_t smem_cap) {
-  for (int s = kPfMaxStages; s >= 2; --s)
+  for (int s = kPfMaxStages; s >= kPfMinStages; --s)
     if (prefill_smem_bytes(BM, s) <= smem_cap) return s;
   return 0;
 }

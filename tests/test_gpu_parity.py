@@ -147,10 +147,10 @@ PREFILL_SHAPES = [
     # the smallest row counts the prefill kernel takes: one 256-row tile, mostly past M
     gq_synth.Config("pf_m33", M=33, K=512, N=136, G=128),
     gq_synth.Config("pf_m64_zp", M=64, K=1024, N=256, G=64, zp=True, sc="bf16", out="f32"),
-    # the mid-M tiles: 64- and 128-row activation tiles, split K over whole groups with a
-    # ragged last 128-column tile, rows past M in the last tile
-    gq_synth.Config("pf_m33_split", M=33, K=4096, N=1032, G=128, zp=True),
-    gq_synth.Config("pf_m64_split", M=64, K=4096, N=2056, G=128, outlier_frac=0.001),
+    # the mid-M tiles: 64- and 128-row activation tiles over the full K = 4096 (64 stages
+    # through the ring) with a ragged last 128-column tile, rows past M in the last tile
+    gq_synth.Config("pf_m33_k4096", M=33, K=4096, N=1032, G=128, zp=True),
+    gq_synth.Config("pf_m64_k4096", M=64, K=4096, N=2056, G=128, outlier_frac=0.001),
     gq_synth.Config("pf_m100_bm128", M=100, K=2048, N=520, G=64, sc="bf16"),
     gq_synth.Config("pf_m128_f32", M=128, K=1024, N=392, G=128, sc="f32", out="f32"),
     gq_synth.Config("pf_m300_ragged", M=300, K=1024, N=392, G=256, zp=True),
@@ -169,14 +169,19 @@ def test_prefill_shapes(gq, cfg):
 @pytest.mark.parametrize("M,K,N", [(384, 1024, 256), (64, 4096, 1032), (128, 2048, 264)])
 def test_prefill_integer_inputs_are_bit_exact(gq, M, K, N):
     """Integer activations and power-of-two scales: every partial sum is exact in FP32, so the
-    output equals the oracle bit for bit, the split-K slices' sums included."""
+    output equals the oracle bit for bit, unsplit and with K split in four slices."""
     cfg = gq_synth.Config("pf_exact", M=M, K=K, N=N, G=128, zp=True, a_kind="int",
                           pow2_scales=True)
     inp = gq_synth.make_inputs(cfg, seed=2)
-    out, _ = run_gemm(gq, cfg, inp)
     ref, _ = _oracle(cfg, inp)
-    h = out.view(torch.int16).cpu().numpy().view(np.uint16)
-    assert np.array_equal(h, oracle.f64_to_bf16_bits(ref))
+    try:
+        for n in (0, 4):
+            gq.gq_set_split_override(n)
+            out, _ = run_gemm(gq, cfg, inp)
+            h = out.view(torch.int16).cpu().numpy().view(np.uint16)
+            assert np.array_equal(h, oracle.f64_to_bf16_bits(ref)), n
+    finally:
+        gq.gq_set_split_override(0)
 
 
 def test_prefill_forced_split_counts_match_the_oracle(gq):

@@ -452,11 +452,18 @@ def test_fault_injection_and_wait_limit_settings_are_validated():
 
 
 def test_prefill_plan_tiles_and_split_follow_the_rows():
-    """Few rows: 64-row activation tiles and a K split of whole groups that keeps every SM
-    busy (112 tiles x 4 slices = 448 units, about three waves of 152), while the partial sums
-    stay within the packed weight bytes; from 65 rows 128-row tiles, from 129 rows 256."""
+    """Few rows: 64-row activation tiles, one K slice (112 tiles on 112 SMs; every measured
+    split was slower) and no scratch; a forced split of whole groups gets its partial sums;
+    from 65 rows 128-row tiles, from 129 rows 256."""
     W4 = C.GQ_W4
     p = gq.gq_plan(64, 4096, 14336, 128, W4, sm_count=152)
+    assert (p["path"], p["m_tile"], p["nsplit"], p["grid_x"], p["workspace_bytes"]) == \
+        (2, 64, 1, 112, 0)
+    prev = gq.gq_set_split_override(4)
+    try:
+        p = gq.gq_plan(64, 4096, 14336, 128, W4, sm_count=152)
+    finally:
+        gq.gq_set_split_override(prev)
     assert (p["path"], p["m_tile"], p["nsplit"], p["grid_x"]) == (2, 64, 4, 152)
     assert p["workspace_bytes"] >= 4 * 64 * 14336 * 4
     p = gq.gq_plan(128, 4096, 14336, 128, W4, sm_count=152)
