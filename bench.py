@@ -369,7 +369,7 @@ def main():
     if not args.no_sweep and rank == 0:
         sweep = _m_sweep(gq, torch, dev, peaks)
 
-    traffic = _kernel_traffic("gq_stripe.cu", "w4_stripe_decode_gateup.md")
+    traffic = _kernel_traffic("gq_gemv.cu", "w4_gemv_decode_gateup.md")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -385,7 +385,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "w4_stripe_kernel", "peak_source": f"hbm_gbs of {peak_kind}",
+                     "kernel": "w4_gemv_kernel", "peak_source": f"hbm_gbs of {peak_kind}",
                      "kernel_us": kernel_us, "kernel_us_distribution": dist_us},
         "e2e": e2e,
         "gpu_launches": launches,

@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
     return __half2float(__ushort_as_half((unsigned short)bits));
   };
   const int NW = N >> 3;
-  // zero-point words of slot jz (of the slice) of tile tz: groups, column words 2 tz, 2 tz + 1
+  // zero-point words of slot jz (of the slice) of tile tz: groups, column words 2 tz, 2 tz + 1,
+  // loaded a slot ahead (zn) and turned into the decode's subtrahends bf16(128 + z) once per
+  // slot (zc), not at every 16-k step
   uint32_t zc[GPS][2], zn[GPS][2];
   auto load_zeros = [&](int tz, int jz) {
 #pragma unroll
@@ -379,8 +381,8 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
       if (ZP || ZF) {
 #pragma unroll
         for (int gi = 0; gi < GPS; ++gi) {
-          zc[gi][0] = zn[gi][0];
-          zc[gi][1] = zn[gi][1];
+          zc[gi][0] = ZP ? zz_of(zn[gi][0]) : zn[gi][0];
+          zc[gi][1] = ZP ? zz_of(zn[gi][1]) : zn[gi][1];
         }
         if (l + 1 < nloads) {
           if (ZP) {
@@ -414,8 +416,8 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
           const int stp = ch * 4 + jj;               // 16-k step of the slot
           const int gi = stp / SPG;
           // float zero points: the codes themselves (z = 0); the zero enters after scaling
-          const uint32_t z0 = ZP ? zz_of(zc[gi][0]) : ZF ? kMagic : kSym;
-          const uint32_t z1 = ZP ? zz_of(zc[gi][1]) : ZF ? kMagic : kSym;
+          const uint32_t z0 = ZP ? zc[gi][0] : ZF ? kMagic : kSym;
+          const uint32_t z1 = ZP ? zc[gi][1] : ZF ? kMagic : kSym;
           const uint32_t w = words[jj];
           // pair i of the word (bits 4i and 4i + 16): rows r0 + 8 (i & 1), k half i >> 1
           const uint32_t a0 = bsub2(lo_nibbles(w, kMagic), z0);
