@@ -52,6 +52,7 @@ _SIGS = {
     "gq_workspace_size": [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)],
     "gq_set_workspace": [_p, _sz],
     "gq_gemm": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
+    "gq_gemm_host": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p],
     "gq_gemm_static_scratch": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_gemm_a8": [_i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p],
     "gq_quantize_act": [_i, _i, _i, _i, _p, _p, _p, _p],
@@ -116,6 +117,14 @@ def gq_set_workspace(ptr, nbytes: int) -> int:
 def gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream=None) -> int:
     """Raw call; returns the status."""
     return _lib.gq_gemm(M, K, N, G, prec, A_ptr, Wq_ptr, scales_ptr, zeros_ptr, out_ptr, stream)
+
+
+def gq_gemm_host(M, K, N, G, prec, A_host_ptr, A_dev_ptr, Wq_ptr, scales_ptr, zeros_ptr,
+                 out_dev_ptr, out_host_ptr, stream=None) -> int:
+    """gq_gemm on host activations and output (copied in and out on the stream).  Raw call;
+    returns the status."""
+    return _lib.gq_gemm_host(M, K, N, G, prec, A_host_ptr, A_dev_ptr, Wq_ptr, scales_ptr,
+                             zeros_ptr, out_dev_ptr, out_host_ptr, stream)
 
 
 def gq_gemm_a8(M, K, N, G, prec, Aq_ptr, a_scales_ptr, Wq_ptr, scales_ptr, out_ptr,

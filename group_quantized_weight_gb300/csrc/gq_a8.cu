@@ -330,8 +330,8 @@ cudaError_t launch_q8a8(const Plan &pl, int M, int K, int N, int G, int prec, co
   ap.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   const dim3 grid(pl.grid_x, pl.grid_z);
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)pl.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                         pl.smem_bytes);
     if (e != cudaSuccess) return e;
     kern<<<grid, kA8Threads, pl.smem_bytes, s>>>(ap);
     return cudaGetLastError();

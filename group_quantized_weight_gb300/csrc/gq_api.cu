@@ -3,6 +3,7 @@
 #include <atomic>
 #include <mutex>
 #include <string.h>
+#include <unordered_map>
 #include <vector>
 
 #include <cstdio>
@@ -60,14 +61,50 @@ size_t packed_bytes(int K, int N, int prec) {
   return (size_t)K * N;
 }
 
+// device ordinals with a cached SM count and shared-memory limits (others query each time)
+constexpr int kMaxDevices = 64;
+// SM counts, one per device ordinal, read from the driver once
+static std::atomic<int> g_sm_count[kMaxDevices];
+
 int device_sm_count(int *sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GQ_ERR_NO_DEVICE; }
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *sms = c;
+      return GQ_OK;
+    }
+  }
   if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     return GQ_ERR_NO_DEVICE;
   }
+  if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(*sms, std::memory_order_relaxed);
   return GQ_OK;
+}
+
+// the dynamic shared-memory limits this process has set, per (device, kernel)
+static std::mutex g_smem_mu;
+static std::unordered_map<const void *, size_t> g_smem_set[kMaxDevices];
+
+cudaError_t ensure_dynamic_smem(const void *func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cacheable = dev >= 0 && dev < kMaxDevices;
+  if (cacheable) {
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    auto it = g_smem_set[dev].find(func);
+    if (it != g_smem_set[dev].end() && it->second >= bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && cacheable) {
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    size_t &v = g_smem_set[dev][func];
+    if (v < bytes) v = bytes;
+  }
+  return e;
 }
 
 // Split K into nsplit slices of whole units so that the grid holds about `target` CTAs,
@@ -677,12 +714,19 @@ static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,
 
 }  // extern "C"
 
-int gq::gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
-                  const void *scales, const void *zeros, void *out, void *stream) {
+// Everything gq_gemm checks and prepares before its launch: the arguments, the plan and the
+// scratch.  *empty is set when there is nothing to compute (M or N is 0).
+static int gemm_prepare(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
+                        const void *scales, const void *zeros, const void *out, Plan *p,
+                        void **ws, bool *empty) {
+  *empty = false;
   if (prec & GQ_ACT_I8) return GQ_ERR_INVALID_ARG;   // needs the activation scales: gq_gemm_a8
   int st = validate(M, K, N, G, prec);
   if (st != GQ_OK) return st;
-  if (M == 0 || N == 0) return GQ_OK;
+  if (M == 0 || N == 0) {
+    *empty = true;
+    return GQ_OK;
+  }
   if (!A || !Wq || !scales || !out) return GQ_ERR_INVALID_ARG;
   if (((prec & (GQ_ZP | GQ_ZP_FLOAT)) != 0) != (zeros != nullptr)) return GQ_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(Wq) || !aligned16(scales) || !aligned16(out) ||
@@ -691,15 +735,16 @@ int gq::gemm_impl(int M, int K, int N, int G, int prec, const void *A, const voi
   int sms = 0;
   st = device_sm_count(&sms);
   if (st != GQ_OK) return st;
-  Plan p;
-  st = make_plan(M, K, N, G, prec, sms, &p);
+  st = make_plan(M, K, N, G, prec, sms, p);
   if (st != GQ_OK) return st;
-  void *ws = nullptr;
-  st = get_scratch(p.workspace_bytes, &ws);
-  if (st != GQ_OK) return st;
+  return get_scratch(p->workspace_bytes, ws);
+}
+
+static int gemm_launch(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                       const void *Wq, const void *scales, const void *zeros, void *out,
+                       void *ws, cudaStream_t s) {
   unsigned *counters = (unsigned *)ws;
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
-  cudaStream_t s = (cudaStream_t)stream;
   if (launch_fault_injected()) return GQ_ERR_CUDA;
   const cudaError_t e = launch_plan(p, M, K, N, G, prec, A, Wq, scales, zeros, out, part,
                                     counters, s);
@@ -711,11 +756,54 @@ int gq::gemm_impl(int M, int K, int N, int G, int prec, const void *A, const voi
   return GQ_OK;
 }
 
+int gq::gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
+                  const void *scales, const void *zeros, void *out, void *stream) {
+  Plan p;
+  void *ws = nullptr;
+  bool empty = false;
+  const int st = gemm_prepare(M, K, N, G, prec, A, Wq, scales, zeros, out, &p, &ws, &empty);
+  if (st != GQ_OK || empty) return st;
+  return gemm_launch(p, M, K, N, G, prec, A, Wq, scales, zeros, out, ws, (cudaStream_t)stream);
+}
+
 extern "C" {
 
 int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
             const void *scales, const void *zeros, void *out, void *stream) {
   return gemm_impl(M, K, N, G, prec, A, Wq, scales, zeros, out, stream);
+}
+
+int gq_gemm_host(int M, int K, int N, int G, int prec, const void *A_host, void *A_dev,
+                 const void *Wq, const void *scales, const void *zeros, void *out_dev,
+                 void *out_host, void *stream) {
+  int st = validate(M, K, N, G, prec);
+  if (st != GQ_OK) return st;
+  if (M == 0 || N == 0) return GQ_OK;
+  if (!A_host || !out_host) return GQ_ERR_INVALID_ARG;
+  Plan p;
+  void *ws = nullptr;
+  bool empty = false;
+  st = gemm_prepare(M, K, N, G, prec, A_dev, Wq, scales, zeros, out_dev, &p, &ws, &empty);
+  if (st != GQ_OK || empty) return st;
+  const size_t a_bytes = (size_t)M * K * ((prec & GQ_ACT_F32) ? 4 : 2);
+  const size_t o_cols = (prec & GQ_GATE_UP) ? (size_t)N / 2 : (size_t)N;
+  const size_t o_bytes = (size_t)M * o_cols * ((prec & GQ_OUT_F32) ? 4 : 2);
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    note_cuda_error("cudaMemcpyAsync(activations to the device)", e);
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  st = gemm_launch(p, M, K, N, G, prec, A_dev, Wq, scales, zeros, out_dev, ws, s);
+  if (st != GQ_OK) return st;
+  e = cudaMemcpyAsync(out_host, out_dev, o_bytes, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) {
+    note_cuda_error("cudaMemcpyAsync(output to the host)", e);
+    cudaGetLastError();
+    return GQ_ERR_CUDA;
+  }
+  return GQ_OK;
 }
 
 static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,

@@ -544,8 +544,8 @@ __global__ void __launch_bounds__(batch_warps(MT) * 32, 1) w4_batch_kernel(const
 template <int G, int SC, int ZM, int MT>
 static cudaError_t launch_bt_t(const Plan &pl, const BtParams &bp, cudaStream_t s) {
   auto kern = w4_batch_kernel<G, SC, ZM, MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)pl.smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                       pl.smem_bytes);
   if (e != cudaSuccess) return e;
   // programmatic stream serialization: the next kernel may begin launching while this one
   // runs; this kernel touches its inputs and outputs only after griddepcontrol.wait

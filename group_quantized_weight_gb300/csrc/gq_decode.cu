@@ -323,8 +323,8 @@ static cudaError_t launch_w4_t(const Plan &p, int M, int K, int N, int G, const 
                                void *out, float *part, unsigned *counters, cudaStream_t s) {
   auto kern = w4_mma_decode_kernel<MT, SC, ZP, OUTF32>;
   if (p.smem_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                         p.smem_bytes);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(p.grid_x, p.grid_y, p.grid_z);
@@ -386,8 +386,8 @@ static cudaError_t launch_q8_t(const Plan &p, int M, int K, int N, int G, const 
                                unsigned *counters, cudaStream_t s) {
   auto kern = q8_decode_kernel<MR, OUTF32>;
   if (p.smem_bytes > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)p.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                         p.smem_bytes);
     if (e != cudaSuccess) return e;
   }
   dim3 grid(p.grid_x, p.grid_y, p.grid_z);

@@ -479,10 +479,9 @@ int launch_fp8_block(int M, int K, int N, int prec, const void *A, const void *a
   st = f8_encode(&ma, A, M, K, kF8TileM, "cuTensorMapEncodeTiled(fp8 activations)");
   if (st != GQ_OK) return st;
   const size_t smem = fp8_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(fp8_block_gemm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(fp8_block_gemm_kernel), smem);
   if (e != cudaSuccess) {
-    note_cuda_error("cudaFuncSetAttribute(fp8)", e);
+    note_cuda_error("cudaFuncSetAttribute(fp8 shared memory)", e);
     return GQ_ERR_CUDA;
   }
   // the setmaxnreg split inside the kernel adds up to 640 threads x 96 registers: a build

@@ -420,10 +420,10 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
   const uint8_t *ringw = ring + (size_t)warp * kSlotCodes;
   const uint8_t *ts = tbl;                         // the current slot's table entry
   const uint32_t *bslot = brow + j * (kSlotChunks * 32);
-  // A group's 16-k steps alternate between two MMA accumulators (even and odd steps), so
-  // that two independent dependency chains are in flight; the group's dot is their sum.
-  // Groups never straddle a slot (G <= 256 = one slot), so both start afresh in every slot.
-  float d[2][4];
+  // the current group's MMA accumulator (a group may span chunks, never a slot: G <= 256;
+  // two accumulators alternating by step measured slower here: the consumers are bound by
+  // instruction issue, not by the MMA chain's latency)
+  float d[4];
   for (int i = 0; i < n; ++i) {
     const int st = i % S;
     if (!wait_phase(saddr(&full_bar[st][warp]), (uint32_t)((i / S) & 1))) break;
@@ -451,18 +451,17 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
         const uint32_t a1 = hfma2_u(lop3_and_or<0x00F000F0u>(w, kMagic), kSixteenth, zh);
         const uint32_t a2 = hsub2_u(lop3_and_or<0x000F000Fu>(w8, kMagic), zl);
         const uint32_t a3 = hfma2_u(lop3_and_or<0x00F000F0u>(w8, kMagic), kSixteenth, zh);
-        float *dd = d[stp & 1];
-        if (stp % SPG < 2)
-          mma_16816_f16_zc(dd, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
+        if (stp % SPG == 0)
+          mma_16816_f16_zc(d, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
         else
-          mma_16816_f16(dd, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
+          mma_16816_f16(d, a0, a1, a2, a3, bq[2 * jj], bq[2 * jj + 1]);
         if ((stp + 1) % SPG == 0) {                 // a whole group: scale it in
           const float fa = scale_f((uint32_t)sg[gi * 16 + r0]);
           const float fb = scale_f((uint32_t)sg[gi * 16 + r0 + 8]);
-          acc[0] = fmaf(fa, d[0][0] + d[1][0], acc[0]);
-          acc[1] = fmaf(fa, d[0][1] + d[1][1], acc[1]);
-          acc[2] = fmaf(fb, d[0][2] + d[1][2], acc[2]);
-          acc[3] = fmaf(fb, d[0][3] + d[1][3], acc[3]);
+          acc[0] = fmaf(fa, d[0], acc[0]);
+          acc[1] = fmaf(fa, d[1], acc[1]);
+          acc[2] = fmaf(fb, d[2], acc[2]);
+          acc[3] = fmaf(fb, d[3], acc[3]);
         }
       }
     }
@@ -611,8 +610,8 @@ int gemv_threads() { return (gv::kConsumers + 1) * 32; }
 template <int G, int SC, bool ZP>
 static cudaError_t launch_gemv_t(const Plan &pl, const GemvParams &gp, cudaStream_t s) {
   auto kern = w4_gemv_kernel<G, SC, ZP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)pl.smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                       pl.smem_bytes);
   if (e != cudaSuccess) return e;
   // programmatic stream serialization: the next kernel may begin launching while this one
   // runs; this kernel reads activations and writes outputs only after griddepcontrol.wait

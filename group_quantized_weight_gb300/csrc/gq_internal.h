@@ -74,6 +74,10 @@ int gemm_impl(int M, int K, int N, int G, int prec, const void *A, const void *W
               const void *scales, const void *zeros, void *out, void *stream);
 size_t packed_bytes(int K, int N, int prec);
 int device_sm_count(int *sms);
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes) on the current device, issued
+// only when this process has not yet raised that kernel's limit to at least `bytes` there
+// (a per-call driver call costs host time on every launch of the decode path).
+cudaError_t ensure_dynamic_smem(const void *func, size_t bytes);
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_pack_w4(int K, int N, const uint32_t *codes, uint32_t *packed, bool gate_up,

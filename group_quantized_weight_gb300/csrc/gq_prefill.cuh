@@ -622,8 +622,8 @@ static cudaError_t launch_pf(const Plan &p, int M, int K, int N, int prec, const
                              void *out, float *part, unsigned *counters, unsigned token,
                              cudaStream_t s) {
   auto kern = w4_prefill_kernel<SPG, SC, ZP, FIXED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)p.smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                       p.smem_bytes);
   if (e != cudaSuccess) {
     note_cuda_error("cudaFuncSetAttribute(prefill)", e);
     return e;

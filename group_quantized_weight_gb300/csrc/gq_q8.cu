@@ -652,8 +652,8 @@ cudaError_t launch_q8_mma(const Plan &pl, int M, int K, int N, int G, int prec, 
   qp.NB = (N + 63) / 64;
   qp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)pl.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                         pl.smem_bytes);
     if (e != cudaSuccess) return e;
     kern<<<pl.grid_x, kQmThreads, pl.smem_bytes, s>>>(qp);
     return cudaGetLastError();
@@ -730,8 +730,8 @@ cudaError_t launch_q8_block(const Plan &pl, int M, int K, int N, int G, int prec
   qp.NB = (N + kQbCols - 1) / kQbCols;
   qp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   auto go = [&](auto kern) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)pl.smem_bytes);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                         pl.smem_bytes);
     if (e != cudaSuccess) return e;
     kern<<<pl.grid_x, kQbThreads, pl.smem_bytes, s>>>(qp);
     return cudaGetLastError();

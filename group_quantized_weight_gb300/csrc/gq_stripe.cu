@@ -568,8 +568,8 @@ __global__ void __launch_bounds__(kStrWarps * 32, 1) w4_stripe_kernel(const Stri
 template <int G, int SC, bool ZP, int MT>
 static cudaError_t launch_stripe_t(const Plan &pl, const StripeParams &sp, cudaStream_t s) {
   auto kern = w4_stripe_kernel<G, SC, ZP, MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)pl.smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern),
+                                       pl.smem_bytes);
   if (e != cudaSuccess) return e;
   // programmatic stream serialization: the next kernel may begin launching while this one
   // runs; this kernel touches its inputs and outputs only after griddepcontrol.wait

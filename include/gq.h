@@ -136,6 +136,22 @@ int gq_set_workspace(void *dev_ptr, size_t bytes);
 int gq_gemm(int M, int K, int N, int G, int prec, const void *A, const void *Wq,
             const void *scales, const void *zeros, void *out, void *stream);
 
+/* gq_gemm on host-resident activations and output: the activations are copied to the
+ * caller's device staging buffer, the GEMM runs, and the output is copied back, all three
+ * asynchronous on `stream` in that order (the host buffers must stay valid, and `out_host`
+ * must not be read, until the stream has passed the call; page-locked host memory keeps the
+ * copies asynchronous).
+ *   A_host    host [M][K], bf16 (or fp32 with GQ_ACT_F32).
+ *   A_dev     device staging buffer of the same size, overwritten.
+ *   Wq, scales, zeros  device, as for gq_gemm.
+ *   out_dev   device [M][N] (gate+up: [M][N/2]), bf16 or fp32 with GQ_OUT_F32, overwritten.
+ *   out_host  host buffer of the same size, receives the output.
+ * The activations' and output's sizes follow from (M, K, N, prec).  Errors as gq_gemm, all
+ * but CUDA reported before anything is issued; INVALID_ARG also for a NULL host pointer. */
+int gq_gemm_host(int M, int K, int N, int G, int prec, const void *A_host, void *A_dev,
+                 const void *Wq, const void *scales, const void *zeros, void *out_dev,
+                 void *out_host, void *stream);
+
 /* gq_gemm without any device allocation.  The pages have no counterpart: this call exists
  * for callers that cannot allocate device memory — serving runtimes that reserve all
  * device memory up front and forbid allocation once running, latency-critical loops where

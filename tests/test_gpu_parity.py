@@ -779,3 +779,37 @@ def test_fp8_quantize_then_gemm(gq):
     Aq_r, a_s_r = oracle.quantize_act_fp8(A, "bf16")
     ref, mag = oracle.fp8_block_gemm(Aq_r, a_s_r, W, w_s)
     _assert_parity(cfg, out_to_f64(o, "bf16"), ref, mag)
+
+
+@pytest.mark.parametrize("cfg", [
+    gq_synth.Config("host_gemv", M=1, K=4096, N=2048, G=128),
+    gq_synth.Config("host_asym_f32", M=3, K=1024, N=264, G=128, zp=True, sc="bf16", out="f32"),
+    gq_synth.Config("host_prefill", M=200, K=1024, N=392, G=64),
+    gq_synth.Config("host_q8_f32", M=2, K=1024, N=384, G=32, w4=False, act="f32", sc="f32",
+                    out="f32"),
+], ids=lambda c: c.name)
+def test_host_buffer_call_matches_the_device_call(gq, cfg):
+    """gq_gemm_host on page-locked host activations and output: the same bits as gq_gemm on
+    device buffers, and the oracle's values."""
+    inp = gq_synth.make_inputs(cfg, seed=4)
+    out_dev_ref, packed = run_gemm(gq, cfg, inp)
+    ref, mag = _oracle(cfg, inp)
+    prec = prec_of(cfg)
+    a = np.ascontiguousarray(inp["A"])
+    a = a.view(np.int16) if a.dtype == np.uint16 else a
+    A_h = torch.from_numpy(a).pin_memory()
+    A_d = torch.empty(A_h.shape, dtype=A_h.dtype, device="cuda")
+    S = np_to_dev(inp["scales"])
+    Z = np_to_dev(inp["zeros"]) if inp["zeros"] is not None else None
+    out_d = alloc_out(cfg.M, cfg.N, cfg.out)
+    out_h = torch.empty(tuple(out_d.shape), dtype=out_d.dtype).pin_memory()
+    st = gq.gq_gemm_host(cfg.M, cfg.K, cfg.N, cfg.G, prec, A_h.data_ptr(), A_d.data_ptr(),
+                         packed.data_ptr(), S.data_ptr(), Z.data_ptr() if Z is not None else None,
+                         out_d.data_ptr(), out_h.data_ptr(),
+                         torch.cuda.current_stream().cuda_stream)
+    assert st == 0, gq.gq_status_string(st)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16 if cfg.out != "f32" else torch.int32),
+                       out_dev_ref.cpu().view(torch.int16 if cfg.out != "f32" else torch.int32))
+    _assert_parity(cfg, out_to_f64(out_h, cfg.out), ref, mag)
+    assert gq.gq_device_error() == 0

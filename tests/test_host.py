@@ -108,6 +108,21 @@ def test_null_and_misaligned_pointers():
     assert gq.gq_gemm(4, 512, 0, 128, C.GQ_W4, 16, 16, 16, None, 16, None) == 0
 
 
+def test_host_buffer_call_checks_its_arguments_before_any_copy():
+    """gq_gemm_host: a NULL host buffer, a NULL or misaligned device buffer and a bad shape
+    come back as statuses before anything is issued (no device is touched for them here);
+    an empty problem is a no-op."""
+    W4 = C.GQ_W4
+    h = gq.gq_gemm_host
+    assert h(1, 512, 16, 128, W4, None, 16, 16, 16, None, 16, 16, None) == 1     # A_host
+    assert h(1, 512, 16, 128, W4, 16, 16, 16, 16, None, 16, None, None) == 1     # out_host
+    assert h(1, 500, 16, 128, W4, 16, 16, 16, 16, None, 16, 16, None) != 0       # K % G
+    assert h(1, 512, 16, 128, W4 | C.GQ_ACT_I8, 16, 16, 16, 16, None, 16, 16, None) != 0
+    assert h(1, 512, 16, 128, W4, 16, None, 16, 16, None, 16, 16, None) == 1     # A_dev
+    assert h(1, 512, 16, 128, W4, 16, 8, 16, 16, None, 16, 16, None) == 3        # alignment
+    assert h(0, 512, 16, 128, W4, None, None, None, None, None, None, None, None) == 0
+
+
 
 def _q8_row_blocks(M):
     """Row blocks of 8 rows a CTA of the INT8 CUDA-core kernel splits M rows into."""
