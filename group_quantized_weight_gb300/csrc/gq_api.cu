@@ -597,13 +597,8 @@ int gq_set_wait_limit(long long cycles) {
 int gq_set_fault_injection(int fault) {
   if (fault < GQ_FAULT_NONE || fault > GQ_FAULT_DEVICE_WAIT) return -1;
   const int prev = g_fault.load();
-  // the device-side form lives in the warp-specialized decode kernel's translation unit; a
-  // machine without a device keeps the host-side forms only
-  if ((fault == GQ_FAULT_DEVICE_WAIT) != (prev == GQ_FAULT_DEVICE_WAIT)) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess) gemv_set_withhold(fault == GQ_FAULT_DEVICE_WAIT);
-    cudaGetLastError();
-  }
+  // the device-side form is a launch parameter of the warp-specialized decode kernel
+  gemv_set_withhold(fault == GQ_FAULT_DEVICE_WAIT);
   g_fault.store(fault);
   return prev;
 }

@@ -30,6 +30,7 @@
 // columns 2m and 2m + 1), as in the striped kernel; each group starts a fresh FP32
 // accumulator and is multiplied by its scale after its last MMA step (the group-wise GEMM of
 // "04 · 分组量化 GEMM 内核", section 2).
+#include <atomic>
 #include <type_traits>
 
 #include "gq_device.cuh"
@@ -51,9 +52,11 @@ static __device__ int g_gemv_error;
 // bounded waits: SM clock cycles before a wait gives up (about two seconds by default;
 // gq_set_wait_limit changes it)
 static __device__ long long g_gemv_wait_limit = 4000000000ll;
-// Failure-path test (gq_set_fault_injection(GQ_FAULT_DEVICE_WAIT)): when set, every producer
-// withholds consumer 0's first slot, so that consumer's bounded wait runs out.
-static __device__ int g_gemv_withhold;
+// Failure-path test (gq_set_fault_injection(GQ_FAULT_DEVICE_WAIT)): launches made while it is
+// set tell every producer (GemvParams::withhold) to withhold consumer 0's first slot, so that
+// consumer's bounded wait runs out.  A kernel parameter, not a device variable: the
+// producer's first copies must not wait for a global load.
+static std::atomic<int> g_gemv_withhold{0};
 
 namespace gv {
 
@@ -111,6 +114,7 @@ struct GemvParams {
   int out_f32;
   int static_w;                  // weights may be read before the preceding kernel ends
   int gate_up;                   // fused gate+up: out[m][j] = silu(col j) * (col N/2 + j)
+  int withhold;                  // failure test: withhold consumer 0's first slot
 };
 
 namespace gv {
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
       wb += cb;
       we += cb;
       const int mine = we - wb;
-      const bool withhold = lane == 0 && *(volatile int *)&g_gemv_withhold != 0;
+      const bool withhold = lane == 0 && p.withhold != 0;
       int issued = 0;
       for (int j = 0; j < mine; ++j) {
         const int st = j % S;
@@ -661,6 +665,7 @@ cudaError_t launch_gemv(const Plan &pl, int M, int K, int N, int G, int prec, co
   gp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   gp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   gp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
+  gp.withhold = g_gemv_withhold.load(std::memory_order_relaxed);
   switch (G) {
     case 32: return launch_gemv_g<32>(pl, prec, gp, s);
     case 64: return launch_gemv_g<64>(pl, prec, gp, s);
@@ -675,8 +680,8 @@ int gemv_set_wait_limit(long long cycles) {
 }
 
 int gemv_set_withhold(bool on) {
-  const int v = on ? 1 : 0;
-  return cudaMemcpyToSymbol(g_gemv_withhold, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
+  g_gemv_withhold.store(on ? 1 : 0, std::memory_order_relaxed);
+  return 0;
 }
 
 int gemv_read_error(int clear) {

@@ -100,7 +100,7 @@ cudaError_t launch_gemv(const Plan &p, int M, int K, int N, int G, int prec, con
 int gemv_read_error(int clear);
 // per translation unit: the SM clock cycles after which a bounded device-side wait gives up
 int gemv_set_wait_limit(long long cycles);
-// GQ_FAULT_DEVICE_WAIT: the producer warps withhold one slot (device flag of the current device)
+// GQ_FAULT_DEVICE_WAIT: the producer warps of later launches withhold one slot
 int gemv_set_withhold(bool on);
 // gq_set_fault_injection(GQ_FAULT_LAUNCH): true, with the error detail noted, when the next
 // launch is to fail
