@@ -10,9 +10,9 @@
 //   warp 1        TMEM allocator and MMA issuer: tcgen05.mma.cta_group::1.kind::f16,
 //                 M = 128 (weight columns n) x N = BM (activation rows m) x K = 16, BF16 x
 //                 BF16 -> FP32, into one of two TMEM accumulators (one per group parity).
-//   warpgroup 1   dequantization: warp i mod 4 turns stage i's codes into operand buffer
-//                 i mod 4 (K-major, exact bf16 integers q - z), so up to four stages are
-//                 being dequantized at once.
+//   warpgroup 1   dequantization of stage i's codes into operand buffer i mod 4 (K-major,
+//                 exact bf16 integers q - z): by warp i mod 4 (up to four stages at once),
+//                 or with 256-row tiles by a pair of warps (two stages at once, each faster).
 //   warpgroups 2-3  promotion: tcgen05.ld of a finished group, times its scale (one per
 //                 thread: a TMEM lane is one column n), into FP32 running sums; epilogue.
 // The operand tiles hold the exact integers q - z (bf16 represents |q - z| <= 15 exactly);
@@ -40,7 +40,7 @@ namespace gq {
 constexpr int kPfMaxStages = 12;             // TMA ring depth (64-k stages), at most
 constexpr int kPfDqBufs = 4;                 // dequantized-operand buffers
 constexpr int kPfDqWarps = 4;                // warpgroup 1
-static_assert(kPfDqWarps == kPfDqBufs, "dequant warp d fills operand buffer d");
+static_assert(kPfDqWarps == kPfDqBufs, "one warp per stage: warp d fills operand buffer d");
 constexpr int kPfProducers = 3;              // TMA-issuing warps (0, 2 and 3)
 // ring depth at least: the producers' and the dequant warps' waits rely on it (see the roles)
 constexpr int kPfMinStages = kPfDqBufs > kPfProducers ? kPfDqBufs : kPfProducers;
@@ -285,6 +285,9 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   const int BM = kFixed ? kPfFixedTileM : sh.BM;
   const int S = kFixed ? kPfFixedStages : sh.S;
   const int KS = kFixed ? 1 : sh.KS;
+  // dequant warps per stage: a pair with 256-row tiles (whose four-deep ring needs the shorter
+  // latency), one otherwise (64- and 128-row tiles have deep rings and fewer waits win)
+  constexpr int kDqPerStage = kFixed ? 2 : 1;
   const uint32_t stage_bytes = pf_stage_bytes(BM), act_bytes = (uint32_t)BM * 128;
   auto act_at = [&](int s) { return smem + (size_t)s * stage_bytes; };
   auto pk_at = [&](int s) { return smem + (size_t)s * stage_bytes + act_bytes; };
@@ -303,11 +306,11 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bar_full[s]), 1);
       // a stage is free once the MMA read its activations and the dequantized operand made
-      // from it (commit) and its dequant warp read its codes
-      mbar_init(smem_u32(&bar_empty[s]), 2);
+      // from it (commit) and its dequant warps read its codes
+      mbar_init(smem_u32(&bar_empty[s]), 1 + kDqPerStage);
     }
     for (int d = 0; d < kPfDqBufs; ++d)
-      mbar_init(smem_u32(&bar_dq[d]), 1);                 // the stage's dequant warp
+      mbar_init(smem_u32(&bar_dq[d]), kDqPerStage);       // the stage's dequant warps
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&bar_acc_full[b]), 1);
       mbar_init(smem_u32(&bar_acc_empty[b]), kPfSumWarps);  // one per promotion warp
@@ -417,9 +420,14 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
     // Stage i goes to operand buffer i mod 4, last read by the MMA of stage i - 4, whose
     // commit completed that stage's empty barrier (the ring is at least four deep, so that
     // barrier is never more than one phase away from the phase waited for).
-    // Stage i is dequantized whole by warp i mod 4 into operand buffer i mod 4, so that each
-    // warp's two waits per stage cover a whole stage of work (four warps sharing every stage
-    // measured slower: their waits, not the conversion, set the pace).  Lane `lane` of
+    // Stage i goes to operand buffer i mod 4.  With 64- and 128-row tiles warp i mod 4
+    // dequantizes it whole, so that each warp's two waits per stage cover a whole stage of
+    // work (four warps sharing every stage measured slower: their waits, not the conversion,
+    // set the pace); with 256-row tiles, whose ring is only four stages deep, the pair of
+    // warps 2 (i mod 2) and 2 (i mod 2) + 1 takes half of it each, halving the stage's
+    // latency (M=4096: 401 -> 355 us; with 64-row tiles the pair was slower, 31 -> 38 us).
+    // Either way the buffer-reuse wait below (the MMA of stage i - 4) implies that stage
+    // i - S was consumed, so the stage's full barrier is at most one phase behind.  Lane `lane` of
     // sub-tile u (columns 16u .. 16u + 15 of the tile) holds the 16-byte fragment: rows
     // r0 = lane / 4 and r0 + 8 of the sub-tile, k = 16j + 2(lane % 4) + 8h + {0,1}.  The
     // dequantized operand is K-major core matrices (8 rows x 16 bytes), core matrix (8-row
@@ -437,7 +445,9 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
       for (int gi = 0; gi < g1 - g0 && ok; ++gi) {
         const int g = pf_group(g0, g1, tn, gi);
         for (int st = 0; st < SPG; ++st, ++i) {
-          if ((int)(i % kPfDqBufs) != d) continue;
+          // one warp per stage: stage i is warp i mod 4's; a pair: warps 2 (i mod 2) and
+          // 2 (i mod 2) + 1, each with half of the stage's sub-tiles
+          if (kDqPerStage == 1 ? (int)(i % kPfDqBufs) != d : (int)(i & 1) != (d >> 1)) continue;
           const int s = (int)(i % (uint32_t)S);
           // the buffer was last read by the MMA of stage i - 4, whose commit completed that
           // stage's empty barrier; the ring is at least four deep, so that barrier is never
@@ -448,11 +458,15 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
                mbar_wait(smem_u32(&bar_full[s]), (i / (uint32_t)S) & 1, token);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
-          uint8_t *dqb = dq_at(d);
+          const int dbuf = (int)(i % kPfDqBufs);
+          uint8_t *dqb = dq_at(dbuf);
           // (with zero points the loop is kept rolled: fully unrolled, their loads are all
           // hoisted and spill)
-#pragma unroll (ZP ? 1 : 8)
-          for (int sub = 0; sub < 8; ++sub) {
+          constexpr int kSubs = 8 / kDqPerStage;       // 16-column sub-tiles per warp
+          const int sub0 = kDqPerStage == 1 ? 0 : (d & 1) * kSubs;
+#pragma unroll (ZP ? 1 : kSubs)
+          for (int su = 0; su < kSubs; ++su) {
+            const int sub = sub0 + su;
             uint32_t zl = pc.sym, zh = pc.sym;
             if (ZP) {
               const int n = tn * kPfTileN + sub * 16 + r0;
@@ -477,7 +491,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic -> tensor core
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&bar_dq[d]));
+            mbar_arrive(smem_u32(&bar_dq[dbuf]));
             mbar_arrive(smem_u32(&bar_empty[s]));          // this warp is done with the codes
           }
         }
