@@ -447,7 +447,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
         for (int st = 0; st < SPG; ++st, ++i) {
           // one warp per stage: stage i is warp i mod 4's; a pair: warps 2 (i mod 2) and
           // 2 (i mod 2) + 1, each with half of the stage's sub-tiles
-          if (kDqPerStage == 1 ? (int)(i % kPfDqBufs) != d : (int)(i & 1) != (d >> 1)) continue;
+          if ((int)(i % (kPfDqWarps / kDqPerStage)) != d / kDqPerStage) continue;
           const int s = (int)(i % (uint32_t)S);
           // the buffer was last read by the MMA of stage i - 4, whose commit completed that
           // stage's empty barrier; the ring is at least four deep, so that barrier is never
@@ -463,7 +463,7 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
           // (with zero points the loop is kept rolled: fully unrolled, their loads are all
           // hoisted and spill)
           constexpr int kSubs = 8 / kDqPerStage;       // 16-column sub-tiles per warp
-          const int sub0 = kDqPerStage == 1 ? 0 : (d & 1) * kSubs;
+          const int sub0 = (d % kDqPerStage) * kSubs;
 #pragma unroll (ZP ? 1 : kSubs)
           for (int su = 0; su < kSubs; ++su) {
             const int sub = sub0 + su;
