@@ -166,12 +166,12 @@ __global__ void __launch_bounds__((gv::kConsumers + 1) * 32, 1)
   uint8_t *tables = ring + (size_t)S * NC * kSlotCodes;
   float *pieces = reinterpret_cast<float *>(tables + (size_t)NC * p.table_bytes);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s)
-      for (int w = 0; w < NC; ++w) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full_bar[s][w])) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&empty_bar[s][w])) : "memory");
-      }
+  // one (stage, consumer) pair of barriers per thread: initialised by a single thread, the 128
+  // barriers held the producer's first copy back by about 1.5 us
+  if (threadIdx.x < S * NC) {
+    const int s = threadIdx.x / NC, w = threadIdx.x - s * NC;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&full_bar[s][w])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&empty_bar[s][w])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (threadIdx.x < 4) {

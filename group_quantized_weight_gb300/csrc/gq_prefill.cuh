@@ -38,6 +38,7 @@
 namespace gq {
 
 constexpr int kPfMaxStages = 12;             // TMA ring depth (64-k stages), at most
+static_assert(kPfMaxStages <= 32, "one initialising thread per stage in a warp");
 constexpr int kPfDqBufs = 4;                 // dequantized-operand buffers
 constexpr int kPfDqWarps = 4;                // warpgroup 1
 static_assert(kPfDqWarps == kPfDqBufs, "one warp per stage: warp d fills operand buffer d");
@@ -302,20 +303,26 @@ w4_prefill_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_consta
   // work units: (tile, K slice) pairs, tile fastest; slice z covers groups zsplit(ng, KS, z)
   const int units = tiles * KS;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), 1);
+  // barrier initialisation spread over the dequant warpgroup's threads (one thread doing all
+  // of them delays every role's start), each fencing its own
+  {
+    const int t = (int)threadIdx.x - 128;          // warpgroup 1
+    bool did = false;
+    if (t >= 0 && t < S) {
+      mbar_init(smem_u32(&bar_full[t]), 1);
       // a stage is free once the MMA read its activations and the dequantized operand made
       // from it (commit) and its dequant warps read its codes
-      mbar_init(smem_u32(&bar_empty[s]), 1 + kDqPerStage);
+      mbar_init(smem_u32(&bar_empty[t]), 1 + kDqPerStage);
+      did = true;
+    } else if (t >= 32 && t < 32 + kPfDqBufs) {
+      mbar_init(smem_u32(&bar_dq[t - 32]), kDqPerStage);  // the stage's dequant warps
+      did = true;
+    } else if (t >= 64 && t < 66) {
+      mbar_init(smem_u32(&bar_acc_full[t - 64]), 1);
+      mbar_init(smem_u32(&bar_acc_empty[t - 64]), kPfSumWarps);  // one per promotion warp
+      did = true;
     }
-    for (int d = 0; d < kPfDqBufs; ++d)
-      mbar_init(smem_u32(&bar_dq[d]), kDqPerStage);       // the stage's dequant warps
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bar_acc_full[b]), 1);
-      mbar_init(smem_u32(&bar_acc_empty[b]), kPfSumWarps);  // one per promotion warp
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (did) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {   // TMEM: two accumulators of 256 columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
