@@ -299,9 +299,10 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   }
   // the fused gate+up epilogue lives in the decode and small-batch kernels only
   const bool gate_up = (prec & GQ_GATE_UP) != 0;
-  if (!gate_up && M >= kPrefillMinM && !(prec & GQ_ZP_FLOAT) &&
+  if (!gate_up && M >= ((prec & GQ_ZP) ? kPrefillMinMZp : kPrefillMinM) &&
+      !(prec & GQ_ZP_FLOAT) &&
       prefill_supported(M, K, N, G, prec)) {
-    // M >= 33: TMA + tcgen05 persistent kernel, one CTA per SM.  Activation tiles of 64,
+    // M >= 25 (33 with zero points): TMA + tcgen05 persistent kernel, one CTA per SM.  Activation tiles of 64,
     // 128 or 256 rows (the MMA's N) so that few rows do not pay for a 256-row product, and
     // the deepest TMA ring that fits.  The kernel can also split K into slices of whole
     // groups (a last-arriver reduction of FP32 partials), but on GB300 every split measured

@@ -142,9 +142,12 @@ void note_cuda_error_code(const char *where, int code);
 // largest M of the small-batch kernel (it takes 33..64 rows only where the prefill kernel
 // does not apply: G = 32)
 constexpr int kBatchMaxM = 64;
-// smallest M routed to the tensor-core prefill kernel: from 33 rows the small-batch kernel
-// needs a second 32-row block and the prefill kernel's 256-row tile is faster
-constexpr int kPrefillMinM = 33;
+// smallest M routed to the tensor-core prefill kernel: from 25 rows the small-batch kernel
+// needs four 8-row MMA tiles per step and the prefill kernel's 64-row tile is faster
+// (K=4096 N=14336 G=128: 33.0 against 31.3 us at M=28, 27.5 against 31.2 us at M=24);
+// with INT4 zero points from 33 rows, where the small-batch kernel needs a second row block
+constexpr int kPrefillMinM = 25;
+constexpr int kPrefillMinMZp = 33;
 constexpr int kPrefillThreads = 512;   // block size of the prefill kernel
 cudaError_t launch_q8_decode(const Plan &p, int M, int K, int N, int G, int prec,
                              const void *A, const void *Wq, const void *scales,

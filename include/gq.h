@@ -333,7 +333,7 @@ int gq_set_fault_injection(int fault);
  * sm_count > 0 overrides the device query, so it works without a GPU. */
 typedef struct gq_plan_t {
   int path;          /* 0 = small-M tensor-core decode (mma.sync, K split across CTAs),
-                        1 = INT8 CUDA-core decode (M > 32), 2 = tcgen05 prefill (W4, M >= 33),
+                        1 = INT8 CUDA-core decode (M > 32), 2 = tcgen05 prefill (W4, M >= 25; 33 with GQ_ZP),
                         3 = striped decode (M <= 8, warps stream contiguous slot ranges),
                         4 = small-batch tensor-core kernel (M <= 32, up to 64 with G = 32;
                             persistent CTAs over (K slice, tile range) pairs),

@@ -144,7 +144,7 @@ def test_plan_is_a_pure_function_of_shape(name):
         # tcgen05 prefill: persistent, at most one CTA per SM; one CTA holds the shared-memory
         # ring (at most 227 KiB per CTA on sm_103a); activation tiles of 64, 128 or 256 rows;
         # scratch only with a K split
-        assert cfg.M >= 33 and cfg.w4
+        assert cfg.M >= (33 if cfg.zp else 25) and cfg.w4
         assert 1 <= p1["grid_x"] <= 152
         assert p1["m_tile"] == (64 if cfg.M <= 64 else 128 if cfg.M <= 128 else 256)
         assert (p1["workspace_bytes"] > 0) == (p1["nsplit"] > 1)
@@ -307,7 +307,7 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     assert e.value.status == 2
     # the decode and small-batch kernels (K % 256 == 0) carry the epilogue: the
     # warp-specialized one up to four rows, the striped one to eight, the small-batch one to
-    # 64 rows; not the prefill kernel, which would take 33 rows and more without it
+    # 64 rows; not the prefill kernel, which would take 25 rows and more without it
     assert gq.gq_plan(1, 4096, 28672, 128, gu, sm_count=152)["path"] == 8
     assert gq.gq_plan(1, 4096, 2048, 128, gu, sm_count=152)["path"] == 8
     assert gq.gq_plan(8, 1024, 512, 64, gu | C.GQ_ZP, sm_count=152)["path"] == 3
@@ -316,6 +316,10 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     assert gq.gq_plan(64, 4096, 1024, 32, gu, sm_count=152)["path"] == 4
     assert gq.gq_plan(33, 4096, 1024, 64, gu, sm_count=152)["path"] == 4
     assert gq.gq_plan(33, 4096, 1024, 64, C.GQ_W4, sm_count=152)["path"] == 2
+    assert gq.gq_plan(25, 4096, 1024, 64, gu, sm_count=152)["path"] == 4
+    assert gq.gq_plan(25, 4096, 1024, 64, C.GQ_W4, sm_count=152)["path"] == 2
+    assert gq.gq_plan(24, 4096, 1024, 64, C.GQ_W4, sm_count=152)["path"] == 4
+    assert gq.gq_plan(32, 4096, 1024, 64, C.GQ_W4 | C.GQ_ZP, sm_count=152)["path"] == 4
     for M, K, G in ((1, 320, 64), (65, 4096, 32), (65, 4096, 128)):
         with pytest.raises(C.GqError) as e:
             gq.gq_plan(M, K, 1024, G, gu, sm_count=152)
