@@ -181,7 +181,7 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     }
     const int max_cta_slots = ceil_div(split_count, grid) * split_mult;
     const size_t smem = gemv_smem_bytes(Mc, K, G, prec, max_cta_slots);
-    if (smem <= kCtaSmemCap) {
+    if (smem + 256 <= kCtaSmemCap) {                // 256: its static barriers past 1 KB
       p->path = kPathGemv;
       p->mt = 1;
       p->m_tile = 4;
@@ -242,6 +242,52 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     }
     p->nsplit = p->grid_x;
     return GQ_OK;
+  }
+  // INT8 codes, M <= 4, N a multiple of 64: warp-specialized decode, one CTA per SM (a
+  // producer warp streaming 2 KB slots for sixteen consumer warps) over a contiguous range of
+  // (64-column block, group) units; whole blocks per CTA when that keeps the SMs within 10%
+  // of even, else equal unit ranges with a cross-CTA reduction.  Not a K split: the split
+  // override leaves it alone.
+  if (q8_gemv_supported(Mc, K, Nc, G, prec)) {
+    const int NB = Nc / 64, gpb = K / G;
+    const int units = NB * gpb, per = ceil_div(NB, sms);
+    int grid, split_count, split_mult;
+    if (NB >= sms && (double)NB >= 0.9 * (double)sms * per) {
+      grid = sms;
+      split_count = NB;
+      split_mult = gpb;
+    } else {
+      // equal unit ranges: at least two units per consumer warp, at most one CTA per SM
+      grid = ceil_div(units, 32);
+      if (grid > sms) grid = sms;
+      split_count = units;
+      split_mult = 1;
+    }
+    const int max_cta_units = ceil_div(split_count, grid) * split_mult;
+    const size_t smem = q8_gemv_smem_bytes(Mc, K, max_cta_units);
+    if (smem + 256 <= kCtaSmemCap) {                // 256: its static barriers past 1 KB
+      p->path = kPathQ8Gemv;
+      p->mt = 1;
+      p->m_tile = Mc;
+      p->n_tile = 64;
+      p->unit_k = G;
+      p->units = units;
+      p->table_bytes = q8_gemv_table_bytes(max_cta_units);
+      p->block_threads = q8_gemv_threads();
+      p->smem_bytes = smem;
+      p->grid_x = grid;
+      p->grid_y = p->grid_z = 1;
+      p->split_count = split_count;
+      p->split_mult = split_mult;
+      if (split_mult == 1) {
+        p->part_bytes = round_up(q8_gemv_part_bytes(grid), 256);
+        p->counter_bytes = kCounterRegionBytes;
+        if ((size_t)NB * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
+      }
+      p->workspace_bytes = p->part_bytes + p->counter_bytes;
+      p->nsplit = p->grid_x;
+      return GQ_OK;
+    }
   }
   // INT8 codes, 5 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 4
   // rows the CUDA-core kernel below is faster: it is load-latency-bound there)
@@ -458,6 +504,7 @@ size_t plan_counter_bytes_used(const Plan &p, int M, int N) {
     case kPathPrefill: n = (size_t)ceil_div(Nc, 128) * ceil_div(M > 0 ? M : 1, p.m_tile) * 8; break;
     case kPathQ8Mma: n = (size_t)ceil_div(Nc, 64); break;
     case kPathQ8Block: n = (size_t)ceil_div(Nc, p.n_tile); break;
+    case kPathQ8Gemv: n = (size_t)ceil_div(Nc, 64); break;
     case kPathBatch: n = (size_t)p.grid_z * ceil_div(Nc, kTileN); break;
     default: n = (size_t)p.grid_x * p.grid_z; break;
   }
@@ -536,6 +583,8 @@ cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, con
       return launch_q8_mma(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     case kPathQ8Block:
       return launch_q8_block(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
+    case kPathQ8Gemv:
+      return launch_q8_gemv(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     case kPathQ8Decode:
       return launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     default:
@@ -586,7 +635,7 @@ int gq_set_wait_limit(long long cycles) {
   if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return GQ_ERR_NO_DEVICE; }
   const long long v = cycles == 0 ? 4000000000ll : cycles;
   const int r = gemv_set_wait_limit(v) | stripe_set_wait_limit(v) | batch_set_wait_limit(v) |
-                prefill_set_wait_limit(v) | fp8_set_wait_limit(v);
+                prefill_set_wait_limit(v) | fp8_set_wait_limit(v) | q8_gemv_set_wait_limit(v);
   if (r != 0) {
     note_cuda_error_code("gq_set_wait_limit", r);
     cudaGetLastError();
@@ -937,7 +986,8 @@ int gq_device_error(int clear) {
   const int x = batch_read_error(clear);
   const int y = fp8_read_error(clear);
   const int g = gemv_read_error(clear);
-  return v != 0 ? v : (w != 0 ? w : (x != 0 ? x : (y != 0 ? y : g)));
+  const int q = q8_gemv_read_error(clear);
+  return v != 0 ? v : (w != 0 ? w : (x != 0 ? x : (y != 0 ? y : (g != 0 ? g : q))));
 }
 
 int gq_quantize_act_fp8(int M, int K, int prec, const void *A, void *Aq, void *a_scales,

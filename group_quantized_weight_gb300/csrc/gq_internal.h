@@ -38,7 +38,8 @@ constexpr int kQ8MaxRows = 32;
 constexpr size_t kCounterRegionBytes = 256u << 10;   // 65536 counters
 
 enum Path { kPathMmaDecode = 0, kPathQ8Decode = 1, kPathPrefill = 2, kPathStripe = 3,
-            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6, kPathQ8A8 = 7, kPathGemv = 8 };
+            kPathBatch = 4, kPathQ8Block = 5, kPathQ8Mma = 6, kPathQ8A8 = 7, kPathGemv = 8,
+            kPathQ8Gemv = 9 };
 
 struct Plan {
   int path;
@@ -54,9 +55,9 @@ struct Plan {
   size_t part_bytes;     // split-K partials
   size_t counter_bytes;  // arrival counters
   size_t workspace_bytes;
-  int split_count, split_mult;   // path 3: CTA c owns slots zsplit(split_count, grid, c) * split_mult
+  int split_count, split_mult;   // paths 3, 8, 9: CTA c owns zsplit(split_count, grid, c) * split_mult
   int slots;                     // path 3: ring slots per warp; path 2: TMA ring stages
-  int table_bytes;               // path 8: bytes of a consumer warp's scale table
+  int table_bytes;               // paths 8, 9: bytes of a consumer warp's scale table
 };
 
 // scale / output type codes used as template parameters
@@ -102,6 +103,18 @@ int gemv_read_error(int clear);
 int gemv_set_wait_limit(long long cycles);
 // GQ_FAULT_DEVICE_WAIT: the producer warps of later launches withhold one slot
 int gemv_set_withhold(bool on);
+// warp-specialized INT8 decode kernel (M <= 4, N a multiple of 64): a producer warp and sixteen
+// consumer warps per CTA over (64-column block, group) units
+bool q8_gemv_supported(int M, int K, int N, int G, int prec);
+int q8_gemv_table_bytes(int max_cta_units);
+size_t q8_gemv_smem_bytes(int M, int K, int max_cta_units);
+size_t q8_gemv_part_bytes(int grid);
+int q8_gemv_threads();
+cudaError_t launch_q8_gemv(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
+                           const void *Wq, const void *scales, void *out, float *part,
+                           unsigned *counters, cudaStream_t s);
+int q8_gemv_read_error(int clear);
+int q8_gemv_set_wait_limit(long long cycles);
 // gq_set_fault_injection(GQ_FAULT_LAUNCH): true, with the error detail noted, when the next
 // launch is to fail
 bool launch_fault_injected();

@@ -341,7 +341,12 @@ typedef struct gq_plan_t {
                             per CTA, paired FP32 FMAs),
                         6 = INT8 on BF16 tensor cores for 5 <= M <= 32 (codes exact in
                             BF16, fp32 activations as three exact BF16 parts),
-                        7 = W8A8 integer group GEMM (GQ_ACT_I8, dp4a) */
+                        7 = W8A8 integer group GEMM (GQ_ACT_I8, dp4a),
+                        8 = warp-specialized W4 decode (M <= 4: a producer warp streaming
+                            2 KB slots of codes with cp.async.bulk, sixteen consumer warps
+                            on mma.sync),
+                        9 = warp-specialized INT8 decode (M <= 4, N a multiple of 64, G of
+                            32, 64 or 128: the same roles, FP32 products on CUDA cores) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
   int n_tile;        /* output columns one CTA covers */

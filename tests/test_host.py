@@ -179,6 +179,23 @@ def test_plan_is_a_pure_function_of_shape(name):
         else:
             assert tiles >= 152
         return
+    if p1["path"] == 9:
+        # warp-specialized INT8 decode (M <= 4, N a multiple of 64): a producer warp and
+        # sixteen consumer warps per CTA over (64-column block, group) units, at most one CTA
+        # per SM; whole blocks per CTA need no scratch, equal unit ranges per-CTA partial sums
+        # and per-block counters
+        blocks = cfg.N // 64
+        units = blocks * (cfg.K // cfg.G)
+        assert not cfg.w4 and cfg.M <= 4 and cfg.N % 64 == 0
+        assert p1["block_threads"] == 17 * 32
+        assert 1 <= p1["grid_x"] <= min(152, units)
+        assert p1["nsplit"] == p1["grid_x"] and p1["n_tile"] == 64
+        assert p1["smem_bytes"] <= 227 * 1024 - 1024 - 256
+        if p1["workspace_bytes"]:
+            assert p1["workspace_bytes"] >= p1["grid_x"] * 2 * 4 * 64 * 4 + 4 * blocks
+        else:
+            assert blocks >= 152
+        return
     if p1["path"] == 4:
         # small-batch kernel: (K slice, tile range) CTAs x 32-row blocks, at most one wave
         assert 1 <= cfg.M <= 64 and cfg.K % 256 == 0
@@ -267,6 +284,42 @@ def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
     assert p["workspace_bytes"] >= 4 * 16 * 28672 * 4
 
 
+def test_q8_decode_plan_partitions_block_group_units():
+    """INT8 rows M <= 4 with N a multiple of 64: the warp-specialized kernel, one CTA per SM at
+    most over contiguous (64-column block, group) ranges; the split override (a K-slice
+    count) does not apply to it."""
+    W8 = C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_OUT_F32
+    # the Q8_0 projection: 192 blocks x 64 groups on 152 SMs, equal unit ranges
+    p = gq.gq_plan(1, 2048, 12288, 32, W8, sm_count=152)
+    assert p["path"] == 9 and p["grid_x"] == 152 and p["workspace_bytes"] > 0
+    # 304 blocks: two whole blocks per CTA, no scratch
+    p = gq.gq_plan(2, 1024, 304 * 64, 64, W8, sm_count=152)
+    assert p["path"] == 9 and p["grid_x"] == 152 and p["workspace_bytes"] == 0
+    # a small shape (4 blocks x 16 groups): at least two units per consumer warp
+    p = gq.gq_plan(3, 512, 256, 32, W8, sm_count=152)
+    assert p["path"] == 9 and p["grid_x"] == 2
+    # not taken: N not a multiple of 64, G of 16 or 256, five rows, activations too wide
+    assert gq.gq_plan(1, 2048, 1000, 32, W8, sm_count=152)["path"] == 5
+    assert gq.gq_plan(1, 2048, 1024, 256, W8, sm_count=152)["path"] == 5
+    assert gq.gq_plan(5, 2048, 1024, 32, W8, sm_count=152)["path"] == 6
+    assert gq.gq_plan(4, 16384, 1024, 32, W8, sm_count=152)["path"] == 5
+    # the GPU parity shapes named q8g_* and the gate+up ones meant for it take this kernel
+    for M, K, N, G in ((3, 1024, 640, 64), (4, 2048, 448, 128), (2, 512, 19456, 32),
+                       (1, 96, 64, 32)):
+        assert gq.gq_plan(M, K, N, G, W8, sm_count=152)["path"] == 9, (M, K, N, G)
+    assert gq.gq_plan(2, 512, 19456, 32, W8, sm_count=152)["workspace_bytes"] == 0
+    gu = W8 | C.GQ_GATE_UP
+    assert gq.gq_plan(1, 2048, 1024, 32, gu, sm_count=152)["path"] == 9
+    assert gq.gq_plan(3, 2048, 128, 32, gu, sm_count=152)["path"] == 9
+    assert gq.gq_plan(2, 2048, 128, 256, gu, sm_count=152)["path"] == 5
+    prev = gq.gq_set_split_override(2)
+    try:
+        q = gq.gq_plan(1, 2048, 12288, 32, W8, sm_count=152)
+        assert q["path"] == 9 and q["grid_x"] == 152
+    finally:
+        gq.gq_set_split_override(prev)
+
+
 def test_small_decode_plan_splits_slots_between_ctas():
     p = gq.gq_plan(1, 4096, 1024, 128, C.GQ_W4, sm_count=152)
     assert p["path"] == 8
@@ -299,8 +352,11 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     W8GU = C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_GATE_UP
     assert gq.gq_gemm(1, 512, 24, 128, gu, 16, 16, 16, None, 16, None) == 1
     assert gq.gq_gemm(1, 512, 32, 32, W8GU, 16, 16, 16, None, 16, None) == 1
-    # INT8: the CUDA-core kernel up to four rows, the tensor-core one to 32; not above
-    assert gq.gq_plan(1, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 5
+    # INT8: the warp-specialized kernel up to four rows (the CUDA-core block kernel when N is
+    # not a multiple of 64), the tensor-core one to 32; not above
+    assert gq.gq_plan(1, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 9
+    assert gq.gq_plan(4, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 9
+    assert gq.gq_plan(1, 2048, 12224, 32, W8GU, sm_count=152)["path"] == 9
     assert gq.gq_plan(32, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 6
     with pytest.raises(C.GqError) as e:
         gq.gq_plan(33, 2048, 12288, 32, W8GU, sm_count=152)
