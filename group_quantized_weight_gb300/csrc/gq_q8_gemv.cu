@@ -1,4 +1,4 @@
-// Warp-specialized INT8 (Q8_0-style) decode kernel for M <= 4, fp32 activations and scales.
+// Warp-specialized INT8 (Q8_0-style) decode kernel for M <= 2, fp32 activations and scales.
 //
 // At decode the INT8 path is bound by the bytes of its codes ("GPU Kernel 工程（09）：量化与
 // 融合 kernel", section 3.2), and a short problem (the Q8_0 projection reads 28 MB) is set by
@@ -36,11 +36,11 @@ namespace gq {
 
 namespace q8g {
 constexpr int kConsumers = 16;                  // consumer warps per CTA
-constexpr int kStages = 4;                      // ring stages (one slot per consumer each)
+constexpr int kStages = 3;                      // ring stages (one slot per consumer each)
 constexpr int kSlotBytes = 2048;                // 32 k x 64 columns of codes
 constexpr int kSlotK = 32;
 constexpr int kCols = 64;                       // columns per block (two per lane)
-constexpr int kMaxRows = 4;
+constexpr int kMaxRows = 2;
 constexpr int kUnitTable = kCols * 4;           // table bytes per unit: 64 fp32 scales
 }  // namespace q8g
 
@@ -54,7 +54,7 @@ struct Q8GemvParams {
   const float *A;             // [M][K]
   const float *S;             // [K/G][N]
   void *out;                  // [M][N] (gate+up: [M][N/2])
-  float *part;                // [gridDim.x][2][4][64] per-CTA partial sums (shared blocks)
+  float *part;                // [gridDim.x][2][2][64] per-CTA partial sums (shared blocks)
   unsigned *counters;         // per-block arrival counters (shared blocks)
   int M, K, N, G;
   int split_count, split_mult;   // CTA c owns units zsplit(split_count, grid, c) * split_mult
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
 // ------------------------------------------------------------------ host side
 
 namespace {
-int q8_gemv_rows(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
+int q8_gemv_rows(int M) { return M <= 1 ? 1 : 2; }
 }  // namespace
 
 bool q8_gemv_supported(int M, int K, int N, int G, int prec) {
@@ -498,11 +498,8 @@ cudaError_t launch_q8_gemv(const Plan &pl, int M, int K, int N, int G, int prec,
   qp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   qp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   qp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
-  switch (q8_gemv_rows(M)) {
-    case 1: return launch_q8g_g<1>(pl, qp, s);
-    case 2: return launch_q8g_g<2>(pl, qp, s);
-    default: return launch_q8g_g<4>(pl, qp, s);
-  }
+  if (q8_gemv_rows(M) == 1) return launch_q8g_g<1>(pl, qp, s);
+  return launch_q8g_g<2>(pl, qp, s);
 }
 
 int q8_gemv_set_wait_limit(long long cycles) {

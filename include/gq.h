@@ -345,7 +345,7 @@ typedef struct gq_plan_t {
                         8 = warp-specialized W4 decode (M <= 4: a producer warp streaming
                             2 KB slots of codes with cp.async.bulk, sixteen consumer warps
                             on mma.sync),
-                        9 = warp-specialized INT8 decode (M <= 4, N a multiple of 64, G of
+                        9 = warp-specialized INT8 decode (M <= 2, N a multiple of 64, G of
                             32, 64 or 128: the same roles, FP32 products on CUDA cores) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
