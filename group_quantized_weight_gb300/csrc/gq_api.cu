@@ -121,6 +121,54 @@ static int choose_nsplit(int base_ctas, int units, int unit_k, int target,
   return ns;
 }
 
+// INT8 codes, N a multiple of 64, few rows: the warp-specialized decode kernel, one CTA per
+// SM (a producer warp streaming 2 KB slots for sixteen consumer warps) over a contiguous range
+// of (64-column block, group) units; whole blocks per CTA when that keeps the SMs within 10%
+// of even, else equal unit ranges with a cross-CTA reduction.  Not a K split: the split
+// override leaves it alone.  False (p untouched) when the kernel does not take the shape.
+static bool plan_q8_gemv(int Mc, int K, int Nc, int G, int prec, int sms, size_t smem_cap,
+                         Plan *p) {
+  if (!q8_gemv_supported(Mc, K, Nc, G, prec)) return false;
+  const int NB = Nc / 64, gpb = K / G;
+  if ((size_t)NB * sizeof(unsigned) > kCounterRegionBytes) return false;
+  const int units = NB * gpb, per = ceil_div(NB, sms);
+  int grid, split_count, split_mult;
+  if (NB >= sms && (double)NB >= 0.9 * (double)sms * per) {
+    grid = sms;
+    split_count = NB;
+    split_mult = gpb;
+  } else {
+    // equal unit ranges: at least two units per consumer warp, at most one CTA per SM
+    grid = ceil_div(units, 32);
+    if (grid > sms) grid = sms;
+    split_count = units;
+    split_mult = 1;
+  }
+  const int max_cta_units = ceil_div(split_count, grid) * split_mult;
+  const size_t smem = q8_gemv_smem_bytes(Mc, K, G, prec, max_cta_units);
+  if (smem + 256 > smem_cap) return false;           // 256: its static barriers past 1 KB
+  p->path = kPathQ8Gemv;
+  p->mt = 1;
+  p->m_tile = Mc;
+  p->n_tile = 64;
+  p->unit_k = G;
+  p->units = units;
+  p->table_bytes = q8_gemv_table_bytes(max_cta_units);
+  p->block_threads = q8_gemv_threads();
+  p->smem_bytes = smem;
+  p->grid_x = grid;
+  p->grid_y = p->grid_z = 1;
+  p->split_count = split_count;
+  p->split_mult = split_mult;
+  if (split_mult == 1) {
+    p->part_bytes = round_up(q8_gemv_part_bytes(grid), 256);
+    p->counter_bytes = kCounterRegionBytes;
+  }
+  p->workspace_bytes = p->part_bytes + p->counter_bytes;
+  p->nsplit = p->grid_x;
+  return true;
+}
+
 int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   int st = validate(M, K, N, G, prec);
   if (st != GQ_OK) return st;
@@ -135,6 +183,8 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   // float zero points: the small-batch kernel only
   if ((prec & GQ_ZP_FLOAT) && !(Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)))
     return GQ_ERR_UNSUPPORTED;
+  // W8A8 (GQ_ACT_I8), M <= 4: the warp-specialized decode kernel with dp4a group dots
+  if ((prec & GQ_ACT_I8) && plan_q8_gemv(Mc, K, Nc, G, prec, sms, kCtaSmemCap, p)) return GQ_OK;
   // W8A8 (GQ_ACT_I8): integer group dots, 64 columns x one K slice x 32 rows per CTA
   if (prec & GQ_ACT_I8) {
     const int ks = q8a8_slices(Mc, K, Nc, G, sms, kPartCap, split_override());
@@ -243,53 +293,10 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->nsplit = p->grid_x;
     return GQ_OK;
   }
-  // INT8 codes, M <= 2, N a multiple of 64: warp-specialized decode, one CTA per SM (a
-  // producer warp streaming 2 KB slots for sixteen consumer warps) over a contiguous range of
-  // (64-column block, group) units; whole blocks per CTA when that keeps the SMs within 10%
-  // of even, else equal unit ranges with a cross-CTA reduction.  Not a K split: the split
-  // override leaves it alone.  (Three and four rows: the block kernel below measured faster,
-  // 16.6 / 16.9 against 18.1 / 20.6 us on the Q8_0 shape.)
-  if (q8_gemv_supported(Mc, K, Nc, G, prec)) {
-    const int NB = Nc / 64, gpb = K / G;
-    const int units = NB * gpb, per = ceil_div(NB, sms);
-    int grid, split_count, split_mult;
-    if (NB >= sms && (double)NB >= 0.9 * (double)sms * per) {
-      grid = sms;
-      split_count = NB;
-      split_mult = gpb;
-    } else {
-      // equal unit ranges: at least two units per consumer warp, at most one CTA per SM
-      grid = ceil_div(units, 32);
-      if (grid > sms) grid = sms;
-      split_count = units;
-      split_mult = 1;
-    }
-    const int max_cta_units = ceil_div(split_count, grid) * split_mult;
-    const size_t smem = q8_gemv_smem_bytes(Mc, K, max_cta_units);
-    if (smem + 256 <= kCtaSmemCap) {                // 256: its static barriers past 1 KB
-      p->path = kPathQ8Gemv;
-      p->mt = 1;
-      p->m_tile = Mc;
-      p->n_tile = 64;
-      p->unit_k = G;
-      p->units = units;
-      p->table_bytes = q8_gemv_table_bytes(max_cta_units);
-      p->block_threads = q8_gemv_threads();
-      p->smem_bytes = smem;
-      p->grid_x = grid;
-      p->grid_y = p->grid_z = 1;
-      p->split_count = split_count;
-      p->split_mult = split_mult;
-      if (split_mult == 1) {
-        p->part_bytes = round_up(q8_gemv_part_bytes(grid), 256);
-        p->counter_bytes = kCounterRegionBytes;
-        if ((size_t)NB * sizeof(unsigned) > kCounterRegionBytes) return GQ_ERR_UNSUPPORTED;
-      }
-      p->workspace_bytes = p->part_bytes + p->counter_bytes;
-      p->nsplit = p->grid_x;
-      return GQ_OK;
-    }
-  }
+  // INT8 codes with fp32 activations, M <= 2: the warp-specialized decode kernel (three and
+  // four rows: the block kernel below measured faster, 16.6 / 16.9 against 18.1 / 20.6 us on
+  // the Q8_0 shape)
+  if (plan_q8_gemv(Mc, K, Nc, G, prec, sms, kCtaSmemCap, p)) return GQ_OK;
   // INT8 codes, 5 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 4
   // rows the CUDA-core kernel below is faster: it is load-latency-bound there)
   if (Mc > 4 && Mc <= 32 && q8_mma_supported(Mc, K, G, prec) &&
@@ -585,7 +592,8 @@ cudaError_t launch_plan(const Plan &p, int M, int K, int N, int G, int prec, con
     case kPathQ8Block:
       return launch_q8_block(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     case kPathQ8Gemv:
-      return launch_q8_gemv(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
+      return launch_q8_gemv(p, M, K, N, G, prec, A, nullptr, Wq, scales, out, part, counters,
+                            s);
     case kPathQ8Decode:
       return launch_q8_decode(p, M, K, N, G, prec, A, Wq, scales, out, part, counters, s);
     default:
@@ -875,9 +883,12 @@ static int gemm_a8_impl(int M, int K, int N, int G, int prec, const void *Aq,
   unsigned *counters = (unsigned *)ws;
   float *part = ws ? (float *)((char *)ws + p.counter_bytes) : nullptr;
   if (launch_fault_injected()) return GQ_ERR_CUDA;
-  const cudaError_t e = launch_q8a8(p, M, K, N, G, prec, (const int8_t *)Aq,
-                                    (const float *)a_scales, Wq, scales, out, part, counters,
-                                    (cudaStream_t)stream);
+  const cudaError_t e =
+      p.path == kPathQ8Gemv
+          ? launch_q8_gemv(p, M, K, N, G, prec, Aq, (const float *)a_scales, Wq, scales, out,
+                           part, counters, (cudaStream_t)stream)
+          : launch_q8a8(p, M, K, N, G, prec, (const int8_t *)Aq, (const float *)a_scales, Wq,
+                        scales, out, part, counters, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     note_cuda_error("launch", e);
     cudaGetLastError();

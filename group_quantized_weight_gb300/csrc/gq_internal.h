@@ -103,16 +103,17 @@ int gemv_read_error(int clear);
 int gemv_set_wait_limit(long long cycles);
 // GQ_FAULT_DEVICE_WAIT: the producer warps of later launches withhold one slot
 int gemv_set_withhold(bool on);
-// warp-specialized INT8 decode kernel (M <= 2, N a multiple of 64): a producer warp and sixteen
-// consumer warps per CTA over (64-column block, group) units
+// warp-specialized INT8 decode kernel (N a multiple of 64; M <= 2, W8A8 M <= 4): a producer
+// warp and sixteen consumer warps per CTA over (64-column block, group) units
 bool q8_gemv_supported(int M, int K, int N, int G, int prec);
 int q8_gemv_table_bytes(int max_cta_units);
-size_t q8_gemv_smem_bytes(int M, int K, int max_cta_units);
+size_t q8_gemv_smem_bytes(int M, int K, int G, int prec, int max_cta_units);
 size_t q8_gemv_part_bytes(int grid);
 int q8_gemv_threads();
+// A: fp32 activations, or INT8 ones with a_scales [M][K/G] (GQ_ACT_I8)
 cudaError_t launch_q8_gemv(const Plan &p, int M, int K, int N, int G, int prec, const void *A,
-                           const void *Wq, const void *scales, void *out, float *part,
-                           unsigned *counters, cudaStream_t s);
+                           const float *a_scales, const void *Wq, const void *scales,
+                           void *out, float *part, unsigned *counters, cudaStream_t s);
 int q8_gemv_read_error(int clear);
 int q8_gemv_set_wait_limit(long long cycles);
 // gq_set_fault_injection(GQ_FAULT_LAUNCH): true, with the error detail noted, when the next

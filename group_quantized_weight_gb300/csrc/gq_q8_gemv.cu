@@ -1,4 +1,5 @@
-// Warp-specialized INT8 (Q8_0-style) decode kernel for M <= 2, fp32 activations and scales.
+// Warp-specialized INT8 (Q8_0-style) decode kernel: fp32 activations (M <= 2) or INT8
+// activations with a scale per (row, group) (W8A8, M <= 4), fp32 weight scales.
 //
 // At decode the INT8 path is bound by the bytes of its codes ("GPU Kernel 工程（09）：量化与
 // 融合 kernel", section 3.2), and a short problem (the Q8_0 projection reads 28 MB) is set by
@@ -10,8 +11,8 @@
 //                   GQ_STATIC_W it starts before the wait on the previous kernel.
 //   consumer warps  copy the group scales of their units into a table of their own, stage
 //                   the activations, then per slot: one bounded wait, four 16-byte reads of
-//                   codes, the slot released at once (the codes are in registers), and FP32
-//                   products on CUDA cores.
+//                   codes, the slot released at once (the codes are in registers), and the
+//                   products on CUDA cores (FP32, or dp4a for INT8 activations).
 // The consumers need about two instructions per code, well under what the SM can issue in the
 // time HBM takes to deliver the bytes, so the ring runs nearly empty and little is left to do
 // when the last copy lands.
@@ -20,7 +21,10 @@
 // per (column, group) the FP32 dot of the exact codes with the activations (even and odd k in
 // two sums, one fma.rn.f32x2 per two products), then the group's scale times that dot added to
 // the column's running sum.  An INT8 code c becomes the exact float c by placing (c xor 0x80)
-// in the low byte of 2^23 and subtracting 2^23 + 128.
+// in the low byte of 2^23 and subtracting 2^23 + 128.  With INT8 activations the group's dot
+// is the exact INT32 sum of dp4a products, converted exactly (|dot| <= 128 * 127^2 < 2^24)
+// and multiplied by the activation scale times the weight scale (the same FMA as the W8A8
+// block kernel).
 //
 // Work partition (the striped partitioning of section 3.3 item 4 of the first page): with N a
 // multiple of 64 the packed codes are the units (64-column block b, group g) one after another,
@@ -40,7 +44,8 @@ constexpr int kStages = 3;                      // ring stages (one slot per con
 constexpr int kSlotBytes = 2048;                // 32 k x 64 columns of codes
 constexpr int kSlotK = 32;
 constexpr int kCols = 64;                       // columns per block (two per lane)
-constexpr int kMaxRows = 2;
+constexpr int kMaxRows = 4;                     // W8A8; 2 with fp32 activations
+constexpr int kMaxRowsF32 = 2;
 constexpr int kUnitTable = kCols * 4;           // table bytes per unit: 64 fp32 scales
 }  // namespace q8g
 
@@ -51,10 +56,12 @@ static __device__ long long g_q8g_wait_limit = 4000000000ll;
 
 struct Q8GemvParams {
   const uint8_t *Wp;          // packed codes, 64-column blocks of K/16 chunk rows
-  const float *A;             // [M][K]
+  const float *A;             // [M][K] fp32 activations, or
+  const int8_t *Aq;           // [M][K] INT8 activations and
+  const float *As;            // [M][K/G] their scales
   const float *S;             // [K/G][N]
   void *out;                  // [M][N] (gate+up: [M][N/2])
-  float *part;                // [gridDim.x][2][2][64] per-CTA partial sums (shared blocks)
+  float *part;                // [gridDim.x][2][4][64] per-CTA partial sums (shared blocks)
   unsigned *counters;         // per-block arrival counters (shared blocks)
   int M, K, N, G;
   int split_count, split_mult;   // CTA c owns units zsplit(split_count, grid, c) * split_mult
@@ -112,15 +119,30 @@ __device__ __forceinline__ void codes2(uint32_t w, int b0, float &c0, float &c1)
   fma2(c0, c1, 1.f, 1.f, -8388736.f, -8388736.f);   // - (2^23 + 128), exact
 }
 
+// bytes of the activation area: MR rows of K fp32 values, or MR rows of K INT8 codes and then
+// MR rows of K / G fp32 scales
+__host__ __device__ inline size_t act_bytes(int MR, int K, int G, bool a8) {
+  const size_t b = a8 ? (((size_t)MR * K + 15) & ~(size_t)15) + (size_t)MR * (K / G) * 4
+                      : (size_t)MR * K * 4;
+  return (b + 127) & ~(size_t)127;
+}
+
+__device__ __forceinline__ int dp4a(int a, int b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 }  // namespace q8g
 
 // Shared memory (dynamic, base rounded up to 128 bytes): [act][ring][tables][pieces]
-//   act     MR rows of K fp32 activations (rows past M zero)
+//   act     MR rows of K fp32 activations, or of K INT8 codes followed by MR rows of K / G
+//           activation scales (rows past M zero)
 //   ring    kStages x kConsumers slots of 2 KB of codes
 //   tables  per consumer warp, for each of its units in order: the 64 columns' fp32 scales
 //           (lane l's columns l and 32 + l at words l and 32 + l)
 //   pieces  kConsumers x 2 x MR x 64 floats: a warp's partial sums of its first and last block
-template <int MR, int SPU>
+template <int MR, int SPU, bool A8>
 __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
     q8_gemv_kernel(const Q8GemvParams p) {
   using namespace q8g;
@@ -140,7 +162,9 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
   cb *= p.split_mult;
   ce *= p.split_mult;
   float *act = reinterpret_cast<float *>(smem);
-  uint8_t *ring = smem + (((size_t)MR * K * 4 + 127) & ~(size_t)127);
+  const int8_t *acode = reinterpret_cast<const int8_t *>(smem);         // A8: [MR][K]
+  float *ascale = reinterpret_cast<float *>(smem + (((size_t)MR * K + 15) & ~(size_t)15));
+  uint8_t *ring = smem + act_bytes(MR, K, G, A8);
   uint8_t *tables = ring + (size_t)S * NC * kSlotBytes;
   float *pieces = reinterpret_cast<float *>(tables + (size_t)NC * p.table_bytes);
 
@@ -212,16 +236,41 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
   if (p.static_w) load_table();
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (!p.static_w) load_table();
-  // ---- activations, [MR][K] fp32, zero rows past M
-  const int nth = NC * 32, K4 = K >> 2;
-  for (int idx = threadIdx.x; idx < MR * K4; idx += nth) {
-    const int m = idx / K4, k4 = idx - m * K4;
-    if (m < M)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr(act + (size_t)m * K + 4 * k4)),
-                   "l"(p.A + (size_t)m * K + 4 * k4)
-                   : "memory");
-    else
-      *reinterpret_cast<float4 *>(act + (size_t)m * K + 4 * k4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  // ---- activations, zero rows past M: [MR][K] fp32, or [MR][K] INT8 codes (16 bytes per
+  // copy) and [MR][K / G] scales (4 bytes per copy)
+  const int nth = NC * 32;
+  if (A8) {
+    const int K16 = K >> 4;
+    for (int idx = threadIdx.x; idx < MR * K16; idx += nth) {
+      const int m = idx / K16, k16 = idx - m * K16;
+      uint8_t *dst = smem + (size_t)m * K + 16 * k16;
+      if (m < M)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr(dst)),
+                     "l"(p.Aq + (size_t)m * K + 16 * k16)
+                     : "memory");
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int idx = threadIdx.x; idx < MR * GPB; idx += nth) {
+      const int m = idx / GPB, g = idx - m * GPB;
+      if (m < M)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr(ascale + idx)),
+                     "l"(p.As + (size_t)m * GPB + g)
+                     : "memory");
+      else
+        ascale[idx] = 0.f;
+    }
+  } else {
+    const int K4 = K >> 2;
+    for (int idx = threadIdx.x; idx < MR * K4; idx += nth) {
+      const int m = idx / K4, k4 = idx - m * K4;
+      if (m < M)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr(act + (size_t)m * K + 4 * k4)),
+                     "l"(p.A + (size_t)m * K + 4 * k4)
+                     : "memory");
+      else
+        *reinterpret_cast<float4 *>(act + (size_t)m * K + 4 * k4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -267,11 +316,16 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
   bool ok = true;
   int i = 0;                                       // slot number within this warp's stream
   for (int iu = 0; iu < nu && ok; ++iu) {
-    // the group's dot per row and column, even and odd k
+    // the group's dot per row and column: even and odd k (fp32 activations), or INT32 (A8)
     float de[MR][2], dd[MR][2];
+    int di[MR][2];
 #pragma unroll
-    for (int m = 0; m < MR; ++m) de[m][0] = de[m][1] = dd[m][0] = dd[m][1] = 0.f;
+    for (int m = 0; m < MR; ++m) {
+      de[m][0] = de[m][1] = dd[m][0] = dd[m][1] = 0.f;
+      di[m][0] = di[m][1] = 0;
+    }
     const float *ag = act + gcur * G;
+    const int8_t *aq = acode + gcur * G;
 #pragma unroll
     for (int ps = 0; ps < SPU; ++ps, ++i) {
       const int st = i % S;
@@ -295,6 +349,24 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
           : "memory");
       const uint32_t wa[8] = {va0.x, va0.y, va0.z, va0.w, va1.x, va1.y, va1.z, va1.w};
       const uint32_t wc[8] = {vc0.x, vc0.y, vc0.z, vc0.w, vc1.x, vc1.y, vc1.z, vc1.w};
+      if (A8) {
+        // word q of a column: k = 4q .. 4q + 3 of the slot; the row's codes of k = 16h ..
+        // 16h + 15 in one 16-byte broadcast
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 av = *reinterpret_cast<const uint4 *>(aq + (size_t)m * K + ps * kSlotK + 16 * h);
+            const int aw[4] = {(int)av.x, (int)av.y, (int)av.z, (int)av.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              di[m][0] = dp4a((int)wa[4 * h + e], aw[e], di[m][0]);
+              di[m][1] = dp4a((int)wc[4 * h + e], aw[e], di[m][1]);
+            }
+          }
+        }
+        continue;
+      }
       const float *ak = ag + ps * kSlotK;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {                // k = 4q .. 4q + 3 of the slot
@@ -319,8 +391,14 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
     const float sa = tbl[iu * kCols + lane], sc = tbl[iu * kCols + 32 + lane];
 #pragma unroll
     for (int m = 0; m < MR; ++m) {
-      acc[m][0] = fmaf(sa, de[m][0] + dd[m][0], acc[m][0]);
-      acc[m][1] = fmaf(sc, de[m][1] + dd[m][1], acc[m][1]);
+      if (A8) {
+        const float as = ascale[m * GPB + gcur];
+        acc[m][0] = fmaf(as * sa, (float)di[m][0], acc[m][0]);
+        acc[m][1] = fmaf(as * sc, (float)di[m][1], acc[m][1]);
+      } else {
+        acc[m][0] = fmaf(sa, de[m][0] + dd[m][0], acc[m][0]);
+        acc[m][1] = fmaf(sc, de[m][1] + dd[m][1], acc[m][1]);
+      }
     }
     if (++gcur == GPB) {
       flush(GPB);
@@ -417,13 +495,18 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
 // ------------------------------------------------------------------ host side
 
 namespace {
-int q8_gemv_rows(int M) { return M <= 1 ? 1 : 2; }
+bool is_a8(int prec) { return (prec & GQ_ACT_I8) != 0; }
+// template rows: 1 or 2 with fp32 activations; 1, 2 or 4 with INT8 ones
+int q8_gemv_rows(int M, int prec) { return M <= 1 ? 1 : M <= 2 ? 2 : is_a8(prec) ? 4 : 0; }
 }  // namespace
 
 bool q8_gemv_supported(int M, int K, int N, int G, int prec) {
-  return !(prec & GQ_W4) && (prec & GQ_ACT_F32) && (prec & GQ_SC_F32) &&
-         !(prec & (GQ_ZP | GQ_ZP_FLOAT)) && M >= 1 && M <= q8g::kMaxRows && N > 0 &&
-         N % q8g::kCols == 0 && G % q8g::kSlotK == 0 && G <= 128 && K % G == 0;
+  const bool a8 = is_a8(prec);
+  const bool acts = a8 ? !(prec & (GQ_ACT_F32 | GQ_GATE_UP)) && M <= q8g::kMaxRows
+                       : (prec & GQ_ACT_F32) && M <= q8g::kMaxRowsF32;
+  return !(prec & GQ_W4) && acts && (prec & GQ_SC_F32) && !(prec & (GQ_ZP | GQ_ZP_FLOAT)) &&
+         M >= 1 && N > 0 && N % q8g::kCols == 0 && G % q8g::kSlotK == 0 && G <= 128 &&
+         K % G == 0;
 }
 
 int q8_gemv_table_bytes(int max_cta_units) {
@@ -431,9 +514,9 @@ int q8_gemv_table_bytes(int max_cta_units) {
   return per_warp * q8g::kUnitTable;
 }
 
-size_t q8_gemv_smem_bytes(int M, int K, int max_cta_units) {
-  const int mr = q8_gemv_rows(M);
-  const size_t act = ((size_t)mr * K * 4 + 127) & ~(size_t)127;
+size_t q8_gemv_smem_bytes(int M, int K, int G, int prec, int max_cta_units) {
+  const int mr = q8_gemv_rows(M, prec);
+  const size_t act = q8g::act_bytes(mr, K, G, is_a8(prec));
   const size_t ring = (size_t)q8g::kStages * q8g::kConsumers * q8g::kSlotBytes;
   const size_t tables = (size_t)q8g::kConsumers * q8_gemv_table_bytes(max_cta_units);
   const size_t pieces = (size_t)q8g::kConsumers * 2 * mr * q8g::kCols * 4;
@@ -447,9 +530,9 @@ size_t q8_gemv_part_bytes(int grid) {
   return (size_t)grid * 2 * q8g::kMaxRows * q8g::kCols * sizeof(float);
 }
 
-template <int MR, int SPU>
+template <int MR, int SPU, bool A8>
 static cudaError_t launch_q8g_t(const Plan &pl, const Q8GemvParams &qp, cudaStream_t s) {
-  auto kern = q8_gemv_kernel<MR, SPU>;
+  auto kern = q8_gemv_kernel<MR, SPU, A8>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), pl.smem_bytes);
   if (e != cudaSuccess) return e;
   // programmatic stream serialization: this kernel reads activations and writes outputs only
@@ -467,23 +550,27 @@ static cudaError_t launch_q8g_t(const Plan &pl, const Q8GemvParams &qp, cudaStre
   return cudaLaunchKernelEx(&cfg, kern, qp);
 }
 
-template <int MR>
+template <int MR, bool A8>
 static cudaError_t launch_q8g_g(const Plan &pl, const Q8GemvParams &qp, cudaStream_t s) {
   switch (qp.G) {
-    case 32: return launch_q8g_t<MR, 1>(pl, qp, s);
-    case 64: return launch_q8g_t<MR, 2>(pl, qp, s);
-    case 128: return launch_q8g_t<MR, 4>(pl, qp, s);
+    case 32: return launch_q8g_t<MR, 1, A8>(pl, qp, s);
+    case 64: return launch_q8g_t<MR, 2, A8>(pl, qp, s);
+    case 128: return launch_q8g_t<MR, 4, A8>(pl, qp, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_q8_gemv(const Plan &pl, int M, int K, int N, int G, int prec, const void *A,
-                           const void *Wq, const void *scales, void *out, float *part,
-                           unsigned *counters, cudaStream_t s) {
+                           const float *a_scales, const void *Wq, const void *scales,
+                           void *out, float *part, unsigned *counters, cudaStream_t s) {
   if (!q8_gemv_supported(M, K, N, G, prec)) return cudaErrorInvalidValue;
+  const bool a8 = is_a8(prec);
+  if (a8 && !a_scales) return cudaErrorInvalidValue;
   Q8GemvParams qp;
   qp.Wp = reinterpret_cast<const uint8_t *>(Wq);
-  qp.A = reinterpret_cast<const float *>(A);
+  qp.A = a8 ? nullptr : reinterpret_cast<const float *>(A);
+  qp.Aq = a8 ? reinterpret_cast<const int8_t *>(A) : nullptr;
+  qp.As = a8 ? a_scales : nullptr;
   qp.S = reinterpret_cast<const float *>(scales);
   qp.out = out;
   qp.part = part;
@@ -498,8 +585,12 @@ cudaError_t launch_q8_gemv(const Plan &pl, int M, int K, int N, int G, int prec,
   qp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   qp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   qp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
-  if (q8_gemv_rows(M) == 1) return launch_q8g_g<1>(pl, qp, s);
-  return launch_q8g_g<2>(pl, qp, s);
+  switch (q8_gemv_rows(M, prec)) {
+    case 1: return a8 ? launch_q8g_g<1, true>(pl, qp, s) : launch_q8g_g<1, false>(pl, qp, s);
+    case 2: return a8 ? launch_q8g_g<2, true>(pl, qp, s) : launch_q8g_g<2, false>(pl, qp, s);
+    case 4: return a8 ? launch_q8g_g<4, true>(pl, qp, s) : cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int q8_gemv_set_wait_limit(long long cycles) {

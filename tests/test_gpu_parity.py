@@ -652,6 +652,14 @@ A8_SHAPES = [
                     out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("a8_m32_g256", M=32, K=2048, N=200, G=256, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
+    # the warp-specialized decode kernel (N a multiple of 64, M <= 4): G = 64 with bf16
+    # output, a padded fourth row at G = 128, whole blocks per CTA (304 blocks, no scratch)
+    gq_synth.Config("a8g_m2_g64_bf16", M=2, K=1024, N=640, G=64, w4=False, act="f32",
+                    sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8g_m3_g128", M=3, K=2048, N=448, G=128, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8g_m4_whole_blocks", M=4, K=512, N=19456, G=32, w4=False, act="f32",
+                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
 ]
 
 
@@ -699,6 +707,46 @@ def test_a8_quantize_then_gemm_and_integer_exactness(gq):
     torch.cuda.synchronize()
     ref_i, _ = oracle.reference_a8(Aq_i, As_i, inp["codes"], S_i, K=cfg.K, N=cfg.N, G=cfg.G)
     assert np.array_equal(out_to_f64(out_i, "f32"), ref_i)
+
+
+def test_a8_decode_kernel_integer_inputs_exact_and_repeatable(gq):
+    """The warp-specialized decode kernel's W8A8 form (N a multiple of 64): integer inputs
+    with power-of-two scales give the oracle's exact result bit for bit, and the Q8_0 M=1
+    workload gives the same bits call after call."""
+    from group_quantized_weight_gb300.constants import GQ_ACT_I8, GQ_OUT_F32, GQ_SC_F32
+    prec = GQ_ACT_I8 | GQ_SC_F32 | GQ_OUT_F32
+    cfg = gq_synth.Config("a8g_exact", M=3, K=1024, N=256, G=32, w4=False, act="f32",
+                          sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2)
+    assert gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)["path"] == 9
+    inp = gq_synth.make_inputs(cfg, seed=13)
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), cfg.K, cfg.N, cfg.G, prec)
+    rng = np.random.default_rng(5)
+    Aq_i = rng.integers(-8, 9, (cfg.M, cfg.K)).astype(np.int8)
+    As_i = np.ldexp(1.0, rng.integers(-4, -2, (cfg.M, cfg.K // cfg.G))).astype(np.float32)
+    S_i = np.ldexp(1.0, rng.integers(-6, -4, (cfg.K // cfg.G, cfg.N))).astype(np.float32)
+    out_i = alloc_out(cfg.M, cfg.N, "f32")
+    gq.gemm_a8_t(np_to_dev(Aq_i), np_to_dev(As_i), packed, np_to_dev(S_i), out_i, cfg.M, cfg.K,
+                 cfg.N, cfg.G, prec)
+    torch.cuda.synchronize()
+    ref_i, _ = oracle.reference_a8(Aq_i, As_i, inp["codes"], S_i, K=cfg.K, N=cfg.N, G=cfg.G)
+    assert np.array_equal(out_to_f64(out_i, "f32"), ref_i)
+    full = gq_synth.CONFIGS["q8_m1"]
+    assert gq.gq_plan(full.M, full.K, full.N, full.G, prec)["path"] == 9
+    inp, Aq, As = _a8_inputs(full, seed=2)
+    packed = gq.pack_weights_t(np_to_dev(inp["codes"]), full.K, full.N, full.G, prec)
+    Aq_d, As_d, S = np_to_dev(Aq), np_to_dev(As), np_to_dev(inp["scales"])
+    outs = []
+    for _ in range(3):
+        o = alloc_out(full.M, full.N, "f32")
+        gq.gemm_a8_t(Aq_d, As_d, packed, S, o, full.M, full.K, full.N, full.G, prec)
+        outs.append(o.view(torch.int32))
+    torch.cuda.synchronize()
+    assert gq.gq_device_error(clear=True) == 0
+    assert all(torch.equal(outs[0], x) for x in outs[1:])
+    ref, mag = oracle.reference_a8(Aq, As, inp["codes"], inp["scales"], K=full.K, N=full.N,
+                                   G=full.G)
+    _assert_parity(full.replace(name="a8g_q8_m1"), out_to_f64(outs[0].view(torch.float32), "f32"),
+                   ref, mag)
 
 
 # ------------------------------------------------------------------ FP8 block-scaled GEMM
