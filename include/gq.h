@@ -346,7 +346,8 @@ typedef struct gq_plan_t {
                             2 KB slots of codes with cp.async.bulk, sixteen consumer warps
                             on mma.sync),
                         9 = warp-specialized INT8 decode (M <= 2, N a multiple of 64, G of
-                            32, 64 or 128: the same roles, FP32 products on CUDA cores) */
+                            32, 64 or 128: the same roles, FP32 products on CUDA cores; with
+                            GQ_ACT_I8 one row, dp4a group dots) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
   int n_tile;        /* output columns one CTA covers */

@@ -652,13 +652,13 @@ A8_SHAPES = [
                     out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("a8_m32_g256", M=32, K=2048, N=200, G=256, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
-    # the warp-specialized decode kernel (N a multiple of 64, M <= 4): G = 64 with bf16
-    # output, a padded fourth row at G = 128, whole blocks per CTA (304 blocks, no scratch)
-    gq_synth.Config("a8g_m2_g64_bf16", M=2, K=1024, N=640, G=64, w4=False, act="f32",
+    # the warp-specialized decode kernel (N a multiple of 64, one row): G = 64 with bf16
+    # output, G = 128, whole blocks per CTA (304 blocks, no scratch)
+    gq_synth.Config("a8g_m1_g64_bf16", M=1, K=1024, N=640, G=64, w4=False, act="f32",
                     sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),
-    gq_synth.Config("a8g_m3_g128", M=3, K=2048, N=448, G=128, w4=False, act="f32", sc="f32",
+    gq_synth.Config("a8g_m1_g128", M=1, K=2048, N=448, G=128, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
-    gq_synth.Config("a8g_m4_whole_blocks", M=4, K=512, N=19456, G=32, w4=False, act="f32",
+    gq_synth.Config("a8g_m1_whole_blocks", M=1, K=512, N=19456, G=32, w4=False, act="f32",
                     sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
 ]
 
@@ -715,7 +715,7 @@ def test_a8_decode_kernel_integer_inputs_exact_and_repeatable(gq):
     workload gives the same bits call after call."""
     from group_quantized_weight_gb300.constants import GQ_ACT_I8, GQ_OUT_F32, GQ_SC_F32
     prec = GQ_ACT_I8 | GQ_SC_F32 | GQ_OUT_F32
-    cfg = gq_synth.Config("a8g_exact", M=3, K=1024, N=256, G=32, w4=False, act="f32",
+    cfg = gq_synth.Config("a8g_exact", M=1, K=1024, N=256, G=32, w4=False, act="f32",
                           sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2)
     assert gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)["path"] == 9
     inp = gq_synth.make_inputs(cfg, seed=13)

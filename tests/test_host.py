@@ -388,11 +388,11 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
 
 def test_int8_activation_variant_validation_and_plan():
     a8 = C.GQ_ACT_I8 | C.GQ_SC_F32 | C.GQ_OUT_F32
-    # up to four rows with N a multiple of 64 and G <= 128: the warp-specialized decode kernel
-    # (dp4a group dots); otherwise the W8A8 block kernel
-    for M in (1, 2, 3, 4):
-        assert gq.gq_plan(M, 2048, 12288, 32, a8, sm_count=152)["path"] == 9
-    assert gq.gq_plan(5, 2048, 12288, 32, a8, sm_count=152)["path"] == 7
+    # one row with N a multiple of 64 and G <= 128: the warp-specialized decode kernel (dp4a
+    # group dots); otherwise the W8A8 block kernel
+    assert gq.gq_plan(1, 2048, 12288, 32, a8, sm_count=152)["path"] == 9
+    for M in (2, 3, 4, 5):
+        assert gq.gq_plan(M, 2048, 12288, 32, a8, sm_count=152)["path"] == 7
     assert gq.gq_plan(1, 2048, 1000, 32, a8, sm_count=152)["path"] == 7
     assert gq.gq_plan(1, 2048, 1024, 256, a8, sm_count=152)["path"] == 7
     p = gq.gq_plan(40, 2048, 1000, 32, a8, sm_count=152)
