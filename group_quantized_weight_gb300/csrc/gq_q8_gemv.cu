@@ -47,6 +47,7 @@ constexpr int kCols = 64;                       // columns per block (two per la
 constexpr int kMaxRows = 2;                     // fp32 activations; one row with INT8 ones
 constexpr int kMaxRowsA8 = 1;
 constexpr int kUnitTable = kCols * 4;           // table bytes per unit: 64 fp32 scales
+constexpr int kBatch = 4;                       // partial sums loaded per batch in reductions
 }  // namespace q8g
 
 // Sticky device-side status (GQ_ERR_TIMEOUT after a bounded wait gave up) and the wait limit
@@ -431,24 +432,49 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
     if (pass == 0 && wb > cb && wb % GPB != 0) continue;          // a lower warp reduces it
     const bool cta_whole = tb >= cb && te <= ce;
     const int region = tb < cb ? 0 : 1;
-    for (int m = 0; m < M; ++m) {
-      float sa = 0.f, sc = 0.f;
-      for (int w2 = warp; w2 < NC; ++w2) {
+    // the warps of this CTA holding units of the block: warp .. w_hi
+    int w_hi = warp;
+    for (int w2 = warp + 1; w2 < NC; ++w2) {
+      int b2, e2;
+      zsplit_dev(ce - cb, NC, w2, b2, e2);
+      if (e2 <= b2 || b2 + cb >= te) break;
+      w_hi = w2;
+    }
+    // their shares added in warp order; the loads of kBatch warps are issued before their adds
+    float sa[MR], sc[MR];
+#pragma unroll
+    for (int m = 0; m < MR; ++m) sa[m] = sc[m] = 0.f;
+    for (int w0 = warp; w0 <= w_hi; w0 += kBatch) {
+      float va[kBatch][MR], vc[kBatch][MR];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int w2 = min(w0 + j, w_hi);
         int b2, e2;
         zsplit_dev(ce - cb, NC, w2, b2, e2);
-        b2 += cb;
-        e2 += cb;
-        if (e2 <= b2 || b2 >= te) break;
-        const float *pc = pieces + (size_t)(w2 * 2 + (b2 / GPB == tt ? 0 : 1)) * MR * kCols;
-        sa += pc[m * kCols + lane];
-        sc += pc[m * kCols + 32 + lane];
+        const float *pc = pieces + (size_t)(w2 * 2 + ((b2 + cb) / GPB == tt ? 0 : 1)) * MR * kCols;
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          va[j][m] = pc[m * kCols + lane];
+          vc[j][m] = pc[m * kCols + 32 + lane];
+        }
       }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (w0 + j > w_hi) break;
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          sa[m] += va[j][m];
+          sc[m] += vc[j][m];
+        }
+      }
+    }
+    for (int m = 0; m < M; ++m) {
       if (cta_whole) {
-        store_block(tt, m, sa, sc);
+        store_block(tt, m, sa[m], sc[m]);
       } else {
         float *dst = p.part + ((size_t)blockIdx.x * 2 + region) * (kMaxRows * kCols) + m * kCols;
-        __stcg(dst + lane, sa);
-        __stcg(dst + 32 + lane, sc);
+        __stcg(dst + lane, sa[m]);
+        __stcg(dst + 32 + lane, sc[m]);
       }
     }
     if (cta_whole) continue;
@@ -465,7 +491,8 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
     __syncwarp();
     if (!s_last[warp]) continue;
     __threadfence();
-    int c_lo = blockIdx.x;
+    // the CTAs holding units of the block: c_lo .. c_hi (a CTA's range may be empty)
+    int c_lo = blockIdx.x, c_hi = blockIdx.x;
     for (;;) {
       if (c_lo == 0) break;
       int b2, e2;
@@ -473,22 +500,47 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
       if (e2 * p.split_mult <= tb) break;
       --c_lo;
     }
-    for (int m = 0; m < M; ++m) {
-      float sa = 0.f, sc = 0.f;
-      for (int c2 = c_lo; c2 < (int)gridDim.x; ++c2) {
+    for (;;) {
+      if (c_hi + 1 >= (int)gridDim.x) break;
+      int b2, e2;
+      zsplit_dev(p.split_count, gridDim.x, c_hi + 1, b2, e2);
+      if (b2 * p.split_mult >= te) break;
+      ++c_hi;
+    }
+    // their partial sums added in CTA order; the L2 reads of kBatch CTAs are issued before
+    // their adds (one round trip per batch, not per CTA)
+#pragma unroll
+    for (int m = 0; m < MR; ++m) sa[m] = sc[m] = 0.f;
+    for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+      float va[kBatch][MR], vc[kBatch][MR];
+      bool use[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int c2 = min(c0 + j, c_hi);
         int b2, e2;
         zsplit_dev(p.split_count, gridDim.x, c2, b2, e2);
         b2 *= p.split_mult;
         e2 *= p.split_mult;
-        if (b2 >= te) break;
-        if (e2 <= b2) continue;
+        use[j] = c0 + j <= c_hi && e2 > b2;
         const int r2 = tb < b2 ? 0 : 1;           // the region that CTA wrote
-        const float *src = p.part + ((size_t)c2 * 2 + r2) * (kMaxRows * kCols) + m * kCols;
-        sa += __ldcg(src + lane);
-        sc += __ldcg(src + 32 + lane);
+        const float *src = p.part + ((size_t)c2 * 2 + r2) * (kMaxRows * kCols);
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          va[j][m] = use[j] ? __ldcg(src + m * kCols + lane) : 0.f;
+          vc[j][m] = use[j] ? __ldcg(src + m * kCols + 32 + lane) : 0.f;
+        }
       }
-      store_block(tt, m, sa, sc);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (!use[j]) continue;
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+          sa[m] += va[j][m];
+          sc[m] += vc[j][m];
+        }
+      }
     }
+    for (int m = 0; m < M; ++m) store_block(tt, m, sa[m], sc[m]);
   }
 }
 
