@@ -183,9 +183,9 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
   // float zero points: the small-batch kernel only
   if ((prec & GQ_ZP_FLOAT) && !(Mc <= kBatchMaxM && batch_supported(Mc, K, G, prec)))
     return GQ_ERR_UNSUPPORTED;
-  // W8A8 (GQ_ACT_I8), one row: the warp-specialized decode kernel with dp4a group dots (two
-  // to four rows: the block kernel below measured as fast or faster, 10.8 / 11.5 / 11.6
-  // against 10.9 / 14.4 / 16.8 us on the Q8_0 shape)
+  // W8A8 (GQ_ACT_I8), M <= 4: the warp-specialized decode kernel with dp4a group dots (on the
+  // Q8_0 shape 8.3 / 8.8 / 10.0 / 10.1 us for one to four rows against 10.5 / 10.9 / 11.6 /
+  // 11.7 for the block kernel below)
   if ((prec & GQ_ACT_I8) && plan_q8_gemv(Mc, K, Nc, G, prec, sms, kCtaSmemCap, p)) return GQ_OK;
   // W8A8 (GQ_ACT_I8): integer group dots, 64 columns x one K slice x 32 rows per CTA
   if (prec & GQ_ACT_I8) {
@@ -295,9 +295,9 @@ int make_plan(int M, int K, int N, int G, int prec, int sms, Plan *p) {
     p->nsplit = p->grid_x;
     return GQ_OK;
   }
-  // INT8 codes with fp32 activations, M <= 2: the warp-specialized decode kernel (three and
-  // four rows: the block kernel below measured faster, 16.6 / 16.9 against 18.1 / 20.6 us on
-  // the Q8_0 shape)
+  // INT8 codes with fp32 activations, M <= 4: the warp-specialized decode kernel (on the Q8_0
+  // shape 9.4 / 10.6 / 13.7 / 13.7 us for one to four rows against 11.5 / 13.3 / 16.7 / 16.9
+  // for the block kernel below)
   if (plan_q8_gemv(Mc, K, Nc, G, prec, sms, kCtaSmemCap, p)) return GQ_OK;
   // INT8 codes, 5 <= M <= 32: BF16 tensor cores, 64 columns x one K slice per CTA (up to 4
   // rows the CUDA-core kernel below is faster: it is load-latency-bound there)

@@ -103,7 +103,7 @@ int gemv_read_error(int clear);
 int gemv_set_wait_limit(long long cycles);
 // GQ_FAULT_DEVICE_WAIT: the producer warps of later launches withhold one slot
 int gemv_set_withhold(bool on);
-// warp-specialized INT8 decode kernel (N a multiple of 64; M <= 2, W8A8 M = 1): a producer
+// warp-specialized INT8 decode kernel (N a multiple of 64, M <= 4, W8A16 or W8A8): a producer
 // warp and sixteen consumer warps per CTA over (64-column block, group) units
 bool q8_gemv_supported(int M, int K, int N, int G, int prec);
 int q8_gemv_table_bytes(int max_cta_units);

@@ -1,5 +1,5 @@
-// Warp-specialized INT8 (Q8_0-style) decode kernel: fp32 activations (M <= 2) or one row of
-// INT8 activations with a scale per group (W8A8, M = 1), fp32 weight scales.
+// Warp-specialized INT8 (Q8_0-style) decode kernel for M <= 4: fp32 activations, or INT8
+// activations with a scale per (row, group) (W8A8); fp32 weight scales.
 //
 // At decode the INT8 path is bound by the bytes of its codes ("GPU Kernel 工程（09）：量化与
 // 融合 kernel", section 3.2), and a short problem (the Q8_0 projection reads 28 MB) is set by
@@ -44,8 +44,8 @@ constexpr int kStages = 3;                      // ring stages (one slot per con
 constexpr int kSlotBytes = 2048;                // 32 k x 64 columns of codes
 constexpr int kSlotK = 32;
 constexpr int kCols = 64;                       // columns per block (two per lane)
-constexpr int kMaxRows = 2;                     // fp32 activations; one row with INT8 ones
-constexpr int kMaxRowsA8 = 1;
+constexpr int kMaxRows = 4;                     // fp32 activations
+constexpr int kMaxRowsA8 = 4;                   // INT8 activations (the same bound)
 constexpr int kUnitTable = kCols * 4;           // table bytes per unit: 64 fp32 scales
 constexpr int kBatch = 4;                       // partial sums loaded per batch in reductions
 }  // namespace q8g
@@ -62,7 +62,7 @@ struct Q8GemvParams {
   const float *As;            // [M][K/G] their scales
   const float *S;             // [K/G][N]
   void *out;                  // [M][N] (gate+up: [M][N/2])
-  float *part;                // [gridDim.x][2][2][64] per-CTA partial sums (shared blocks)
+  float *part;                // [gridDim.x][2][4][64] per-CTA partial sums (shared blocks)
   unsigned *counters;         // per-block arrival counters (shared blocks)
   int M, K, N, G;
   int split_count, split_mult;   // CTA c owns units zsplit(split_count, grid, c) * split_mult
@@ -548,8 +548,8 @@ __global__ void __launch_bounds__((q8g::kConsumers + 1) * 32, 1)
 
 namespace {
 bool is_a8(int prec) { return (prec & GQ_ACT_I8) != 0; }
-// template rows: 1 or 2 with fp32 activations, 1 with INT8 ones
-int q8_gemv_rows(int M, int) { return M <= 1 ? 1 : 2; }
+// template rows: 1, 2 or 4
+int q8_gemv_rows(int M, int) { return M <= 1 ? 1 : M <= 2 ? 2 : 4; }
 }  // namespace
 
 bool q8_gemv_supported(int M, int K, int N, int G, int prec) {
@@ -637,9 +637,11 @@ cudaError_t launch_q8_gemv(const Plan &pl, int M, int K, int N, int G, int prec,
   qp.out_f32 = (prec & GQ_OUT_F32) ? 1 : 0;
   qp.static_w = (prec & GQ_STATIC_W) ? 1 : 0;
   qp.gate_up = (prec & GQ_GATE_UP) ? 1 : 0;
-  if (a8) return launch_q8g_g<1, true>(pl, qp, s);
-  if (q8_gemv_rows(M, prec) == 1) return launch_q8g_g<1, false>(pl, qp, s);
-  return launch_q8g_g<2, false>(pl, qp, s);
+  switch (q8_gemv_rows(M, prec)) {
+    case 1: return a8 ? launch_q8g_g<1, true>(pl, qp, s) : launch_q8g_g<1, false>(pl, qp, s);
+    case 2: return a8 ? launch_q8g_g<2, true>(pl, qp, s) : launch_q8g_g<2, false>(pl, qp, s);
+    default: return a8 ? launch_q8g_g<4, true>(pl, qp, s) : launch_q8g_g<4, false>(pl, qp, s);
+  }
 }
 
 int q8_gemv_set_wait_limit(long long cycles) {

@@ -337,17 +337,17 @@ typedef struct gq_plan_t {
                         3 = striped decode (M <= 8, warps stream contiguous slot ranges),
                         4 = small-batch tensor-core kernel (M <= 32, up to 64 with G = 32;
                             persistent CTAs over (K slice, tile range) pairs),
-                        5 = INT8 CUDA-core kernel for M <= 4 (64 columns x one K slice
-                            per CTA, paired FP32 FMAs),
+                        5 = INT8 CUDA-core kernel for M <= 4 where path 9 does not take the
+                            shape (64 columns x one K slice per CTA, paired FP32 FMAs),
                         6 = INT8 on BF16 tensor cores for 5 <= M <= 32 (codes exact in
                             BF16, fp32 activations as three exact BF16 parts),
                         7 = W8A8 integer group GEMM (GQ_ACT_I8, dp4a),
                         8 = warp-specialized W4 decode (M <= 4: a producer warp streaming
                             2 KB slots of codes with cp.async.bulk, sixteen consumer warps
                             on mma.sync),
-                        9 = warp-specialized INT8 decode (M <= 2, N a multiple of 64, G of
-                            32, 64 or 128: the same roles, FP32 products on CUDA cores; with
-                            GQ_ACT_I8 one row, dp4a group dots) */
+                        9 = warp-specialized INT8 decode (M <= 4, N a multiple of 64, G of
+                            32, 64 or 128: the same roles, FP32 products on CUDA cores, or
+                            dp4a group dots with GQ_ACT_I8) */
   int nsplit;        /* K-slices of whole groups (1 = no split) */
   int m_tile;        /* rows of A one CTA covers */
   int n_tile;        /* output columns one CTA covers */

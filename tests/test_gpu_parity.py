@@ -99,12 +99,14 @@ Q8_SHAPES = [
                     sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),     # 2 blocks per CTA
     gq_synth.Config("q8_m16_5blocks", M=16, K=1024, N=20008, G=64, w4=False, act="f32",
                     sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),    # 5 blocks per CTA
-    # the warp-specialized INT8 decode kernel (M <= 2, N a multiple of 64): G = 64 and 128,
-    # blocks split between warps and CTAs, whole blocks per CTA (304 blocks on 152 SMs, no
-    # scratch), a CTA whose later warps hold no unit
+    # the warp-specialized INT8 decode kernel (M <= 4, N a multiple of 64): G = 64 and 128, a
+    # padded fourth row, blocks split between warps and CTAs, whole blocks per CTA (304 blocks
+    # on 152 SMs, no scratch), a CTA whose later warps hold no unit
     gq_synth.Config("q8g_m2_g64", M=2, K=1024, N=640, G=64, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
-    gq_synth.Config("q8g_m2_g128_bf16", M=2, K=2048, N=448, G=128, w4=False, act="f32",
+    gq_synth.Config("q8g_m3_g64", M=3, K=1024, N=640, G=64, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("q8g_m4_g128_bf16", M=4, K=2048, N=448, G=128, w4=False, act="f32",
                     sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("q8g_m2_whole_blocks", M=2, K=512, N=19456, G=32, w4=False, act="f32",
                     sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
@@ -517,8 +519,8 @@ GATE_UP_SHAPES = [
     gq_synth.Config("gu_m12_split_f32", M=12, K=8192, N=288, G=64, sc="f32", out="f32"),
     gq_synth.Config("gu_m40_g32_split", M=40, K=4096, N=544, G=32, zp=True),
     gq_synth.Config("gu_m33_g64", M=33, K=1024, N=160, G=64),
-    # INT8 codes (Q8_0 form): the warp-specialized kernel (M <= 2), the CUDA-core block kernel
-    # (three rows; G = 256) and the tensor-core one, with and without a K split, fp32 and bf16 output
+    # INT8 codes (Q8_0 form): the warp-specialized kernel (M <= 4), the CUDA-core block kernel
+    # (G = 256) and the tensor-core one, with and without a K split, fp32 and bf16 output
     gq_synth.Config("gu_q8_m1", M=1, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("gu_q8_m2_g256", M=2, K=2048, N=128, G=256, w4=False, act="f32",
@@ -652,14 +654,16 @@ A8_SHAPES = [
                     out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("a8_m32_g256", M=32, K=2048, N=200, G=256, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
-    # the warp-specialized decode kernel (N a multiple of 64, one row): G = 64 with bf16
-    # output, G = 128, whole blocks per CTA (304 blocks, no scratch)
-    gq_synth.Config("a8g_m1_g64_bf16", M=1, K=1024, N=640, G=64, w4=False, act="f32",
+    # the warp-specialized decode kernel (N a multiple of 64, M <= 4): G = 64 with bf16
+    # output, a padded fourth row at G = 128, whole blocks per CTA (304 blocks, no scratch)
+    gq_synth.Config("a8g_m2_g64_bf16", M=2, K=1024, N=640, G=64, w4=False, act="f32",
                     sc="f32", out="bf16", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8g_m3_g128", M=3, K=2048, N=448, G=128, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),
+    gq_synth.Config("a8g_m4_whole_blocks", M=4, K=512, N=19456, G=32, w4=False, act="f32",
+                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
     gq_synth.Config("a8g_m1_g128", M=1, K=2048, N=448, G=128, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),
-    gq_synth.Config("a8g_m1_whole_blocks", M=1, K=512, N=19456, G=32, w4=False, act="f32",
-                    sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2),
 ]
 
 
@@ -715,7 +719,7 @@ def test_a8_decode_kernel_integer_inputs_exact_and_repeatable(gq):
     workload gives the same bits call after call."""
     from group_quantized_weight_gb300.constants import GQ_ACT_I8, GQ_OUT_F32, GQ_SC_F32
     prec = GQ_ACT_I8 | GQ_SC_F32 | GQ_OUT_F32
-    cfg = gq_synth.Config("a8g_exact", M=1, K=1024, N=256, G=32, w4=False, act="f32",
+    cfg = gq_synth.Config("a8g_exact", M=3, K=1024, N=256, G=32, w4=False, act="f32",
                           sc="f32", out="f32", s_lo=1e-3, s_hi=1e-2)
     assert gq.gq_plan(cfg.M, cfg.K, cfg.N, cfg.G, prec)["path"] == 9
     inp = gq_synth.make_inputs(cfg, seed=13)

@@ -180,13 +180,13 @@ def test_plan_is_a_pure_function_of_shape(name):
             assert tiles >= 152
         return
     if p1["path"] == 9:
-        # warp-specialized INT8 decode (M <= 2, N a multiple of 64): a producer warp and
+        # warp-specialized INT8 decode (M <= 4, N a multiple of 64): a producer warp and
         # sixteen consumer warps per CTA over (64-column block, group) units, at most one CTA
         # per SM; whole blocks per CTA need no scratch, equal unit ranges per-CTA partial sums
         # and per-block counters
         blocks = cfg.N // 64
         units = blocks * (cfg.K // cfg.G)
-        assert not cfg.w4 and cfg.M <= 2 and cfg.N % 64 == 0
+        assert not cfg.w4 and cfg.M <= 4 and cfg.N % 64 == 0
         assert p1["block_threads"] == 17 * 32
         assert 1 <= p1["grid_x"] <= min(152, units)
         assert p1["nsplit"] == p1["grid_x"] and p1["n_tile"] == 64
@@ -285,7 +285,7 @@ def test_small_batch_plan_warps_follow_the_rows_and_fill_one_wave():
 
 
 def test_q8_decode_plan_partitions_block_group_units():
-    """INT8 rows M <= 2 with N a multiple of 64: the warp-specialized kernel, one CTA per SM at
+    """INT8 rows M <= 4 with N a multiple of 64: the warp-specialized kernel, one CTA per SM at
     most over contiguous (64-column block, group) ranges; the split override (a K-slice
     count) does not apply to it."""
     W8 = C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_OUT_F32
@@ -298,20 +298,20 @@ def test_q8_decode_plan_partitions_block_group_units():
     # a small shape (4 blocks x 16 groups): at least two units per consumer warp
     p = gq.gq_plan(2, 512, 256, 32, W8, sm_count=152)
     assert p["path"] == 9 and p["grid_x"] == 2
-    # not taken: N not a multiple of 64, G of 256, three and five rows, activations too wide
+    # not taken: N not a multiple of 64, G of 256, five rows, activations too wide
     assert gq.gq_plan(1, 2048, 1000, 32, W8, sm_count=152)["path"] == 5
     assert gq.gq_plan(1, 2048, 1024, 256, W8, sm_count=152)["path"] == 5
-    assert gq.gq_plan(3, 2048, 1024, 32, W8, sm_count=152)["path"] == 5
+    assert gq.gq_plan(3, 2048, 1024, 32, W8, sm_count=152)["path"] == 9
     assert gq.gq_plan(5, 2048, 1024, 32, W8, sm_count=152)["path"] == 6
     assert gq.gq_plan(2, 32768, 1024, 32, W8, sm_count=152)["path"] == 5
     # the GPU parity shapes named q8g_* and the gate+up ones meant for it take this kernel
-    for M, K, N, G in ((2, 1024, 640, 64), (2, 2048, 448, 128), (2, 512, 19456, 32),
+    for M, K, N, G in ((3, 1024, 640, 64), (4, 2048, 448, 128), (2, 512, 19456, 32),
                        (1, 96, 64, 32)):
         assert gq.gq_plan(M, K, N, G, W8, sm_count=152)["path"] == 9, (M, K, N, G)
     assert gq.gq_plan(2, 512, 19456, 32, W8, sm_count=152)["workspace_bytes"] == 0
     gu = W8 | C.GQ_GATE_UP
     assert gq.gq_plan(1, 2048, 1024, 32, gu, sm_count=152)["path"] == 9
-    assert gq.gq_plan(3, 2048, 128, 32, gu, sm_count=152)["path"] == 5
+    assert gq.gq_plan(3, 2048, 128, 32, gu, sm_count=152)["path"] == 9
     assert gq.gq_plan(2, 2048, 128, 256, gu, sm_count=152)["path"] == 5
     prev = gq.gq_set_split_override(2)
     try:
@@ -353,11 +353,11 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
     W8GU = C.GQ_ACT_F32 | C.GQ_SC_F32 | C.GQ_GATE_UP
     assert gq.gq_gemm(1, 512, 24, 128, gu, 16, 16, 16, None, 16, None) == 1
     assert gq.gq_gemm(1, 512, 32, 32, W8GU, 16, 16, 16, None, 16, None) == 1
-    # INT8: the warp-specialized kernel up to two rows, the CUDA-core block kernel to four (and
-    # when N is not a multiple of 64), the tensor-core one to 32; not above
-    assert gq.gq_plan(1, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 9
-    assert gq.gq_plan(2, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 9
-    assert gq.gq_plan(3, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 5
+    # INT8: the warp-specialized kernel up to four rows (the CUDA-core block kernel where it
+    # does not take the shape), the tensor-core one to 32; not above
+    for M in (1, 2, 3, 4):
+        assert gq.gq_plan(M, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 9
+    assert gq.gq_plan(2, 2048, 12288, 256, W8GU, sm_count=152)["path"] == 5
     assert gq.gq_plan(1, 2048, 12224, 32, W8GU, sm_count=152)["path"] == 9
     assert gq.gq_plan(32, 2048, 12288, 32, W8GU, sm_count=152)["path"] == 6
     with pytest.raises(C.GqError) as e:
@@ -388,11 +388,11 @@ def test_gate_up_flag_is_validated_and_planned_on_the_decode_kernels():
 
 def test_int8_activation_variant_validation_and_plan():
     a8 = C.GQ_ACT_I8 | C.GQ_SC_F32 | C.GQ_OUT_F32
-    # one row with N a multiple of 64 and G <= 128: the warp-specialized decode kernel (dp4a
-    # group dots); otherwise the W8A8 block kernel
-    assert gq.gq_plan(1, 2048, 12288, 32, a8, sm_count=152)["path"] == 9
-    for M in (2, 3, 4, 5):
-        assert gq.gq_plan(M, 2048, 12288, 32, a8, sm_count=152)["path"] == 7
+    # up to four rows with N a multiple of 64 and G <= 128: the warp-specialized decode kernel
+    # (dp4a group dots); otherwise the W8A8 block kernel
+    for M in (1, 2, 3, 4):
+        assert gq.gq_plan(M, 2048, 12288, 32, a8, sm_count=152)["path"] == 9
+    assert gq.gq_plan(5, 2048, 12288, 32, a8, sm_count=152)["path"] == 7
     assert gq.gq_plan(1, 2048, 1000, 32, a8, sm_count=152)["path"] == 7
     assert gq.gq_plan(1, 2048, 1024, 256, a8, sm_count=152)["path"] == 7
     p = gq.gq_plan(40, 2048, 1000, 32, a8, sm_count=152)
