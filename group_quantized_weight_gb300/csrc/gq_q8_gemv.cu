@@ -13,20 +13,20 @@
 //                   the activations, then per slot: one bounded wait, four 16-byte reads of
 //                   codes, the slot released at once (the codes are in registers), and the
 //                   products on CUDA cores (FP32, or dp4a for INT8 activations).
-// The consumers need about two instructions per code, well under what the SM can issue in the
-// time HBM takes to deliver the bytes, so the ring runs nearly empty and little is left to do
-// when the last copy lands.
+// The consumers need about two instructions per code (FP32) or a quarter of one (dp4a), under
+// what the SM can issue in the time HBM takes to deliver the bytes, so they keep up with the
+// stream and little is left to do when the last copy lands.
 //
 // Arithmetic: the group-wise product of "04 · 分组量化 GEMM 内核", section 2 in its own order —
 // per (column, group) the FP32 dot of the exact codes with the activations (even and odd k in
 // two sums, one fma.rn.f32x2 per two products), then the group's scale times that dot added to
 // the column's running sum.  An INT8 code c becomes the exact float c by placing (c xor 0x80)
 // in the low byte of 2^23 and subtracting 2^23 + 128.  With INT8 activations the group's dot
-// is the exact INT32 sum of dp4a products, converted exactly (|dot| <= 128 * 127^2 < 2^24)
+// is the exact INT32 sum of dp4a products, converted exactly (|dot| <= 128 * 128 * 127 < 2^24)
 // and multiplied by the activation scale times the weight scale (the same FMA as the W8A8
 // block kernel).
 //
-// Work partition (the striped partitioning of section 3.3 item 4 of the first page): with N a
+// Work partition (the striped partitioning of "量化与融合 kernel", section 3.3 item 4): with N a
 // multiple of 64 the packed codes are the units (64-column block b, group g) one after another,
 // unit u = b (K / G) + g at byte u · 64 G.  CTA c owns a contiguous range of units (whole
 // blocks when there are enough of them, otherwise an equal share) and its sixteen consumer
