@@ -32,6 +32,8 @@ def gq():
     gq_synth.Config("nsa_q8_m16", M=16, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
                     out="f32", s_lo=1e-3, s_hi=1e-2),        # INT8 CUDA-core kernel, K split
     gq_synth.Config("nsa_zf_m12", M=12, K=4096, N=520, G=64, zf=True, sc="bf16"),  # float zeros, K split
+    gq_synth.Config("nsa_q8g_m2", M=2, K=2048, N=1024, G=32, w4=False, act="f32", sc="f32",
+                    out="f32", s_lo=1e-3, s_hi=1e-2),        # INT8 decode kernel, CTAs share blocks
 ], ids=lambda c: c.name)
 def test_static_scratch_matches_gq_gemm_twice(gq, cfg):
     inp = gq_synth.make_inputs(cfg, seed=4)
